@@ -1,0 +1,277 @@
+"""Seeded synthetic workloads for the sparse MoE FFN forward pass.
+
+This module only makes input data: shapes of the named workloads and seeded
+random tensors.  It holds none of the layer's arithmetic, so both the CPU
+oracle (through the tests) and the CUDA path (through the tests and the
+benchmark) can take their inputs from it.
+
+Seed tree
+---------
+Every tensor block is drawn from its own PCG64 stream,
+``SeedSequence(entropy=seed, spawn_key=(tensor_id, block))``, where
+``block`` is the expert index for per-expert tensors, the row-chunk index
+(``X_CHUNK_ROWS`` rows per chunk) for the activations, and 0 otherwise.
+A block's values therefore do not depend on which other blocks are drawn,
+on the order of drawing or on the number of threads; the oracle can
+regenerate the handful of experts a sampled token needs without drawing
+the rest.
+
+Values are drawn in float32 and, for the bf16 tensors, rounded to bf16 with
+round-to-nearest-even; the bf16 tensors are returned as their uint16 bit
+patterns so that the oracle and the GPU read identical bytes.
+"""
+from __future__ import annotations
+
+import math
+import os
+from concurrent.futures import ThreadPoolExecutor
+from dataclasses import dataclass, replace
+from typing import Callable, Dict, Optional
+
+import numpy as np
+
+X_CHUNK_ROWS = 4096
+_TENSOR_ID = {
+    "x": 0, "Wg": 1, "bg": 2, "sel_bias": 3,
+    "W1": 4, "b1": 5, "W2": 6, "b2": 7,
+    "W1s": 8, "b1s": 9, "W2s": 10, "b2s": 11,
+}
+
+
+@dataclass(frozen=True)
+class Workload:
+    """Shape and value recipe of one synthetic MoE layer workload."""
+    name: str
+    T: int                  # tokens (batch * seq flattened)
+    H: int                  # hidden size
+    F: int                  # expert FFN inner size
+    N: int                  # routed experts
+    k: int                  # experts per token
+    capacity_factor: float = 0.0      # <= 0: no capacity limit
+    gate_bias: Optional[str] = None   # None | "zero" | "zipf1.1" | "normal"
+    expert_bias: Optional[str] = None  # None | "zero" | "normal"
+    sel_bias: Optional[str] = None    # None | "uniform0.1"
+    F_shared: int = 0                 # 0: no shared expert
+    aux_alpha: float = 0.01
+    phase: str = "prefill"            # "prefill" | "decode" (which roof bounds it)
+
+    def with_tokens(self, T: int, name: Optional[str] = None) -> "Workload":
+        return replace(self, T=T, name=name or f"{self.name}_T{T}")
+
+
+# The layer shapes of the pages' models; all values synthetic.
+WORKLOADS: Dict[str, Workload] = {w.name: w for w in [
+    # tiny oracle case: fp32 in the source description, bf16-rounded here
+    Workload("tiny", T=64, H=32, F=128, N=4, k=2, gate_bias="zero", expert_bias="zero"),
+    # the pages' MoELayer: batch 8 x seq 512, hidden 1024, 8 experts, top-2, FFN 4x
+    Workload("moelayer", T=4096, H=1024, F=4096, N=8, k=2, gate_bias="zero", expert_bias="zero"),
+    # Mixtral-sized layer (hidden 4096, 8 experts, top-2, FFN 14336), bias-free
+    Workload("mixtral_prefill", T=16384, H=4096, F=14336, N=8, k=2),
+    Workload("mixtral_decode", T=64, H=4096, F=14336, N=8, k=2, phase="decode"),
+    # DeepSeek-V3-sized fine-grained layer: 256 routed (top-8) + 1 shared expert
+    Workload("deepseek_prefill", T=8192, H=7168, F=2048, N=256, k=8,
+             sel_bias="uniform0.1", F_shared=2048),
+    Workload("deepseek_decode", T=128, H=7168, F=2048, N=256, k=8,
+             sel_bias="uniform0.1", F_shared=2048, phase="decode"),
+    # Switch-style top-1 with capacity 1.25 and Zipf(1.1)-skewed gate offsets
+    Workload("switch_capacity", T=32768, H=2048, F=8192, N=64, k=1,
+             capacity_factor=1.25, gate_bias="zipf1.1"),
+]}
+
+# Extra small cases for tests (not benchmark lines).
+TEST_WORKLOADS: Dict[str, Workload] = {w.name: w for w in [
+    Workload("tiny_biased", T=64, H=32, F=128, N=4, k=2, gate_bias="normal",
+             expert_bias="normal"),
+    Workload("small_shared", T=300, H=256, F=384, N=16, k=4, sel_bias="uniform0.1",
+             F_shared=256, expert_bias="normal"),
+    Workload("small_capacity", T=1000, H=128, F=256, N=8, k=2, capacity_factor=1.0,
+             gate_bias="zipf1.1"),
+    Workload("small_top1", T=777, H=192, F=320, N=12, k=1, capacity_factor=1.25,
+             gate_bias="zipf1.1"),
+    Workload("wide_router", T=520, H=512, F=256, N=256, k=8, sel_bias="uniform0.1",
+             F_shared=256),
+]}
+
+
+def get_workload(name: str) -> Workload:
+    if name in WORKLOADS:
+        return WORKLOADS[name]
+    if name in TEST_WORKLOADS:
+        return TEST_WORKLOADS[name]
+    raise KeyError(f"unknown workload {name!r}")
+
+
+# ---------------------------------------------------------------------------
+# bf16 bit helpers (data conversion only)
+
+def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
+    """Round float32 values to bf16 (round-to-nearest-even); returns uint16 bits."""
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
+    r = u + np.uint32(0x7FFF)
+    r += (u >> np.uint32(16)) & np.uint32(1)
+    r >>= np.uint32(16)
+    return r.astype(np.uint16)
+
+
+def bf16_bits_to_f64(b: np.ndarray) -> np.ndarray:
+    """Exact widening of bf16 bit patterns to float64."""
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(
+        np.float32).astype(np.float64)
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+# ---------------------------------------------------------------------------
+# seeded draws
+
+def _rng(seed: int, tensor: str, block: int) -> np.random.Generator:
+    ss = np.random.SeedSequence(entropy=seed, spawn_key=(_TENSOR_ID[tensor], block))
+    return np.random.Generator(np.random.PCG64(ss))
+
+
+def _normal(seed, tensor, block, shape, std) -> np.ndarray:
+    a = _rng(seed, tensor, block).standard_normal(size=shape, dtype=np.float32)
+    if std != 1.0:
+        a *= np.float32(std)
+    return a
+
+
+def gen_x_rows(w: Workload, seed: int, row0: int, row1: int) -> np.ndarray:
+    """bf16 bits of activation rows [row0, row1) of x ~ N(0, 1)."""
+    out = np.empty((row1 - row0, w.H), dtype=np.uint16)
+    c0 = row0 // X_CHUNK_ROWS
+    c1 = (row1 + X_CHUNK_ROWS - 1) // X_CHUNK_ROWS
+    for c in range(c0, c1):
+        lo = c * X_CHUNK_ROWS
+        hi = min(lo + X_CHUNK_ROWS, w.T)
+        blk = f32_to_bf16_bits(_normal(seed, "x", c, (hi - lo, w.H), 1.0))
+        s0, s1 = max(lo, row0), min(hi, row1)
+        out[s0 - row0:s1 - row0] = blk[s0 - lo:s1 - lo]
+    return out
+
+
+def gen_x(w: Workload, seed: int = 0, threads: Optional[int] = None) -> np.ndarray:
+    if w.T == 0:
+        return np.zeros((0, w.H), dtype=np.uint16)
+    chunks = [(c * X_CHUNK_ROWS, min((c + 1) * X_CHUNK_ROWS, w.T))
+              for c in range((w.T + X_CHUNK_ROWS - 1) // X_CHUNK_ROWS)]
+    out = np.empty((w.T, w.H), dtype=np.uint16)
+
+    def job(rc):
+        out[rc[0]:rc[1]] = gen_x_rows(w, seed, rc[0], rc[1])
+    _pool_map(job, chunks, threads)
+    return out
+
+
+def gen_router(w: Workload, seed: int = 0):
+    """(Wg fp32 [N,H], bg fp32 [N] or None, sel_bias fp32 [N] or None)."""
+    Wg = _normal(seed, "Wg", 0, (w.N, w.H), 1.0 / math.sqrt(w.H))
+    bg = None
+    if w.gate_bias == "zero":
+        bg = np.zeros(w.N, dtype=np.float32)
+    elif w.gate_bias == "zipf1.1":
+        # log of a Zipf(s=1.1) pmf over experts 1..N; its normaliser is a
+        # constant shift that softmax and top-k ignore, so it is dropped
+        bg = (-1.1 * np.log(np.arange(1, w.N + 1, dtype=np.float64))).astype(np.float32)
+    elif w.gate_bias == "normal":
+        bg = _normal(seed, "bg", 0, (w.N,), 0.5)
+    elif w.gate_bias is not None:
+        raise ValueError(w.gate_bias)
+    sel = None
+    if w.sel_bias == "uniform0.1":
+        sel = _rng(seed, "sel_bias", 0).uniform(-0.1, 0.1, size=w.N).astype(np.float32)
+    elif w.sel_bias is not None:
+        raise ValueError(w.sel_bias)
+    return Wg, bg, sel
+
+
+def gen_expert(w: Workload, seed: int, e: int):
+    """bf16 bits of routed expert e: (W1 [F,H], b1 [F]|None, W2 [H,F], b2 [H]|None)."""
+    W1 = f32_to_bf16_bits(_normal(seed, "W1", e, (w.F, w.H), 1.0 / math.sqrt(w.H)))
+    W2 = f32_to_bf16_bits(_normal(seed, "W2", e, (w.H, w.F), 1.0 / math.sqrt(w.F)))
+    b1 = b2 = None
+    if w.expert_bias == "zero":
+        b1 = np.zeros(w.F, dtype=np.uint16)
+        b2 = np.zeros(w.H, dtype=np.uint16)
+    elif w.expert_bias == "normal":
+        b1 = f32_to_bf16_bits(_normal(seed, "b1", e, (w.F,), 0.1))
+        b2 = f32_to_bf16_bits(_normal(seed, "b2", e, (w.H,), 0.1))
+    elif w.expert_bias is not None:
+        raise ValueError(w.expert_bias)
+    return W1, b1, W2, b2
+
+
+def gen_shared(w: Workload, seed: int = 0):
+    """bf16 bits of the shared expert, or None: (W1s [Fs,H], b1s|None, W2s [H,Fs], b2s|None)."""
+    if w.F_shared <= 0:
+        return None
+    Fs = w.F_shared
+    W1s = f32_to_bf16_bits(_normal(seed, "W1s", 0, (Fs, w.H), 1.0 / math.sqrt(w.H)))
+    W2s = f32_to_bf16_bits(_normal(seed, "W2s", 0, (w.H, Fs), 1.0 / math.sqrt(Fs)))
+    b1s = b2s = None
+    if w.expert_bias == "normal":
+        b1s = f32_to_bf16_bits(_normal(seed, "b1s", 0, (Fs,), 0.1))
+        b2s = f32_to_bf16_bits(_normal(seed, "b2s", 0, (w.H,), 0.1))
+    elif w.expert_bias == "zero":
+        b1s = np.zeros(Fs, dtype=np.uint16)
+        b2s = np.zeros(w.H, dtype=np.uint16)
+    return W1s, b1s, W2s, b2s
+
+
+def gen_all(w: Workload, seed: int = 0, threads: Optional[int] = None) -> dict:
+    """Every input of the layer as host arrays (bf16 tensors as uint16 bits)."""
+    x = gen_x(w, seed, threads)
+    Wg, bg, sel = gen_router(w, seed)
+    W1 = np.empty((w.N, w.F, w.H), dtype=np.uint16)
+    W2 = np.empty((w.N, w.H, w.F), dtype=np.uint16)
+    has_b = w.expert_bias is not None
+    b1 = np.empty((w.N, w.F), dtype=np.uint16) if has_b else None
+    b2 = np.empty((w.N, w.H), dtype=np.uint16) if has_b else None
+
+    def job(e):
+        a, b, c, d = gen_expert(w, seed, e)
+        W1[e] = a
+        W2[e] = c
+        if has_b:
+            b1[e] = b
+            b2[e] = d
+    _pool_map(job, range(w.N), threads)
+    sh = gen_shared(w, seed)
+    d = dict(x=x, Wg=Wg, bg=bg, sel_bias=sel, W1=W1, b1=b1, W2=W2, b2=b2,
+             W1s=None, b1s=None, W2s=None, b2s=None)
+    if sh is not None:
+        d.update(W1s=sh[0], b1s=sh[1], W2s=sh[2], b2s=sh[3])
+    return d
+
+
+def expert_getter_f64(w: Workload, seed: int = 0) -> Callable[[int], tuple]:
+    """Callable e -> float64 (W1, b1, W2, b2) of routed expert e, drawn on demand."""
+    cache: Dict[int, tuple] = {}
+
+    def get(e: int):
+        if e not in cache:
+            W1, b1, W2, b2 = gen_expert(w, seed, e)
+            cache[e] = (bf16_bits_to_f64(W1), None if b1 is None else bf16_bits_to_f64(b1),
+                        bf16_bits_to_f64(W2), None if b2 is None else bf16_bits_to_f64(b2))
+        return cache[e]
+    return get
+
+
+def shared_f64(w: Workload, seed: int = 0):
+    sh = gen_shared(w, seed)
+    if sh is None:
+        return None
+    return tuple(None if a is None else bf16_bits_to_f64(a) for a in sh)
+
+
+def _pool_map(fn, items, threads):
+    items = list(items)
+    n = threads or min(len(items), os.cpu_count() or 1, 64)
+    if n <= 1 or len(items) <= 1:
+        for it in items:
+            fn(it)
+        return
+    with ThreadPoolExecutor(n) as ex:
+        list(ex.map(fn, items))
