@@ -1,0 +1,417 @@
+#!/usr/bin/env python3
+"""Benchmark of the sparse MoE FFN forward pass on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one moe_forward call (router, dispatch, expert GEMMs, combine) over
+one batch of seeded synthetic input already resident in HBM; L2 is flushed
+(a 256 MiB write) between timed steps, outside the timed events.  Prints one
+JSON line on rank 0.  Under torchrun (N > 1) every rank runs an independent
+replica on its own batch (weak scaling) and the slowest rank's time counts.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import moe_workloads as wl  # noqa: E402
+
+DEFAULT_WORKLOAD = "moelayer"
+METRIC = "MoE-layer fwd tokens/s; % of bf16 TC peak (prefill) or HBM BW (decode)"
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+# ---------------------------------------------------------------------------
+# helpers shared by both arms (host logic, testable on CPU)
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Maximum of a per-rank float over all ranks (identity when world == 1)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(tokens_per_rank: int, world: int, ms_per_step_max: float) -> float:
+    """Whole-job throughput: tokens every rank processed per step / slowest rank's step time."""
+    return tokens_per_rank * world / (ms_per_step_max * 1e-3)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("gemm_tc.cu", "common.cuh", "kernels.cuh"):
+        with open(os.path.join(ROOT, "sparse_mixture_experts_72_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; otherwise None."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        e = d.get(workload, {}).get(kernel)
+        if e and e.get("src_sha") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except (ValueError, KeyError, TypeError):
+        return None
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, interval_ms: int = 50):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", f"-lms", str(interval_ms)],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def algorithmic_work(w: wl.Workload, counts: np.ndarray, R: int):
+    """FLOPs and bytes each expert GEMM launch must do at minimum.
+
+    Per kept row: 2*H*F FLOPs in each GEMM.  Bytes: the weights of every
+    expert that received a row (F*H bf16 per GEMM), the activation rows read
+    (R*K bf16) and the rows written (R*n_out bf16)."""
+    hit = int((np.asarray(counts) > 0).sum())
+    g1 = dict(flops=2.0 * R * w.H * w.F, bytes=2.0 * (hit * w.F * w.H + R * w.H + R * w.F))
+    g2 = dict(flops=2.0 * R * w.F * w.H, bytes=2.0 * (hit * w.H * w.F + R * w.F + R * w.H))
+    out = {"gemm1": g1, "gemm2": g2}
+    if w.F_shared:
+        Fs = w.F_shared
+        out["gemm1_shared"] = dict(flops=2.0 * w.T * w.H * Fs,
+                                   bytes=2.0 * (Fs * w.H + w.T * w.H + w.T * Fs))
+        out["gemm2_shared"] = dict(flops=2.0 * w.T * Fs * w.H,
+                                   bytes=2.0 * (w.H * Fs + w.T * Fs + w.T * w.H))
+    return out
+
+
+def launch_names(w: wl.Workload, has_rows: bool):
+    names = ["status_memset", "router_logits", "router_select", "router_pmean",
+             "permute_rank", "permute_scan", "permute_scatter"]
+    if has_rows:
+        names += ["gather", "gemm1", "gemm2"]
+    if w.F_shared:
+        names += ["gemm1_shared", "gemm2_shared"]
+    names += ["combine"]
+    return names
+
+
+# ---------------------------------------------------------------------------
+# oracle arm (CPU baseline and --impl reference)
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        return max(n) if n else 1
+    except Exception:  # noqa: BLE001
+        return 1
+
+
+def oracle_step(w: wl.Workload, x_bits, router, getter, shared, rows: slice):
+    """One oracle forward over the token rows `rows` (a sub-batch of the
+    workload: with no capacity limit the rows are routed exactly as in the
+    full batch)."""
+    from oracle import moe_oracle as O
+    Wg, bg, sel = router
+    xs = wl.bf16_bits_to_f64(x_bits[rows])
+    return O.forward(xs, Wg, bg, sel, w.k, w.capacity_factor, w.aux_alpha, getter, shared)
+
+
+def oracle_timing(w: wl.Workload, steps: int, warmup: int, budget_s: float, seed: int = 0):
+    """Times the oracle on bounded token samples; returns (tokens/s, sample tokens, desc)."""
+    x_bits = wl.gen_x(w, seed)
+    router = wl.gen_router(w, seed)
+    getter = wl.expert_getter_f64(w, seed)
+    for e in range(w.N):
+        getter(e)  # draw and widen the weights before timing
+    shared = wl.shared_f64(w, seed)
+    # size the sample so that warmup + steps fit in the budget
+    probe = min(w.T, 64)
+    t0 = time.perf_counter()
+    oracle_step(w, x_bits, router, getter, shared, slice(0, probe))
+    per_tok = (time.perf_counter() - t0) / probe
+    total_steps = max(1, steps + warmup)
+    S = int(max(8, min(w.T, budget_s / total_steps / max(per_tok, 1e-9))))
+    if w.capacity_factor > 0:
+        S = w.T  # capacity couples tokens: only the whole batch is exact
+    for i in range(warmup):
+        oracle_step(w, x_bits, router, getter, shared, slice(0, S))
+    times = []
+    for i in range(steps):
+        s0 = (i * S) % max(1, w.T - S + 1)
+        t0 = time.perf_counter()
+        oracle_step(w, x_bits, router, getter, shared, slice(s0, s0 + S))
+        times.append(time.perf_counter() - t0)
+    tps = S / statistics.median(times)
+    desc = (f"oracle forward over {S}-token slices of the {w.name} batch "
+            f"(T={w.T}), {steps} timed slices, float64 numpy on host")
+    return tps, S, desc
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = wl.get_workload(args.workload)
+    budget = 150.0
+    tps, S, desc = oracle_timing(w, args.steps, args.warmup, budget)
+    cores = blas_threads()
+    line = {"metric": METRIC, "value": tps, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": S / tps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": w.name, "T": w.T, "H": w.H, "F": w.F, "N": w.N, "k": w.k,
+                       "capacity_factor": w.capacity_factor, "F_shared": w.F_shared},
+            "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# CUDA arm
+
+def run_ours(args):
+    import torch
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    device = torch.device("cuda", local_rank if world > 1 else 0)
+    torch.cuda.set_device(device)
+
+    import sparse_mixture_experts_72_b300 as m
+
+    w = wl.get_workload(args.workload)
+    cfg = m.MoEConfig(T=w.T, H=w.H, F=w.F, N=w.N, k=w.k, capacity_factor=w.capacity_factor,
+                      F_shared=w.F_shared, aux_alpha=w.aux_alpha)
+    # replicas share the weights; each rank draws its own batch
+    d = wl.to_device(w, seed=0, device=device, x_seed=None if rank == 0 else 1000 + rank)
+    weights = m.MoEWeights(Wg=d["Wg"], W1=d["W1"], W2=d["W2"], bg=d["bg"], sel_bias=d["sel_bias"],
+                           b1=d["b1"], b2=d["b2"], W1s=d["W1s"], b1s=d["b1s"], W2s=d["W2s"],
+                           b2s=d["b2s"])
+    x_bits_host, x = d["x_bits"], d["x"]
+    ws = m.make_workspace(cfg, device)
+    outs = m.alloc_outputs(cfg, device)
+    out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=device)
+    wc = weights.c(cfg)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    n_launch = m.moe_forward_num_launches(cfg)
+
+    def step(trace=None):
+        m.moe_forward(cfg, weights, x, out=out, outputs=outs, ws=ws, trace_events=trace,
+                      weights_c=wc)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if m.moe_workspace_status(ws) != 0:
+        raise RuntimeError("device status after warm-up is not OK")
+    counts = outs["counts"].cpu().numpy()
+    R = int(outs["offsets"][-1].item())
+    names = launch_names(w, m.moe_max_rows(cfg) > 0)
+    assert len(names) == n_launch, (names, n_launch)
+
+    K = args.steps
+    ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    n_traced = min(K, 32)
+    traced_steps = set(np.linspace(0, K - 1, n_traced).astype(int).tolist())
+    traces = {i: [torch.cuda.Event(enable_timing=True) for _ in range(n_launch + 1)]
+              for i in traced_steps}
+
+    clocks = ClockSampler(device.index or 0)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for i in range(K):
+        flush.zero_()
+        ev_s[i].record()
+        step(traces.get(i))
+        ev_e[i].record()
+    torch.cuda.synchronize()
+    wall_s = time.perf_counter() - t_wall
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    if m.moe_workspace_status(ws) != 0:
+        raise RuntimeError("device status after the timed steps is not OK")
+
+    step_ms = [ev_s[i].elapsed_time(ev_e[i]) for i in range(K)]
+    ms_local = float(np.mean(step_ms))
+    ms_max = reduce_max(ms_local, world, device)
+    value = aggregate(w.T, world, ms_max)
+
+    # per-launch times from the traced steps
+    per = {n: [] for n in names}
+    for i, evs in traces.items():
+        for j, n in enumerate(names):
+            per[n].append(evs[j].elapsed_time(evs[j + 1]))
+    per_ms = {n: float(np.mean(v)) for n, v in per.items()}
+
+    peaks, peak_src = load_peaks()
+    work = algorithmic_work(w, counts, R)
+    gemms = [n for n in names if n.startswith("gemm")]
+    dom = max(gemms, key=lambda n: per_ms[n]) if gemms else max(per_ms, key=per_ms.get)
+    t_dom = per_ms[dom] * 1e-3
+    wk = work.get(dom)
+    roof = None
+    if wk is not None and t_dom > 0:
+        t_tc = wk["flops"] / (peaks["bf16_tflops"] * 1e12)
+        t_bw = wk["bytes"] / (peaks["hbm_gbs"] * 1e9)
+        if t_tc >= t_bw:
+            ach = wk["flops"] / t_dom / 1e12
+            roof = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"],
+                    "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"]}
+        else:
+            ach = wk["bytes"] / t_dom / 1e9
+            roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": ach / peaks["hbm_gbs"]}
+        roof["traffic"] = committed_traffic(w.name, dom)
+        roof["kernel"] = f"grouped_gemm_kernel ({dom})"
+        roof["launch_ms"] = per_ms[dom]
+        roof["peak_source"] = f"{peak_src} (burst)"
+
+    # end to end through the C ABI with host buffers: H2D of x, forward, D2H of out
+    x_pin = torch.from_numpy(np.ascontiguousarray(x_bits_host).view(np.int16)).pin_memory()
+    out_pin = torch.empty((w.T, w.H), dtype=torch.int16).pin_memory()
+    x_dev16 = x.view(torch.int16)
+    E = max(10, min(K, 200))
+    e_s = [torch.cuda.Event(enable_timing=True) for _ in range(E)]
+    e_e = [torch.cuda.Event(enable_timing=True) for _ in range(E)]
+    for i in range(E):
+        flush.zero_()
+        e_s[i].record()
+        x_dev16.copy_(x_pin, non_blocking=True)
+        step()
+        out_pin.copy_(out.view(torch.int16), non_blocking=True)
+        e_e[i].record()
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(float(np.mean([e_s[i].elapsed_time(e_e[i]) for i in range(E)])), world,
+                        device)
+    e2e = {"value": aggregate(w.T, world, e2e_ms), "unit": "tokens/s",
+           "h2d_bytes_per_step": int(x_pin.numel() * 2), "d2h_bytes_per_step": int(out_pin.numel() * 2)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tps, S, desc = oracle_timing(w, steps=3, warmup=1, budget_s=20.0)
+        cpu = {"value": tps, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+               "sample": desc}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+                "steps": K, "warmup": max(args.warmup, 3), "ms_per_step": ms_max,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic",
+                "config": {"workload": w.name, "T": w.T, "H": w.H, "F": w.F, "N": w.N, "k": w.k,
+                           "capacity_factor": w.capacity_factor, "F_shared": w.F_shared,
+                           "kept_rows": R, "experts_hit": int((counts > 0).sum()),
+                           "l2": "flushed between steps (256 MiB write, untimed)",
+                           "parallelism": f"replicas x{world}"},
+                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": int(K * (n_launch - 1)),
+                "clocks": clk,
+                "launch_ms": per_ms,
+                "wall_s_timed_region": wall_s}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=sorted(wl.WORKLOADS) + sorted(wl.TEST_WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,206 @@
+/*
+ * moe.h - C ABI of the B300 (sm_103a) sparse Mixture-of-Experts FFN forward pass.
+ *
+ * One MoE FFN layer ("AI-Research-SKILLs MoE 训练实战：稀疏专家模型的架构、路由、
+ * 负载均衡与推理优化全指南", §3.1 MoELayer; "混合专家模型 MoE 架构深度解析：从路由
+ * 机制到生产级推理部署", §1.2-§3):
+ *
+ *   l     = x . W_g^T + b_g                       gate Linear, fp32
+ *   P     = softmax(l)                            over the N experts
+ *   idx   = top-k of (l - b_sel)                  b_sel: selection-only bias
+ *   w     = P[idx] / sum_j P[idx_j]               renormalised over the k
+ *   C     = floor(T / N * capacity_factor)        capacity, overflow dropped
+ *   y     = W2_e . GELU(W1_e . x_t + b1_e) + b2_e  per kept assignment
+ *   out_t = sum_j w_tj y_tj  (+ shared expert)    dropped slots add zero
+ *   L_aux = alpha * N * sum_i f_i p_i
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *    never allocates device memory.  Scratch comes from the caller's
+ *    workspace `ws` of at least moe_workspace_size(cfg) bytes.
+ *  - bf16 tensors are passed as uint16_t bit patterns.  Layouts are row-major;
+ *    weights use the nn.Linear [out, in] layout (K contiguous):
+ *      W_g [N, H] fp32, W1 [N, F, H], W2 [N, H, F], W1s [Fs, H], W2s [H, Fs].
+ *  - Every pointer must be 16-byte aligned; H, F and F_shared must be
+ *    multiples of 8.  Violations return MOE_ERR_UNSUPPORTED before any launch.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream).  Arguments are validated on the host before anything
+ *    is launched; a non-OK return means nothing was enqueued, except
+ *    MOE_ERR_CUDA, which reports a failed launch.
+ *  - Device-side failures never trap.  A kernel whose bounded wait runs out
+ *    records MOE_ERR_TIMEOUT in a status word inside `ws` and returns; every
+ *    entry point that takes `ws` clears that word first, and
+ *    moe_workspace_status() reads it.
+ *  - Calls are stateless and re-entrant; concurrent calls need distinct `ws`.
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,  /* null required pointer, negative size, k < 1 or k > N, ... */
+  MOE_ERR_UNSUPPORTED = 2,  /* misaligned pointer, H/F not a multiple of 8, N > MOE_MAX_EXPERTS */
+  MOE_ERR_WORKSPACE = 3,    /* ws is NULL, misaligned or smaller than moe_workspace_size() */
+  MOE_ERR_CUDA = 4,         /* a CUDA runtime call or kernel launch failed */
+  MOE_ERR_TIMEOUT = 5,      /* a device-side bounded wait ran out (see moe_workspace_status) */
+  MOE_ERR_NO_DEVICE = 6     /* no usable sm_103 device or driver entry point */
+} moe_status_t;
+
+#define MOE_MAX_EXPERTS 1024
+#define MOE_MAX_TOP_K 32
+/* moe_forward records at most this many events when given a trace array. */
+#define MOE_TRACE_MAX_EVENTS 32
+
+/* Layer shape and routing parameters. */
+typedef struct {
+  int32_t T;                /* tokens (rows of x); 0 is allowed */
+  int32_t H;                /* hidden size */
+  int32_t F;                /* routed expert FFN inner size */
+  int32_t N;                /* routed experts, 1..MOE_MAX_EXPERTS */
+  int32_t k;                /* experts per token, 1..min(N, MOE_MAX_TOP_K) */
+  float capacity_factor;    /* > 0: C = floor(T / N * capacity_factor); <= 0: no limit */
+  int32_t F_shared;         /* shared expert inner size; 0 = no shared expert */
+  float aux_alpha;          /* alpha of L_aux (the pages use 0.01) */
+} moe_config_t;
+
+/* Layer parameters (device pointers). */
+typedef struct {
+  const float* Wg;          /* [N, H] fp32 gate weight, required */
+  const float* bg;          /* [N] fp32 gate bias, or NULL (= 0) */
+  const float* sel_bias;    /* [N] fp32 selection-only bias b_i, or NULL (= 0) */
+  const uint16_t* W1;       /* [N, F, H] bf16, required */
+  const uint16_t* b1;       /* [N, F] bf16 or NULL */
+  const uint16_t* W2;       /* [N, H, F] bf16, required */
+  const uint16_t* b2;       /* [N, H] bf16 or NULL */
+  const uint16_t* W1s;      /* [Fs, H] bf16, required iff F_shared > 0 */
+  const uint16_t* b1s;      /* [Fs] bf16 or NULL */
+  const uint16_t* W2s;      /* [H, Fs] bf16, required iff F_shared > 0 */
+  const uint16_t* b2s;      /* [H] bf16 or NULL */
+} moe_weights_t;
+
+/* Optional device outputs of moe_forward; each may be NULL (kept in ws). */
+typedef struct {
+  int32_t* topk_idx;        /* [T, k] */
+  float* topk_w;            /* [T, k] */
+  float* probs;             /* [T, N] full softmax; written only when non-NULL */
+  float* p_mean;            /* [N]   p_i = mean_t P[t, i] */
+  int32_t* counts;          /* [N]   assignments per expert before capacity drops */
+  int32_t* offsets;         /* [N+1] expert-contiguous row offsets after drops */
+  int32_t* perm;            /* [moe_max_rows(cfg)] row -> assignment t*k+j */
+  int32_t* inv;             /* [T*k] assignment -> row, -1 if dropped */
+  float* f;                 /* [N]   f_i = counts_i / (T*k) */
+  float* l_aux;             /* [1]   alpha * N * sum f_i p_i */
+} moe_outputs_t;
+
+/* Bytes of workspace the entry points need for this configuration. */
+size_t moe_workspace_size(const moe_config_t* cfg);
+
+/* Upper bound on kept rows R: T*k, or min(T*k, N*C) with a capacity limit. */
+int64_t moe_max_rows(const moe_config_t* cfg);
+
+/* Capacity C of "混合专家模型 MoE 架构深度解析" §2.3, computed in double as
+ * floor((double)T / N * capacity_factor); -1 when there is no limit. */
+int64_t moe_capacity(const moe_config_t* cfg);
+
+/* Number of kernel launches (and memsets) one moe_forward call enqueues. */
+int32_t moe_forward_num_launches(const moe_config_t* cfg);
+
+/*
+ * moe_route - gate, softmax, top-k selection and renormalisation.
+ * ("混合专家模型 MoE 架构深度解析" §1.2 gate formula, §1.3 top-K steps 1-3,
+ *  §2.4 selection bias; "AI-Research-SKILLs MoE 训练实战" §3.1 MoELayer gate.)
+ *   x        [T, H] bf16          Wg [N, H] fp32, bg [N] fp32 or NULL
+ *   sel_bias [N] fp32 or NULL     subtracted from the logits for selection only
+ *   topk_idx [T, k] int32 out     experts in descending (l - b_sel); ties -> lower index
+ *   topk_w   [T, k] fp32 out      unbiased softmax at idx, renormalised to sum 1
+ *   probs    [T, N] fp32 out or NULL   full softmax
+ *   p_mean   [N] fp32 out         mean over tokens of the softmax (p_i of L_aux)
+ * Logits accumulate in fp32.
+ */
+moe_status_t moe_route(const moe_config_t* cfg, const uint16_t* x, const float* Wg,
+                       const float* bg, const float* sel_bias, int32_t* topk_idx,
+                       float* topk_w, float* probs, float* p_mean, void* ws,
+                       size_t ws_bytes, void* stream);
+
+/*
+ * moe_permute - histogram, capacity, stable expert-contiguous dispatch and L_aux.
+ * ("混合专家模型 MoE 架构深度解析" §2.3 capacity and overflow, §2.2 L_aux;
+ *  "AI-Research-SKILLs MoE 训练实战" §4.3 expert fraction, §4.4 drop_tokens.)
+ * Assignment a = t*k + j claims slots in increasing a; rank within its
+ * expert >= C means dropped.
+ *   topk_idx [T, k] int32 in; values must lie in [0, N) (not checked on device:
+ *            out-of-range indices are ignored by the histogram and dropped)
+ *   p_mean   [N] fp32 in (from moe_route); may be NULL when l_aux is NULL
+ *   counts   [N] int32 out        offsets [N+1] int32 out
+ *   perm     [moe_max_rows] int32 out (first offsets[N] entries written)
+ *   inv      [T*k] int32 out      -1 for dropped assignments
+ *   f        [N] fp32 out or NULL l_aux [1] fp32 out or NULL
+ */
+moe_status_t moe_permute(const moe_config_t* cfg, const int32_t* topk_idx, const float* p_mean,
+                         int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
+                         float* f, float* l_aux, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * moe_expert_ffn - gather, expert Linear -> GELU -> Linear, gate weighting.
+ * ("AI-Research-SKILLs MoE 训练实战" §3.1 expert = Linear(H,F), GELU, Linear(F,H);
+ *  §7.1 and "混合专家模型 MoE 架构深度解析" §3 shared expert.)
+ *   y[r]        = bf16( w_a * (W2_e . bf16(GELU(W1_e . x_t + b1_e)) + b2_e) )
+ *                 for rows r < offsets[N], a = perm[r], t = a / k, e the expert of r
+ *   y_shared[t] = bf16( W2s . bf16(GELU(W1s . x_t + b1s)) + b2s )   when F_shared > 0
+ *   x [T, H] bf16; perm/offsets from moe_permute; topk_w [T, k] fp32
+ *   y [moe_max_rows, H] bf16 out; y_shared [T, H] bf16 out (NULL iff F_shared == 0)
+ * bf16 x bf16 products accumulate in fp32 on the tensor cores.
+ */
+moe_status_t moe_expert_ffn(const moe_config_t* cfg, const uint16_t* x, const int32_t* perm,
+                            const int32_t* offsets, const float* topk_w,
+                            const moe_weights_t* weights, uint16_t* y, uint16_t* y_shared,
+                            void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * moe_combine - weighted sum back per token ("AI-Research-SKILLs MoE 训练实战"
+ * §3.1 output[mask] += score * expert_out; §6.1 index_add_ combine).
+ *   out[t] = bf16( sum_{j<k, inv[t*k+j] >= 0} y[inv[t*k+j]] (+ y_shared[t]) )
+ * summed in fp32 in the order j = 0..k-1, then the shared term.  A token
+ * whose every slot was dropped gets 0 (+ its shared term).
+ *   y [moe_max_rows, H] bf16, inv [T*k] int32, y_shared [T, H] bf16 or NULL
+ *   out [T, H] bf16
+ */
+moe_status_t moe_combine(const moe_config_t* cfg, const uint16_t* y, const int32_t* inv,
+                         const uint16_t* y_shared, uint16_t* out, void* stream);
+
+/*
+ * moe_forward - the whole layer: route, permute, experts, combine, stream-
+ * ordered with no host synchronisation.
+ *   x [T, H] bf16 in; out [T, H] bf16 out; weights as moe_weights_t;
+ *   outputs: optional device copies of the intermediate results, or NULL.
+ *   trace_events: NULL, or an array of MOE_TRACE_MAX_EVENTS cudaEvent_t
+ *   (NULL entries are skipped); when given, event i is recorded on `stream`
+ *   just before launch i and event moe_forward_num_launches(cfg) just after
+ *   the last one.
+ */
+moe_status_t moe_forward(const moe_config_t* cfg, const moe_weights_t* weights,
+                         const uint16_t* x, uint16_t* out, const moe_outputs_t* outputs,
+                         void* ws, size_t ws_bytes, void* stream, void* const* trace_events);
+
+/* Synchronises `stream` and returns the device status word of `ws`
+ * (MOE_OK or MOE_ERR_TIMEOUT), or MOE_ERR_CUDA if the synchronisation fails. */
+moe_status_t moe_workspace_status(const void* ws, void* stream);
+
+/* Static description of a status code. */
+const char* moe_status_string(moe_status_t status);
+
+/* Library version string. */
+const char* moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_B300_H */

@@ -90,6 +90,13 @@ TEST_WORKLOADS: Dict[str, Workload] = {w.name: w for w in [
              gate_bias="zipf1.1"),
     Workload("wide_router", T=520, H=512, F=256, N=256, k=8, sel_bias="uniform0.1",
              F_shared=256),
+    # ragged everything: K tails (H, F not multiples of 64), partial output
+    # blocks, ragged row blocks, capacity drops, a shared expert
+    Workload("odd_shapes", T=1000, H=136, F=264, N=5, k=2, capacity_factor=1.1,
+             gate_bias="normal", expert_bias="normal", F_shared=72),
+    Workload("dense_n1", T=300, H=64, F=96, N=1, k=1),
+    Workload("all_experts", T=200, H=64, F=64, N=6, k=6, gate_bias="normal"),
+    Workload("all_dropped", T=40, H=64, F=64, N=16, k=2, capacity_factor=0.1, F_shared=64),
 ]}
 
 
@@ -275,3 +282,44 @@ def _pool_map(fn, items, threads):
         return
     with ThreadPoolExecutor(n) as ex:
         list(ex.map(fn, items))
+
+
+# ---------------------------------------------------------------------------
+# device upload (data movement only; torch is imported lazily)
+
+def bits_to_torch_bf16(a: np.ndarray, device="cpu"):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def to_device(w: Workload, seed: int = 0, device="cuda", x_seed: Optional[int] = None) -> dict:
+    """Draws every input on the host (per-expert blocks in threads) and copies
+    it to `device`.  Returns a dict of torch tensors with the layer's names
+    plus ``x_bits`` (the host bf16 bits of x)."""
+    import torch
+    x_bits = gen_x(w, seed if x_seed is None else x_seed)
+    Wg, bg, sel = gen_router(w, seed)
+    W1 = torch.empty((w.N, w.F, w.H), dtype=torch.bfloat16, device=device)
+    W2 = torch.empty((w.N, w.H, w.F), dtype=torch.bfloat16, device=device)
+    has_b = w.expert_bias is not None
+    b1 = torch.empty((w.N, w.F), dtype=torch.bfloat16, device=device) if has_b else None
+    b2 = torch.empty((w.N, w.H), dtype=torch.bfloat16, device=device) if has_b else None
+    batch = 32
+    with ThreadPoolExecutor(min(32, max(1, w.N))) as ex:
+        for e0 in range(0, w.N, batch):
+            blocks = ex.map(lambda e: gen_expert(w, seed, e), range(e0, min(w.N, e0 + batch)))
+            for j, (a, b, c, d) in enumerate(blocks):
+                e = e0 + j
+                W1[e].copy_(bits_to_torch_bf16(a))
+                W2[e].copy_(bits_to_torch_bf16(c))
+                if has_b:
+                    b1[e].copy_(bits_to_torch_bf16(b))
+                    b2[e].copy_(bits_to_torch_bf16(d))
+    f32 = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(device)
+    bf = lambda a: None if a is None else bits_to_torch_bf16(a, device)
+    d = dict(x_bits=x_bits, x=bits_to_torch_bf16(x_bits, device), Wg=f32(Wg), bg=f32(bg),
+             sel_bias=f32(sel), W1=W1, b1=b1, W2=W2, b2=b2, W1s=None, b1s=None, W2s=None, b2s=None)
+    sh = gen_shared(w, seed)
+    if sh is not None:
+        d.update(W1s=bf(sh[0]), b1s=bf(sh[1]), W2s=bf(sh[2]), b2s=bf(sh[3]))
+    return d

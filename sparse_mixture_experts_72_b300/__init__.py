@@ -1,0 +1,259 @@
+"""Sparse Mixture-of-Experts FFN forward pass on B300 (sm_103a).
+
+Thin Python binding over the C ABI in include/moe.h: the functions below
+have the C entry points' names, check tensor dtypes/devices/shapes, pass
+raw device pointers and the current CUDA stream, and raise ``MoeError`` on a
+non-OK status.  Every step of the layer runs in the library's CUDA kernels;
+PyTorch only provides device memory and streams.  Importing the package
+fails if the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes as C
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+import torch
+
+from . import _lib
+from ._lib import MOE_TRACE_MAX_EVENTS, MoeError, check
+
+_L = _lib.load()
+
+__all__ = ["MoEConfig", "MoEWeights", "MoeError", "moe_workspace_size", "moe_max_rows",
+           "moe_capacity", "moe_forward_num_launches", "moe_route", "moe_permute",
+           "moe_expert_ffn", "moe_combine", "moe_forward", "moe_workspace_status",
+           "make_workspace", "library_path", "MOE_TRACE_MAX_EVENTS"]
+
+
+def library_path() -> str:
+    return _lib.LIB_PATH
+
+
+@dataclass(frozen=True)
+class MoEConfig:
+    T: int
+    H: int
+    F: int
+    N: int
+    k: int
+    capacity_factor: float = 0.0
+    F_shared: int = 0
+    aux_alpha: float = 0.01
+
+    def c(self) -> _lib.MoeConfig:
+        return _lib.MoeConfig(self.T, self.H, self.F, self.N, self.k,
+                              float(self.capacity_factor), self.F_shared, float(self.aux_alpha))
+
+
+@dataclass
+class MoEWeights:
+    Wg: torch.Tensor                     # [N, H] fp32
+    W1: torch.Tensor                     # [N, F, H] bf16
+    W2: torch.Tensor                     # [N, H, F] bf16
+    bg: Optional[torch.Tensor] = None    # [N] fp32
+    sel_bias: Optional[torch.Tensor] = None  # [N] fp32
+    b1: Optional[torch.Tensor] = None    # [N, F] bf16
+    b2: Optional[torch.Tensor] = None    # [N, H] bf16
+    W1s: Optional[torch.Tensor] = None   # [Fs, H] bf16
+    b1s: Optional[torch.Tensor] = None   # [Fs] bf16
+    W2s: Optional[torch.Tensor] = None   # [H, Fs] bf16
+    b2s: Optional[torch.Tensor] = None   # [H] bf16
+
+    def c(self, cfg: MoEConfig) -> _lib.MoeWeights:
+        N, H, F, Fs = cfg.N, cfg.H, cfg.F, cfg.F_shared
+        return _lib.MoeWeights(
+            _p(self.Wg, torch.float32, (N, H), "Wg"),
+            _p(self.bg, torch.float32, (N,), "bg", True),
+            _p(self.sel_bias, torch.float32, (N,), "sel_bias", True),
+            _p(self.W1, torch.bfloat16, (N, F, H), "W1"),
+            _p(self.b1, torch.bfloat16, (N, F), "b1", True),
+            _p(self.W2, torch.bfloat16, (N, H, F), "W2"),
+            _p(self.b2, torch.bfloat16, (N, H), "b2", True),
+            _p(self.W1s, torch.bfloat16, (Fs, H), "W1s", Fs == 0),
+            _p(self.b1s, torch.bfloat16, (Fs,), "b1s", True),
+            _p(self.W2s, torch.bfloat16, (H, Fs), "W2s", Fs == 0),
+            _p(self.b2s, torch.bfloat16, (H,), "b2s", True))
+
+
+def _p(t: Optional[torch.Tensor], dtype, shape, name, optional=False):
+    if t is None:
+        if optional:
+            return None
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return C.c_void_p(t.data_ptr()) if t.numel() > 0 else None
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return C.c_void_p(s.cuda_stream)
+
+
+def moe_workspace_size(cfg: MoEConfig) -> int:
+    return int(_L.moe_workspace_size(C.byref(cfg.c())))
+
+
+def moe_max_rows(cfg: MoEConfig) -> int:
+    return int(_L.moe_max_rows(C.byref(cfg.c())))
+
+
+def moe_capacity(cfg: MoEConfig) -> Optional[int]:
+    v = int(_L.moe_capacity(C.byref(cfg.c())))
+    return None if v < 0 else v
+
+
+def moe_forward_num_launches(cfg: MoEConfig) -> int:
+    return int(_L.moe_forward_num_launches(C.byref(cfg.c())))
+
+
+def make_workspace(cfg: MoEConfig, device=None) -> torch.Tensor:
+    n = moe_workspace_size(cfg)
+    if n == 0:
+        raise ValueError(f"invalid configuration {cfg}")
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def _ws(cfg, ws, device):
+    if ws is None:
+        ws = make_workspace(cfg, device)
+    return ws, C.c_void_p(ws.data_ptr()), C.c_size_t(ws.numel())
+
+
+def moe_route(cfg: MoEConfig, x, Wg, bg=None, sel_bias=None, *, want_probs=False, ws=None,
+              stream=None):
+    """Returns (topk_idx int32 [T,k], topk_w fp32 [T,k], probs fp32 [T,N] or None, p_mean [N])."""
+    dev = x.device
+    T, N, k = cfg.T, cfg.N, cfg.k
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    probs = torch.empty((T, N), dtype=torch.float32, device=dev) if want_probs else None
+    p_mean = torch.empty(N, dtype=torch.float32, device=dev)
+    ws, wsp, wsn = _ws(cfg, ws, dev)
+    st = _L.moe_route(C.byref(cfg.c()), _p(x, torch.bfloat16, (T, cfg.H), "x", T == 0),
+                      _p(Wg, torch.float32, (N, cfg.H), "Wg"),
+                      _p(bg, torch.float32, (N,), "bg", True),
+                      _p(sel_bias, torch.float32, (N,), "sel_bias", True),
+                      _p(idx, torch.int32, None, "idx", True), _p(w, torch.float32, None, "w", True),
+                      _p(probs, torch.float32, None, "probs", True),
+                      _p(p_mean, torch.float32, None, "p_mean"), wsp, wsn, _stream(stream))
+    check(st, "moe_route")
+    return idx, w, probs, p_mean
+
+
+def moe_permute(cfg: MoEConfig, topk_idx, p_mean=None, *, ws=None, stream=None) -> dict:
+    """Returns dict(counts, offsets, perm, inv, f, l_aux) as device tensors."""
+    dev = topk_idx.device
+    T, N, k = cfg.T, cfg.N, cfg.k
+    R = moe_max_rows(cfg)
+    out = dict(counts=torch.empty(N, dtype=torch.int32, device=dev),
+               offsets=torch.empty(N + 1, dtype=torch.int32, device=dev),
+               perm=torch.empty(max(R, 0), dtype=torch.int32, device=dev),
+               inv=torch.empty(T * k, dtype=torch.int32, device=dev),
+               f=torch.empty(N, dtype=torch.float32, device=dev),
+               l_aux=torch.empty(1, dtype=torch.float32, device=dev) if p_mean is not None else None)
+    ws, wsp, wsn = _ws(cfg, ws, dev)
+    st = _L.moe_permute(C.byref(cfg.c()), _p(topk_idx, torch.int32, (T, k), "topk_idx", T == 0),
+                        _p(p_mean, torch.float32, (N,), "p_mean", True),
+                        _p(out["counts"], torch.int32, None, "counts"),
+                        _p(out["offsets"], torch.int32, None, "offsets"),
+                        _p(out["perm"], torch.int32, None, "perm", True),
+                        _p(out["inv"], torch.int32, None, "inv", True),
+                        _p(out["f"], torch.float32, None, "f"),
+                        _p(out["l_aux"], torch.float32, None, "l_aux", True),
+                        wsp, wsn, _stream(stream))
+    check(st, "moe_permute")
+    return out
+
+
+def moe_expert_ffn(cfg: MoEConfig, x, perm, offsets, topk_w, weights: MoEWeights, *, ws=None,
+                   stream=None):
+    """Returns (y bf16 [max_rows, H] (first offsets[N] rows valid), y_shared bf16 [T, H] or None)."""
+    dev = x.device
+    R = moe_max_rows(cfg)
+    y = torch.empty((max(R, 0), cfg.H), dtype=torch.bfloat16, device=dev)
+    ys = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=dev) if cfg.F_shared > 0 else None
+    ws, wsp, wsn = _ws(cfg, ws, dev)
+    wc = weights.c(cfg)
+    st = _L.moe_expert_ffn(C.byref(cfg.c()), _p(x, torch.bfloat16, (cfg.T, cfg.H), "x", True),
+                           _p(perm, torch.int32, None, "perm", True),
+                           _p(offsets, torch.int32, (cfg.N + 1,), "offsets"),
+                           _p(topk_w, torch.float32, (cfg.T, cfg.k), "topk_w", True),
+                           C.byref(wc), _p(y, torch.bfloat16, None, "y", True),
+                           _p(ys, torch.bfloat16, None, "y_shared", True), wsp, wsn,
+                           _stream(stream))
+    check(st, "moe_expert_ffn")
+    return y, ys
+
+
+def moe_combine(cfg: MoEConfig, y, inv, y_shared=None, *, stream=None):
+    dev = inv.device
+    out = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=dev)
+    st = _L.moe_combine(C.byref(cfg.c()), _p(y, torch.bfloat16, None, "y", True),
+                        _p(inv, torch.int32, (cfg.T * cfg.k,), "inv", True),
+                        _p(y_shared, torch.bfloat16, (cfg.T, cfg.H), "y_shared", True),
+                        _p(out, torch.bfloat16, None, "out", True), _stream(stream))
+    check(st, "moe_combine")
+    return out
+
+
+_OUT_FIELDS = ("topk_idx", "topk_w", "probs", "p_mean", "counts", "offsets", "perm", "inv", "f",
+               "l_aux")
+
+
+def alloc_outputs(cfg: MoEConfig, device, want_probs=False) -> dict:
+    T, N, k = cfg.T, cfg.N, cfg.k
+    i32, f32 = torch.int32, torch.float32
+    return dict(topk_idx=torch.empty((T, k), dtype=i32, device=device),
+                topk_w=torch.empty((T, k), dtype=f32, device=device),
+                probs=torch.empty((T, N), dtype=f32, device=device) if want_probs else None,
+                p_mean=torch.empty(N, dtype=f32, device=device),
+                counts=torch.empty(N, dtype=i32, device=device),
+                offsets=torch.empty(N + 1, dtype=i32, device=device),
+                perm=torch.empty(max(moe_max_rows(cfg), 0), dtype=i32, device=device),
+                inv=torch.empty(T * k, dtype=i32, device=device),
+                f=torch.empty(N, dtype=f32, device=device),
+                l_aux=torch.empty(1, dtype=f32, device=device))
+
+
+def moe_forward(cfg: MoEConfig, weights: MoEWeights, x, *, out=None, outputs: Optional[dict] = None,
+                ws=None, stream=None, trace_events: Optional[Sequence] = None,
+                weights_c=None):
+    """The whole layer.  ``outputs`` (from ``alloc_outputs``) receives the
+    intermediate results; ``trace_events`` is a list of torch.cuda.Event
+    (enable_timing=True) recorded around each launch."""
+    dev = x.device
+    if out is None:
+        out = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=dev)
+    oc = None
+    if outputs is not None:
+        oc = _lib.MoeOutputs(*[(C.c_void_p(outputs[n].data_ptr())
+                                if outputs.get(n) is not None and outputs[n].numel() > 0 else None)
+                               for n in _OUT_FIELDS])
+    ws, wsp, wsn = _ws(cfg, ws, dev)
+    wc = weights_c if weights_c is not None else weights.c(cfg)
+    ev = None
+    if trace_events is not None:
+        if len(trace_events) > MOE_TRACE_MAX_EVENTS:
+            raise ValueError("too many trace events")
+        handles = [e.cuda_event for e in trace_events]
+        handles += [None] * (MOE_TRACE_MAX_EVENTS - len(handles))
+        ev = (C.c_void_p * MOE_TRACE_MAX_EVENTS)(*handles)
+    st = _L.moe_forward(C.byref(cfg.c()), C.byref(wc),
+                        _p(x, torch.bfloat16, (cfg.T, cfg.H), "x", True),
+                        _p(out, torch.bfloat16, (cfg.T, cfg.H), "out", True),
+                        C.byref(oc) if oc is not None else None, wsp, wsn, _stream(stream), ev)
+    check(st, "moe_forward")
+    return out
+
+
+def moe_workspace_status(ws: torch.Tensor, stream=None) -> int:
+    """Synchronises the stream and returns the status word (0 = MOE_OK)."""
+    return int(_L.moe_workspace_status(C.c_void_p(ws.data_ptr()), _stream(stream)))

@@ -1,0 +1,105 @@
+// Host-side launch descriptions of the MoE kernels (one translation unit
+// per pipeline stage; moe_api.cu strings them together).
+#pragma once
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda.h>
+#include <stdint.h>
+
+namespace moe {
+
+// Optional per-launch event trace: event i is recorded before launch i.
+struct LaunchTrace {
+  cudaEvent_t* events;
+  int n_events;
+  int next;
+};
+
+inline void trace_mark(LaunchTrace* tr, cudaStream_t st) {
+  if (tr && tr->events && tr->next < tr->n_events) {
+    cudaEvent_t e = tr->events[tr->next++];
+    if (e) cudaEventRecord(e, st);
+  }
+}
+
+// ---------------------------------------------------------------- router
+struct RouterLaunch {
+  const __nv_bfloat16* x;
+  const float* Wg;
+  const float* bg;
+  const float* sel_bias;
+  int32_t* topk_idx;
+  float* topk_w;
+  float* probs;     // nullable
+  float* p_mean;
+  float* logits;    // scratch [T, N]
+  float* p_part;    // scratch [router_num_select_blocks(T), N]
+  int T, H, N, k;
+};
+int router_num_select_blocks(int T);
+int router_num_launches(int T);
+cudaError_t launch_router(const RouterLaunch& a, cudaStream_t st, LaunchTrace* tr);
+
+// ---------------------------------------------------------------- permute
+struct PermuteLaunch {
+  const int32_t* topk_idx;
+  const float* p_mean;  // nullable when l_aux == nullptr
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* perm;
+  int32_t* inv;
+  float* f;             // nullable
+  float* l_aux;         // nullable
+  int32_t* local_rank;  // scratch [T*k]
+  int32_t* blk_hist;    // scratch [nblk, N]
+  int32_t* blk_base;    // scratch [nblk, N]
+  int T, N, k;
+  int64_t capacity;     // < 0: no limit
+  float alpha;
+};
+constexpr int kPermuteChunk = 256;  // assignments per block
+inline int permute_num_blocks(int64_t A) { return (int)((A + kPermuteChunk - 1) / kPermuteChunk); }
+int permute_num_launches(int T, int k);
+cudaError_t launch_permute(const PermuteLaunch& a, cudaStream_t st, LaunchTrace* tr);
+
+// ---------------------------------------------------------------- gather / combine
+cudaError_t launch_gather(const __nv_bfloat16* x, const int32_t* perm, const int32_t* offsets,
+                          int N, int k, int64_t max_rows, int H, __nv_bfloat16* xp,
+                          cudaStream_t st, LaunchTrace* tr);
+cudaError_t launch_combine(const __nv_bfloat16* y, const int32_t* inv,
+                           const __nv_bfloat16* y_shared, __nv_bfloat16* out, int T, int k,
+                           int H, cudaStream_t st, LaunchTrace* tr);
+
+// ---------------------------------------------------------------- grouped tcgen05 GEMM
+enum EpilogueMode : int32_t { EPI_GELU = 0, EPI_SCALE = 1 };
+
+struct GemmArgs {
+  const int32_t* offsets;        // [G+1] row segments of A per group, or nullptr
+  int32_t num_groups;            // G (routed experts), or 1 with offsets == nullptr
+  int32_t rows_single;           // rows of the single group when offsets == nullptr
+  int32_t n_out;                 // output columns per group (= B rows per group)
+  int32_t K;                     // reduction length
+  int32_t mode;                  // EpilogueMode
+  const __nv_bfloat16* bias;     // [G, n_out] or nullptr
+  const float* topk_w;           // EPI_SCALE: weight per assignment, or nullptr (weight 1)
+  const int32_t* perm;           // EPI_SCALE: row -> assignment (with topk_w)
+  __nv_bfloat16* out;            // [rows, ld_out]
+  int32_t ld_out;
+  int* status;                   // device status word
+};
+
+struct GemmPlan {
+  CUtensorMap tmA;  // A [rows, K] bf16, box 64 x 128, 128B swizzle
+  CUtensorMap tmB;  // B [G * n_out, K] bf16, box 64 x 256, 128B swizzle
+  GemmArgs args;
+  int grid;
+};
+
+// Encodes the tensor maps; returns cudaErrorInvalidValue if encoding fails.
+cudaError_t make_gemm_plan(GemmPlan* plan, const __nv_bfloat16* A, int64_t a_rows,
+                           const __nv_bfloat16* B, int64_t b_rows, const GemmArgs& args,
+                           int num_sms);
+cudaError_t launch_gemm(const GemmPlan& plan, cudaStream_t st, LaunchTrace* tr);
+bool tensor_map_encoder_available();
+
+}  // namespace moe

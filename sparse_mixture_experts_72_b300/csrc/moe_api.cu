@@ -1,0 +1,488 @@
+// C ABI of the MoE FFN forward pass: argument checks, workspace layout and
+// the stream-ordered launch sequence.  Declarations and the contract of each
+// entry point are in include/moe.h.
+#include <climits>
+#include <cmath>
+#include <cstring>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+#define MOE_API extern "C" __attribute__((visibility("default")))
+
+namespace moe {
+namespace {
+
+constexpr size_t kAlign = 256;
+
+inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t capacity_of(const moe_config_t& c) {
+  if (!(c.capacity_factor > 0.0f)) return -1;
+  // floor(T / N * cf), in double, in that order
+  const double v = std::floor((double)c.T / (double)c.N * (double)c.capacity_factor);
+  return v < 0 ? 0 : (int64_t)v;
+}
+
+int64_t max_rows_of(const moe_config_t& c) {
+  const int64_t A = (int64_t)c.T * c.k;
+  const int64_t C = capacity_of(c);
+  if (C < 0) return A;
+  const int64_t cap = C * c.N;
+  return cap < A ? cap : A;
+}
+
+struct WsLayout {
+  size_t status, logits, p_part, local_rank, blk_hist, blk_base;
+  size_t topk_idx, topk_w, p_mean, counts, offsets, perm, inv, f, l_aux;
+  size_t xp, hid, y, hid_s, y_s;
+  size_t total;
+};
+
+WsLayout layout_of(const moe_config_t& c) {
+  WsLayout L;
+  const int64_t T = c.T, N = c.N, A = T * c.k, R = max_rows_of(c);
+  const int64_t nsel = router_num_select_blocks(c.T);
+  const int64_t nblk = permute_num_blocks(A);
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t at = o; o += align_up(bytes > 0 ? bytes : 1); return at; };
+  L.status = take(16);
+  L.logits = take(sizeof(float) * T * N);
+  L.p_part = take(sizeof(float) * (nsel > 0 ? nsel : 1) * N);
+  L.local_rank = take(sizeof(int32_t) * A);
+  L.blk_hist = take(sizeof(int32_t) * (nblk > 0 ? nblk : 1) * N);
+  L.blk_base = take(sizeof(int32_t) * (nblk > 0 ? nblk : 1) * N);
+  L.topk_idx = take(sizeof(int32_t) * A);
+  L.topk_w = take(sizeof(float) * A);
+  L.p_mean = take(sizeof(float) * N);
+  L.counts = take(sizeof(int32_t) * N);
+  L.offsets = take(sizeof(int32_t) * (N + 1));
+  L.perm = take(sizeof(int32_t) * R);
+  L.inv = take(sizeof(int32_t) * A);
+  L.f = take(sizeof(float) * N);
+  L.l_aux = take(sizeof(float));
+  L.xp = take(2 * (size_t)R * c.H);
+  L.hid = take(2 * (size_t)R * c.F);
+  L.y = take(2 * (size_t)R * c.H);
+  L.hid_s = take(c.F_shared > 0 ? 2 * (size_t)T * c.F_shared : 0);
+  L.y_s = take(c.F_shared > 0 ? 2 * (size_t)T * c.H : 0);
+  L.total = o;
+  return L;
+}
+
+moe_status_t check_config(const moe_config_t* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->T < 0 || c->H <= 0 || c->F <= 0 || c->N <= 0 || c->k <= 0 || c->F_shared < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (c->k > c->N) return MOE_ERR_INVALID_ARG;
+  if (c->N > MOE_MAX_EXPERTS || c->k > MOE_MAX_TOP_K) return MOE_ERR_UNSUPPORTED;
+  if (c->H % 8 || c->F % 8 || c->F_shared % 8) return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)c->T * c->k > INT32_MAX / 2) return MOE_ERR_UNSUPPORTED;
+  if (std::isnan(c->capacity_factor) || std::isnan(c->aux_alpha)) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+// 16-byte alignment of every non-null pointer; `required` ones must be non-null
+template <typename... P>
+moe_status_t check_ptrs(bool required, P... ps) {
+  const void* arr[] = {static_cast<const void*>(ps)...};
+  for (const void* p : arr) {
+    if (!p) {
+      if (required) return MOE_ERR_INVALID_ARG;
+      continue;
+    }
+    if (!aligned16(p)) return MOE_ERR_UNSUPPORTED;
+  }
+  return MOE_OK;
+}
+
+moe_status_t check_ws(const moe_config_t& c, void* ws, size_t ws_bytes) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) % kAlign)) return MOE_ERR_WORKSPACE;
+  if (ws_bytes < layout_of(c).total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+struct DeviceInfo {
+  int sms = 0;
+  bool ok = false;
+};
+
+// Per-process cache for the current device (one GPU per process here).
+moe_status_t device_info(DeviceInfo* out) {
+  static DeviceInfo cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_NO_DEVICE;
+  DeviceInfo& d = cached[dev];
+  if (!d.ok) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return MOE_ERR_NO_DEVICE;
+    if (major != 10 || minor != 3) return MOE_ERR_NO_DEVICE;
+    if (!tensor_map_encoder_available()) return MOE_ERR_NO_DEVICE;
+    d.sms = sms;
+    d.ok = true;
+  }
+  *out = d;
+  return MOE_OK;
+}
+
+inline moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+#define MOE_TRY(expr)                    \
+  do {                                   \
+    moe_status_t _s = (expr);            \
+    if (_s != MOE_OK) return _s;         \
+  } while (0)
+
+#define MOE_CUDA(expr)                                   \
+  do {                                                   \
+    if ((expr) != cudaSuccess) return MOE_ERR_CUDA;      \
+  } while (0)
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+moe_status_t clear_status(void* ws, const WsLayout& L, cudaStream_t st, LaunchTrace* tr) {
+  trace_mark(tr, st);
+  return cuda_status(cudaMemsetAsync(at<int>(ws, L.status), 0, sizeof(int), st));
+}
+
+// ---------------------------------------------------------------- stages
+moe_status_t do_route(const moe_config_t& c, const uint16_t* x, const float* Wg, const float* bg,
+                      const float* sel, int32_t* idx, float* w, float* probs, float* p_mean,
+                      void* ws, const WsLayout& L, cudaStream_t st, LaunchTrace* tr) {
+  RouterLaunch a;
+  a.x = reinterpret_cast<const __nv_bfloat16*>(x);
+  a.Wg = Wg;
+  a.bg = bg;
+  a.sel_bias = sel;
+  a.topk_idx = idx;
+  a.topk_w = w;
+  a.probs = probs;
+  a.p_mean = p_mean;
+  a.logits = at<float>(ws, L.logits);
+  a.p_part = at<float>(ws, L.p_part);
+  a.T = c.T;
+  a.H = c.H;
+  a.N = c.N;
+  a.k = c.k;
+  return cuda_status(launch_router(a, st, tr));
+}
+
+moe_status_t do_permute(const moe_config_t& c, const int32_t* idx, const float* p_mean,
+                        int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv, float* f,
+                        float* l_aux, void* ws, const WsLayout& L, cudaStream_t st,
+                        LaunchTrace* tr) {
+  PermuteLaunch a;
+  a.topk_idx = idx;
+  a.p_mean = p_mean;
+  a.counts = counts;
+  a.offsets = offsets;
+  a.perm = perm;
+  a.inv = inv;
+  a.f = f;
+  a.l_aux = l_aux;
+  a.local_rank = at<int32_t>(ws, L.local_rank);
+  a.blk_hist = at<int32_t>(ws, L.blk_hist);
+  a.blk_base = at<int32_t>(ws, L.blk_base);
+  a.T = c.T;
+  a.N = c.N;
+  a.k = c.k;
+  a.capacity = capacity_of(c);
+  a.alpha = c.aux_alpha;
+  return cuda_status(launch_permute(a, st, tr));
+}
+
+moe_status_t do_ffn(const moe_config_t& c, const uint16_t* x, const int32_t* perm,
+                    const int32_t* offsets, const float* topk_w, const moe_weights_t& W,
+                    uint16_t* y, uint16_t* y_shared, void* ws, const WsLayout& L, int sms,
+                    cudaStream_t st, LaunchTrace* tr) {
+  using bf = __nv_bfloat16;
+  const int64_t R = max_rows_of(c);
+  int* status = at<int>(ws, L.status);
+  if (R > 0) {
+    bf* xp = at<bf>(ws, L.xp);
+    bf* hid = at<bf>(ws, L.hid);
+    MOE_CUDA(launch_gather(reinterpret_cast<const bf*>(x), perm, offsets, c.N, c.k, R, c.H, xp,
+                           st, tr));
+    GemmArgs g1{};
+    g1.offsets = offsets;
+    g1.num_groups = c.N;
+    g1.n_out = c.F;
+    g1.K = c.H;
+    g1.mode = EPI_GELU;
+    g1.bias = reinterpret_cast<const bf*>(W.b1);
+    g1.out = hid;
+    g1.ld_out = c.F;
+    g1.status = status;
+    GemmPlan p1;
+    MOE_CUDA(make_gemm_plan(&p1, xp, R, reinterpret_cast<const bf*>(W.W1), (int64_t)c.N * c.F,
+                            g1, sms));
+    MOE_CUDA(launch_gemm(p1, st, tr));
+    GemmArgs g2{};
+    g2.offsets = offsets;
+    g2.num_groups = c.N;
+    g2.n_out = c.H;
+    g2.K = c.F;
+    g2.mode = EPI_SCALE;
+    g2.bias = reinterpret_cast<const bf*>(W.b2);
+    g2.topk_w = topk_w;
+    g2.perm = perm;
+    g2.out = reinterpret_cast<bf*>(y);
+    g2.ld_out = c.H;
+    g2.status = status;
+    GemmPlan p2;
+    MOE_CUDA(make_gemm_plan(&p2, hid, R, reinterpret_cast<const bf*>(W.W2), (int64_t)c.N * c.H,
+                            g2, sms));
+    MOE_CUDA(launch_gemm(p2, st, tr));
+  }
+  if (c.F_shared > 0 && c.T > 0) {
+    bf* hs = at<bf>(ws, L.hid_s);
+    GemmArgs s1{};
+    s1.offsets = nullptr;
+    s1.num_groups = 1;
+    s1.rows_single = c.T;
+    s1.n_out = c.F_shared;
+    s1.K = c.H;
+    s1.mode = EPI_GELU;
+    s1.bias = reinterpret_cast<const bf*>(W.b1s);
+    s1.out = hs;
+    s1.ld_out = c.F_shared;
+    s1.status = status;
+    GemmPlan ps1;
+    MOE_CUDA(make_gemm_plan(&ps1, reinterpret_cast<const bf*>(x), c.T,
+                            reinterpret_cast<const bf*>(W.W1s), c.F_shared, s1, sms));
+    MOE_CUDA(launch_gemm(ps1, st, tr));
+    GemmArgs s2{};
+    s2.offsets = nullptr;
+    s2.num_groups = 1;
+    s2.rows_single = c.T;
+    s2.n_out = c.H;
+    s2.K = c.F_shared;
+    s2.mode = EPI_SCALE;
+    s2.bias = reinterpret_cast<const bf*>(W.b2s);
+    s2.topk_w = nullptr;
+    s2.perm = nullptr;
+    s2.out = reinterpret_cast<bf*>(y_shared);
+    s2.ld_out = c.H;
+    s2.status = status;
+    GemmPlan ps2;
+    MOE_CUDA(make_gemm_plan(&ps2, hs, c.T, reinterpret_cast<const bf*>(W.W2s), c.H, s2, sms));
+    MOE_CUDA(launch_gemm(ps2, st, tr));
+  }
+  return MOE_OK;
+}
+
+int ffn_num_launches(const moe_config_t& c) {
+  int n = 0;
+  if (max_rows_of(c) > 0) n += 3;
+  if (c.F_shared > 0 && c.T > 0) n += 2;
+  return n;
+}
+
+moe_status_t check_weights(const moe_config_t& c, const moe_weights_t* W, bool need_router,
+                           bool need_experts) {
+  if (!W) return MOE_ERR_INVALID_ARG;
+  if (need_router) {
+    MOE_TRY(check_ptrs(true, W->Wg));
+    MOE_TRY(check_ptrs(false, W->bg, W->sel_bias));
+  }
+  if (need_experts) {
+    MOE_TRY(check_ptrs(true, W->W1, W->W2));
+    MOE_TRY(check_ptrs(false, W->b1, W->b2));
+    if (c.F_shared > 0) {
+      MOE_TRY(check_ptrs(true, W->W1s, W->W2s));
+      MOE_TRY(check_ptrs(false, W->b1s, W->b2s));
+    }
+  }
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+MOE_API size_t moe_workspace_size(const moe_config_t* cfg) {
+  if (check_config(cfg) != MOE_OK) return 0;
+  return layout_of(*cfg).total;
+}
+
+MOE_API int64_t moe_max_rows(const moe_config_t* cfg) {
+  if (check_config(cfg) != MOE_OK) return -1;
+  return max_rows_of(*cfg);
+}
+
+MOE_API int64_t moe_capacity(const moe_config_t* cfg) {
+  if (check_config(cfg) != MOE_OK) return -1;
+  return capacity_of(*cfg);
+}
+
+MOE_API int32_t moe_forward_num_launches(const moe_config_t* cfg) {
+  if (check_config(cfg) != MOE_OK) return -1;
+  const moe_config_t& c = *cfg;
+  int n = 1;  // status clear
+  n += router_num_launches(c.T);
+  n += permute_num_launches(c.T, c.k);
+  n += ffn_num_launches(c);
+  if (c.T > 0) n += 1;  // combine
+  return n;
+}
+
+MOE_API moe_status_t moe_route(const moe_config_t* cfg, const uint16_t* x, const float* Wg,
+                               const float* bg, const float* sel_bias, int32_t* topk_idx,
+                               float* topk_w, float* probs, float* p_mean, void* ws,
+                               size_t ws_bytes, void* stream) {
+  MOE_TRY(check_config(cfg));
+  const moe_config_t& c = *cfg;
+  const bool has_t = c.T > 0;
+  MOE_TRY(check_ptrs(true, Wg, p_mean));
+  if (has_t) MOE_TRY(check_ptrs(true, x, topk_idx, topk_w));
+  MOE_TRY(check_ptrs(false, bg, sel_bias, probs));
+  MOE_TRY(check_ws(c, ws, ws_bytes));
+  DeviceInfo d;
+  MOE_TRY(device_info(&d));
+  const WsLayout L = layout_of(c);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MOE_TRY(clear_status(ws, L, st, nullptr));
+  return do_route(c, x, Wg, bg, sel_bias, topk_idx, topk_w, probs, p_mean, ws, L, st, nullptr);
+}
+
+MOE_API moe_status_t moe_permute(const moe_config_t* cfg, const int32_t* topk_idx,
+                                 const float* p_mean, int32_t* counts, int32_t* offsets,
+                                 int32_t* perm, int32_t* inv, float* f, float* l_aux, void* ws,
+                                 size_t ws_bytes, void* stream) {
+  MOE_TRY(check_config(cfg));
+  const moe_config_t& c = *cfg;
+  MOE_TRY(check_ptrs(true, counts, offsets));
+  if ((int64_t)c.T * c.k > 0) MOE_TRY(check_ptrs(true, topk_idx, inv));
+  if (max_rows_of(c) > 0) MOE_TRY(check_ptrs(true, perm));
+  if (l_aux) MOE_TRY(check_ptrs(true, p_mean));
+  MOE_TRY(check_ptrs(false, f, l_aux, p_mean));
+  MOE_TRY(check_ws(c, ws, ws_bytes));
+  DeviceInfo d;
+  MOE_TRY(device_info(&d));
+  const WsLayout L = layout_of(c);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MOE_TRY(clear_status(ws, L, st, nullptr));
+  return do_permute(c, topk_idx, p_mean, counts, offsets, perm, inv, f, l_aux, ws, L, st,
+                    nullptr);
+}
+
+MOE_API moe_status_t moe_expert_ffn(const moe_config_t* cfg, const uint16_t* x,
+                                    const int32_t* perm, const int32_t* offsets,
+                                    const float* topk_w, const moe_weights_t* weights,
+                                    uint16_t* y, uint16_t* y_shared, void* ws, size_t ws_bytes,
+                                    void* stream) {
+  MOE_TRY(check_config(cfg));
+  const moe_config_t& c = *cfg;
+  MOE_TRY(check_weights(c, weights, false, true));
+  if (c.T > 0) MOE_TRY(check_ptrs(true, x));
+  if (max_rows_of(c) > 0) MOE_TRY(check_ptrs(true, perm, offsets, topk_w, y));
+  if (c.F_shared > 0 && c.T > 0) MOE_TRY(check_ptrs(true, y_shared));
+  MOE_TRY(check_ptrs(false, y, y_shared));
+  MOE_TRY(check_ws(c, ws, ws_bytes));
+  DeviceInfo d;
+  MOE_TRY(device_info(&d));
+  const WsLayout L = layout_of(c);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MOE_TRY(clear_status(ws, L, st, nullptr));
+  return do_ffn(c, x, perm, offsets, topk_w, *weights, y, y_shared, ws, L, d.sms, st, nullptr);
+}
+
+MOE_API moe_status_t moe_combine(const moe_config_t* cfg, const uint16_t* y, const int32_t* inv,
+                                 const uint16_t* y_shared, uint16_t* out, void* stream) {
+  MOE_TRY(check_config(cfg));
+  const moe_config_t& c = *cfg;
+  if (c.T > 0) MOE_TRY(check_ptrs(true, inv, out));
+  if (max_rows_of(c) > 0 && c.T > 0) MOE_TRY(check_ptrs(true, y));
+  MOE_TRY(check_ptrs(false, y, y_shared));
+  if (c.F_shared > 0 && c.T > 0 && !y_shared) return MOE_ERR_INVALID_ARG;
+  DeviceInfo d;
+  MOE_TRY(device_info(&d));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  using bf = __nv_bfloat16;
+  return cuda_status(launch_combine(reinterpret_cast<const bf*>(y), inv,
+                                    c.F_shared > 0 ? reinterpret_cast<const bf*>(y_shared) : nullptr,
+                                    reinterpret_cast<bf*>(out), c.T, c.k, c.H, st, nullptr));
+}
+
+MOE_API moe_status_t moe_forward(const moe_config_t* cfg, const moe_weights_t* weights,
+                                 const uint16_t* x, uint16_t* out, const moe_outputs_t* outputs,
+                                 void* ws, size_t ws_bytes, void* stream,
+                                 void* const* trace_events) {
+  MOE_TRY(check_config(cfg));
+  const moe_config_t& c = *cfg;
+  MOE_TRY(check_weights(c, weights, true, true));
+  if (c.T > 0) MOE_TRY(check_ptrs(true, x, out));
+  moe_outputs_t o;
+  std::memset(&o, 0, sizeof(o));
+  if (outputs) o = *outputs;
+  MOE_TRY(check_ptrs(false, o.topk_idx, o.topk_w, o.probs, o.p_mean, o.counts, o.offsets, o.perm,
+                     o.inv, o.f, o.l_aux));
+  MOE_TRY(check_ws(c, ws, ws_bytes));
+  DeviceInfo d;
+  MOE_TRY(device_info(&d));
+  const WsLayout L = layout_of(c);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  LaunchTrace trace{reinterpret_cast<cudaEvent_t*>(const_cast<void**>(trace_events)),
+                    MOE_TRACE_MAX_EVENTS, 0};
+  LaunchTrace* tr = trace_events ? &trace : nullptr;
+
+  int32_t* idx = o.topk_idx ? o.topk_idx : at<int32_t>(ws, L.topk_idx);
+  float* w = o.topk_w ? o.topk_w : at<float>(ws, L.topk_w);
+  float* p_mean = o.p_mean ? o.p_mean : at<float>(ws, L.p_mean);
+  int32_t* counts = o.counts ? o.counts : at<int32_t>(ws, L.counts);
+  int32_t* offsets = o.offsets ? o.offsets : at<int32_t>(ws, L.offsets);
+  int32_t* perm = o.perm ? o.perm : at<int32_t>(ws, L.perm);
+  int32_t* inv = o.inv ? o.inv : at<int32_t>(ws, L.inv);
+  float* f = o.f ? o.f : at<float>(ws, L.f);
+  float* l_aux = o.l_aux ? o.l_aux : at<float>(ws, L.l_aux);
+  uint16_t* y = at<uint16_t>(ws, L.y);
+  uint16_t* ys = c.F_shared > 0 ? at<uint16_t>(ws, L.y_s) : nullptr;
+
+  MOE_TRY(clear_status(ws, L, st, tr));
+  MOE_TRY(do_route(c, x, weights->Wg, weights->bg, weights->sel_bias, idx, w, o.probs, p_mean, ws,
+                   L, st, tr));
+  MOE_TRY(do_permute(c, idx, p_mean, counts, offsets, perm, inv, f, l_aux, ws, L, st, tr));
+  MOE_TRY(do_ffn(c, x, perm, offsets, w, *weights, y, ys, ws, L, d.sms, st, tr));
+  if (c.T > 0) {
+    using bf = __nv_bfloat16;
+    MOE_CUDA(launch_combine(reinterpret_cast<const bf*>(y), inv, reinterpret_cast<const bf*>(ys),
+                            reinterpret_cast<bf*>(out), c.T, c.k, c.H, st, tr));
+  }
+  trace_mark(tr, st);
+  return MOE_OK;
+}
+
+MOE_API moe_status_t moe_workspace_status(const void* ws, void* stream) {
+  if (!ws) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int v = 0;
+  // the status word sits at offset 0 of every layout
+  if (cudaMemcpyAsync(&v, ws, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  return v == 0 ? MOE_OK : static_cast<moe_status_t>(v);
+}
+
+MOE_API const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape or alignment";
+    case MOE_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case MOE_ERR_CUDA: return "CUDA runtime error";
+    case MOE_ERR_TIMEOUT: return "device-side wait timed out";
+    case MOE_ERR_NO_DEVICE: return "no usable sm_103 device";
+  }
+  return "unknown status";
+}
+
+MOE_API const char* moe_version(void) { return "moe_b300 0.1 (sm_103a)"; }

@@ -1,0 +1,141 @@
+// Dispatch: per-expert histogram, capacity, stable expert-contiguous scatter,
+// and the load-balance statistic.
+//
+// "混合专家模型 MoE 架构深度解析" §2.3 (Capacity = floor(T/N * capacity_factor);
+// tokens over capacity pass through with no expert output), §2.2
+// (L_aux = alpha * N * sum f_i p_i); "AI-Research-SKILLs MoE 训练实战" §4.3
+// (f from bincount of the top-k indices over their count), §4.4 (drop_tokens).
+//
+// Assignments a = t*k + j are ranked within their expert in increasing a
+// (a stable scatter), so the first C assignments of each expert keep a row.
+// Three launches, all integer work and no atomics on values:
+//   1. rank:    per 256-assignment chunk, rank of each assignment among the
+//               chunk's assignments to the same expert + chunk histogram
+//   2. scan:    chunk bases per expert (in chunk order), counts, capacity,
+//               row offsets, f and L_aux (one block)
+//   3. scatter: row = offsets[e] + base + local rank, or dropped
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace moe {
+
+constexpr int PR_THREADS = kPermuteChunk;
+constexpr int PR_WARPS = PR_THREADS / 32;
+
+__global__ void __launch_bounds__(PR_THREADS) permute_rank_kernel(
+    const int32_t* __restrict__ idx, int32_t* __restrict__ local_rank,
+    int32_t* __restrict__ blk_hist, int64_t A, int N) {
+  extern __shared__ int32_t wcnt[];  // [PR_WARPS][N]
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  for (int i = tid; i < PR_WARPS * N; i += PR_THREADS) wcnt[i] = 0;
+  __syncthreads();
+  const int64_t a = (int64_t)blockIdx.x * PR_THREADS + tid;
+  int e = (a < A) ? idx[a] : -1;
+  if (e < 0 || e >= N) e = -1;  // out-of-range indices take no slot
+  const uint32_t peers = __match_any_sync(0xffffffffu, e);
+  const int wrank = __popc(peers & ((1u << lane) - 1u));
+  if (e >= 0 && wrank == 0) wcnt[warp * N + e] = __popc(peers);
+  __syncthreads();
+  // exclusive scan over the warps, per expert; the chunk total is the histogram
+  for (int ex = tid; ex < N; ex += PR_THREADS) {
+    int run = 0;
+#pragma unroll
+    for (int w = 0; w < PR_WARPS; ++w) {
+      const int c = wcnt[w * N + ex];
+      wcnt[w * N + ex] = run;
+      run += c;
+    }
+    blk_hist[(size_t)blockIdx.x * N + ex] = run;
+  }
+  __syncthreads();
+  if (a < A) local_rank[a] = (e >= 0) ? wcnt[warp * N + e] + wrank : -1;
+}
+
+// One block of up to 1024 threads; thread e owns expert e.
+__global__ void __launch_bounds__(1024) permute_scan_kernel(
+    const int32_t* __restrict__ blk_hist, int32_t* __restrict__ blk_base,
+    int32_t* __restrict__ counts, int32_t* __restrict__ offsets, const float* __restrict__ p_mean,
+    float* __restrict__ f, float* __restrict__ l_aux, int nblk, int N, int64_t A,
+    int64_t capacity, float alpha) {
+  __shared__ int32_t sc[1024];
+  __shared__ double red[1024];
+  const int e = threadIdx.x;
+  int run = 0;
+  if (e < N) {
+    for (int b = 0; b < nblk; ++b) {
+      const int c = blk_hist[(size_t)b * N + e];
+      blk_base[(size_t)b * N + e] = run;
+      run += c;
+    }
+    counts[e] = run;
+  }
+  const int kept = (e < N) ? (int)((capacity >= 0 && run > capacity) ? capacity : run) : 0;
+  // inclusive Hillis-Steele scan of kept over the experts
+  sc[e] = kept;
+  __syncthreads();
+  for (int o = 1; o < blockDim.x; o <<= 1) {
+    const int v = (e >= o) ? sc[e - o] : 0;
+    __syncthreads();
+    sc[e] += v;
+    __syncthreads();
+  }
+  if (e < N) offsets[e] = sc[e] - kept;
+  if (e == N - 1) offsets[N] = sc[e];
+  // f_i and L_aux (fixed-order tree reduction in double)
+  double term = 0.0;
+  if (e < N) {
+    const double fe = A > 0 ? (double)run / (double)A : 0.0;
+    if (f) f[e] = (float)fe;
+    if (l_aux) term = fe * (double)p_mean[e];
+  }
+  red[e] = term;
+  __syncthreads();
+  for (int s = blockDim.x / 2; s > 0; s >>= 1) {
+    if (e < s) red[e] += red[e + s];
+    __syncthreads();
+  }
+  if (e == 0 && l_aux) *l_aux = (float)((double)alpha * (double)N * red[0]);
+}
+
+__global__ void __launch_bounds__(256) permute_scatter_kernel(
+    const int32_t* __restrict__ idx, const int32_t* __restrict__ local_rank,
+    const int32_t* __restrict__ blk_base, const int32_t* __restrict__ offsets,
+    int32_t* __restrict__ perm, int32_t* __restrict__ inv, int64_t A, int N, int64_t capacity) {
+  const int64_t a = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (a >= A) return;
+  const int e = idx[a];
+  if (e < 0 || e >= N) { inv[a] = -1; return; }
+  const int64_t pos = (int64_t)blk_base[(a / kPermuteChunk) * N + e] + local_rank[a];
+  if (capacity >= 0 && pos >= capacity) { inv[a] = -1; return; }
+  const int32_t row = offsets[e] + (int32_t)pos;
+  perm[row] = (int32_t)a;
+  inv[a] = row;
+}
+
+int permute_num_launches(int T, int k) { return (int64_t)T * k > 0 ? 3 : 1; }
+
+cudaError_t launch_permute(const PermuteLaunch& a, cudaStream_t st, LaunchTrace* tr) {
+  const int64_t A = (int64_t)a.T * a.k;
+  const int nblk = permute_num_blocks(A);
+  if (A > 0) {
+    trace_mark(tr, st);
+    permute_rank_kernel<<<nblk, PR_THREADS, PR_WARPS * a.N * sizeof(int32_t), st>>>(
+        a.topk_idx, a.local_rank, a.blk_hist, A, a.N);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+  }
+  int threads = 32;
+  while (threads < a.N) threads <<= 1;
+  trace_mark(tr, st);
+  permute_scan_kernel<<<1, threads, 0, st>>>(a.blk_hist, a.blk_base, a.counts, a.offsets,
+                                             a.p_mean, a.f, a.l_aux, nblk, a.N, A, a.capacity,
+                                             a.alpha);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess || A == 0) return err;
+  trace_mark(tr, st);
+  permute_scatter_kernel<<<(unsigned)((A + 255) / 256), 256, 0, st>>>(
+      a.topk_idx, a.local_rank, a.blk_base, a.offsets, a.perm, a.inv, A, a.N, a.capacity);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,115 @@
+"""CPU tests of the C ABI library: it loads without a GPU, exports every symbol
+include/moe.h declares, and rejects bad arguments on the host before any
+device call (fake, never-dereferenced pointers)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sparse_mixture_experts_72_b300 import _lib
+    return _lib.load()
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "moe.h")) as f:
+        src = f.read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    from sparse_mixture_experts_72_b300 import _lib
+    decl = _declared()
+    assert decl, "no declarations parsed"
+    for name in decl:
+        assert hasattr(lib, name), f"{name} declared but not exported"
+    assert sorted(_lib.EXPORTED) == decl
+
+
+def test_exports_nothing_else():
+    import subprocess
+    from sparse_mixture_experts_72_b300 import _lib
+    r = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True,
+                       text=True)
+    if r.returncode != 0:
+        pytest.skip("nm unavailable")
+    syms = [ln.split()[-1] for ln in r.stdout.splitlines() if " T " in ln]
+    ours = [s for s in syms if not s.startswith("_")]
+    assert sorted(ours) == _declared(), ours
+
+
+def _cfg(**kw):
+    from sparse_mixture_experts_72_b300._lib import MoeConfig
+    d = dict(T=64, H=32, F=128, N=4, k=2, capacity_factor=0.0, F_shared=0, aux_alpha=0.01)
+    d.update(kw)
+    return MoeConfig(**d)
+
+
+def test_host_shape_functions(lib):
+    from oracle import moe_oracle as O
+    for T, N, cf in [(32768, 64, 1.25), (4096, 8, 2.0), (100, 8, 1.0), (777, 12, 1.25),
+                     (64, 4, 0.0), (40, 16, 0.1), (0, 8, 1.0)]:
+        c = _cfg(T=T, N=N, capacity_factor=cf, k=1)
+        want = O.capacity(T, N, cf)
+        assert lib.moe_capacity(C.byref(c)) == (-1 if want is None else want)
+        R = T if want is None else min(T, want * N)
+        assert lib.moe_max_rows(C.byref(c)) == R
+    c = _cfg()
+    assert lib.moe_workspace_size(C.byref(c)) > 0
+    assert lib.moe_workspace_size(C.byref(_cfg(k=5))) == 0  # k > N is invalid
+    assert lib.moe_workspace_size(None) == 0
+
+
+def test_launch_count_matches_bench_names(lib):
+    import bench
+    import moe_workloads as wl
+    for w in list(wl.WORKLOADS.values()) + list(wl.TEST_WORKLOADS.values()):
+        c = _cfg(T=w.T, H=w.H, F=w.F, N=w.N, k=w.k, capacity_factor=w.capacity_factor,
+                 F_shared=w.F_shared)
+        n = lib.moe_forward_num_launches(C.byref(c))
+        assert n == len(bench.launch_names(w, lib.moe_max_rows(C.byref(c)) > 0)), w.name
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: every check fails before a device call
+
+
+def _weights(**kw):
+    from sparse_mixture_experts_72_b300._lib import MoeWeights
+    d = dict(Wg=FAKE, bg=None, sel_bias=None, W1=FAKE, b1=None, W2=FAKE, b2=None, W1s=None,
+             b1s=None, W2s=None, b2s=None)
+    d.update(kw)
+    return MoeWeights(**d)
+
+
+def _forward(lib, cfg, weights, x=FAKE, out=FAKE, ws=FAKE * 16, ws_bytes=None):
+    if ws_bytes is None:
+        ws_bytes = lib.moe_workspace_size(C.byref(cfg)) or 1
+    return lib.moe_forward(C.byref(cfg), C.byref(weights), x, out, None, ws, ws_bytes, None, None)
+
+
+def test_rejects_bad_arguments_before_any_launch(lib):
+    ok = _cfg()
+    assert _forward(lib, _cfg(k=0), _weights()) == 1           # INVALID_ARG
+    assert _forward(lib, _cfg(k=5), _weights()) == 1           # k > N
+    assert _forward(lib, _cfg(T=-1), _weights()) == 1
+    assert _forward(lib, _cfg(H=36), _weights()) == 2          # H % 8
+    assert _forward(lib, _cfg(N=2000, k=2), _weights()) == 2   # N > MOE_MAX_EXPERTS
+    assert _forward(lib, ok, _weights(Wg=None)) == 1           # required pointer
+    assert _forward(lib, ok, _weights(W1=FAKE + 4)) == 2       # misaligned
+    assert _forward(lib, ok, _weights(), x=FAKE + 2) == 2
+    assert _forward(lib, _cfg(F_shared=64), _weights()) == 1   # shared weights missing
+    assert _forward(lib, ok, _weights(), ws=None) == 3         # WORKSPACE
+    assert _forward(lib, ok, _weights(), ws=FAKE * 16 + 16) == 3
+    assert _forward(lib, ok, _weights(), ws_bytes=16) == 3
+    # all checks pass: without a GPU the first device query fails cleanly
+    # (never run with a GPU present: the fake pointers would reach a kernel)
+    import torch
+    if not torch.cuda.is_available():
+        assert _forward(lib, ok, _weights()) == 6
+    assert lib.moe_status_string(3) == b"workspace missing, misaligned or too small"
