@@ -243,7 +243,11 @@ def moe_forward(cfg: MoEConfig, weights: MoEWeights, x, *, out=None, outputs: Op
     if trace_events is not None:
         if len(trace_events) > MOE_TRACE_MAX_EVENTS:
             raise ValueError("too many trace events")
-        handles = [e.cuda_event for e in trace_events]
+        handles = []
+        for e in trace_events:
+            if not e.cuda_event:
+                e.record()  # torch creates its events lazily, on first record
+            handles.append(e.cuda_event)
         handles += [None] * (MOE_TRACE_MAX_EVENTS - len(handles))
         ev = (C.c_void_p * MOE_TRACE_MAX_EVENTS)(*handles)
     st = _L.moe_forward(C.byref(cfg.c()), C.byref(wc),
