@@ -30,7 +30,10 @@ quote):
 * selection is made on the scores s = l - b directly (softmax is monotone, so
   this is the same ranking as top-k of probabilities, without rounding ties).
 * ties: equal scores rank the lower expert index first; the k slots of a
-  token are in descending score order.
+  token are in descending score order.  Tokens whose k-th and (k+1)-th
+  selection probabilities are within 1e-5 (the set can flip) or whose
+  adjacent slots inside the top k are within 1e-5 (the slot order can flip)
+  are flagged by the margins select_topk returns.
 * capacity: floor(T / N * cf) evaluated in double in that order;
   cf <= 0 means no limit.  Assignments a = t*k + j claim slots in increasing
   a; an assignment whose rank within its expert is >= C is dropped and
@@ -82,20 +85,22 @@ def select_topk(s: np.ndarray, k: int):
     """[ARCH] §1.3 step 2: the k experts with the largest scores.
 
     Returns (idx int64 [T,k] in descending score order, ties to the lower
-    index; margin float64 [T] = q_k - q_{k+1} where q = softmax(s), +inf when
-    k == N).  The margin flags tokens whose choice a tiny change of the
-    scores can flip.
+    index; margin float64 [T] = q_k - q_{k+1} where q = softmax(s) sorted
+    descending, +inf when k == N; order_margin float64 [T] = the smallest
+    gap q_j - q_{j+1} for j < k, +inf when k == 1).  The margin flags tokens
+    whose chosen set a tiny change of the scores can flip; the order margin
+    flags tokens whose slot order it can flip.
     """
     s = np.asarray(s, np.float64)
     T, N = s.shape
     order = np.argsort(-s, axis=1, kind="stable")
     idx = order[:, :k].copy()
-    if k >= N or T == 0:
-        return idx, np.full(T, np.inf)
-    q = softmax(s)
-    rows = np.arange(T)
-    margin = q[rows, order[:, k - 1]] - q[rows, order[:, k]]
-    return idx, margin
+    if T == 0:
+        return idx, np.full(T, np.inf), np.full(T, np.inf)
+    q = np.take_along_axis(softmax(s), order, axis=1)
+    margin = q[:, k - 1] - q[:, k] if k < N else np.full(T, np.inf)
+    order_margin = (-np.diff(q[:, :k], axis=1)).min(axis=1) if k > 1 else np.full(T, np.inf)
+    return idx, margin, order_margin
 
 
 def renormalise(P: np.ndarray, idx: np.ndarray) -> np.ndarray:
@@ -111,9 +116,10 @@ def route(x, Wg, bg, sel_bias, k: int) -> dict:
     l = gate_logits(x, Wg, bg)
     P = softmax(l)
     s = l if sel_bias is None else l - np.asarray(sel_bias, np.float64)[None, :]
-    idx, margin = select_topk(s, k)
+    idx, margin, order_margin = select_topk(s, k)
     w = renormalise(P, idx)
-    return dict(logits=l, probs=P, idx=idx, w=w, margin=margin)
+    return dict(logits=l, probs=P, idx=idx, w=w, margin=margin, order_margin=order_margin,
+                scores=s)
 
 
 # ---------------------------------------------------------------------------

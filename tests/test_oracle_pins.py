@@ -47,6 +47,7 @@ def check_router_worked_example():
     assert r["idx"][0].tolist() == g["idx"]
     np.testing.assert_allclose(r["w"][0], g["w"], rtol=0, atol=1e-15)
     np.testing.assert_allclose(r["margin"][0], g["margin"], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(r["order_margin"][0], g["order_margin"], rtol=0, atol=1e-15)
 
 
 def check_capacity_examples():
@@ -111,7 +112,7 @@ def check_topk_bruteforce(seed=1):
             s = rng.integers(-2, 3, size=(T, N)).astype(np.float64)   # many exact ties
         else:
             s = rng.standard_normal((T, N))
-        idx, _ = O.select_topk(s, k)
+        idx = O.select_topk(s, k)[0]
         for t in range(T):
             # best subset: largest sum, then the lexicographically smallest index set
             best = max(itertools.combinations(range(N), k),
@@ -174,7 +175,7 @@ def check_weights_invariants(seed=4):
     np.testing.assert_allclose(r["w"].sum(1), 1.0, rtol=0, atol=1e-12)
     assert (r["w"] >= 0).all()
     assert (np.diff(r["w"], axis=1) <= 0).all()
-    assert (r["margin"] >= 0).all()
+    assert (r["margin"] >= 0).all() and (r["order_margin"] >= 0).all()
 
 
 def check_permute_vs_stable_sort(seed=5):
@@ -379,7 +380,7 @@ def _mut_ties_high_index(s, k):
     s = np.asarray(s, np.float64)
     T, N = s.shape
     order = (N - 1 - np.argsort(-s[:, ::-1], axis=1, kind="stable"))
-    return order[:, :k].copy(), np.full(T, np.inf)
+    return order[:, :k].copy(), np.full(T, np.inf), np.full(T, np.inf)
 
 
 def _mut_capacity_ceil(T, N, cf):
@@ -396,8 +397,9 @@ def _mut_bias_in_weights(x, Wg, bg, sel_bias, k):
     l = O.gate_logits(x, Wg, bg)
     s = l if sel_bias is None else l - np.asarray(sel_bias)[None, :]
     P = O.softmax(s)
-    idx, margin = O.select_topk(s, k)
-    return dict(logits=l, probs=O.softmax(l), idx=idx, w=O.renormalise(P, idx), margin=margin)
+    idx, margin, om = O.select_topk(s, k)
+    return dict(logits=l, probs=O.softmax(l), idx=idx, w=O.renormalise(P, idx), margin=margin,
+                order_margin=om, scores=s)
 
 
 def _mut_ffn_missing_b2(xe, W1, b1, W2, b2):
