@@ -189,6 +189,33 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_weights_t* weights,
                          const uint16_t* x, uint16_t* out, const moe_outputs_t* outputs,
                          void* ws, size_t ws_bytes, void* stream, void* const* trace_events);
 
+/*
+ * moe_permute_static - moe_permute for callers that cannot allocate device
+ * memory and have no workspace to give: for example a plugin running inside
+ * an inference engine that owns all device memory and forbids allocation on
+ * its execution path, or a service that reserves all memory at start-up.
+ * The source pages have no counterpart to this entry point: it computes
+ * exactly what moe_permute computes (same kernels, same outputs), but its
+ * scratch is one fixed array in device memory that the library holds on
+ * every device it is loaded on until the process exits.
+ *   Arguments and outputs are those of moe_permute, without ws/ws_bytes.
+ *   Limits: T*k <= MOE_STATIC_MAX_ASSIGNMENTS and N <= MOE_STATIC_MAX_EXPERTS;
+ *   larger sizes return MOE_ERR_UNSUPPORTED before anything is enqueued.
+ *   The call allocates nothing (no cudaMalloc/cudaFree).  Its first call on a
+ *   device looks up the array's device address (cudaGetSymbolAddress) with
+ *   that device current, so make the first call on each device before any
+ *   stream capture.  Every call shares the one array, which keeps the last
+ *   call's contents (nothing in it needs clearing: each call writes every
+ *   entry it reads); calls that overlap on the GPU - on different streams,
+ *   or from different threads - race on it and must be serialised.
+ */
+#define MOE_STATIC_MAX_ASSIGNMENTS 65536
+#define MOE_STATIC_MAX_EXPERTS 256
+moe_status_t moe_permute_static(const moe_config_t* cfg, const int32_t* topk_idx,
+                                const float* p_mean, int32_t* counts, int32_t* offsets,
+                                int32_t* perm, int32_t* inv, float* f, float* l_aux,
+                                void* stream);
+
 /* Synchronises `stream` and returns the device status word of `ws`
  * (MOE_OK or MOE_ERR_TIMEOUT), or MOE_ERR_CUDA if the synchronisation fails. */
 moe_status_t moe_workspace_status(const void* ws, void* stream);

@@ -22,6 +22,7 @@ _L = _lib.load()
 
 __all__ = ["MoEConfig", "MoEWeights", "MoeError", "moe_workspace_size", "moe_max_rows",
            "moe_capacity", "moe_forward_num_launches", "moe_route", "moe_permute",
+           "moe_permute_static",
            "moe_expert_ffn", "moe_combine", "moe_forward", "moe_workspace_status",
            "make_workspace", "library_path", "MOE_TRACE_MAX_EVENTS"]
 
@@ -170,6 +171,36 @@ def moe_permute(cfg: MoEConfig, topk_idx, p_mean=None, *, ws=None, stream=None) 
                         _p(out["l_aux"], torch.float32, None, "l_aux", True),
                         wsp, wsn, _stream(stream))
     check(st, "moe_permute")
+    return out
+
+
+def moe_permute_static(cfg: MoEConfig, topk_idx, p_mean=None, *, stream=None) -> dict:
+    """moe_permute without a workspace, for callers that cannot allocate:
+    the scratch is a fixed device array inside the library (T*k <= 65536,
+    N <= 256).  Calls share that array, so calls that overlap on the GPU race.
+    Make the first call on a device before any stream capture.  (This
+    binding allocates its output tensors; a caller that cannot allocate
+    calls the C entry point with its own buffers.)"""
+    dev = topk_idx.device
+    T, N, k = cfg.T, cfg.N, cfg.k
+    R = moe_max_rows(cfg)
+    out = dict(counts=torch.empty(N, dtype=torch.int32, device=dev),
+               offsets=torch.empty(N + 1, dtype=torch.int32, device=dev),
+               perm=torch.empty(max(R, 0), dtype=torch.int32, device=dev),
+               inv=torch.empty(T * k, dtype=torch.int32, device=dev),
+               f=torch.empty(N, dtype=torch.float32, device=dev),
+               l_aux=torch.empty(1, dtype=torch.float32, device=dev) if p_mean is not None else None)
+    st = _L.moe_permute_static(C.byref(cfg.c()),
+                               _p(topk_idx, torch.int32, (T, k), "topk_idx", T == 0),
+                               _p(p_mean, torch.float32, (N,), "p_mean", True),
+                               _p(out["counts"], torch.int32, None, "counts"),
+                               _p(out["offsets"], torch.int32, None, "offsets"),
+                               _p(out["perm"], torch.int32, None, "perm", True),
+                               _p(out["inv"], torch.int32, None, "inv", True),
+                               _p(out["f"], torch.float32, None, "f"),
+                               _p(out["l_aux"], torch.float32, None, "l_aux", True),
+                               _stream(stream))
+    check(st, "moe_permute_static")
     return out
 
 

@@ -16,7 +16,9 @@ MOE_TRACE_MAX_EVENTS = 32
 # every symbol include/moe.h declares
 EXPORTED = ["moe_workspace_size", "moe_max_rows", "moe_capacity", "moe_forward_num_launches",
             "moe_route", "moe_permute", "moe_expert_ffn", "moe_combine", "moe_forward",
-            "moe_workspace_status", "moe_status_string", "moe_version"]
+            "moe_permute_static", "moe_workspace_status", "moe_status_string", "moe_version"]
+MOE_STATIC_MAX_ASSIGNMENTS = 65536
+MOE_STATIC_MAX_EXPERTS = 256
 
 
 class MoeConfig(C.Structure):
@@ -46,7 +48,7 @@ def load() -> C.CDLL:
         return _lib
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"{LIB_PATH} is missing: build it with "
-                          "`python -m sparse_mixture_experts_72_b300.build`")
+                          "`python sparse_mixture_experts_72_b300/build.py`")
     lib = C.CDLL(LIB_PATH)
     P = C.c_void_p
     cfgp = C.POINTER(MoeConfig)
@@ -69,6 +71,8 @@ def load() -> C.CDLL:
     lib.moe_forward.argtypes = [cfgp, C.POINTER(MoeWeights), P, P, C.POINTER(MoeOutputs), P,
                                 C.c_size_t, P, P]
     lib.moe_forward.restype = C.c_int
+    lib.moe_permute_static.argtypes = [cfgp, P, P, P, P, P, P, P, P, P]
+    lib.moe_permute_static.restype = C.c_int
     lib.moe_workspace_status.argtypes = [P, P]
     lib.moe_workspace_status.restype = C.c_int
     lib.moe_status_string.argtypes = [C.c_int]

@@ -1,6 +1,8 @@
 """Builds libmoe_b300.so (the C ABI + sm_103a kernels) in-tree with nvcc.
 
-    python -m sparse_mixture_experts_72_b300.build [--force]
+    python sparse_mixture_experts_72_b300/build.py [--force]
+
+(Run it by path: importing the package needs the library it builds.)
 
 Cross-compiles without a GPU.  The CUDA runtime is linked statically and the
 driver's tensor-map encoder is looked up at run time, so the library loads
@@ -21,7 +23,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_b300.so")
-SOURCES = ["moe_api.cu", "router.cu", "permute.cu", "combine.cu", "gemm_tc.cu"]
+SOURCES = ["moe_api.cu", "router.cu", "permute.cu", "combine.cu", "gemm_tc.cu",
+           "permute_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-fvisibility=hidden", "--expt-relaxed-constexpr",
