@@ -159,13 +159,21 @@ def algorithmic_work(w: wl.Workload, counts: np.ndarray, R: int):
 
 
 def launch_names(w: wl.Workload, has_rows: bool):
-    names = ["status_memset", "router_logits", "router_select", "router_pmean",
-             "permute_rank", "permute_scan", "permute_scatter"]
+    names = ["status_memset"]
+    if w.N <= 256:  # tensor-core router: W_g split + fused router
+        names += ["router_split", "router_tc"] if w.T > 0 else ["p_mean_memset"]
+    else:
+        names += ["router_logits", "router_select", "router_pmean"] if w.T > 0 else ["router_pmean"]
+    if w.T * w.k > 0:
+        names += ["permute_rank", "permute_scan", "permute_scatter"]
+    else:
+        names += ["permute_scan"]
     if has_rows:
         names += ["gather", "gemm1", "gemm2"]
     if w.F_shared:
         names += ["gemm1_shared", "gemm2_shared"]
-    names += ["combine"]
+    if w.T > 0:
+        names += ["combine"]
     return names
 
 

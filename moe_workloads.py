@@ -97,6 +97,8 @@ TEST_WORKLOADS: Dict[str, Workload] = {w.name: w for w in [
     Workload("dense_n1", T=300, H=64, F=96, N=1, k=1),
     Workload("all_experts", T=200, H=64, F=64, N=6, k=6, gate_bias="normal"),
     Workload("all_dropped", T=40, H=64, F=64, N=16, k=2, capacity_factor=0.1, F_shared=64),
+    # more experts than the tensor-core router takes: the fp32 SIMT router runs
+    Workload("many_experts", T=200, H=64, F=64, N=300, k=4, gate_bias="normal"),
 ]}
 
 

@@ -334,13 +334,13 @@ static EncodeTiledFn get_encoder() {
 
 bool tensor_map_encoder_available() { return get_encoder() != nullptr; }
 
-static bool encode_kmajor(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
-                          int box_rows) {
+bool encode_tensor_map_bf16(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
+                            int box_cols, int box_rows) {
   EncodeTiledFn enc = get_encoder();
   if (!enc) return false;
   cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -352,8 +352,8 @@ cudaError_t make_gemm_plan(GemmPlan* plan, const __nv_bfloat16* A, int64_t a_row
                            const __nv_bfloat16* B, int64_t b_rows, const GemmArgs& args,
                            int num_sms) {
   if (a_rows <= 0 || b_rows <= 0 || args.K <= 0 || args.n_out <= 0) return cudaErrorInvalidValue;
-  if (!encode_kmajor(&plan->tmA, A, a_rows, args.K, BM)) return cudaErrorInvalidValue;
-  if (!encode_kmajor(&plan->tmB, B, b_rows, args.K, BN)) return cudaErrorInvalidValue;
+  if (!encode_tensor_map_bf16(&plan->tmA, A, a_rows, args.K, BK, BM)) return cudaErrorInvalidValue;
+  if (!encode_tensor_map_bf16(&plan->tmB, B, b_rows, args.K, BK, BN)) return cudaErrorInvalidValue;
   plan->args = args;
   const int64_t n_tiles = (args.n_out + BN - 1) / BN;
   const int64_t max_tiles = ((a_rows + BM - 1) / BM + args.num_groups) * n_tiles;

@@ -37,8 +37,34 @@ struct RouterLaunch {
   int T, H, N, k;
 };
 int router_num_select_blocks(int T);
-int router_num_launches(int T);
+int router_num_launches(int T, int N);
+// fp32 SIMT router (any N <= MOE_MAX_EXPERTS)
 cudaError_t launch_router(const RouterLaunch& a, cudaStream_t st, LaunchTrace* tr);
+
+// tensor-core router (N <= kRouterTcMaxExperts): split kernel + fused kernel
+constexpr int kRouterTcMaxExperts = 256;
+struct RouterTcArgs {
+  const float* bg;
+  const float* sel_bias;
+  int32_t* topk_idx;
+  float* topk_w;
+  float* probs;     // nullable
+  float* p_part;    // [ceil(T/128), N]
+  float* p_mean;
+  int* ticket;      // zero on entry; reset to zero by the last CTA
+  int* status;
+  int T, N, N_pad, H_pad, k, tmem_cols;
+};
+inline size_t router_w3_bytes(int N, int H) {
+  const size_t N_pad = (N + 15) / 16 * 16, H_pad = (H + 63) / 64 * 64;
+  return N_pad * 3 * H_pad * 2;
+}
+cudaError_t launch_router_tc(const RouterLaunch& a, __nv_bfloat16* W3, int* ticket, int* status,
+                             cudaStream_t st, LaunchTrace* tr);
+
+// TMA map of a row-major bf16 matrix [rows, K], box 64 (K) x box_rows, 128B swizzle
+bool encode_tensor_map_bf16(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
+                            int box_cols, int box_rows);
 
 // ---------------------------------------------------------------- permute
 struct PermuteLaunch {

@@ -35,7 +35,7 @@ int64_t max_rows_of(const moe_config_t& c) {
 }
 
 struct WsLayout {
-  size_t status, logits, p_part, local_rank, blk_hist, blk_base;
+  size_t status, w3, logits, p_part, local_rank, blk_hist, blk_base;
   size_t topk_idx, topk_w, p_mean, counts, offsets, perm, inv, f, l_aux;
   size_t xp, hid, y, hid_s, y_s;
   size_t total;
@@ -48,8 +48,10 @@ WsLayout layout_of(const moe_config_t& c) {
   const int64_t nblk = permute_num_blocks(A);
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o += align_up(bytes > 0 ? bytes : 1); return at; };
-  L.status = take(16);
-  L.logits = take(sizeof(float) * T * N);
+  L.status = take(16);  // [0] status word, [1] router ticket
+  const bool tc = c.N <= kRouterTcMaxExperts;
+  L.w3 = take(tc ? router_w3_bytes(c.N, c.H) : 0);
+  L.logits = take(tc ? 0 : sizeof(float) * T * N);
   L.p_part = take(sizeof(float) * (nsel > 0 ? nsel : 1) * N);
   L.local_rank = take(sizeof(int32_t) * A);
   L.blk_hist = take(sizeof(int32_t) * (nblk > 0 ? nblk : 1) * N);
@@ -150,7 +152,7 @@ T* at(void* ws, size_t off) {
 
 moe_status_t clear_status(void* ws, const WsLayout& L, cudaStream_t st, LaunchTrace* tr) {
   trace_mark(tr, st);
-  return cuda_status(cudaMemsetAsync(at<int>(ws, L.status), 0, sizeof(int), st));
+  return cuda_status(cudaMemsetAsync(at<int>(ws, L.status), 0, 4 * sizeof(int), st));
 }
 
 // ---------------------------------------------------------------- stages
@@ -172,6 +174,9 @@ moe_status_t do_route(const moe_config_t& c, const uint16_t* x, const float* Wg,
   a.H = c.H;
   a.N = c.N;
   a.k = c.k;
+  if (c.N <= kRouterTcMaxExperts)
+    return cuda_status(launch_router_tc(a, at<__nv_bfloat16>(ws, L.w3), at<int>(ws, L.status) + 1,
+                                        at<int>(ws, L.status), st, tr));
   return cuda_status(launch_router(a, st, tr));
 }
 
@@ -328,7 +333,7 @@ MOE_API int32_t moe_forward_num_launches(const moe_config_t* cfg) {
   if (check_config(cfg) != MOE_OK) return -1;
   const moe_config_t& c = *cfg;
   int n = 1;  // status clear
-  n += router_num_launches(c.T);
+  n += router_num_launches(c.T, c.N);
   n += permute_num_launches(c.T, c.k);
   n += ffn_num_launches(c);
   if (c.T > 0) n += 1;  // combine

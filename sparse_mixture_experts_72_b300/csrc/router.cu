@@ -223,6 +223,9 @@ cudaError_t launch_router(const RouterLaunch& a, cudaStream_t st, LaunchTrace* t
   return cudaGetLastError();
 }
 
-int router_num_launches(int T) { return T > 0 ? 3 : 1; }
+int router_num_launches(int T, int N) {
+  if (N <= kRouterTcMaxExperts) return T > 0 ? 2 : 1;
+  return T > 0 ? 3 : 1;
+}
 
 }  // namespace moe

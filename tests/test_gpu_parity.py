@@ -18,7 +18,7 @@ from tests import _helpers as h
 pytestmark = pytest.mark.gpu
 
 SMALL = ["tiny", "tiny_biased", "small_shared", "small_capacity", "small_top1", "wide_router",
-         "odd_shapes", "dense_n1", "all_experts", "all_dropped"]
+         "odd_shapes", "dense_n1", "all_experts", "all_dropped", "many_experts"]
 FULL_EXACT = ["moelayer", "mixtral_decode", "deepseek_decode"]
 FULL_SAMPLED = ["mixtral_prefill", "switch_capacity", "deepseek_prefill"]
 
