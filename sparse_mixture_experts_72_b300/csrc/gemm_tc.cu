@@ -10,37 +10,55 @@
 // §3.1's Linear(H, 4H) -> GELU -> Linear(4H, H); the weighting by the
 // renormalised gate score is its output[mask] += score * expert_output.
 //
-// Structure (one persistent CTA per SM, 320 threads):
-//   warp 0      TMA producer: A tile 128 x 64 and B tile 256 x 64 per stage,
-//               4-stage ring of full/empty mbarriers
-//   warp 1      TMEM allocator and single-thread MMA issuer:
-//               tcgen05.mma kind::f16, M=128 N=256 K=16, fp32 accumulators in
-//               TMEM, double-buffered (2 x 256 columns)
-//   warps 2..9  epilogue: tcgen05.ld -> bias -> GELU or scale -> bf16 stores;
-//               warp w reads TMEM lanes 32*(w%4).. and column half (w-2)/4
+// Two shapes of the same persistent, warp-specialised kernel (576 threads):
+//
+//   PAIR = 1  one CTA per tile of 128 rows x 256 columns: A tile 128 x 64 and
+//             B tile 256 x 64 per stage, 4 stages; tcgen05.mma.cta_group::1,
+//             M = 128.  Used when experts hold few rows (decode batches).
+//   PAIR = 2  a cluster of two CTAs per tile of 256 rows x 256 columns:
+//             each CTA loads its own 128 rows of A and 128 rows of B per
+//             stage (32 KB, 6 stages), the even CTA issues
+//             tcgen05.mma.cta_group::2 with M = 256 over both CTAs' shared
+//             memory, and each CTA's TMEM receives its 128 rows.  Two thirds
+//             of the shared-memory bytes per FLOP of PAIR = 1, so the same
+//             ring hides 1.5x more load latency.
+//
+// Roles: warp 0 TMA producer; warp 1 TMEM allocator and single-thread MMA
+// issuer (even CTA only for PAIR = 2) into one of two 256-column fp32
+// accumulators; warps 2..17 epilogue (tcgen05.ld -> bias -> GELU or scale ->
+// bf16 stores; warp w reads TMEM lanes 32*(w%4).. and the 64-column slice
+// (w-2)/4 of the tile).
 // Tiles are ordered expert-major, then output block, then row block, so the
-// CTAs working at one time share the same weight slab through L2.
-// Every wait is bounded: on expiry the CTA records MOE_ERR_TIMEOUT, drains
-// its in-flight copies and MMAs, frees TMEM and exits.
+// CTAs working at one time share one weight slab through L2.
+// Every wait is bounded: on expiry the CTA records MOE_ERR_TIMEOUT, lets its
+// in-flight copies land, drains its MMAs, frees TMEM and exits.
 #include "common.cuh"
 #include "kernels.cuh"
 
 namespace moe {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = BN * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int EPI_WARPS = 8;
+constexpr int BK = 64, BN = 256;
+constexpr int EPI_WARPS = 16;               // 4 per TMEM lane quarter, 64 columns each
+constexpr int EPI_COLS = BN / (EPI_WARPS / 4);
 constexpr int GEMM_THREADS = 64 + EPI_WARPS * 32;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int MAX_GROUPS = MOE_MAX_EXPERTS;
-constexpr int NUM_BARS = 2 * STAGES + 5;
-constexpr int SMEM_TILES = STAGES * STAGE_BYTES;
-constexpr int SMEM_BYTES =
-    1024 + SMEM_TILES + NUM_BARS * 8 + 16 + 2 * (MAX_GROUPS + 1) * 4;
-static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+constexpr int A_BYTES = 128 * BK * 2;  // 128 rows of A per CTA and stage
 constexpr long long kDrainLimitCycles = 200000000LL;  // ~0.1 s
+
+template <int PAIR>
+struct GemmShape {
+  static constexpr int TILE_M = 128 * PAIR;              // rows per tile (whole pair)
+  static constexpr int B_ROWS = BN / PAIR;               // B rows each CTA loads
+  static constexpr int B_BYTES = B_ROWS * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // per CTA
+  static constexpr int STAGES = PAIR == 2 ? 6 : 4;
+  static constexpr int NUM_BARS = 2 * STAGES + 5;
+  static constexpr int SMEM_TILES = STAGES * STAGE_BYTES;
+  static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + NUM_BARS * 8 + 16 +
+                                    2 * (MAX_GROUPS + 1) * 4 + 16 + EPI_WARPS * EPI_COLS * 2;
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
 
 // Wait used only while draining after an abort: ignores the abort flag.
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
@@ -51,44 +69,53 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
   return true;
 }
 
+template <int TILE_M>
 struct TileCursor {
   int g = 0;
   __device__ __forceinline__ void locate(int tile, const int32_t* tile_start, const int32_t* seg,
-                                         int n_out, int& a_row, int& rows_left, int& m, int& n) {
+                                         int& a_row, int& rows_left, int& n) {
     while (tile >= tile_start[g + 1]) ++g;
     const int local = tile - tile_start[g];
     const int rows = seg[g + 1] - seg[g];
-    const int mt = (rows + BM - 1) / BM;
+    const int mt = (rows + TILE_M - 1) / TILE_M;
     n = local / mt;
-    m = local - n * mt;
-    a_row = seg[g] + m * BM;
-    rows_left = rows - m * BM;
-    (void)n_out;
+    const int m = local - n * mt;
+    a_row = seg[g] + m * TILE_M;
+    rows_left = rows - m * TILE_M;
   }
 };
 
+template <int PAIR>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
+  using S = GemmShape<PAIR>;
+  constexpr int STAGES = S::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sA = smem_u32(smem);
   const uint32_t sB = sA + STAGES * A_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SMEM_TILES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::SMEM_TILES);
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
   const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + S::NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int32_t* seg = reinterpret_cast<int32_t*>(tmem_holder + 4);   // [G+1] row offsets
   int32_t* tile_start = seg + (MAX_GROUPS + 1);                 // [G+1] tile prefix
+  uint16_t* bias_stage = reinterpret_cast<uint16_t*>(  // [EPI_WARPS][EPI_COLS], 16-B aligned
+      (reinterpret_cast<uintptr_t>(tile_start + (MAX_GROUPS + 1)) + 15) & ~static_cast<uintptr_t>(15));
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
+  const uint32_t rank = PAIR == 2 ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int unit = PAIR == 2 ? (int)cluster_id_x() : (int)blockIdx.x;   // pair (or CTA) index
+  const int units = PAIR == 2 ? (int)num_clusters_x() : (int)gridDim.x;
   const int G = args.num_groups;
   const int n_out = args.n_out;
   const int n_tiles = (n_out + BN - 1) / BN;
@@ -105,7 +132,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), EPI_WARPS);
+      mbar_init(tempty_bar(a), EPI_WARPS * PAIR);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -116,8 +143,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     tma_prefetch_desc(&tmB);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_holder), TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (PAIR == 2) {
+      tmem_alloc_pair(smem_u32(tmem_holder), TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_holder), TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   __syncthreads();  // seg[] visible
   if (warp == 2) {
@@ -126,7 +158,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const int g0 = lane * per;
     int local = 0;
     for (int g = g0; g < g0 + per && g < G; ++g)
-      local += ((seg[g + 1] - seg[g] + BM - 1) / BM) * n_tiles;
+      local += ((seg[g + 1] - seg[g] + S::TILE_M - 1) / S::TILE_M) * n_tiles;
     int incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -136,12 +168,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     int run = incl - local;
     for (int g = g0; g < g0 + per && g < G; ++g) {
       tile_start[g] = run;
-      run += ((seg[g + 1] - seg[g] + BM - 1) / BM) * n_tiles;
+      run += ((seg[g + 1] - seg[g] + S::TILE_M - 1) / S::TILE_M) * n_tiles;
     }
     if (lane == 31) tile_start[G] = incl;
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR == 2) {
+    cluster_sync_all();  // barriers of both CTAs initialised before any cross-CTA use
+  } else {
+    __syncthreads();
+  }
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   const int total = tile_start[G];
@@ -153,19 +189,28 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       uint32_t stage = 0, phase = 0;
       long long issued = 0;
       bool ok = true;
-      TileCursor cur;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        int a_row, rows_left, m, n;
-        cur.locate(tile, tile_start, seg, n_out, a_row, rows_left, m, n);
-        const int b_row = cur.g * n_out + n * BN;
+      TileCursor<S::TILE_M> cur;
+      for (int tile = unit; tile < total && ok; tile += units) {
+        int a_row, rows_left, n;
+        cur.locate(tile, tile_start, seg, a_row, rows_left, n);
+        const int b_row = cur.g * n_out + n * BN + (int)rank * S::B_ROWS;
+        const int a_row_cta = a_row + (int)rank * 128;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, status)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES);
-          tma_load_2d(sA + stage * A_BYTES, &tmA, full_bar(stage), kb * BK, a_row);
-          tma_load_2d(sB + stage * B_BYTES, &tmB, full_bar(stage), kb * BK, b_row);
+          if constexpr (PAIR == 2) {
+            // both CTAs' copies complete on the even CTA's full barrier
+            const uint32_t fb = mapa_shared(full_bar(stage), 0);
+            if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * S::STAGE_BYTES);
+            tma_load_2d_pair(sA + stage * A_BYTES, &tmA, fb, kb * BK, a_row_cta);
+            tma_load_2d_pair(sB + stage * S::B_BYTES, &tmB, fb, kb * BK, b_row);
+          } else {
+            mbar_arrive_expect_tx(full_bar(stage), S::STAGE_BYTES);
+            tma_load_2d(sA + stage * A_BYTES, &tmA, full_bar(stage), kb * BK, a_row_cta);
+            tma_load_2d(sB + stage * S::B_BYTES, &tmB, full_bar(stage), kb * BK, b_row);
+          }
           ++issued;
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -175,11 +220,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc = idesc_bf16_f32(128 * PAIR, BN);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      for (int tile = unit; tile < total && ok; tile += units) {
         if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, status)) {
           ok = false;
           break;
@@ -193,17 +238,23 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           }
           tc_fence_after();
           const uint64_t adesc = sdesc_kmajor_sw128(sA + stage * A_BYTES);
-          const uint64_t bdesc = sdesc_kmajor_sw128(sB + stage * B_BYTES);
+          const uint64_t bdesc = sdesc_kmajor_sw128(sB + stage * S::B_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             // +32 bytes along K per step of 16 bf16 inside the 128-byte swizzle atom
-            umma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+            const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
+            if constexpr (PAIR == 2)
+              umma_bf16_pair(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, accum);
+            else
+              umma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, accum);
           }
-          umma_commit(empty_bar(stage));
+          if constexpr (PAIR == 2) umma_commit_pair_mc(empty_bar(stage), 0x3);
+          else umma_commit(empty_bar(stage));
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        umma_commit(tfull_bar(acc));
+        if constexpr (PAIR == 2) umma_commit_pair_mc(tfull_bar(acc), 0x3);
+        else umma_commit(tfull_bar(acc));
         acc ^= 1u;
         if (acc == 0) acc_phase ^= 1u;
       }
@@ -211,74 +262,100 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;            // TMEM lane quarter this warp may access
-    const int h = (warp - 2) >> 2;     // column half of the 256-wide tile
+    const int q = warp & 3;                  // TMEM lane quarter this warp may access
+    const int cpart = (warp - 2) >> 2;       // which EPI_COLS-wide column slice of the tile
     const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+    const int warp_row0 = (int)rank * 128 + q * 32;  // first tile row of this warp
+    uint16_t* my_bias = bias_stage + (warp - 2) * EPI_COLS;
     uint32_t acc = 0, acc_phase = 0;
-    TileCursor cur;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      int a_row, rows_left, m, n;
-      cur.locate(tile, tile_start, seg, n_out, a_row, rows_left, m, n);
+    TileCursor<S::TILE_M> cur;
+    for (int tile = unit; tile < total; tile += units) {
+      int a_row, rows_left, n;
+      cur.locate(tile, tile_start, seg, a_row, rows_left, n);
+      const int r_in = warp_row0 + lane;
+      const bool row_ok = r_in < rows_left;
+      const int64_t out_row = (int64_t)a_row + r_in;
+      const int col0 = n * BN + cpart * EPI_COLS;     // first column of this warp's slice
+      // everything that does not need the accumulator is fetched before waiting
+      float wscale = 1.0f;
+      if (args.mode == EPI_SCALE && args.topk_w != nullptr && row_ok)
+        wscale = args.topk_w[args.perm[out_row]];
+      const bool has_bias = args.bias != nullptr;
+      if (has_bias) {
+        // EPI_COLS (64) columns: 2 per lane
+        const int c2 = col0 + lane * 2;
+        uint32_t b = 0u;
+        if (c2 < n_out) b = __ldg(reinterpret_cast<const uint32_t*>(args.bias + (size_t)cur.g * n_out + c2));
+        *reinterpret_cast<uint32_t*>(my_bias + lane * 2) = b;
+        __syncwarp();
+      }
       int ok = 1;
       if (lane == 0) ok = mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, status) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      const int r_in = q * 32 + lane;
-      const bool row_ok = r_in < rows_left;
-      const int64_t out_row = (int64_t)a_row + r_in;
-      float wscale = 1.0f;
-      if (args.mode == EPI_SCALE && args.topk_w != nullptr && row_ok)
-        wscale = args.topk_w[args.perm[out_row]];
-      const __nv_bfloat16* bias = args.bias ? args.bias + (size_t)cur.g * n_out : nullptr;
       __nv_bfloat16* orow = args.out + out_row * args.ld_out;
+      const bool warp_has_rows = warp_row0 < rows_left;     // warp-uniform
+      const bool full_cols = col0 + EPI_COLS <= n_out;      // warp-uniform
+      if (warp_has_rows && col0 < n_out) {
+        const uint32_t taddr = tmem_base + lane_addr + acc * BN + cpart * EPI_COLS;
 #pragma unroll 1
-      for (int c = 0; c < (BN / 2) / 32; ++c) {
-        const int tcol = h * (BN / 2) + c * 32;  // column inside the tile
-        const int col = n * BN + tcol;           // column inside the group's n_out
-        if (col >= n_out) break;                 // warp-uniform
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tmem_base + lane_addr + acc * BN + tcol, r);
-        tmem_ld_wait();
-        float v[32];
+        for (int c = 0; c < 2; ++c) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(taddr + c * 32, r);
+          tmem_ld_wait();
+          float v[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-        if (bias) {
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+          if (has_bias) {
 #pragma unroll
-          for (int j8 = 0; j8 < 4; ++j8) {
-            if (col + 8 * j8 < n_out) {
-              const uint4 u = __ldg(reinterpret_cast<const uint4*>(bias + col + 8 * j8));
+            for (int j8 = 0; j8 < 4; ++j8) {
+              const uint4 u = *reinterpret_cast<const uint4*>(my_bias + c * 32 + 8 * j8);
               v[8 * j8 + 0] += bf16lo(u.x); v[8 * j8 + 1] += bf16hi(u.x);
               v[8 * j8 + 2] += bf16lo(u.y); v[8 * j8 + 3] += bf16hi(u.y);
               v[8 * j8 + 4] += bf16lo(u.z); v[8 * j8 + 5] += bf16hi(u.z);
               v[8 * j8 + 6] += bf16lo(u.w); v[8 * j8 + 7] += bf16hi(u.w);
             }
           }
-        }
-        if (args.mode == EPI_GELU) {
+          if (args.mode == EPI_GELU) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
-        } else {
+            for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
+          } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] *= wscale;
-        }
-        if (row_ok) {
+            for (int i = 0; i < 32; ++i) v[i] *= wscale;
+          }
+          uint4 o[4];
 #pragma unroll
           for (int j8 = 0; j8 < 4; ++j8) {
-            if (col + 8 * j8 < n_out) {
-              uint4 o;
-              o.x = pack_bf16x2(v[8 * j8 + 0], v[8 * j8 + 1]);
-              o.y = pack_bf16x2(v[8 * j8 + 2], v[8 * j8 + 3]);
-              o.z = pack_bf16x2(v[8 * j8 + 4], v[8 * j8 + 5]);
-              o.w = pack_bf16x2(v[8 * j8 + 6], v[8 * j8 + 7]);
-              *reinterpret_cast<uint4*>(orow + col + 8 * j8) = o;
+            o[j8].x = pack_bf16x2(v[8 * j8 + 0], v[8 * j8 + 1]);
+            o[j8].y = pack_bf16x2(v[8 * j8 + 2], v[8 * j8 + 3]);
+            o[j8].z = pack_bf16x2(v[8 * j8 + 4], v[8 * j8 + 5]);
+            o[j8].w = pack_bf16x2(v[8 * j8 + 6], v[8 * j8 + 7]);
+          }
+          const int col = col0 + c * 32;
+          uint4* dst = reinterpret_cast<uint4*>(orow + col);
+          if (row_ok) {
+            if (full_cols) {
+#pragma unroll
+              for (int j8 = 0; j8 < 4; ++j8) dst[j8] = o[j8];
+            } else {
+#pragma unroll
+              for (int j8 = 0; j8 < 4; ++j8)
+                if (col + 8 * j8 < n_out) dst[j8] = o[j8];
             }
           }
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar(acc));
+      if (lane == 0) {
+        if constexpr (PAIR == 2) {
+          if (leader) mbar_arrive(tempty_bar(acc));
+          else mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
+        } else {
+          mbar_arrive(tempty_bar(acc));
+        }
+      }
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }
@@ -289,23 +366,38 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   if (*abort_flag) {
-    // Some role gave up, so copies or MMAs may still be in flight.  Let the
-    // copies (at most the last STAGES issued) land and the MMAs finish
-    // before the shared memory and TMEM go away.
+    // Some role gave up, so copies or MMAs may still be in flight.  Let them
+    // land / finish before shared memory and TMEM go away.
     if (warp == 0 && lane == 0) {
-      const long long first = tma_issued > STAGES ? tma_issued - STAGES : 0;
-      for (long long j = first; j < tma_issued; ++j)
-        mbar_wait_drain(full_bar((int)(j % STAGES)), (uint32_t)((j / STAGES) & 1));
+      if (PAIR == 1 || leader) {
+        // the full barriers count every byte issued to this CTA's ring
+        const long long first = tma_issued > STAGES ? tma_issued - STAGES : 0;
+        for (long long j = first; j < tma_issued; ++j)
+          mbar_wait_drain(full_bar((int)(j % STAGES)), (uint32_t)((j / STAGES) & 1));
+      } else {
+        // the odd CTA's copies complete on its peer's barriers: give them a
+        // bounded grace period (they land within microseconds)
+        const long long t0 = clock64();
+        while (clock64() - t0 < 4000000LL) {
+        }
+      }
     }
-    if (warp == 1 && lane == 0) {
-      umma_commit(drain_bar);
+    if (warp == 1 && lane == 0 && leader) {
+      if constexpr (PAIR == 2) umma_commit_pair_mc(drain_bar, 0x1);
+      else umma_commit(drain_bar);
       mbar_wait_drain(drain_bar, 0);
     }
     __syncwarp();
   }
+  if constexpr (PAIR == 2) {
+    // neither CTA leaves while its peer may still touch its shared memory,
+    // barriers or TMEM
+    cluster_sync_all();
+  }
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    if constexpr (PAIR == 2) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    else tmem_dealloc(tmem_base, TMEM_COLS);
   }
 }
 
@@ -352,25 +444,65 @@ cudaError_t make_gemm_plan(GemmPlan* plan, const __nv_bfloat16* A, int64_t a_row
                            const __nv_bfloat16* B, int64_t b_rows, const GemmArgs& args,
                            int num_sms) {
   if (a_rows <= 0 || b_rows <= 0 || args.K <= 0 || args.n_out <= 0) return cudaErrorInvalidValue;
-  if (!encode_tensor_map_bf16(&plan->tmA, A, a_rows, args.K, BK, BM)) return cudaErrorInvalidValue;
-  if (!encode_tensor_map_bf16(&plan->tmB, B, b_rows, args.K, BK, BN)) return cudaErrorInvalidValue;
+  // CTA pairs (256-row tiles) once the average group holds enough rows to
+  // fill them; single CTAs (128-row tiles) for decode-sized groups.
+  const int64_t avg_rows = a_rows / (args.num_groups > 0 ? args.num_groups : 1);
+  const int pair = (avg_rows >= 192 && num_sms >= 2) ? 2 : 1;
+  if (!encode_tensor_map_bf16(&plan->tmA, A, a_rows, args.K, BK, 128)) return cudaErrorInvalidValue;
+  if (!encode_tensor_map_bf16(&plan->tmB, B, b_rows, args.K, BK, BN / pair))
+    return cudaErrorInvalidValue;
   plan->args = args;
+  plan->pair = pair;
+  const int64_t tile_m = 128 * pair;
   const int64_t n_tiles = (args.n_out + BN - 1) / BN;
-  const int64_t max_tiles = ((a_rows + BM - 1) / BM + args.num_groups) * n_tiles;
-  plan->grid = (int)(max_tiles < num_sms ? max_tiles : num_sms);
+  const int64_t max_tiles = ((a_rows + tile_m - 1) / tile_m + args.num_groups) * n_tiles;
+  const int64_t max_units = num_sms / pair;
+  const int64_t units = max_tiles < max_units ? max_tiles : max_units;
+  plan->grid = (int)(units * pair);
   return cudaSuccess;
 }
 
-cudaError_t launch_gemm(const GemmPlan& plan, cudaStream_t st, LaunchTrace* tr) {
+template <int PAIR>
+static cudaError_t launch_gemm_t(const GemmPlan& plan, cudaStream_t st) {
+  using S = GemmShape<PAIR>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<PAIR>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         S::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(plan.grid);
+  cfg.blockDim = dim3(GEMM_THREADS);
+  cfg.dynamicSmemBytes = S::SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = PAIR;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (PAIR == 2) {
+    // a persistent grid must fit at once: no more pairs than can be co-resident
+    static int max_clusters = -1;
+    if (max_clusters < 0) {
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<PAIR>, &cfg) != cudaSuccess || n <= 0)
+        n = 1;
+      max_clusters = n;
+    }
+    if ((int)cfg.gridDim.x > 2 * max_clusters) cfg.gridDim.x = 2 * max_clusters;
+  }
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<PAIR>, plan.tmA, plan.tmB, plan.args);
+}
+
+cudaError_t launch_gemm(const GemmPlan& plan, cudaStream_t st, LaunchTrace* tr) {
   trace_mark(tr, st);
-  grouped_gemm_kernel<<<plan.grid, GEMM_THREADS, SMEM_BYTES, st>>>(plan.tmA, plan.tmB, plan.args);
+  cudaError_t e = plan.pair == 2 ? launch_gemm_t<2>(plan, st) : launch_gemm_t<1>(plan, st);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

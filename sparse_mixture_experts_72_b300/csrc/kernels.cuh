@@ -116,9 +116,10 @@ struct GemmArgs {
 
 struct GemmPlan {
   CUtensorMap tmA;  // A [rows, K] bf16, box 64 x 128, 128B swizzle
-  CUtensorMap tmB;  // B [G * n_out, K] bf16, box 64 x 256, 128B swizzle
+  CUtensorMap tmB;  // B [G * n_out, K] bf16, box 64 x (256 / pair), 128B swizzle
   GemmArgs args;
   int grid;
+  int pair;         // 1: one CTA per 128-row tile; 2: a CTA pair per 256-row tile
 };
 
 // Encodes the tensor maps; returns cudaErrorInvalidValue if encoding fails.
