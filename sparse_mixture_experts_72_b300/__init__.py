@@ -24,6 +24,7 @@ __all__ = ["MoEConfig", "MoEWeights", "MoeError", "moe_workspace_size", "moe_max
            "moe_capacity", "moe_forward_num_launches", "moe_route", "moe_permute",
            "moe_permute_static",
            "moe_expert_ffn", "moe_combine", "moe_forward", "moe_workspace_status",
+           "MoEForwardGraph", "alloc_outputs",
            "make_workspace", "library_path", "MOE_TRACE_MAX_EVENTS"]
 
 
@@ -287,6 +288,45 @@ def moe_forward(cfg: MoEConfig, weights: MoEWeights, x, *, out=None, outputs: Op
                         C.byref(oc) if oc is not None else None, wsp, wsn, _stream(stream), ev)
     check(st, "moe_forward")
     return out
+
+
+class MoEForwardGraph:
+    """One moe_forward over fixed buffers, captured into a CUDA graph.
+
+    The launch sequence, its kernel arguments (including the TMA tensor
+    maps) and the buffers are frozen at capture; replay() re-runs the whole
+    layer with one graph launch, reading whatever x holds at that time and
+    writing out / outputs / ws in place.  A warm-up call before the capture
+    sets kernel attributes and fills the library's per-device caches."""
+
+    def __init__(self, cfg: MoEConfig, weights: MoEWeights, x, out, outputs=None, ws=None,
+                 trace_events=None):
+        self.cfg, self.x, self.out, self.outputs = cfg, x, out, outputs
+        self.ws = ws if ws is not None else make_workspace(cfg, x.device)
+        self.weights_c = weights.c(cfg)
+        self._run()
+        torch.cuda.synchronize()
+        if trace_events is not None:
+            for e in trace_events:  # create the lazily made torch events outside the capture
+                e.record()
+            torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            # with trace_events the graph also carries one event-record node
+            # before each launch and one after the last
+            self._run(trace_events)
+        torch.cuda.synchronize()
+
+    def _run(self, trace_events=None):
+        moe_forward(self.cfg, None, self.x, out=self.out, outputs=self.outputs, ws=self.ws,
+                    weights_c=self.weights_c, trace_events=trace_events)
+
+    def replay(self):
+        self.graph.replay()
+
+    def run_eager(self, trace_events=None):
+        """The same forward launched directly (optionally with per-launch events)."""
+        self._run(trace_events)
 
 
 def moe_workspace_status(ws: torch.Tensor, stream=None) -> int:

@@ -15,10 +15,17 @@ struct LaunchTrace {
   int next;
 };
 
+// While the stream is being captured into a CUDA graph the events become
+// event-record nodes of the graph (so replays carry the timestamps).
 inline void trace_mark(LaunchTrace* tr, cudaStream_t st) {
   if (tr && tr->events && tr->next < tr->n_events) {
     cudaEvent_t e = tr->events[tr->next++];
-    if (e) cudaEventRecord(e, st);
+    if (!e) return;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+      cudaEventRecordWithFlags(e, st, cudaEventRecordExternal);
+    else
+      cudaEventRecord(e, st);
   }
 }
 
@@ -49,12 +56,25 @@ struct RouterTcArgs {
   int32_t* topk_idx;
   float* topk_w;
   float* probs;     // nullable
-  float* p_part;    // [ceil(T/128), N]
+  float* p_part;    // [m_tiles * splits, N] per-CTA column sums of P
   float* p_mean;
-  int* ticket;      // zero on entry; reset to zero by the last CTA
+  int* ticket;      // CTAs done; zero on entry
   int* status;
   int T, N, N_pad, H_pad, k, tmem_cols;
+  int stacked;           // 1: planes stacked along N; 0: planes along K
+  int nacc;              // independent TMEM accumulators
+  int planes_per_stage;  // planes along K: B tiles per stage (1 or 3)
+  int stages;
+  int kb_per_split;      // x tiles (64 wide) per K split
+  int splits;            // K splits = cluster size (1, 2, 4 or 8)
+  int work_bytes;        // ring / logits-tile shared memory
 };
+struct RouterTcPlan {
+  int N_pad, H_pad, stacked, pp, nacc, tmem_cols, stage_bytes, stages, m_tiles, splits,
+      kb_per_split, work_bytes, smem;
+};
+RouterTcPlan router_tc_plan(int T, int N, int H);
+int router_tc_num_ctas(int T, int N, int H);
 inline size_t router_w3_bytes(int N, int H) {
   const size_t N_pad = (N + 15) / 16 * 16, H_pad = (H + 63) / 64 * 64;
   return N_pad * 3 * H_pad * 2;

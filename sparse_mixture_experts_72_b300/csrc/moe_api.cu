@@ -35,7 +35,7 @@ int64_t max_rows_of(const moe_config_t& c) {
 }
 
 struct WsLayout {
-  size_t status, w3, logits, p_part, local_rank, blk_hist, blk_base;
+  size_t status, status_bytes, w3, logits, p_part, local_rank, blk_hist, blk_base;
   size_t topk_idx, topk_w, p_mean, counts, offsets, perm, inv, f, l_aux;
   size_t xp, hid, y, hid_s, y_s;
   size_t total;
@@ -48,11 +48,14 @@ WsLayout layout_of(const moe_config_t& c) {
   const int64_t nblk = permute_num_blocks(A);
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o += align_up(bytes > 0 ? bytes : 1); return at; };
-  L.status = take(16);  // [0] status word, [1] router ticket
+  // [0] status word, [1] router ticket
+  L.status_bytes = 16;
+  L.status = take(L.status_bytes);
   const bool tc = c.N <= kRouterTcMaxExperts;
   L.w3 = take(tc ? router_w3_bytes(c.N, c.H) : 0);
   L.logits = take(tc ? 0 : sizeof(float) * T * N);
-  L.p_part = take(sizeof(float) * (nsel > 0 ? nsel : 1) * N);
+  const int64_t pblocks = tc ? router_tc_num_ctas(c.T, c.N, c.H) : nsel;
+  L.p_part = take(sizeof(float) * (pblocks > 0 ? pblocks : 1) * N);
   L.local_rank = take(sizeof(int32_t) * A);
   L.blk_hist = take(sizeof(int32_t) * (nblk > 0 ? nblk : 1) * N);
   L.blk_base = take(sizeof(int32_t) * (nblk > 0 ? nblk : 1) * N);
@@ -152,7 +155,7 @@ T* at(void* ws, size_t off) {
 
 moe_status_t clear_status(void* ws, const WsLayout& L, cudaStream_t st, LaunchTrace* tr) {
   trace_mark(tr, st);
-  return cuda_status(cudaMemsetAsync(at<int>(ws, L.status), 0, 4 * sizeof(int), st));
+  return cuda_status(cudaMemsetAsync(at<int>(ws, L.status), 0, L.status_bytes, st));
 }
 
 // ---------------------------------------------------------------- stages
