@@ -159,17 +159,23 @@ def algorithmic_work(w: wl.Workload, counts: np.ndarray, R: int):
 
 
 def launch_names(w: wl.Workload, has_rows: bool):
-    names = ["status_memset"]
-    if w.N <= 256:  # tensor-core router: W_g split + fused router
+    """Names of the launches moe_forward makes, in order (the status clear is
+    folded into the tensor-core router's first kernel, and the dispatch
+    scatter also gathers the expert rows)."""
+    names = []
+    tc_router = w.N <= 256
+    if not (tc_router and w.T > 0):
+        names += ["status_memset"]
+    if tc_router:  # tensor-core router: W_g split + fused router
         names += ["router_split", "router_tc"] if w.T > 0 else ["p_mean_memset"]
     else:
         names += ["router_logits", "router_select", "router_pmean"] if w.T > 0 else ["router_pmean"]
     if w.T * w.k > 0:
-        names += ["permute_rank", "permute_scan", "permute_scatter"]
+        names += ["permute_rank", "permute_scan", "scatter_gather"]
     else:
         names += ["permute_scan"]
     if has_rows:
-        names += ["gather", "gemm1", "gemm2"]
+        names += ["gemm1", "gemm2"]
     if w.F_shared:
         names += ["gemm1_shared", "gemm2_shared"]
     if w.T > 0:

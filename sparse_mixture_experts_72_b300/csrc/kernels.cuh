@@ -79,8 +79,10 @@ inline size_t router_w3_bytes(int N, int H) {
   const size_t N_pad = (N + 15) / 16 * 16, H_pad = (H + 63) / 64 * 64;
   return N_pad * 3 * H_pad * 2;
 }
+// `clear` (nullable, clear_n ints) is zeroed by the first kernel of the
+// router, before the router kernel itself runs.
 cudaError_t launch_router_tc(const RouterLaunch& a, __nv_bfloat16* W3, int* ticket, int* status,
-                             cudaStream_t st, LaunchTrace* tr);
+                             int* clear, int clear_n, cudaStream_t st, LaunchTrace* tr);
 
 // TMA map of a row-major bf16 matrix [rows, K], box 64 (K) x box_rows, 128B swizzle
 bool encode_tensor_map_bf16(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
@@ -102,6 +104,10 @@ struct PermuteLaunch {
   int T, N, k;
   int64_t capacity;     // < 0: no limit
   float alpha;
+  // optional fused gather: xp[row] = x[perm[row] / k] for every kept row
+  const __nv_bfloat16* x = nullptr;
+  __nv_bfloat16* xp = nullptr;
+  int H = 0;
 };
 constexpr int kPermuteChunk = 256;  // assignments per block
 inline int permute_num_blocks(int64_t A) { return (int)((A + kPermuteChunk - 1) / kPermuteChunk); }

@@ -159,6 +159,17 @@ moe_status_t clear_status(void* ws, const WsLayout& L, cudaStream_t st, LaunchTr
 }
 
 // ---------------------------------------------------------------- stages
+// The tensor-core router's first kernel can zero the status header itself.
+bool router_clears_status(const moe_config_t& c) { return c.N <= kRouterTcMaxExperts && c.T > 0; }
+
+// Zeroes the status word and router ticket, unless the router's first kernel
+// does it (router_clears_status).
+moe_status_t begin_call(const moe_config_t& c, void* ws, const WsLayout& L, cudaStream_t st,
+                        LaunchTrace* tr) {
+  if (router_clears_status(c)) return MOE_OK;
+  return clear_status(ws, L, st, tr);
+}
+
 moe_status_t do_route(const moe_config_t& c, const uint16_t* x, const float* Wg, const float* bg,
                       const float* sel, int32_t* idx, float* w, float* probs, float* p_mean,
                       void* ws, const WsLayout& L, cudaStream_t st, LaunchTrace* tr) {
@@ -178,15 +189,17 @@ moe_status_t do_route(const moe_config_t& c, const uint16_t* x, const float* Wg,
   a.N = c.N;
   a.k = c.k;
   if (c.N <= kRouterTcMaxExperts)
-    return cuda_status(launch_router_tc(a, at<__nv_bfloat16>(ws, L.w3), at<int>(ws, L.status) + 1,
-                                        at<int>(ws, L.status), st, tr));
+    return cuda_status(launch_router_tc(
+        a, at<__nv_bfloat16>(ws, L.w3), at<int>(ws, L.status) + 1, at<int>(ws, L.status),
+        router_clears_status(c) ? at<int>(ws, L.status) : nullptr, (int)(L.status_bytes / 4), st,
+        tr));
   return cuda_status(launch_router(a, st, tr));
 }
 
 moe_status_t do_permute(const moe_config_t& c, const int32_t* idx, const float* p_mean,
                         int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv, float* f,
                         float* l_aux, void* ws, const WsLayout& L, cudaStream_t st,
-                        LaunchTrace* tr) {
+                        LaunchTrace* tr, const uint16_t* gather_x = nullptr) {
   PermuteLaunch a;
   a.topk_idx = idx;
   a.p_mean = p_mean;
@@ -204,21 +217,27 @@ moe_status_t do_permute(const moe_config_t& c, const int32_t* idx, const float* 
   a.k = c.k;
   a.capacity = capacity_of(c);
   a.alpha = c.aux_alpha;
+  if (gather_x && max_rows_of(c) > 0) {
+    a.x = reinterpret_cast<const __nv_bfloat16*>(gather_x);
+    a.xp = at<__nv_bfloat16>(ws, L.xp);
+    a.H = c.H;
+  }
   return cuda_status(launch_permute(a, st, tr));
 }
 
 moe_status_t do_ffn(const moe_config_t& c, const uint16_t* x, const int32_t* perm,
                     const int32_t* offsets, const float* topk_w, const moe_weights_t& W,
                     uint16_t* y, uint16_t* y_shared, void* ws, const WsLayout& L, int sms,
-                    cudaStream_t st, LaunchTrace* tr) {
+                    cudaStream_t st, LaunchTrace* tr, bool gathered = false) {
   using bf = __nv_bfloat16;
   const int64_t R = max_rows_of(c);
   int* status = at<int>(ws, L.status);
   if (R > 0) {
     bf* xp = at<bf>(ws, L.xp);
     bf* hid = at<bf>(ws, L.hid);
-    MOE_CUDA(launch_gather(reinterpret_cast<const bf*>(x), perm, offsets, c.N, c.k, R, c.H, xp,
-                           st, tr));
+    if (!gathered)
+      MOE_CUDA(launch_gather(reinterpret_cast<const bf*>(x), perm, offsets, c.N, c.k, R, c.H, xp,
+                             st, tr));
     GemmArgs g1{};
     g1.offsets = offsets;
     g1.num_groups = c.N;
@@ -287,9 +306,9 @@ moe_status_t do_ffn(const moe_config_t& c, const uint16_t* x, const int32_t* per
   return MOE_OK;
 }
 
-int ffn_num_launches(const moe_config_t& c) {
+int ffn_num_launches(const moe_config_t& c, bool gathered) {
   int n = 0;
-  if (max_rows_of(c) > 0) n += 3;
+  if (max_rows_of(c) > 0) n += gathered ? 2 : 3;
   if (c.F_shared > 0 && c.T > 0) n += 2;
   return n;
 }
@@ -335,10 +354,10 @@ MOE_API int64_t moe_capacity(const moe_config_t* cfg) {
 MOE_API int32_t moe_forward_num_launches(const moe_config_t* cfg) {
   if (check_config(cfg) != MOE_OK) return -1;
   const moe_config_t& c = *cfg;
-  int n = 1;  // status clear
+  int n = router_clears_status(c) ? 0 : 1;  // status clear
   n += router_num_launches(c.T, c.N);
-  n += permute_num_launches(c.T, c.k);
-  n += ffn_num_launches(c);
+  n += permute_num_launches(c.T, c.k);      // the scatter also gathers the rows
+  n += ffn_num_launches(c, true);
   if (c.T > 0) n += 1;  // combine
   return n;
 }
@@ -358,7 +377,7 @@ MOE_API moe_status_t moe_route(const moe_config_t* cfg, const uint16_t* x, const
   MOE_TRY(device_info(&d));
   const WsLayout L = layout_of(c);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  MOE_TRY(clear_status(ws, L, st, nullptr));
+  MOE_TRY(begin_call(c, ws, L, st, nullptr));
   return do_route(c, x, Wg, bg, sel_bias, topk_idx, topk_w, probs, p_mean, ws, L, st, nullptr);
 }
 
@@ -455,11 +474,11 @@ MOE_API moe_status_t moe_forward(const moe_config_t* cfg, const moe_weights_t* w
   uint16_t* y = at<uint16_t>(ws, L.y);
   uint16_t* ys = c.F_shared > 0 ? at<uint16_t>(ws, L.y_s) : nullptr;
 
-  MOE_TRY(clear_status(ws, L, st, tr));
+  MOE_TRY(begin_call(c, ws, L, st, tr));
   MOE_TRY(do_route(c, x, weights->Wg, weights->bg, weights->sel_bias, idx, w, o.probs, p_mean, ws,
                    L, st, tr));
-  MOE_TRY(do_permute(c, idx, p_mean, counts, offsets, perm, inv, f, l_aux, ws, L, st, tr));
-  MOE_TRY(do_ffn(c, x, perm, offsets, w, *weights, y, ys, ws, L, d.sms, st, tr));
+  MOE_TRY(do_permute(c, idx, p_mean, counts, offsets, perm, inv, f, l_aux, ws, L, st, tr, x));
+  MOE_TRY(do_ffn(c, x, perm, offsets, w, *weights, y, ys, ws, L, d.sms, st, tr, true));
   if (c.T > 0) {
     using bf = __nv_bfloat16;
     MOE_CUDA(launch_combine(reinterpret_cast<const bf*>(y), inv, reinterpret_cast<const bf*>(ys),

@@ -46,10 +46,13 @@ constexpr int RT_A_BYTES = RT_BM * RT_BK * 2;
 constexpr int kRouterTcSmemMax = 227 * 1024;
 
 // Plane p of W_g: hi, mid, lo with W_g = hi + mid + lo exactly.
+// It also zeroes `clear` (the status word and router ticket of a forward
+// pass), which saves a separate memset launch.
 __global__ void __launch_bounds__(256) router_split_kernel(const float* __restrict__ Wg,
                                                            __nv_bfloat16* __restrict__ W3, int N,
                                                            int H, int N_pad, int H_pad,
-                                                           int stacked) {
+                                                           int stacked, int* clear, int clear_n) {
+  if (clear && blockIdx.x == 0 && threadIdx.x < clear_n) clear[threadIdx.x] = 0;
   const int64_t total = (int64_t)N_pad * H_pad;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -435,7 +438,7 @@ int router_tc_num_ctas(int T, int N, int H) {
 }
 
 cudaError_t launch_router_tc(const RouterLaunch& a, __nv_bfloat16* W3, int* ticket, int* status,
-                             cudaStream_t st, LaunchTrace* tr) {
+                             int* clear, int clear_n, cudaStream_t st, LaunchTrace* tr) {
   const RouterTcPlan P = router_tc_plan(a.T, a.N, a.H);
   if (a.T == 0) {
     trace_mark(tr, st);
@@ -447,7 +450,7 @@ cudaError_t launch_router_tc(const RouterLaunch& a, __nv_bfloat16* W3, int* tick
     if (blocks > 148 * 8) blocks = 148 * 8;
     trace_mark(tr, st);
     router_split_kernel<<<(unsigned)blocks, 256, 0, st>>>(a.Wg, W3, a.N, a.H, P.N_pad, P.H_pad,
-                                                          P.stacked);
+                                                          P.stacked, clear, clear_n);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
