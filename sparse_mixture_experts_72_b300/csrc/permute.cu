@@ -113,30 +113,41 @@ __global__ void __launch_bounds__(256) permute_scatter_kernel(
 }
 
 // The scatter fused with the row gather of the expert GEMMs' A operand: one
-// warp per assignment writes perm / inv and, for a kept assignment, copies
-// x[t] into its expert-contiguous row xp[row] (16-byte vectors across lanes).
+// warp per token writes perm / inv of its k assignments, reads x[t] once and
+// copies it into each kept slot's expert-contiguous row xp[row] (16-byte
+// vectors across lanes).
 __global__ void __launch_bounds__(256) permute_scatter_gather_kernel(
     const int32_t* __restrict__ idx, const int32_t* __restrict__ local_rank,
     const int32_t* __restrict__ blk_base, const int32_t* __restrict__ offsets,
-    int32_t* __restrict__ perm, int32_t* __restrict__ inv, int64_t A, int N, int k,
+    int32_t* __restrict__ perm, int32_t* __restrict__ inv, int T, int N, int k,
     int64_t capacity, const __nv_bfloat16* __restrict__ x, __nv_bfloat16* __restrict__ xp, int H) {
   const int lane = threadIdx.x % 32;
   const int64_t nvec = H / 8;
-  for (int64_t a = (int64_t)blockIdx.x * 8 + threadIdx.x / 32; a < A; a += (int64_t)gridDim.x * 8) {
-    const int e = idx[a];
+  for (int64_t t = (int64_t)blockIdx.x * 8 + threadIdx.x / 32; t < T; t += (int64_t)gridDim.x * 8) {
+    // rows of the token's slots: lane j computes slot j (k <= 32)
     int32_t row = -1;
-    if (e >= 0 && e < N) {
-      const int64_t pos = (int64_t)blk_base[(a / kPermuteChunk) * N + e] + local_rank[a];
-      if (capacity < 0 || pos < capacity) row = offsets[e] + (int32_t)pos;
-    }
-    if (lane == 0) {
+    if (lane < k) {
+      const int64_t a = t * k + lane;
+      const int e = idx[a];
+      if (e >= 0 && e < N) {
+        const int64_t pos = (int64_t)blk_base[(a / kPermuteChunk) * N + e] + local_rank[a];
+        if (capacity < 0 || pos < capacity) row = offsets[e] + (int32_t)pos;
+      }
       inv[a] = row;
       if (row >= 0) perm[row] = (int32_t)a;
     }
-    if (row >= 0) {
-      const uint4* src = reinterpret_cast<const uint4*>(x + (a / k) * H);
-      uint4* dst = reinterpret_cast<uint4*>(xp + (int64_t)row * H);
-      for (int64_t v = lane; v < nvec; v += 32) dst[v] = __ldg(src + v);
+    const unsigned kept_mask = __ballot_sync(0xffffffffu, row >= 0);
+    if (kept_mask == 0u) continue;
+    const uint4* src = reinterpret_cast<const uint4*>(x + t * H);
+    for (int64_t v = lane; v < nvec; v += 32) {
+      const uint4 val = __ldg(src + v);
+      unsigned m = kept_mask;
+      while (m) {
+        const int j = __ffs(m) - 1;
+        m &= m - 1;
+        const int32_t r = __shfl_sync(0xffffffffu, row, j);
+        reinterpret_cast<uint4*>(xp + (int64_t)r * H)[v] = val;
+      }
     }
   }
 }
@@ -163,11 +174,11 @@ cudaError_t launch_permute(const PermuteLaunch& a, cudaStream_t st, LaunchTrace*
   if (err != cudaSuccess || A == 0) return err;
   trace_mark(tr, st);
   if (a.x != nullptr) {
-    int64_t blocks = (A + 7) / 8;
+    int64_t blocks = ((int64_t)a.T + 7) / 8;
     if (blocks > 148 * 16) blocks = 148 * 16;
     permute_scatter_gather_kernel<<<(unsigned)blocks, 256, 0, st>>>(
-        a.topk_idx, a.local_rank, a.blk_base, a.offsets, a.perm, a.inv, A, a.N, a.k, a.capacity,
-        a.x, a.xp, a.H);
+        a.topk_idx, a.local_rank, a.blk_base, a.offsets, a.perm, a.inv, a.T, a.N, a.k,
+        a.capacity, a.x, a.xp, a.H);
   } else {
     permute_scatter_kernel<<<(unsigned)((A + 255) / 256), 256, 0, st>>>(
         a.topk_idx, a.local_rank, a.blk_base, a.offsets, a.perm, a.inv, A, a.N, a.capacity);
