@@ -220,6 +220,18 @@ moe_status_t moe_permute_static(const moe_config_t* cfg, const int32_t* topk_idx
  * (MOE_OK or MOE_ERR_TIMEOUT), or MOE_ERR_CUDA if the synchronisation fails. */
 moe_status_t moe_workspace_status(const void* ws, void* stream);
 
+/* Failure-injection hook for tests; the source pages have no counterpart.
+ * The next `launches` expert-GEMM launches enqueued by this process (by
+ * moe_expert_ffn or moe_forward, on any device) run with their TMA producer
+ * issuing nothing, as if its signals were lost.  The MMA issuer and the
+ * epilogue warps then wait until their bound runs out (about 2 s of SM
+ * clocks), record MOE_ERR_TIMEOUT in the workspace status word and return
+ * without touching the output; the CUDA context stays usable.  The count is
+ * process-wide and is consumed at launch time, so a graph captured while it
+ * is non-zero keeps the suppressed launches.  0 switches the hook off.
+ * Returns MOE_ERR_INVALID_ARG for launches < 0, else MOE_OK. */
+moe_status_t moe_debug_suppress_gemm_producer(int launches);
+
 /* Static description of a status code. */
 const char* moe_status_string(moe_status_t status);
 

@@ -24,6 +24,7 @@ __all__ = ["MoEConfig", "MoEWeights", "MoeError", "moe_workspace_size", "moe_max
            "moe_capacity", "moe_forward_num_launches", "moe_route", "moe_permute",
            "moe_permute_static",
            "moe_expert_ffn", "moe_combine", "moe_forward", "moe_workspace_status",
+           "moe_debug_suppress_gemm_producer",
            "MoEForwardGraph", "alloc_outputs",
            "make_workspace", "library_path", "MOE_TRACE_MAX_EVENTS"]
 
@@ -327,6 +328,13 @@ class MoEForwardGraph:
     def run_eager(self, trace_events=None):
         """The same forward launched directly (optionally with per-launch events)."""
         self._run(trace_events)
+
+
+def moe_debug_suppress_gemm_producer(launches: int) -> None:
+    """Failure injection for tests: the next `launches` expert-GEMM launches
+    run with their TMA producer silent, so their bounded waits run out and
+    the call records MOE_ERR_TIMEOUT in the workspace status word."""
+    check(_L.moe_debug_suppress_gemm_producer(int(launches)), "moe_debug_suppress_gemm_producer")
 
 
 def moe_workspace_status(ws: torch.Tensor, stream=None) -> int:

@@ -16,7 +16,8 @@ MOE_TRACE_MAX_EVENTS = 32
 # every symbol include/moe.h declares
 EXPORTED = ["moe_workspace_size", "moe_max_rows", "moe_capacity", "moe_forward_num_launches",
             "moe_route", "moe_permute", "moe_expert_ffn", "moe_combine", "moe_forward",
-            "moe_permute_static", "moe_workspace_status", "moe_status_string", "moe_version"]
+            "moe_permute_static", "moe_workspace_status", "moe_debug_suppress_gemm_producer",
+            "moe_status_string", "moe_version"]
 MOE_STATIC_MAX_ASSIGNMENTS = 65536
 MOE_STATIC_MAX_EXPERTS = 256
 
@@ -75,6 +76,8 @@ def load() -> C.CDLL:
     lib.moe_permute_static.restype = C.c_int
     lib.moe_workspace_status.argtypes = [P, P]
     lib.moe_workspace_status.restype = C.c_int
+    lib.moe_debug_suppress_gemm_producer.argtypes = [C.c_int]
+    lib.moe_debug_suppress_gemm_producer.restype = C.c_int
     lib.moe_status_string.argtypes = [C.c_int]
     lib.moe_status_string.restype = C.c_char_p
     lib.moe_version.argtypes = []

@@ -185,7 +185,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    // (with skip_producer set no copy and no full-barrier arrival is issued:
+    // the consumers' bounded waits run out, and tma_issued stays 0 so the
+    // abort path drains nothing)
+    if (lane == 0 && !args.skip_producer) {
       uint32_t stage = 0, phase = 0;
       long long issued = 0;
       bool ok = true;

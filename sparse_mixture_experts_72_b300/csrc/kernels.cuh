@@ -138,6 +138,7 @@ struct GemmArgs {
   __nv_bfloat16* out;            // [rows, ld_out]
   int32_t ld_out;
   int* status;                   // device status word
+  int32_t skip_producer;         // failure injection: the TMA producer issues nothing
 };
 
 struct GemmPlan {

@@ -5,6 +5,8 @@
 #include <cmath>
 #include <cstring>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -225,6 +227,17 @@ moe_status_t do_permute(const moe_config_t& c, const int32_t* idx, const float* 
   return cuda_status(launch_permute(a, st, tr));
 }
 
+// Failure-injection count (moe_debug_suppress_gemm_producer): each GEMM
+// launch consumes one unit while it is positive.
+std::atomic<int> g_suppress_producer{0};
+
+int32_t take_suppress_producer() {
+  int v = g_suppress_producer.load();
+  while (v > 0 && !g_suppress_producer.compare_exchange_weak(v, v - 1)) {
+  }
+  return v > 0 ? 1 : 0;
+}
+
 moe_status_t do_ffn(const moe_config_t& c, const uint16_t* x, const int32_t* perm,
                     const int32_t* offsets, const float* topk_w, const moe_weights_t& W,
                     uint16_t* y, uint16_t* y_shared, void* ws, const WsLayout& L, int sms,
@@ -248,6 +261,7 @@ moe_status_t do_ffn(const moe_config_t& c, const uint16_t* x, const int32_t* per
     g1.out = hid;
     g1.ld_out = c.F;
     g1.status = status;
+    g1.skip_producer = take_suppress_producer();
     GemmPlan p1;
     MOE_CUDA(make_gemm_plan(&p1, xp, R, reinterpret_cast<const bf*>(W.W1), (int64_t)c.N * c.F,
                             g1, sms));
@@ -264,6 +278,8 @@ moe_status_t do_ffn(const moe_config_t& c, const uint16_t* x, const int32_t* per
     g2.out = reinterpret_cast<bf*>(y);
     g2.ld_out = c.H;
     g2.status = status;
+    g2.skip_producer = take_suppress_producer();
+
     GemmPlan p2;
     MOE_CUDA(make_gemm_plan(&p2, hid, R, reinterpret_cast<const bf*>(W.W2), (int64_t)c.N * c.H,
                             g2, sms));
@@ -282,6 +298,7 @@ moe_status_t do_ffn(const moe_config_t& c, const uint16_t* x, const int32_t* per
     s1.out = hs;
     s1.ld_out = c.F_shared;
     s1.status = status;
+    s1.skip_producer = take_suppress_producer();
     GemmPlan ps1;
     MOE_CUDA(make_gemm_plan(&ps1, reinterpret_cast<const bf*>(x), c.T,
                             reinterpret_cast<const bf*>(W.W1s), c.F_shared, s1, sms));
@@ -299,6 +316,8 @@ moe_status_t do_ffn(const moe_config_t& c, const uint16_t* x, const int32_t* per
     s2.out = reinterpret_cast<bf*>(y_shared);
     s2.ld_out = c.H;
     s2.status = status;
+    s2.skip_producer = take_suppress_producer();
+
     GemmPlan ps2;
     MOE_CUDA(make_gemm_plan(&ps2, hs, c.T, reinterpret_cast<const bf*>(W.W2s), c.H, s2, sms));
     MOE_CUDA(launch_gemm(ps2, st, tr));
@@ -497,6 +516,12 @@ MOE_API moe_status_t moe_workspace_status(const void* ws, void* stream) {
     return MOE_ERR_CUDA;
   if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
   return v == 0 ? MOE_OK : static_cast<moe_status_t>(v);
+}
+
+MOE_API moe_status_t moe_debug_suppress_gemm_producer(int launches) {
+  if (launches < 0) return MOE_ERR_INVALID_ARG;
+  g_suppress_producer.store(launches);
+  return MOE_OK;
 }
 
 MOE_API const char* moe_status_string(moe_status_t s) {

@@ -113,3 +113,10 @@ def test_rejects_bad_arguments_before_any_launch(lib):
     if not torch.cuda.is_available():
         assert _forward(lib, ok, _weights()) == 6
     assert lib.moe_status_string(3) == b"workspace missing, misaligned or too small"
+
+
+def test_failure_injection_hook_validates_its_count(lib):
+    # host-only: sets or clears a process-wide count, launches nothing
+    assert lib.moe_debug_suppress_gemm_producer(-1) == 1   # INVALID_ARG
+    assert lib.moe_debug_suppress_gemm_producer(3) == 0
+    assert lib.moe_debug_suppress_gemm_producer(0) == 0
