@@ -44,6 +44,24 @@ quote):
 * GELU is the exact erf form (nn.GELU default).
 * T = 0: no outputs, f = p = 0 and L_aux = 0.
 
+Widened rows (the pages name them; each reading is a choice):
+
+* drop order: "token" (default, above) or "slot": every token's first
+  choice claims slots before any second choice, and so on.
+* min_capacity ([SKILLS] §5.1's DeepSpeed block): raises a smaller capacity
+  to the floor; it does not apply without a capacity factor.
+* SiLU / SwiGLU ([SKILLS] §6.1 prints a two-Linear SiLU expert while its text
+  says SwiGLU): "silu" is the printed block; "swiglu" keeps W1 as [2F, H]
+  with the gate rows first and the up rows second, SiLU(gate) * up.
+* expert choice ([SKILLS] §4.2, §7.3): selection on the router logits as
+  printed (router(x) transposed, top-k along tokens), ties to the lower
+  token; the combining weight is the token's gate probability P[t, e]
+  (softmax over experts), not renormalised; C = the capacity formula capped
+  at T; the selection bias is not used.
+* router z-loss ([SKILLS] §4.3): the raw mean of logsumexp(l_t)^2.
+* auxiliary-loss-free bias step ([ARCH] §2.4): b_i += gamma * sign(count_i -
+  mean count); the pages give no rate, so gamma is an input.
+
 Parity pins for every function live in the tests (closed forms, brute force,
 textbook routines, hand-worked fixtures); none is "parity unpinned".
 """
@@ -125,28 +143,48 @@ def route(x, Wg, bg, sel_bias, k: int) -> dict:
 # ---------------------------------------------------------------------------
 # dispatch: [ARCH] §2.3, [SKILLS] §8.2 (capacity) and §4.4 (drop_tokens)
 
-def capacity(T: int, N: int, capacity_factor: float) -> Optional[int]:
-    """Capacity = floor(T / N * capacity_factor); None (no limit) when cf <= 0."""
+def capacity(T: int, N: int, capacity_factor: float, min_capacity: int = 0) -> Optional[int]:
+    """Capacity = floor(T / N * capacity_factor); None (no limit) when cf <= 0.
+
+    ``min_capacity`` is the DeepSpeed ``moe`` block's floor ([SKILLS] §5.1):
+    the capacity is raised to it when the formula gives less."""
     if capacity_factor <= 0:
         return None
-    return int(math.floor(float(T) / float(N) * float(capacity_factor)))
+    c = int(math.floor(float(T) / float(N) * float(capacity_factor)))
+    return max(c, int(min_capacity))
 
 
-def permute(idx: np.ndarray, N: int, C: Optional[int]) -> dict:
+def claim_order(T: int, k: int, order: str = "token") -> np.ndarray:
+    """The order in which the T*k assignments a = t*k + j claim expert slots.
+
+    "token": increasing a (token by token, a token's slots in rank order);
+    "slot": every token's first choice, then every token's second choice,
+    and so on (a = t*k + j for j-major, then t).
+    """
+    if order == "token":
+        return np.arange(T * k, dtype=np.int64)
+    if order == "slot":
+        return np.array([t * k + j for j in range(k) for t in range(T)], dtype=np.int64)
+    raise ValueError(order)
+
+
+def permute(idx: np.ndarray, N: int, C: Optional[int], order: str = "token") -> dict:
     """Stable, capacity-limited dispatch of the T*k assignments to experts.
 
-    Walks the assignments a = t*k + j in increasing a with one counter per
-    expert.  An assignment whose rank within its expert is below C gets row
+    Walks the assignments in claim_order(order) with one counter per expert.
+    An assignment whose rank within its expert is below C gets row
     offsets[e] + rank in the expert-contiguous layout; the rest are dropped.
 
     Returns counts [N] (before drops), kept [N], offsets [N+1],
     perm [R] (row -> a) and inv [T*k] (a -> row, or -1 if dropped).
     """
-    flat = np.asarray(idx).reshape(-1)
+    idx = np.asarray(idx)
+    flat = idx.reshape(-1)
     A = flat.shape[0]
+    T, k = (idx.shape[0], idx.shape[1]) if idx.ndim == 2 else (A, 1)
     counts = np.zeros(N, np.int64)
     rank = np.empty(A, np.int64)
-    for a in range(A):
+    for a in claim_order(T, k, order):
         e = int(flat[a])
         rank[a] = counts[e]
         counts[e] += 1
@@ -179,6 +217,68 @@ def load_balance(P: np.ndarray, counts: np.ndarray, k: int, alpha: float) -> dic
 
 
 # ---------------------------------------------------------------------------
+# router z-loss: [SKILLS] §4.3
+
+def z_loss(l: np.ndarray) -> float:
+    """mean over tokens of logsumexp(l_t)^2 (the raw statistic; the pages
+    weight it by 0.001 in the training loss).  0 for T = 0."""
+    l = np.asarray(l, np.float64)
+    if l.shape[0] == 0:
+        return 0.0
+    m = l.max(axis=1)
+    lse = m + np.log(np.exp(l - m[:, None]).sum(axis=1))
+    return float(np.mean(lse * lse))
+
+
+# ---------------------------------------------------------------------------
+# auxiliary-loss-free balancing step: [ARCH] §2.4
+
+def update_sel_bias(b: np.ndarray, counts: np.ndarray, gamma: float) -> np.ndarray:
+    """b_i + gamma * sign(count_i - mean count): the bias of an expert that
+    took more than its share of assignments rises (it is subtracted from the
+    logits for selection, so it is chosen less), that of one that took less
+    falls, and an expert at exactly the mean keeps its bias.  The pages give
+    no rate; gamma is the caller's."""
+    c = np.asarray(counts, np.float64)
+    mean = c.sum() / c.shape[0]
+    return np.asarray(b, np.float64) + gamma * np.sign(c - mean)
+
+
+# ---------------------------------------------------------------------------
+# expert-choice routing: [SKILLS] §4.2 and §7.3
+
+def expert_choice(l: np.ndarray, C: int) -> dict:
+    """Each expert takes the C tokens with the largest router logits in its
+    column (router(x) transposed, top-k along tokens); equal logits take the
+    lower token index first.  C is capped at T.
+
+    Rows: expert e owns rows [e*C, (e+1)*C), its tokens in increasing token
+    order.  Assignment ids are a = t*N + e.  Returns offsets [N+1],
+    perm [N*C] (row -> a), inv [T*N] (a -> row or -1), counts [N] and the
+    column margins: for each expert, the logit gap between its C-th and
+    (C+1)-th token (+inf when C == T), which flags selections that a tiny
+    change of the logits can flip.
+    """
+    l = np.asarray(l, np.float64)
+    T, N = l.shape
+    C = min(int(C), T)
+    offsets = np.arange(N + 1, dtype=np.int64) * C
+    perm = np.empty(N * C, np.int64)
+    inv = np.full(T * N, -1, np.int64)
+    margin = np.full(N, np.inf)
+    for e in range(N):
+        order = np.argsort(-l[:, e], kind="stable")   # ties: lower token first
+        chosen = np.sort(order[:C])
+        if C < T:
+            margin[e] = l[order[C - 1], e] - l[order[C], e]
+        for r, t in enumerate(chosen):
+            perm[e * C + r] = t * N + e
+            inv[t * N + e] = e * C + r
+    return dict(offsets=offsets, perm=perm, inv=inv, counts=np.full(N, C, np.int64),
+                kept=np.full(N, C, np.int64), ec_margin=margin)
+
+
+# ---------------------------------------------------------------------------
 # experts: [SKILLS] §3.1 (Linear(H,F) -> GELU -> Linear(F,H))
 
 def gelu(z: np.ndarray) -> np.ndarray:
@@ -186,12 +286,44 @@ def gelu(z: np.ndarray) -> np.ndarray:
     return 0.5 * z * (1.0 + _erf(z / math.sqrt(2.0)))
 
 
-def expert_ffn(xe, W1, b1, W2, b2) -> np.ndarray:
-    """y = W2 . GELU(W1 . x + b1) + b2 for the rows of xe ([rows, H])."""
+def silu(z: np.ndarray) -> np.ndarray:
+    """SiLU (the Mixtral block's nn.SiLU, [SKILLS] §6.1): z * sigmoid(z),
+    written z / (1 + exp(-z)) for z >= 0 and z * exp(z) / (1 + exp(z)) below,
+    so that neither branch overflows."""
+    z = np.asarray(z, np.float64)
+    out = np.empty_like(z)
+    pos = z >= 0
+    out[pos] = z[pos] / (1.0 + np.exp(-z[pos]))
+    ez = np.exp(z[~pos])
+    out[~pos] = z[~pos] * ez / (1.0 + ez)
+    return out
+
+
+ACTIVATIONS = ("gelu", "silu", "swiglu")
+
+
+def expert_ffn(xe, W1, b1, W2, b2, activation: str = "gelu") -> np.ndarray:
+    """y = W2 . act(W1 . x + b1) + b2 for the rows of xe ([rows, H]).
+
+    "gelu": [SKILLS] §3.1's Linear(H, F) -> GELU -> Linear(F, H).
+    "silu": the two-Linear SiLU expert printed in [SKILLS] §6.1.
+    "swiglu": the gated form that §6.1's text names for Mixtral: W1 holds the
+    gate rows [0, F) and the up rows [F, 2F) (b1 likewise), and
+    act(z) = SiLU(z_gate) * z_up.
+    """
     z = np.asarray(xe, np.float64) @ W1.T
     if b1 is not None:
         z = z + b1[None, :]
-    y = gelu(z) @ W2.T
+    if activation == "gelu":
+        h = gelu(z)
+    elif activation == "silu":
+        h = silu(z)
+    elif activation == "swiglu":
+        F = z.shape[1] // 2
+        h = silu(z[:, :F]) * z[:, F:]
+    else:
+        raise ValueError(activation)
+    y = h @ W2.T
     if b2 is not None:
         y = y + b2[None, :]
     return y
@@ -202,24 +334,55 @@ def expert_ffn(xe, W1, b1, W2, b2) -> np.ndarray:
 
 def forward(x, Wg, bg, sel_bias, k: int, capacity_factor: float, alpha: float,
             expert: Callable[[int], tuple], shared: Optional[tuple] = None,
-            tokens: Optional[np.ndarray] = None) -> dict:
+            tokens: Optional[np.ndarray] = None, routing: str = "token",
+            activation: str = "gelu", min_capacity: int = 0,
+            drop_order: str = "token") -> dict:
     """Forward pass of one sparse MoE FFN layer.
 
-    ``expert(e)`` returns float64 (W1 [F,H], b1 [F]|None, W2 [H,F], b2 [H]|None)
-    of routed expert e; ``shared`` is the same tuple for the always-on shared
-    expert, or None.  Routing, capacity and the statistics always cover all T
-    tokens; with ``tokens`` given, the expert outputs are evaluated only for
-    those rows (``out`` then has one row per listed token, in that order).
+    ``expert(e)`` returns float64 (W1 [F,H] ([2F,H] for swiglu), b1|None,
+    W2 [H,F], b2 [H]|None) of routed expert e; ``shared`` is the same tuple
+    for the always-on shared expert (same activation), or None.  Routing,
+    capacity and the statistics always cover all T tokens; with ``tokens``
+    given, the expert outputs are evaluated only for those rows (``out`` then
+    has one row per listed token, in that order).
 
-    out[t] = sum over kept slots j of w_tj * FFN_{idx_tj}(x_t)  (+ FFN_s(x_t))
+    routing "token" (token choice, [SKILLS] §3.1):
+        out[t] = sum over kept slots j of w_tj * FFN_{idx_tj}(x_t)  (+ FFN_s(x_t))
+    routing "expert" (expert choice, [SKILLS] §4.2): expert e takes the
+    C = capacity(T, N, cf, min_capacity) tokens with the largest logits l[:, e];
+        out[t] = sum over experts e that took t of P[t, e] * FFN_e(x_t)  (+ FFN_s(x_t))
+    with P the gate softmax (the same gate probability the token-choice
+    weights come from; not renormalised, since a token may be taken by any
+    number of experts).  The selection bias does not apply.
     """
     x = np.asarray(x, np.float64)
     T = x.shape[0]
     N = np.asarray(Wg).shape[0]
-    r = route(x, Wg, bg, sel_bias, k)
-    C = capacity(T, N, capacity_factor)
-    d = permute(r["idx"], N, C)
-    lb = load_balance(r["probs"], d["counts"], k, alpha)
+    if routing == "token":
+        r = route(x, Wg, bg, sel_bias, k)
+        C = capacity(T, N, capacity_factor, min_capacity)
+        d = permute(r["idx"], N, C, drop_order)
+        lb = load_balance(r["probs"], d["counts"], k, alpha)
+        k_slots = k
+        weight_of = lambda a: r["w"][a // k, a % k]   # noqa: E731
+    elif routing == "expert":
+        l = gate_logits(x, Wg, bg)
+        P = softmax(l)
+        r = dict(logits=l, probs=P)
+        C = capacity(T, N, capacity_factor, min_capacity)
+        if C is None:
+            raise ValueError("expert choice needs a capacity factor > 0")
+        d = expert_choice(l, C)
+        # every expert takes the same number of tokens: f_i = 1/N
+        tot = max(int(d["counts"].sum()), 1)
+        f = d["counts"] / tot
+        p = P.mean(axis=0) if T > 0 else np.zeros(N)
+        lb = dict(f=f, p=p, l_aux=float(alpha * N * np.sum(f * p)))
+        k_slots = N
+        weight_of = lambda a: P[a // N, a % N]   # noqa: E731
+    else:
+        raise ValueError(routing)
+    z = z_loss(r["logits"])
 
     rows_out = np.arange(T) if tokens is None else np.asarray(tokens, np.int64)
     where = np.full(T, -1, np.int64)
@@ -229,18 +392,18 @@ def forward(x, Wg, bg, sel_bias, k: int, capacity_factor: float, alpha: float,
     offsets, perm = d["offsets"], d["perm"]
     for e in range(N):
         a = perm[offsets[e]:offsets[e + 1]]
-        t = a // k
+        t = a // k_slots
         keep = where[t] >= 0
         a, t = a[keep], t[keep]
         if a.shape[0] == 0:
             continue
         W1, b1, W2, b2 = expert(e)
-        y = expert_ffn(x[t], W1, b1, W2, b2)
-        wt = r["w"][t, a % k]
-        # one writer per (t, j): each assignment appears once in perm
+        y = expert_ffn(x[t], W1, b1, W2, b2, activation)
+        wt = weight_of(a)
+        # one writer per assignment: each appears once in perm
         np.add.at(out, where[t], wt[:, None] * y)
     if shared is not None:
         W1s, b1s, W2s, b2s = shared
-        out += expert_ffn(x[rows_out], W1s, b1s, W2s, b2s)
-    res = dict(out=out, capacity=C, **r, **d, **lb)
+        out += expert_ffn(x[rows_out], W1s, b1s, W2s, b2s, activation)
+    res = dict(out=out, capacity=C, z_loss=z, **r, **d, **lb)
     return res

@@ -349,6 +349,169 @@ def check_empty_input():
     assert res["capacity"] == 0
 
 
+# ---------------------------------------------------------------------------
+# widened rows: drop order, min_capacity, SiLU / SwiGLU, expert choice,
+# router z-loss, aux-loss-free bias step
+
+def check_slot_major_worked_example():
+    g = _golden("permute_slot_major_example.json")
+    idx = np.asarray(g["idx"])
+    for key in ("capped", "unlimited"):
+        c = g[key]
+        C = O.capacity(g["T"], g["N"], c["cf"])
+        d = O.permute(idx, g["N"], C, "slot")
+        assert d["counts"].tolist() == g["counts"]
+        for f in ("kept", "offsets", "perm", "inv"):
+            assert d[f].tolist() == c[f], (key, f, d[f].tolist())
+
+
+def check_min_capacity_examples():
+    for c in _golden("min_capacity_examples.json")["cases"]:
+        assert O.capacity(c["T"], c["N"], c["cf"], c["min"]) == c["C"], c
+
+
+def check_slot_major_vs_stable_sort(seed=13):
+    """Slot-major dispatch = a stable sort of the assignments by expert after
+    reordering them j-major (numpy's stable argsort as the reference)."""
+    rng = np.random.default_rng(seed)
+    for T, k, N, C in [(37, 3, 5, 9), (50, 2, 4, None), (20, 4, 6, 3)]:
+        idx = np.stack([rng.permutation(N)[:k] for _ in range(T)])
+        d = O.permute(idx, N, C, "slot")
+        order = np.array([t * k + j for j in range(k) for t in range(T)])
+        e_of = idx.reshape(-1)[order]
+        srt = order[np.argsort(e_of, kind="stable")]
+        rows = []
+        for e in range(N):
+            a_e = srt[idx.reshape(-1)[srt] == e]
+            rows.extend(a_e[:C] if C is not None else a_e)
+        assert d["perm"].tolist() == [int(a) for a in rows]
+
+
+def check_silu_textbook():
+    z = np.array([-800.0, -50.0, -3.0, -1.0, -1e-3, 0.0, 1e-3, 0.5, 2.0, 40.0, 800.0])
+    s_ = O.silu(z)
+    assert np.all(np.isfinite(s_)) and s_[5] == 0.0
+    # z*sigmoid(z) - (-z)*sigmoid(-z) = z (sigmoid(z) + sigmoid(-z) = 1)
+    np.testing.assert_allclose(s_ - O.silu(-z), z, rtol=1e-14, atol=1e-300)
+    np.testing.assert_allclose(s_[-1], 800.0, rtol=1e-15)
+    assert abs(s_[0]) < 1e-300
+    rng = np.random.default_rng(14)
+    r = rng.normal(0, 4, size=500)
+    np.testing.assert_allclose(O.silu(r), TF.silu(torch.from_numpy(r)).numpy(), rtol=1e-14,
+                               atol=1e-300)
+
+
+def check_swiglu_structure(seed=15):
+    rng = np.random.default_rng(seed)
+    H, F = 12, 10
+    x = rng.normal(size=(7, H))
+    Wg, Wu, Wu2 = (rng.normal(size=(F, H)) for _ in range(3))
+    W2, b2 = rng.normal(size=(H, F)), rng.normal(size=H)
+    ffn = lambda gate, up, b1=None: O.expert_ffn(x, np.vstack([gate, up]), b1, W2, b2, "swiglu")  # noqa: E731
+    # a zero gate switches the expert off: SiLU(0) = 0
+    np.testing.assert_allclose(ffn(np.zeros((F, H)), Wu), np.tile(b2, (7, 1)), rtol=0, atol=0)
+    # linear in the up projection (and only there)
+    lin = ffn(Wg, Wu + Wu2) - b2
+    np.testing.assert_allclose(lin, (ffn(Wg, Wu) - b2) + (ffn(Wg, Wu2) - b2), rtol=1e-12,
+                               atol=1e-12)
+    assert not np.allclose(ffn(Wg + Wu2, Wu) - b2, (ffn(Wg, Wu) - b2) + (ffn(Wu2, Wu) - b2))
+    # one hidden unit by hand: gate row g, up row u -> silu(g.x) * (u.x) * W2[:, 0]
+    g1, u1 = np.zeros((F, H)), np.zeros((F, H))
+    g1[0, 0], u1[0, 1] = 1.0, 1.0
+    want = (O.silu(x[:, 0]) * x[:, 1])[:, None] * W2[:, 0][None, :] + b2
+    np.testing.assert_allclose(ffn(g1, u1), want, rtol=1e-13, atol=1e-13)
+    # the plain SiLU expert is the GELU expert with the activation swapped
+    z = x @ Wg.T
+    np.testing.assert_allclose(O.expert_ffn(x, Wg, None, W2, None, "silu"),
+                               TF.silu(torch.from_numpy(z)).numpy() @ W2.T, rtol=1e-12,
+                               atol=1e-12)
+
+
+def _ec_bruteforce(l, C):
+    """Per expert, the lexicographically first C-subset of tokens with the
+    largest logit sum (itertools.combinations enumerates in lexicographic
+    order, so the first maximum wins): top-C with ties to lower tokens."""
+    T, N = l.shape
+    out = []
+    for e in range(N):
+        best, best_set = -np.inf, None
+        for comb in itertools.combinations(range(T), C):
+            v = sum(l[t, e] for t in comb)
+            if v > best:
+                best, best_set = v, comb
+        out.append(list(best_set))
+    return out
+
+
+def check_expert_choice_bruteforce(seed=16):
+    rng = np.random.default_rng(seed)
+    for T, N, C in [(6, 3, 2), (7, 2, 3), (5, 4, 5), (6, 2, 1)]:
+        for ties in (False, True):
+            l = rng.integers(-2, 3, size=(T, N)).astype(np.float64) if ties else \
+                rng.normal(size=(T, N))
+            d = O.expert_choice(l, C)
+            want = _ec_bruteforce(l, C)
+            for e in range(N):
+                a = d["perm"][d["offsets"][e]:d["offsets"][e + 1]]
+                assert (a // N).tolist() == want[e], (T, N, C, ties, e)
+                assert np.all(a % N == e)
+
+
+def check_expert_choice_invariants(seed=17):
+    rng = np.random.default_rng(seed)
+    T, N = 40, 5
+    l = rng.normal(size=(T, N))
+    for C in (1, 7, 40, 60):
+        d = O.expert_choice(l, C)
+        Ce = min(C, T)
+        assert d["offsets"].tolist() == [e * Ce for e in range(N + 1)]
+        assert np.all(d["inv"][d["perm"]] == np.arange(N * Ce))
+        assert int((d["inv"] >= 0).sum()) == N * Ce
+        for e in range(N):
+            toks = d["perm"][e * Ce:(e + 1) * Ce] // N
+            assert np.all(np.diff(toks) > 0)
+            rest = np.setdiff1d(np.arange(T), toks)
+            if rest.size:
+                assert l[toks, e].min() >= l[rest, e].max()
+
+
+def check_expert_choice_full_capacity(seed=18):
+    """C = T: every expert takes every token, so with identical experts the
+    layer is the dense FFN (the gate probabilities of a token sum to one)."""
+    rng = np.random.default_rng(seed)
+    T, H, F, N = 9, 6, 8, 3
+    x, Wg, ex = _rand_layer(rng, T, H, F, N)
+    bg = rng.normal(size=N)
+    same = ex[0]
+    res = O.forward(x, Wg, bg, None, 1, float(N), 0.01, lambda e: same, routing="expert")
+    assert res["capacity"] == T
+    np.testing.assert_allclose(res["out"], O.expert_ffn(x, *same), rtol=1e-12, atol=1e-12)
+    # and a token nobody takes gets zero: C = 1 on distinct experts
+    res1 = O.forward(x, Wg, bg, None, 1, N / T, 0.01, lambda e: ex[e], routing="expert")
+    taken = set((res1["perm"] // N).tolist())
+    for t in range(T):
+        if t not in taken:
+            assert np.all(res1["out"][t] == 0.0)
+
+
+def check_z_loss(seed=19):
+    from scipy.special import logsumexp
+    for c, N in [(0.0, 4), (2.5, 8), (-3.0, 256)]:
+        np.testing.assert_allclose(O.z_loss(np.full((5, N), c)), (c + math.log(N)) ** 2,
+                                   rtol=1e-14)
+    l = np.random.default_rng(seed).normal(0, 3, size=(50, 16))
+    np.testing.assert_allclose(O.z_loss(l), np.mean(logsumexp(l, axis=1) ** 2), rtol=1e-13)
+    assert O.z_loss(np.zeros((0, 4))) == 0.0
+
+
+def check_update_sel_bias():
+    # mean count 4: the over-used expert 0 rises, the under-used expert 1 falls
+    b = O.update_sel_bias(np.array([0.1, -0.2, 0.0, 0.3]), np.array([5, 3, 4, 4]), 0.01)
+    np.testing.assert_allclose(b, [0.11, -0.21, 0.0, 0.3], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(O.update_sel_bias(np.zeros(3), np.array([2, 2, 2]), 1.0),
+                               [0.0, 0.0, 0.0])
+
+
 ALL_CHECKS = [
     check_router_worked_example, check_capacity_examples, check_permute_worked_example,
     check_laux_worked_examples, check_gelu_textbook, check_moelayer_worked_example,
@@ -356,7 +519,10 @@ ALL_CHECKS = [
     check_weights_invariants, check_permute_vs_stable_sort, check_dense_reduction,
     check_identical_experts, check_shared_only, check_linearity_in_w2, check_expert_relabelling,
     check_moelayer_restatement, check_tiny_workload_restatement, check_sampled_tokens_match_full,
-    check_empty_input,
+    check_empty_input, check_slot_major_worked_example, check_min_capacity_examples,
+    check_slot_major_vs_stable_sort, check_silu_textbook, check_swiglu_structure,
+    check_expert_choice_bruteforce, check_expert_choice_invariants,
+    check_expert_choice_full_capacity, check_z_loss, check_update_sel_bias,
 ]
 
 
@@ -383,8 +549,8 @@ def _mut_ties_high_index(s, k):
     return order[:, :k].copy(), np.full(T, np.inf), np.full(T, np.inf)
 
 
-def _mut_capacity_ceil(T, N, cf):
-    return None if cf <= 0 else int(math.ceil(T / N * cf))
+def _mut_capacity_ceil(T, N, cf, min_capacity=0):
+    return None if cf <= 0 else max(int(math.ceil(T / N * cf)), min_capacity)
 
 
 def _mut_laux_no_n(P, counts, k, alpha):
@@ -402,23 +568,17 @@ def _mut_bias_in_weights(x, Wg, bg, sel_bias, k):
                 order_margin=om, scores=s)
 
 
-def _mut_ffn_missing_b2(xe, W1, b1, W2, b2):
-    z = np.asarray(xe, np.float64) @ W1.T
-    if b1 is not None:
-        z = z + b1[None, :]
-    return O.gelu(z) @ W2.T
+def _mut_ffn_missing_b2(xe, W1, b1, W2, b2, activation="gelu"):
+    y = O.__dict__["_orig_expert_ffn"](xe, W1, b1, W2, None, activation)
+    return y
 
 
-def _mut_ffn_transposed_w2(xe, W1, b1, W2, b2):
-    z = np.asarray(xe, np.float64) @ W1.T
-    if b1 is not None:
-        z = z + b1[None, :]
-    g = O.gelu(z)
-    y = g @ W2.T if W2.shape[0] != W2.shape[1] else g @ W2
-    return y if b2 is None else y + b2[None, :]
+def _mut_ffn_transposed_w2(xe, W1, b1, W2, b2, activation="gelu"):
+    W2m = W2 if W2.shape[0] != W2.shape[1] else W2.T
+    return O.__dict__["_orig_expert_ffn"](xe, W1, b1, W2m, b2, activation)
 
 
-def _mut_permute_keep_last(idx, N, C):
+def _mut_permute_keep_last(idx, N, C, order="token"):
     """Keeps the last C assignments of each expert instead of the first C."""
     flat = np.asarray(idx).reshape(-1)
     rev = O.__dict__["_orig_permute"](flat[::-1].reshape(-1, 1), N, C)
@@ -433,7 +593,63 @@ def _mut_permute_keep_last(idx, N, C):
     return dict(counts=d["counts"], kept=kept, offsets=offsets, perm=perm, inv=inv)
 
 
+def _mut_min_capacity_ignored(T, N, cf, min_capacity=0):
+    return O.__dict__["_orig_capacity"](T, N, cf)
+
+
+def _mut_slot_order_ignored(T, k, order="token"):
+    return np.arange(T * k, dtype=np.int64)
+
+
+def _mut_silu_is_sigmoid(z):
+    z = np.asarray(z, np.float64)
+    return 1.0 / (1.0 + np.exp(-np.clip(z, -700, 700)))
+
+
+def _mut_swiglu_halves_swapped(xe, W1, b1, W2, b2, activation="gelu"):
+    if activation == "swiglu":
+        F = W1.shape[0] // 2
+        W1 = np.vstack([W1[F:], W1[:F]])
+        if b1 is not None:
+            b1 = np.concatenate([b1[F:], b1[:F]])
+    return O.__dict__["_orig_expert_ffn"](xe, W1, b1, W2, b2, activation)
+
+
+def _mut_ec_ties_high_token(l, C):
+    l = np.asarray(l, np.float64)
+    T = l.shape[0]
+    d = O.__dict__["_orig_expert_choice"](l[::-1], C)
+    N = l.shape[1]
+    perm = d["perm"].copy()
+    for e in range(N):
+        seg = perm[d["offsets"][e]:d["offsets"][e + 1]]
+        toks = np.sort(T - 1 - seg // N)
+        perm[d["offsets"][e]:d["offsets"][e + 1]] = toks * N + e
+    inv = np.full(T * N, -1)
+    inv[perm] = np.arange(perm.shape[0])
+    return dict(d, perm=perm, inv=inv)
+
+
+def _mut_zloss_no_square(l):
+    l = np.asarray(l, np.float64)
+    if l.shape[0] == 0:
+        return 0.0
+    m = l.max(axis=1)
+    return float(np.mean(m + np.log(np.exp(l - m[:, None]).sum(axis=1))))
+
+
+def _mut_bias_update_sign(b, counts, gamma):
+    return O.__dict__["_orig_update_sel_bias"](b, counts, -gamma)
+
+
 MUTANTS = {
+    "min_capacity_ignored": ("capacity", _mut_min_capacity_ignored),
+    "slot_major_as_token_major": ("claim_order", _mut_slot_order_ignored),
+    "silu_as_sigmoid": ("silu", _mut_silu_is_sigmoid),
+    "swiglu_gate_up_swapped": ("expert_ffn", _mut_swiglu_halves_swapped),
+    "expert_choice_ties_high_token": ("expert_choice", _mut_ec_ties_high_token),
+    "z_loss_not_squared": ("z_loss", _mut_zloss_no_square),
+    "bias_update_sign_flipped": ("update_sel_bias", _mut_bias_update_sign),
     "gelu_tanh_approx": ("gelu", _mut_gelu_tanh),
     "renorm_dropped": ("renormalise", _mut_renorm_no_division),
     "ties_to_high_index": ("select_topk", _mut_ties_high_index),
