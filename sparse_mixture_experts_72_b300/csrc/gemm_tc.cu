@@ -10,6 +10,17 @@
 // §3.1's Linear(H, 4H) -> GELU -> Linear(4H, H); the weighting by the
 // renormalised gate score is its output[mask] += score * expert_output.
 //
+// One launch runs the whole expert FFN as two phases over one persistent
+// grid: phase 0 (Hid = GELU(X W1^T + b1)) and phase 1 (y = w (Hid W2^T +
+// b2)).  The tile list is phase 0's tiles followed by phase 1's; CTAs take
+// tiles round-robin.  Every phase-0 epilogue warp releases a per-row-block
+// counter in global memory after its stores (fence.proxy.async + red.release),
+// and the TMA producer acquires the counter of a phase-1 tile's row block
+// before loading its Hid rows.  The second Linear of an expert therefore
+// starts as soon as its rows are ready, with no kernel boundary, and the
+// second Linear's few large tiles fill the gaps of the first's tail instead
+// of forming a partial last wave.
+//
 // Two shapes of the same persistent, warp-specialised kernel (576 threads):
 //
 //   PAIR = 1  one CTA per tile of 128 rows x 256 columns: A tile 128 x 64 and
@@ -28,8 +39,8 @@
 // accumulators; warps 2..17 epilogue (tcgen05.ld -> bias -> GELU or scale ->
 // bf16 stores; warp w reads TMEM lanes 32*(w%4).. and the 64-column slice
 // (w-2)/4 of the tile).
-// Tiles are ordered expert-major, then output block, then row block, so the
-// CTAs working at one time share one weight slab through L2.
+// The grid never exceeds the CTAs (pairs) that can be resident at once, so a
+// phase-1 tile only ever waits for tiles that running CTAs will finish.
 // Every wait is bounded: on expiry the CTA records MOE_ERR_TIMEOUT, lets its
 // in-flight copies land, drains its MMAs, frees TMEM and exits.
 #include "common.cuh"
@@ -69,26 +80,58 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
   return true;
 }
 
+// Walks the tiles of a launch in increasing order: phase 0's tiles, then
+// phase 1's; inside a phase expert-major, then column block, then row block
+// (row block fastest, so the CTAs working at one time share a weight slab).
 template <int TILE_M>
 struct TileCursor {
-  int g = 0;
-  __device__ __forceinline__ void locate(int tile, const int32_t* tile_start, const int32_t* seg,
-                                         int& a_row, int& rows_left, int& n) {
-    while (tile >= tile_start[g + 1]) ++g;
-    const int local = tile - tile_start[g];
-    const int rows = seg[g + 1] - seg[g];
-    const int mt = (rows + TILE_M - 1) / TILE_M;
-    n = local / mt;
-    const int m = local - n * mt;
+  int phase = 0, g = 0;
+  __device__ __forceinline__ void locate(int tile, int tiles0, int nt0, int nt1,
+                                         const int32_t* mt_pre, const int32_t* seg, int& a_row,
+                                         int& rows_left, int& n, int& rb) {
+    int local = tile;
+    if (tile >= tiles0) {
+      if (phase == 0) { phase = 1; g = 0; }
+      local = tile - tiles0;
+    }
+    const int ntp = phase ? nt1 : nt0;
+    while (local >= mt_pre[g + 1] * ntp) ++g;   // groups without rows own no tiles
+    const int mt = mt_pre[g + 1] - mt_pre[g];
+    const int lg = local - mt_pre[g] * ntp;
+    n = lg / mt;
+    const int m = lg - n * mt;
+    rb = mt_pre[g] + m;
     a_row = seg[g] + m * TILE_M;
-    rows_left = rows - m * TILE_M;
+    rows_left = seg[g + 1] - seg[g] - m * TILE_M;
+  }
+};
+
+// Per-tile view of a phase's parameters, read field by field from the
+// kernel parameters (no dynamic indexing into parameter space).
+struct PhaseView {
+  int n_out, K, mode, ld_out;
+  const __nv_bfloat16* bias;
+  const float* topk_w;
+  const int32_t* perm;
+  __nv_bfloat16* out;
+  __device__ __forceinline__ PhaseView(const GemmArgs& a, int p) {
+    n_out = p ? a.ph[1].n_out : a.ph[0].n_out;
+    K = p ? a.ph[1].K : a.ph[0].K;
+    mode = p ? a.ph[1].mode : a.ph[0].mode;
+    ld_out = p ? a.ph[1].ld_out : a.ph[0].ld_out;
+    bias = p ? a.ph[1].bias : a.ph[0].bias;
+    topk_w = p ? a.ph[1].topk_w : a.ph[0].topk_w;
+    perm = p ? a.ph[1].perm : a.ph[0].perm;
+    out = p ? a.ph[1].out : a.ph[0].out;
   }
 };
 
 template <int PAIR>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
-    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                        const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
+                        const __grid_constant__ CUtensorMap tmB0,
+                        const __grid_constant__ CUtensorMap tmA1,
+                        const __grid_constant__ CUtensorMap tmB1, const GemmArgs args) {
   using S = GemmShape<PAIR>;
   constexpr int STAGES = S::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -106,9 +149,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + S::NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int32_t* seg = reinterpret_cast<int32_t*>(tmem_holder + 4);   // [G+1] row offsets
-  int32_t* tile_start = seg + (MAX_GROUPS + 1);                 // [G+1] tile prefix
+  int32_t* mt_pre = seg + (MAX_GROUPS + 1);                     // [G+1] row-block prefix
   uint16_t* bias_stage = reinterpret_cast<uint16_t*>(  // [EPI_WARPS][EPI_COLS], 16-B aligned
-      (reinterpret_cast<uintptr_t>(tile_start + (MAX_GROUPS + 1)) + 15) & ~static_cast<uintptr_t>(15));
+      (reinterpret_cast<uintptr_t>(mt_pre + (MAX_GROUPS + 1)) + 15) & ~static_cast<uintptr_t>(15));
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -117,9 +160,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   const int unit = PAIR == 2 ? (int)cluster_id_x() : (int)blockIdx.x;   // pair (or CTA) index
   const int units = PAIR == 2 ? (int)num_clusters_x() : (int)gridDim.x;
   const int G = args.num_groups;
-  const int n_out = args.n_out;
-  const int n_tiles = (n_out + BN - 1) / BN;
-  const int nkb = (args.K + BK - 1) / BK;
+  const bool two = args.num_phases == 2;
+  const int nt0 = (args.ph[0].n_out + BN - 1) / BN;
+  const int nt1 = two ? (args.ph[1].n_out + BN - 1) / BN : 0;
+  const int nkb0 = (args.ph[0].K + BK - 1) / BK;
+  const int nkb1 = two ? (args.ph[1].K + BK - 1) / BK : 0;
+  // phase-0 epilogue arrivals that complete one row block (every warp of
+  // every CTA of the tile, for every column block)
+  const int rows_done_target = nt0 * EPI_WARPS * PAIR;
   int* status = args.status;
 
   // ---- set-up: group table, barriers, TMEM
@@ -139,8 +187,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmA0);
+    tma_prefetch_desc(&tmB0);
+    if (two) {
+      tma_prefetch_desc(&tmA1);
+      tma_prefetch_desc(&tmB1);
+    }
   }
   if (warp == 1) {
     if constexpr (PAIR == 2) {
@@ -153,12 +205,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   }
   __syncthreads();  // seg[] visible
   if (warp == 2) {
-    // tile_start = exclusive prefix over groups of (row blocks * n_tiles)
+    // mt_pre = exclusive prefix over groups of their row blocks
     const int per = (G + 31) / 32;
     const int g0 = lane * per;
     int local = 0;
     for (int g = g0; g < g0 + per && g < G; ++g)
-      local += ((seg[g + 1] - seg[g] + S::TILE_M - 1) / S::TILE_M) * n_tiles;
+      local += (seg[g + 1] - seg[g] + S::TILE_M - 1) / S::TILE_M;
     int incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -167,10 +219,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
     int run = incl - local;
     for (int g = g0; g < g0 + per && g < G; ++g) {
-      tile_start[g] = run;
-      run += ((seg[g + 1] - seg[g] + S::TILE_M - 1) / S::TILE_M) * n_tiles;
+      mt_pre[g] = run;
+      run += (seg[g + 1] - seg[g] + S::TILE_M - 1) / S::TILE_M;
     }
-    if (lane == 31) tile_start[G] = incl;
+    if (lane == 31) mt_pre[G] = incl;
   }
   tc_fence_before();
   if constexpr (PAIR == 2) {
@@ -180,7 +232,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   }
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
-  const int total = tile_start[G];
+  const int tiles0 = mt_pre[G] * nt0;
+  const int total = tiles0 + (two ? mt_pre[G] * nt1 : 0);
   long long tma_issued = 0;  // producer thread only
 
   if (warp == 0) {
@@ -194,8 +247,30 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       bool ok = true;
       TileCursor<S::TILE_M> cur;
       for (int tile = unit; tile < total && ok; tile += units) {
-        int a_row, rows_left, n;
-        cur.locate(tile, tile_start, seg, a_row, rows_left, n);
+        int a_row, rows_left, n, rb;
+        cur.locate(tile, tiles0, nt0, nt1, mt_pre, seg, a_row, rows_left, n, rb);
+        const int ph = cur.phase;
+        const CUtensorMap* mA = ph ? &tmA1 : &tmA0;
+        const CUtensorMap* mB = ph ? &tmB1 : &tmB0;
+        const int nkb = ph ? nkb1 : nkb0;
+        const int n_out = ph ? args.ph[1].n_out : args.ph[0].n_out;
+        if (ph == 1) {
+          // the A rows of this tile are phase 0's output: wait until every
+          // phase-0 tile of the row block has been stored and released
+          const int* cnt = args.rows_done + rb;
+          const long long t0 = clock64();
+          while (ld_acquire_gpu(cnt) < rows_done_target) {
+            if (*abort_flag) { ok = false; break; }
+            if (clock64() - t0 > kWaitLimitCycles) {
+              *abort_flag = 1;
+              atomicExch(status, (int)MOE_ERR_TIMEOUT);
+              ok = false;
+              break;
+            }
+          }
+          if (!ok) break;
+          fence_proxy_async_global();  // the TMA reads below see those plain stores
+        }
         const int b_row = cur.g * n_out + n * BN + (int)rank * S::B_ROWS;
         const int a_row_cta = a_row + (int)rank * 128;
         for (int kb = 0; kb < nkb; ++kb) {
@@ -207,12 +282,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             // both CTAs' copies complete on the even CTA's full barrier
             const uint32_t fb = mapa_shared(full_bar(stage), 0);
             if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * S::STAGE_BYTES);
-            tma_load_2d_pair(sA + stage * A_BYTES, &tmA, fb, kb * BK, a_row_cta);
-            tma_load_2d_pair(sB + stage * S::B_BYTES, &tmB, fb, kb * BK, b_row);
+            tma_load_2d_pair(sA + stage * A_BYTES, mA, fb, kb * BK, a_row_cta);
+            tma_load_2d_pair(sB + stage * S::B_BYTES, mB, fb, kb * BK, b_row);
           } else {
             mbar_arrive_expect_tx(full_bar(stage), S::STAGE_BYTES);
-            tma_load_2d(sA + stage * A_BYTES, &tmA, full_bar(stage), kb * BK, a_row_cta);
-            tma_load_2d(sB + stage * S::B_BYTES, &tmB, full_bar(stage), kb * BK, b_row);
+            tma_load_2d(sA + stage * A_BYTES, mA, full_bar(stage), kb * BK, a_row_cta);
+            tma_load_2d(sB + stage * S::B_BYTES, mB, full_bar(stage), kb * BK, b_row);
           }
           ++issued;
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -228,6 +303,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       for (int tile = unit; tile < total && ok; tile += units) {
+        const int nkb = tile < tiles0 ? nkb0 : nkb1;
         if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, status)) {
           ok = false;
           break;
@@ -273,22 +349,24 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     uint32_t acc = 0, acc_phase = 0;
     TileCursor<S::TILE_M> cur;
     for (int tile = unit; tile < total; tile += units) {
-      int a_row, rows_left, n;
-      cur.locate(tile, tile_start, seg, a_row, rows_left, n);
+      int a_row, rows_left, n, rb;
+      cur.locate(tile, tiles0, nt0, nt1, mt_pre, seg, a_row, rows_left, n, rb);
+      const PhaseView P(args, cur.phase);
+      const int n_out = P.n_out;
       const int r_in = warp_row0 + lane;
       const bool row_ok = r_in < rows_left;
       const int64_t out_row = (int64_t)a_row + r_in;
       const int col0 = n * BN + cpart * EPI_COLS;     // first column of this warp's slice
       // everything that does not need the accumulator is fetched before waiting
       float wscale = 1.0f;
-      if (args.mode == EPI_SCALE && args.topk_w != nullptr && row_ok)
-        wscale = args.topk_w[args.perm[out_row]];
-      const bool has_bias = args.bias != nullptr;
+      if (P.mode == EPI_SCALE && P.topk_w != nullptr && row_ok)
+        wscale = P.topk_w[P.perm[out_row]];
+      const bool has_bias = P.bias != nullptr;
       if (has_bias) {
         // EPI_COLS (64) columns: 2 per lane
         const int c2 = col0 + lane * 2;
         uint32_t b = 0u;
-        if (c2 < n_out) b = __ldg(reinterpret_cast<const uint32_t*>(args.bias + (size_t)cur.g * n_out + c2));
+        if (c2 < n_out) b = __ldg(reinterpret_cast<const uint32_t*>(P.bias + (size_t)cur.g * n_out + c2));
         *reinterpret_cast<uint32_t*>(my_bias + lane * 2) = b;
         __syncwarp();
       }
@@ -297,7 +375,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      __nv_bfloat16* orow = args.out + out_row * args.ld_out;
+      __nv_bfloat16* orow = P.out + out_row * P.ld_out;
       const bool warp_has_rows = warp_row0 < rows_left;     // warp-uniform
       const bool full_cols = col0 + EPI_COLS <= n_out;      // warp-uniform
       if (warp_has_rows && col0 < n_out) {
@@ -320,7 +398,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               v[8 * j8 + 6] += bf16lo(u.w); v[8 * j8 + 7] += bf16hi(u.w);
             }
           }
-          if (args.mode == EPI_GELU) {
+          if (P.mode == EPI_GELU) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
           } else {
@@ -358,6 +436,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         } else {
           mbar_arrive(tempty_bar(acc));
         }
+      }
+      if (two && cur.phase == 0) {
+        // release this warp's stores of the row block to phase 1's TMA reads
+        fence_proxy_async_global();
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) red_release_gpu_add(args.rows_done + rb, 1);
       }
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
@@ -443,21 +528,37 @@ bool encode_tensor_map_bf16(CUtensorMap* map, const void* base, int64_t rows, in
   return r == CUDA_SUCCESS;
 }
 
-cudaError_t make_gemm_plan(GemmPlan* plan, const __nv_bfloat16* A, int64_t a_rows,
-                           const __nv_bfloat16* B, int64_t b_rows, const GemmArgs& args,
-                           int num_sms) {
-  if (a_rows <= 0 || b_rows <= 0 || args.K <= 0 || args.n_out <= 0) return cudaErrorInvalidValue;
+cudaError_t make_gemm_plan(GemmPlan* plan, const GemmArgs& args, const __nv_bfloat16* A,
+                           int64_t a_rows, const __nv_bfloat16* const B[2],
+                           const int64_t b_rows[2], int num_sms) {
+  const int np = args.num_phases;
+  if (np < 1 || np > 2 || a_rows <= 0) return cudaErrorInvalidValue;
+  for (int p = 0; p < np; ++p)
+    if (b_rows[p] <= 0 || args.ph[p].K <= 0 || args.ph[p].n_out <= 0) return cudaErrorInvalidValue;
+  if (np == 2 && (args.rows_done == nullptr || args.ph[1].K != args.ph[0].n_out ||
+                  args.ph[0].ld_out != args.ph[0].n_out))
+    return cudaErrorInvalidValue;
   // CTA pairs (256-row tiles) once the average group holds enough rows to
   // fill them; single CTAs (128-row tiles) for decode-sized groups.
   const int64_t avg_rows = a_rows / (args.num_groups > 0 ? args.num_groups : 1);
   const int pair = (avg_rows >= 192 && num_sms >= 2) ? 2 : 1;
-  if (!encode_tensor_map_bf16(&plan->tmA, A, a_rows, args.K, BK, 128)) return cudaErrorInvalidValue;
-  if (!encode_tensor_map_bf16(&plan->tmB, B, b_rows, args.K, BK, BN / pair))
-    return cudaErrorInvalidValue;
+  for (int p = 0; p < np; ++p) {
+    // phase 1 reads phase 0's output [a_rows, n_out0] as its A operand
+    const __nv_bfloat16* a = p == 0 ? A : args.ph[0].out;
+    if (!encode_tensor_map_bf16(&plan->tmA[p], a, a_rows, args.ph[p].K, BK, 128))
+      return cudaErrorInvalidValue;
+    if (!encode_tensor_map_bf16(&plan->tmB[p], B[p], b_rows[p], args.ph[p].K, BK, BN / pair))
+      return cudaErrorInvalidValue;
+  }
+  if (np == 1) {
+    plan->tmA[1] = plan->tmA[0];
+    plan->tmB[1] = plan->tmB[0];
+  }
   plan->args = args;
   plan->pair = pair;
   const int64_t tile_m = 128 * pair;
-  const int64_t n_tiles = (args.n_out + BN - 1) / BN;
+  int64_t n_tiles = 0;
+  for (int p = 0; p < np; ++p) n_tiles += (args.ph[p].n_out + BN - 1) / BN;
   const int64_t max_tiles = ((a_rows + tile_m - 1) / tile_m + args.num_groups) * n_tiles;
   const int64_t max_units = num_sms / pair;
   const int64_t units = max_tiles < max_units ? max_tiles : max_units;
@@ -488,18 +589,27 @@ static cudaError_t launch_gemm_t(const GemmPlan& plan, cudaStream_t st) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (PAIR == 2) {
-    // a persistent grid must fit at once: no more pairs than can be co-resident
-    static int max_clusters = -1;
-    if (max_clusters < 0) {
-      int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<PAIR>, &cfg) != cudaSuccess || n <= 0)
-        n = 1;
-      max_clusters = n;
+  // A persistent grid must be co-resident: phase-1 tiles wait for phase-0
+  // tiles owned by other CTAs.  No more CTAs (pairs) than fit at once.
+  static int max_units = -1;
+  if (max_units < 0) {
+    int n = 0;
+    if (PAIR == 2) {
+      if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<PAIR>, &cfg) != cudaSuccess)
+        n = 0;
+    } else {
+      int dev = 0, sms = 0, per_sm = 0;
+      if (cudaGetDevice(&dev) == cudaSuccess &&
+          cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, grouped_gemm_kernel<PAIR>,
+                                                        GEMM_THREADS, S::SMEM_BYTES) == cudaSuccess)
+        n = sms * per_sm;
     }
-    if ((int)cfg.gridDim.x > 2 * max_clusters) cfg.gridDim.x = 2 * max_clusters;
+    max_units = n > 0 ? n : 1;
   }
-  return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<PAIR>, plan.tmA, plan.tmB, plan.args);
+  if ((int)cfg.gridDim.x > PAIR * max_units) cfg.gridDim.x = PAIR * max_units;
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<PAIR>, plan.tmA[0], plan.tmB[0],
+                            plan.tmA[1], plan.tmB[1], plan.args);
 }
 
 cudaError_t launch_gemm(const GemmPlan& plan, cudaStream_t st, LaunchTrace* tr) {

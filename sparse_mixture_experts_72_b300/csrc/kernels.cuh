@@ -125,34 +125,50 @@ cudaError_t launch_combine(const __nv_bfloat16* y, const int32_t* inv,
 // ---------------------------------------------------------------- grouped tcgen05 GEMM
 enum EpilogueMode : int32_t { EPI_GELU = 0, EPI_SCALE = 1 };
 
-struct GemmArgs {
-  const int32_t* offsets;        // [G+1] row segments of A per group, or nullptr
-  int32_t num_groups;            // G (routed experts), or 1 with offsets == nullptr
-  int32_t rows_single;           // rows of the single group when offsets == nullptr
+// One GEMM of a launch: out = epilogue(A_rows . B_g^T) for every group g.
+struct GemmPhase {
   int32_t n_out;                 // output columns per group (= B rows per group)
   int32_t K;                     // reduction length
   int32_t mode;                  // EpilogueMode
+  int32_t ld_out;
   const __nv_bfloat16* bias;     // [G, n_out] or nullptr
   const float* topk_w;           // EPI_SCALE: weight per assignment, or nullptr (weight 1)
   const int32_t* perm;           // EPI_SCALE: row -> assignment (with topk_w)
   __nv_bfloat16* out;            // [rows, ld_out]
-  int32_t ld_out;
+};
+
+// A launch runs one phase, or two where phase 1 reads phase 0's output rows
+// as its A operand (the expert FFN's Linear -> GELU -> Linear in one
+// persistent grid).  Both phases share the row segments of the groups.
+struct GemmArgs {
+  const int32_t* offsets;        // [G+1] row segments of A per group, or nullptr
+  int32_t num_groups;            // G (routed experts), or 1 with offsets == nullptr
+  int32_t rows_single;           // rows of the single group when offsets == nullptr
+  int32_t num_phases;            // 1 or 2
+  GemmPhase ph[2];
+  int32_t* rows_done;            // num_phases == 2: per row block, phase-0 epilogue arrivals
+                                 // (zeroed before the launch; gemm_rows_done_len() entries)
   int* status;                   // device status word
   int32_t skip_producer;         // failure injection: the TMA producer issues nothing
 };
 
 struct GemmPlan {
-  CUtensorMap tmA;  // A [rows, K] bf16, box 64 x 128, 128B swizzle
-  CUtensorMap tmB;  // B [G * n_out, K] bf16, box 64 x (256 / pair), 128B swizzle
+  CUtensorMap tmA[2];  // per phase: A [rows, K] bf16, box 64 x 128, 128B swizzle
+  CUtensorMap tmB[2];  // per phase: B [G * n_out, K] bf16, box 64 x (256 / pair)
   GemmArgs args;
   int grid;
   int pair;         // 1: one CTA per 128-row tile; 2: a CTA pair per 256-row tile
 };
 
-// Encodes the tensor maps; returns cudaErrorInvalidValue if encoding fails.
-cudaError_t make_gemm_plan(GemmPlan* plan, const __nv_bfloat16* A, int64_t a_rows,
-                           const __nv_bfloat16* B, int64_t b_rows, const GemmArgs& args,
-                           int num_sms);
+// Upper bound of the row blocks (tiles along M) of a launch over a_rows rows
+// in G groups: the length of GemmArgs::rows_done.
+inline int64_t gemm_rows_done_len(int64_t a_rows, int G) { return (a_rows + 127) / 128 + G; }
+
+// Encodes the tensor maps (phase 1's A is phase 0's output when num_phases
+// is 2); returns cudaErrorInvalidValue if encoding fails.
+cudaError_t make_gemm_plan(GemmPlan* plan, const GemmArgs& args, const __nv_bfloat16* A,
+                           int64_t a_rows, const __nv_bfloat16* const B[2],
+                           const int64_t b_rows[2], int num_sms);
 cudaError_t launch_gemm(const GemmPlan& plan, cudaStream_t st, LaunchTrace* tr);
 bool tensor_map_encoder_available();
 

@@ -37,7 +37,8 @@ int64_t max_rows_of(const moe_config_t& c) {
 }
 
 struct WsLayout {
-  size_t status, status_bytes, w3, logits, p_part, local_rank, blk_hist, blk_base;
+  size_t status, status_bytes, rows_done, rows_done_s, w3, logits, p_part, local_rank, blk_hist,
+      blk_base;
   size_t topk_idx, topk_w, p_mean, counts, offsets, perm, inv, f, l_aux;
   size_t xp, hid, y, hid_s, y_s;
   size_t total;
@@ -50,9 +51,15 @@ WsLayout layout_of(const moe_config_t& c) {
   const int64_t nblk = permute_num_blocks(A);
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o += align_up(bytes > 0 ? bytes : 1); return at; };
-  // [0] status word, [1] router ticket
-  L.status_bytes = 16;
+  // The header every call zeroes first: [0] status word, [1] router ticket,
+  // then the row-block counters of the routed and the shared expert FFN
+  // launches (phase 0 -> phase 1 hand-over).
+  const int64_t nrd = R > 0 ? gemm_rows_done_len(R, (int)N) : 0;
+  const int64_t nrd_s = (c.F_shared > 0 && T > 0) ? gemm_rows_done_len(T, 1) : 0;
+  L.status_bytes = align_up(sizeof(int32_t) * (4 + nrd + nrd_s));
   L.status = take(L.status_bytes);
+  L.rows_done = L.status + 16;
+  L.rows_done_s = L.rows_done + sizeof(int32_t) * nrd;
   const bool tc = c.N <= kRouterTcMaxExperts;
   L.w3 = take(tc ? router_w3_bytes(c.N, c.H) : 0);
   L.logits = take(tc ? 0 : sizeof(float) * T * N);
@@ -251,84 +258,69 @@ moe_status_t do_ffn(const moe_config_t& c, const uint16_t* x, const int32_t* per
     if (!gathered)
       MOE_CUDA(launch_gather(reinterpret_cast<const bf*>(x), perm, offsets, c.N, c.k, R, c.H, xp,
                              st, tr));
-    GemmArgs g1{};
-    g1.offsets = offsets;
-    g1.num_groups = c.N;
-    g1.n_out = c.F;
-    g1.K = c.H;
-    g1.mode = EPI_GELU;
-    g1.bias = reinterpret_cast<const bf*>(W.b1);
-    g1.out = hid;
-    g1.ld_out = c.F;
-    g1.status = status;
-    g1.skip_producer = take_suppress_producer();
-    GemmPlan p1;
-    MOE_CUDA(make_gemm_plan(&p1, xp, R, reinterpret_cast<const bf*>(W.W1), (int64_t)c.N * c.F,
-                            g1, sms));
-    MOE_CUDA(launch_gemm(p1, st, tr));
-    GemmArgs g2{};
-    g2.offsets = offsets;
-    g2.num_groups = c.N;
-    g2.n_out = c.H;
-    g2.K = c.F;
-    g2.mode = EPI_SCALE;
-    g2.bias = reinterpret_cast<const bf*>(W.b2);
-    g2.topk_w = topk_w;
-    g2.perm = perm;
-    g2.out = reinterpret_cast<bf*>(y);
-    g2.ld_out = c.H;
-    g2.status = status;
-    g2.skip_producer = take_suppress_producer();
-
-    GemmPlan p2;
-    MOE_CUDA(make_gemm_plan(&p2, hid, R, reinterpret_cast<const bf*>(W.W2), (int64_t)c.N * c.H,
-                            g2, sms));
-    MOE_CUDA(launch_gemm(p2, st, tr));
+    // one persistent launch: Hid = GELU(X_perm W1_e^T + b1_e), then
+    // y = w * (Hid W2_e^T + b2_e), row block by row block
+    GemmArgs g{};
+    g.offsets = offsets;
+    g.num_groups = c.N;
+    g.num_phases = 2;
+    g.ph[0].n_out = c.F;
+    g.ph[0].K = c.H;
+    g.ph[0].mode = EPI_GELU;
+    g.ph[0].bias = reinterpret_cast<const bf*>(W.b1);
+    g.ph[0].out = hid;
+    g.ph[0].ld_out = c.F;
+    g.ph[1].n_out = c.H;
+    g.ph[1].K = c.F;
+    g.ph[1].mode = EPI_SCALE;
+    g.ph[1].bias = reinterpret_cast<const bf*>(W.b2);
+    g.ph[1].topk_w = topk_w;
+    g.ph[1].perm = perm;
+    g.ph[1].out = reinterpret_cast<bf*>(y);
+    g.ph[1].ld_out = c.H;
+    g.rows_done = at<int32_t>(ws, L.rows_done);
+    g.status = status;
+    g.skip_producer = take_suppress_producer();
+    const bf* B[2] = {reinterpret_cast<const bf*>(W.W1), reinterpret_cast<const bf*>(W.W2)};
+    const int64_t b_rows[2] = {(int64_t)c.N * c.F, (int64_t)c.N * c.H};
+    GemmPlan p;
+    MOE_CUDA(make_gemm_plan(&p, g, xp, R, B, b_rows, sms));
+    MOE_CUDA(launch_gemm(p, st, tr));
   }
   if (c.F_shared > 0 && c.T > 0) {
-    bf* hs = at<bf>(ws, L.hid_s);
-    GemmArgs s1{};
-    s1.offsets = nullptr;
-    s1.num_groups = 1;
-    s1.rows_single = c.T;
-    s1.n_out = c.F_shared;
-    s1.K = c.H;
-    s1.mode = EPI_GELU;
-    s1.bias = reinterpret_cast<const bf*>(W.b1s);
-    s1.out = hs;
-    s1.ld_out = c.F_shared;
-    s1.status = status;
-    s1.skip_producer = take_suppress_producer();
-    GemmPlan ps1;
-    MOE_CUDA(make_gemm_plan(&ps1, reinterpret_cast<const bf*>(x), c.T,
-                            reinterpret_cast<const bf*>(W.W1s), c.F_shared, s1, sms));
-    MOE_CUDA(launch_gemm(ps1, st, tr));
-    GemmArgs s2{};
-    s2.offsets = nullptr;
-    s2.num_groups = 1;
-    s2.rows_single = c.T;
-    s2.n_out = c.H;
-    s2.K = c.F_shared;
-    s2.mode = EPI_SCALE;
-    s2.bias = reinterpret_cast<const bf*>(W.b2s);
-    s2.topk_w = nullptr;
-    s2.perm = nullptr;
-    s2.out = reinterpret_cast<bf*>(y_shared);
-    s2.ld_out = c.H;
-    s2.status = status;
-    s2.skip_producer = take_suppress_producer();
-
-    GemmPlan ps2;
-    MOE_CUDA(make_gemm_plan(&ps2, hs, c.T, reinterpret_cast<const bf*>(W.W2s), c.H, s2, sms));
-    MOE_CUDA(launch_gemm(ps2, st, tr));
+    GemmArgs g{};
+    g.offsets = nullptr;
+    g.num_groups = 1;
+    g.rows_single = c.T;
+    g.num_phases = 2;
+    g.ph[0].n_out = c.F_shared;
+    g.ph[0].K = c.H;
+    g.ph[0].mode = EPI_GELU;
+    g.ph[0].bias = reinterpret_cast<const bf*>(W.b1s);
+    g.ph[0].out = at<bf>(ws, L.hid_s);
+    g.ph[0].ld_out = c.F_shared;
+    g.ph[1].n_out = c.H;
+    g.ph[1].K = c.F_shared;
+    g.ph[1].mode = EPI_SCALE;
+    g.ph[1].bias = reinterpret_cast<const bf*>(W.b2s);
+    g.ph[1].out = reinterpret_cast<bf*>(y_shared);
+    g.ph[1].ld_out = c.H;
+    g.rows_done = at<int32_t>(ws, L.rows_done_s);
+    g.status = status;
+    g.skip_producer = take_suppress_producer();
+    const bf* B[2] = {reinterpret_cast<const bf*>(W.W1s), reinterpret_cast<const bf*>(W.W2s)};
+    const int64_t b_rows[2] = {(int64_t)c.F_shared, (int64_t)c.H};
+    GemmPlan p;
+    MOE_CUDA(make_gemm_plan(&p, g, reinterpret_cast<const bf*>(x), c.T, B, b_rows, sms));
+    MOE_CUDA(launch_gemm(p, st, tr));
   }
   return MOE_OK;
 }
 
 int ffn_num_launches(const moe_config_t& c, bool gathered) {
   int n = 0;
-  if (max_rows_of(c) > 0) n += gathered ? 2 : 3;
-  if (c.F_shared > 0 && c.T > 0) n += 2;
+  if (max_rows_of(c) > 0) n += gathered ? 1 : 2;
+  if (c.F_shared > 0 && c.T > 0) n += 1;
   return n;
 }
 

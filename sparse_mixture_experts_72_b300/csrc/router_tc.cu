@@ -46,13 +46,15 @@ constexpr int RT_A_BYTES = RT_BM * RT_BK * 2;
 constexpr int kRouterTcSmemMax = 227 * 1024;
 
 // Plane p of W_g: hi, mid, lo with W_g = hi + mid + lo exactly.
-// It also zeroes `clear` (the status word and router ticket of a forward
-// pass), which saves a separate memset launch.
+// It also zeroes `clear` (the header of a forward pass's workspace: status
+// word, router ticket and the expert FFN's row-block counters), which saves
+// a separate memset launch.
 __global__ void __launch_bounds__(256) router_split_kernel(const float* __restrict__ Wg,
                                                            __nv_bfloat16* __restrict__ W3, int N,
                                                            int H, int N_pad, int H_pad,
                                                            int stacked, int* clear, int clear_n) {
-  if (clear && blockIdx.x == 0 && threadIdx.x < clear_n) clear[threadIdx.x] = 0;
+  if (clear && blockIdx.x == 0)
+    for (int i = threadIdx.x; i < clear_n; i += blockDim.x) clear[i] = 0;
   const int64_t total = (int64_t)N_pad * H_pad;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {

@@ -57,14 +57,15 @@ def test_algorithmic_work_counts():
     w = wl.WORKLOADS["moelayer"]
     counts = np.full(w.N, w.T * w.k // w.N)
     work = bench.algorithmic_work(w, counts, w.T * w.k)
-    assert work["gemm1"]["flops"] == 2 * 8192 * 1024 * 4096
-    assert work["gemm1"]["bytes"] == 2 * (8 * 4096 * 1024 + 8192 * 1024 + 8192 * 4096)
+    # both Linears of all 8192 kept rows; both weight matrices of the 8 experts
+    assert work["expert_ffn"]["flops"] == 4 * 8192 * 1024 * 4096
+    assert work["expert_ffn"]["bytes"] == 2 * (2 * 8 * 4096 * 1024 + 2 * 8192 * 1024)
     d = wl.WORKLOADS["deepseek_prefill"]
     wk = bench.algorithmic_work(d, np.ones(d.N), d.T * d.k)
-    assert "gemm1_shared" in wk and wk["gemm2_shared"]["flops"] == 2 * d.T * d.F_shared * d.H
+    assert "shared_ffn" in wk and wk["shared_ffn"]["flops"] == 4 * d.T * d.F_shared * d.H
 
 
 def test_peaks_and_traffic_lookup():
     peaks, src = bench.load_peaks()
     assert peaks["hbm_gbs"] > 0 and peaks["bf16_tflops"] > 0
-    assert bench.committed_traffic("no_such_workload", "gemm1") is None
+    assert bench.committed_traffic("no_such_workload", "expert_ffn") is None
