@@ -142,18 +142,20 @@ class ClockSampler:
 def algorithmic_work(w: wl.Workload, counts: np.ndarray, R: int):
     """FLOPs and bytes each expert-FFN launch must do at minimum.
 
-    Per kept row: 2*H*F FLOPs in each of the two Linears.  Bytes: both weight
+    Per kept row: 2*H*F FLOPs in each Linear (two, or three for SwiGLU's
+    gate, up and down).  Bytes: the weight
     matrices of every expert that received a row (2*F*H bf16), the token rows
     read (R*H bf16) and the weighted rows written (R*H bf16); the hidden
     activations between the two Linears are the implementation's own round
     trip and are not counted."""
     hit = int((np.asarray(counts) > 0).sum())
-    out = {"expert_ffn": dict(flops=4.0 * R * w.H * w.F,
-                              bytes=2.0 * (2 * hit * w.F * w.H + 2 * R * w.H))}
+    m = 3 if w.activation == "swiglu" else 2   # weight matrices per expert (gate, up, down)
+    out = {"expert_ffn": dict(flops=2.0 * m * R * w.H * w.F,
+                              bytes=2.0 * (m * hit * w.F * w.H + 2 * R * w.H))}
     if w.F_shared:
         Fs = w.F_shared
-        out["shared_ffn"] = dict(flops=4.0 * w.T * w.H * Fs,
-                                 bytes=2.0 * (2 * Fs * w.H + 2 * w.T * w.H))
+        out["shared_ffn"] = dict(flops=2.0 * m * w.T * w.H * Fs,
+                                 bytes=2.0 * (m * Fs * w.H + 2 * w.T * w.H))
     return out
 
 
@@ -166,10 +168,14 @@ def launch_names(w: wl.Workload, has_rows: bool):
     if not (tc_router and w.T > 0):
         names += ["status_memset"]
     if tc_router:  # tensor-core router: W_g split + fused router
-        names += ["router_split", "router_tc"] if w.T > 0 else ["p_mean_memset"]
+        names += ["router_split", "router_tc"] if w.T > 0 else ["router_pmean"]
     else:
         names += ["router_logits", "router_select", "router_pmean"] if w.T > 0 else ["router_pmean"]
-    if w.T * w.k > 0:
+    if w.routing == "expert":
+        names += ["expert_choice"]
+        if has_rows:
+            names += ["gather_rows"]
+    elif w.T * w.k > 0:
         names += ["permute_rank", "permute_scan", "scatter_gather"]
     else:
         names += ["permute_scan"]
@@ -217,7 +223,9 @@ def oracle_step(w: wl.Workload, x_bits, router, getter, shared, rows: slice):
     from oracle import moe_oracle as O
     Wg, bg, sel = router
     xs = wl.bf16_bits_to_f64(x_bits[rows])
-    return O.forward(xs, Wg, bg, sel, w.k, w.capacity_factor, w.aux_alpha, getter, shared)
+    return O.forward(xs, Wg, bg, sel, w.k, w.capacity_factor, w.aux_alpha, getter, shared,
+                     routing=w.routing, activation=w.activation, min_capacity=w.min_capacity,
+                     drop_order=w.drop_order)
 
 
 def oracle_timing(w: wl.Workload, steps: int, warmup: int, budget_s: float, seed: int = 0):
@@ -289,8 +297,7 @@ def run_ours(args):
     import sparse_mixture_experts_72_b300 as m
 
     w = wl.get_workload(args.workload)
-    cfg = m.MoEConfig(T=w.T, H=w.H, F=w.F, N=w.N, k=w.k, capacity_factor=w.capacity_factor,
-                      F_shared=w.F_shared, aux_alpha=w.aux_alpha)
+    cfg = m.MoEConfig(**w.config_kwargs())
     # replicas share the weights; each rank draws its own batch
     d = wl.to_device(w, seed=0, device=device, x_seed=None if rank == 0 else 1000 + rank)
     weights = m.MoEWeights(Wg=d["Wg"], W1=d["W1"], W2=d["W2"], bg=d["bg"], sel_bias=d["sel_bias"],
@@ -420,6 +427,7 @@ def run_ours(args):
                 "data": "synthetic",
                 "config": {"workload": w.name, "T": w.T, "H": w.H, "F": w.F, "N": w.N, "k": w.k,
                            "capacity_factor": w.capacity_factor, "F_shared": w.F_shared,
+                           "routing": w.routing, "activation": w.activation,
                            "kept_rows": R, "experts_hit": int((counts > 0).sum()),
                            "l2": "flushed between steps (256 MiB write, untimed)",
                            "launch": "CUDA graph replay of moe_forward; every 10th step replays a copy with an event node before each launch",

@@ -59,15 +59,37 @@ typedef enum {
 #define MOE_TRACE_MAX_EVENTS 32
 
 /* Layer shape and routing parameters. */
+/* routing: who chooses.  Token choice is the pages' top-k router
+ * ("混合专家模型 MoE 架构深度解析" §1.3); expert choice lets each expert take
+ * its C highest-scoring tokens ("AI-Research-SKILLs MoE 训练实战" §4.2, §7.3). */
+#define MOE_ROUTING_TOKEN_CHOICE 0
+#define MOE_ROUTING_EXPERT_CHOICE 1
+/* activation of the expert FFN: GELU (§3.1's MoELayer), SiLU (the two-Linear
+ * expert printed in §6.1) or SwiGLU (the gated form §6.1's text names for
+ * Mixtral: W1 then holds [N, 2F, H], gate rows first, up rows second). */
+#define MOE_ACT_GELU 0
+#define MOE_ACT_SILU 1
+#define MOE_ACT_SWIGLU 2
+/* which assignments claim capacity first: token-major (a = t*k + j in
+ * increasing a) or slot-major (every token's first choice, then every
+ * token's second choice, ...). */
+#define MOE_DROP_TOKEN_MAJOR 0
+#define MOE_DROP_SLOT_MAJOR 1
+
 typedef struct {
   int32_t T;                /* tokens (rows of x); 0 is allowed */
   int32_t H;                /* hidden size */
   int32_t F;                /* routed expert FFN inner size */
   int32_t N;                /* routed experts, 1..MOE_MAX_EXPERTS */
-  int32_t k;                /* experts per token, 1..min(N, MOE_MAX_TOP_K) */
+  int32_t k;                /* experts per token, 1..min(N, MOE_MAX_TOP_K); token choice */
   float capacity_factor;    /* > 0: C = floor(T / N * capacity_factor); <= 0: no limit */
   int32_t F_shared;         /* shared expert inner size; 0 = no shared expert */
   float aux_alpha;          /* alpha of L_aux (the pages use 0.01) */
+  int32_t routing;          /* MOE_ROUTING_*; expert choice needs capacity_factor > 0 */
+  int32_t activation;       /* MOE_ACT_*; the shared expert uses the same one */
+  int32_t min_capacity;     /* >= 0: C = max(C, min_capacity) when a capacity applies
+                               (the DeepSpeed moe block's min_capacity, §5.1) */
+  int32_t drop_order;       /* MOE_DROP_* (token choice with a capacity) */
 } moe_config_t;
 
 /* Layer parameters (device pointers). */
@@ -75,38 +97,44 @@ typedef struct {
   const float* Wg;          /* [N, H] fp32 gate weight, required */
   const float* bg;          /* [N] fp32 gate bias, or NULL (= 0) */
   const float* sel_bias;    /* [N] fp32 selection-only bias b_i, or NULL (= 0) */
-  const uint16_t* W1;       /* [N, F, H] bf16, required */
-  const uint16_t* b1;       /* [N, F] bf16 or NULL */
+  const uint16_t* W1;       /* [N, F, H] bf16 ([N, 2F, H] for SwiGLU), required */
+  const uint16_t* b1;       /* [N, F] ([N, 2F] for SwiGLU) bf16 or NULL */
   const uint16_t* W2;       /* [N, H, F] bf16, required */
   const uint16_t* b2;       /* [N, H] bf16 or NULL */
-  const uint16_t* W1s;      /* [Fs, H] bf16, required iff F_shared > 0 */
-  const uint16_t* b1s;      /* [Fs] bf16 or NULL */
+  const uint16_t* W1s;      /* [Fs, H] ([2Fs, H] for SwiGLU) bf16, required iff F_shared > 0 */
+  const uint16_t* b1s;      /* [Fs] ([2Fs] for SwiGLU) bf16 or NULL */
   const uint16_t* W2s;      /* [H, Fs] bf16, required iff F_shared > 0 */
   const uint16_t* b2s;      /* [H] bf16 or NULL */
 } moe_weights_t;
 
-/* Optional device outputs of moe_forward; each may be NULL (kept in ws). */
+/* Optional device outputs of moe_forward; each may be NULL (kept in ws).
+ * "Slots per token" S is k for token choice and N for expert choice, where
+ * assignment a = t*N + e means expert e took token t. */
 typedef struct {
-  int32_t* topk_idx;        /* [T, k] */
-  float* topk_w;            /* [T, k] */
+  int32_t* topk_idx;        /* [T, k] (token choice) */
+  float* topk_w;            /* [T, k] (token choice) */
   float* probs;             /* [T, N] full softmax; written only when non-NULL */
   float* p_mean;            /* [N]   p_i = mean_t P[t, i] */
   int32_t* counts;          /* [N]   assignments per expert before capacity drops */
   int32_t* offsets;         /* [N+1] expert-contiguous row offsets after drops */
-  int32_t* perm;            /* [moe_max_rows(cfg)] row -> assignment t*k+j */
-  int32_t* inv;             /* [T*k] assignment -> row, -1 if dropped */
-  float* f;                 /* [N]   f_i = counts_i / (T*k) */
+  int32_t* perm;            /* [moe_max_rows(cfg)] row -> assignment t*S+j */
+  int32_t* inv;             /* [T*S] assignment -> row, -1 if dropped / not taken */
+  float* f;                 /* [N]   f_i = counts_i / sum_e counts_e */
   float* l_aux;             /* [1]   alpha * N * sum f_i p_i */
+  float* z_loss;            /* [1]   router z-loss, mean_t logsumexp(l_t)^2 */
+  float* logits;            /* [T, N] gate logits l = x W_g^T + b_g */
 } moe_outputs_t;
 
 /* Bytes of workspace the entry points need for this configuration. */
 size_t moe_workspace_size(const moe_config_t* cfg);
 
-/* Upper bound on kept rows R: T*k, or min(T*k, N*C) with a capacity limit. */
+/* Upper bound on kept rows R: T*k, or min(T*k, N*C) with a capacity limit;
+ * N*min(C, T) for expert choice. */
 int64_t moe_max_rows(const moe_config_t* cfg);
 
 /* Capacity C of "混合专家模型 MoE 架构深度解析" §2.3, computed in double as
- * floor((double)T / N * capacity_factor); -1 when there is no limit. */
+ * floor((double)T / N * capacity_factor), then raised to min_capacity; -1
+ * when there is no limit. */
 int64_t moe_capacity(const moe_config_t* cfg);
 
 /* Number of kernel launches (and memsets) one moe_forward call enqueues. */
@@ -115,26 +143,65 @@ int32_t moe_forward_num_launches(const moe_config_t* cfg);
 /*
  * moe_route - gate, softmax, top-k selection and renormalisation.
  * ("混合专家模型 MoE 架构深度解析" §1.2 gate formula, §1.3 top-K steps 1-3,
- *  §2.4 selection bias; "AI-Research-SKILLs MoE 训练实战" §3.1 MoELayer gate.)
+ *  §2.4 selection bias; "AI-Research-SKILLs MoE 训练实战" §3.1 MoELayer gate,
+ *  §4.3 router z-loss.)
  *   x        [T, H] bf16          Wg [N, H] fp32, bg [N] fp32 or NULL
  *   sel_bias [N] fp32 or NULL     subtracted from the logits for selection only
  *   topk_idx [T, k] int32 out     experts in descending (l - b_sel); ties -> lower index
  *   topk_w   [T, k] fp32 out      unbiased softmax at idx, renormalised to sum 1
+ *            (both NULL, and not computed, for expert choice)
  *   probs    [T, N] fp32 out or NULL   full softmax
+ *   logits   [T, N] fp32 out or NULL   l = x W_g^T + b_g
  *   p_mean   [N] fp32 out         mean over tokens of the softmax (p_i of L_aux)
+ *   z_loss   [1] fp32 out or NULL mean over tokens of logsumexp(l_t)^2
  * Logits accumulate in fp32.
  */
 moe_status_t moe_route(const moe_config_t* cfg, const uint16_t* x, const float* Wg,
                        const float* bg, const float* sel_bias, int32_t* topk_idx,
-                       float* topk_w, float* probs, float* p_mean, void* ws,
-                       size_t ws_bytes, void* stream);
+                       float* topk_w, float* probs, float* logits, float* p_mean,
+                       float* z_loss, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * moe_expert_choice - expert-choice dispatch ("AI-Research-SKILLs MoE 训练实战"
+ * §4.2: expert_scores = router(x) transposed, top-k along the tokens with
+ * k = capacity_per_expert; §7.3: perfect balance, no token dropped for load).
+ * Expert e takes the C = moe_capacity(cfg) (at most T) tokens with the largest
+ * logits[:, e]; equal logits take the lower token first.  Its rows are
+ * [e*C, (e+1)*C), tokens in increasing order; assignment a = t*N + e.
+ *   logits [T, N] fp32 in (moe_route); p_mean [N] fp32 in, or NULL when l_aux is NULL
+ *   counts [N] int32 out (C each)  offsets [N+1] int32 out (e*C)
+ *   perm [N*C] int32 out           inv [T*N] int32 out (row, or -1: not taken)
+ *   f [N] fp32 out or NULL (1/N)   l_aux [1] fp32 out or NULL (alpha * N * sum f_i p_i)
+ * Needs routing = MOE_ROUTING_EXPERT_CHOICE, capacity_factor > 0 and
+ * T <= 51200 (the per-expert column is staged in shared memory); otherwise
+ * MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED before any launch.  One launch,
+ * no workspace.
+ */
+moe_status_t moe_expert_choice(const moe_config_t* cfg, const float* logits,
+                               const float* p_mean, int32_t* counts, int32_t* offsets,
+                               int32_t* perm, int32_t* inv, float* f, float* l_aux,
+                               void* stream);
+
+/*
+ * moe_update_sel_bias - one auxiliary-loss-free balancing step
+ * ("混合专家模型 MoE 架构深度解析" §2.4): the selection bias of an expert that
+ * received more than the mean number of assignments rises by gamma, that of
+ * one that received fewer falls by gamma, an expert at the mean keeps its
+ * bias:  sel_bias[e] += gamma * sign(counts[e] - sum(counts) / N).
+ * The pages give no rate; gamma is the caller's.
+ *   counts [N] int32 in (moe_permute / moe_forward), sel_bias [N] fp32 in/out
+ * One launch, no workspace.
+ */
+moe_status_t moe_update_sel_bias(const moe_config_t* cfg, const int32_t* counts,
+                                 float* sel_bias, float gamma, void* stream);
 
 /*
  * moe_permute - histogram, capacity, stable expert-contiguous dispatch and L_aux.
  * ("混合专家模型 MoE 架构深度解析" §2.3 capacity and overflow, §2.2 L_aux;
  *  "AI-Research-SKILLs MoE 训练实战" §4.3 expert fraction, §4.4 drop_tokens.)
- * Assignment a = t*k + j claims slots in increasing a; rank within its
- * expert >= C means dropped.
+ * Assignments a = t*k + j claim slots in increasing a (drop_order token-
+ * major) or j-major then t (slot-major); rank within its expert >= C means
+ * dropped.  Token choice only.
  *   topk_idx [T, k] int32 in; values must lie in [0, N) (not checked on device:
  *            out-of-range indices are ignored by the histogram and dropped)
  *   p_mean   [N] fp32 in (from moe_route); may be NULL when l_aux is NULL
@@ -148,13 +215,17 @@ moe_status_t moe_permute(const moe_config_t* cfg, const int32_t* topk_idx, const
                          float* f, float* l_aux, void* ws, size_t ws_bytes, void* stream);
 
 /*
- * moe_expert_ffn - gather, expert Linear -> GELU -> Linear, gate weighting.
+ * moe_expert_ffn - gather, expert Linear -> activation -> Linear, gate weighting.
  * ("AI-Research-SKILLs MoE 训练实战" §3.1 expert = Linear(H,F), GELU, Linear(F,H);
- *  §7.1 and "混合专家模型 MoE 架构深度解析" §3 shared expert.)
- *   y[r]        = bf16( w_a * (W2_e . bf16(GELU(W1_e . x_t + b1_e)) + b2_e) )
- *                 for rows r < offsets[N], a = perm[r], t = a / k, e the expert of r
- *   y_shared[t] = bf16( W2s . bf16(GELU(W1s . x_t + b1s)) + b2s )   when F_shared > 0
- *   x [T, H] bf16; perm/offsets from moe_permute; topk_w [T, k] fp32
+ *  §6.1 SiLU / SwiGLU; §7.1 and "混合专家模型 MoE 架构深度解析" §3 shared expert.)
+ *   y[r]        = bf16( w_a * (W2_e . bf16(act(W1_e . x_t + b1_e)) + b2_e) )
+ *                 for rows r < offsets[N], a = perm[r], t = a / S, e the expert of r
+ *                 (S = k, or N for expert choice)
+ *   y_shared[t] = bf16( W2s . bf16(act(W1s . x_t + b1s)) + b2s )   when F_shared > 0
+ *   act: GELU(z), SiLU(z), or SiLU(z[:F]) * z[F:] for SwiGLU
+ *   x [T, H] bf16; perm/offsets from moe_permute or moe_expert_choice;
+ *   topk_w [T, S] fp32 (the renormalised top-k weights, or the softmax
+ *   probs [T, N] for expert choice)
  *   y [moe_max_rows, H] bf16 out; y_shared [T, H] bf16 out (NULL iff F_shared == 0)
  * bf16 x bf16 products accumulate in fp32 on the tensor cores.
  */
@@ -166,10 +237,11 @@ moe_status_t moe_expert_ffn(const moe_config_t* cfg, const uint16_t* x, const in
 /*
  * moe_combine - weighted sum back per token ("AI-Research-SKILLs MoE 训练实战"
  * §3.1 output[mask] += score * expert_out; §6.1 index_add_ combine).
- *   out[t] = bf16( sum_{j<k, inv[t*k+j] >= 0} y[inv[t*k+j]] (+ y_shared[t]) )
- * summed in fp32 in the order j = 0..k-1, then the shared term.  A token
- * whose every slot was dropped gets 0 (+ its shared term).
- *   y [moe_max_rows, H] bf16, inv [T*k] int32, y_shared [T, H] bf16 or NULL
+ *   out[t] = bf16( sum_{j<S, inv[t*S+j] >= 0} y[inv[t*S+j]] (+ y_shared[t]) )
+ * summed in fp32 in the order j = 0..S-1, then the shared term (S = k, or N
+ * for expert choice).  A token whose every slot was dropped (or that no
+ * expert took) gets 0 (+ its shared term).
+ *   y [moe_max_rows, H] bf16, inv [T*S] int32, y_shared [T, H] bf16 or NULL
  *   out [T, H] bf16
  */
 moe_status_t moe_combine(const moe_config_t* cfg, const uint16_t* y, const int32_t* inv,

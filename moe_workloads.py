@@ -54,6 +54,23 @@ class Workload:
     F_shared: int = 0                 # 0: no shared expert
     aux_alpha: float = 0.01
     phase: str = "prefill"            # "prefill" | "decode" (which roof bounds it)
+    routing: str = "token"            # "token" (top-k per token) | "expert" (top-C per expert)
+    activation: str = "gelu"          # "gelu" | "silu" | "swiglu" (W1 holds gate + up rows)
+    min_capacity: int = 0
+    drop_order: str = "token"         # "token" | "slot"
+
+    @property
+    def w1_rows(self) -> int:
+        """Rows of one expert's W1: F, or 2F (gate rows, then up rows) for SwiGLU."""
+        return 2 * self.F if self.activation == "swiglu" else self.F
+
+    def config_kwargs(self) -> dict:
+        """The layer configuration of this workload, as keyword arguments of the
+        binding's MoEConfig (shapes and options only)."""
+        return dict(T=self.T, H=self.H, F=self.F, N=self.N, k=self.k,
+                    capacity_factor=self.capacity_factor, F_shared=self.F_shared,
+                    aux_alpha=self.aux_alpha, routing=self.routing, activation=self.activation,
+                    min_capacity=self.min_capacity, drop_order=self.drop_order)
 
     def with_tokens(self, T: int, name: Optional[str] = None) -> "Workload":
         return replace(self, T=T, name=name or f"{self.name}_T{T}")
@@ -76,6 +93,14 @@ WORKLOADS: Dict[str, Workload] = {w.name: w for w in [
     # Switch-style top-1 with capacity 1.25 and Zipf(1.1)-skewed gate offsets
     Workload("switch_capacity", T=32768, H=2048, F=8192, N=64, k=1,
              capacity_factor=1.25, gate_bias="zipf1.1"),
+    # expert-choice routing on the MoELayer shapes: capacity factor 2 gives
+    # each expert C = 1024 tokens, the same rows (and FLOPs) as top-2
+    Workload("moelayer_expert_choice", T=4096, H=1024, F=4096, N=8, k=2, capacity_factor=2.0,
+             gate_bias="zero", expert_bias="zero", routing="expert"),
+    # Mixtral's gated expert: W1 holds gate and up (SwiGLU), bias-free
+    Workload("mixtral_swiglu_prefill", T=16384, H=4096, F=14336, N=8, k=2, activation="swiglu"),
+    Workload("mixtral_swiglu_decode", T=64, H=4096, F=14336, N=8, k=2, activation="swiglu",
+             phase="decode"),
 ]}
 
 # Extra small cases for tests (not benchmark lines).
@@ -99,6 +124,24 @@ TEST_WORKLOADS: Dict[str, Workload] = {w.name: w for w in [
     Workload("all_dropped", T=40, H=64, F=64, N=16, k=2, capacity_factor=0.1, F_shared=64),
     # more experts than the tensor-core router takes: the fp32 SIMT router runs
     Workload("many_experts", T=200, H=64, F=64, N=300, k=4, gate_bias="normal"),
+    # widened rows
+    Workload("small_silu", T=500, H=128, F=256, N=8, k=2, expert_bias="normal",
+             activation="silu", F_shared=128),
+    Workload("small_swiglu", T=600, H=192, F=320, N=8, k=2, expert_bias="normal",
+             activation="swiglu", F_shared=136, gate_bias="normal"),
+    Workload("swiglu_pairs", T=4096, H=256, F=384, N=4, k=2, activation="swiglu"),
+    Workload("small_expert_choice", T=300, H=128, F=192, N=6, k=1, capacity_factor=1.5,
+             gate_bias="normal", expert_bias="normal", routing="expert", F_shared=64),
+    Workload("expert_choice_ragged", T=777, H=136, F=264, N=12, k=1, capacity_factor=0.9,
+             gate_bias="zipf1.1", routing="expert", activation="swiglu"),
+    Workload("expert_choice_all", T=64, H=64, F=64, N=4, k=1, capacity_factor=4.0,
+             routing="expert"),
+    Workload("many_experts_choice", T=200, H=64, F=64, N=300, k=1, capacity_factor=3.0,
+             gate_bias="normal", routing="expert"),
+    Workload("slot_major_capacity", T=1000, H=128, F=128, N=8, k=2, capacity_factor=0.8,
+             gate_bias="zipf1.1", drop_order="slot"),
+    Workload("min_capacity", T=40, H=64, F=64, N=16, k=2, capacity_factor=0.1, min_capacity=4,
+             F_shared=64),
 ]}
 
 
@@ -197,15 +240,15 @@ def gen_router(w: Workload, seed: int = 0):
 
 
 def gen_expert(w: Workload, seed: int, e: int):
-    """bf16 bits of routed expert e: (W1 [F,H], b1 [F]|None, W2 [H,F], b2 [H]|None)."""
-    W1 = f32_to_bf16_bits(_normal(seed, "W1", e, (w.F, w.H), 1.0 / math.sqrt(w.H)))
+    """bf16 bits of routed expert e: (W1 [F,H] ([2F,H] for SwiGLU), b1|None, W2 [H,F], b2 [H]|None)."""
+    W1 = f32_to_bf16_bits(_normal(seed, "W1", e, (w.w1_rows, w.H), 1.0 / math.sqrt(w.H)))
     W2 = f32_to_bf16_bits(_normal(seed, "W2", e, (w.H, w.F), 1.0 / math.sqrt(w.F)))
     b1 = b2 = None
     if w.expert_bias == "zero":
-        b1 = np.zeros(w.F, dtype=np.uint16)
+        b1 = np.zeros(w.w1_rows, dtype=np.uint16)
         b2 = np.zeros(w.H, dtype=np.uint16)
     elif w.expert_bias == "normal":
-        b1 = f32_to_bf16_bits(_normal(seed, "b1", e, (w.F,), 0.1))
+        b1 = f32_to_bf16_bits(_normal(seed, "b1", e, (w.w1_rows,), 0.1))
         b2 = f32_to_bf16_bits(_normal(seed, "b2", e, (w.H,), 0.1))
     elif w.expert_bias is not None:
         raise ValueError(w.expert_bias)
@@ -217,14 +260,15 @@ def gen_shared(w: Workload, seed: int = 0):
     if w.F_shared <= 0:
         return None
     Fs = w.F_shared
-    W1s = f32_to_bf16_bits(_normal(seed, "W1s", 0, (Fs, w.H), 1.0 / math.sqrt(w.H)))
+    Fs1 = 2 * Fs if w.activation == "swiglu" else Fs
+    W1s = f32_to_bf16_bits(_normal(seed, "W1s", 0, (Fs1, w.H), 1.0 / math.sqrt(w.H)))
     W2s = f32_to_bf16_bits(_normal(seed, "W2s", 0, (w.H, Fs), 1.0 / math.sqrt(Fs)))
     b1s = b2s = None
     if w.expert_bias == "normal":
-        b1s = f32_to_bf16_bits(_normal(seed, "b1s", 0, (Fs,), 0.1))
+        b1s = f32_to_bf16_bits(_normal(seed, "b1s", 0, (Fs1,), 0.1))
         b2s = f32_to_bf16_bits(_normal(seed, "b2s", 0, (w.H,), 0.1))
     elif w.expert_bias == "zero":
-        b1s = np.zeros(Fs, dtype=np.uint16)
+        b1s = np.zeros(Fs1, dtype=np.uint16)
         b2s = np.zeros(w.H, dtype=np.uint16)
     return W1s, b1s, W2s, b2s
 
@@ -233,10 +277,10 @@ def gen_all(w: Workload, seed: int = 0, threads: Optional[int] = None) -> dict:
     """Every input of the layer as host arrays (bf16 tensors as uint16 bits)."""
     x = gen_x(w, seed, threads)
     Wg, bg, sel = gen_router(w, seed)
-    W1 = np.empty((w.N, w.F, w.H), dtype=np.uint16)
+    W1 = np.empty((w.N, w.w1_rows, w.H), dtype=np.uint16)
     W2 = np.empty((w.N, w.H, w.F), dtype=np.uint16)
     has_b = w.expert_bias is not None
-    b1 = np.empty((w.N, w.F), dtype=np.uint16) if has_b else None
+    b1 = np.empty((w.N, w.w1_rows), dtype=np.uint16) if has_b else None
     b2 = np.empty((w.N, w.H), dtype=np.uint16) if has_b else None
 
     def job(e):
@@ -301,10 +345,10 @@ def to_device(w: Workload, seed: int = 0, device="cuda", x_seed: Optional[int] =
     import torch
     x_bits = gen_x(w, seed if x_seed is None else x_seed)
     Wg, bg, sel = gen_router(w, seed)
-    W1 = torch.empty((w.N, w.F, w.H), dtype=torch.bfloat16, device=device)
+    W1 = torch.empty((w.N, w.w1_rows, w.H), dtype=torch.bfloat16, device=device)
     W2 = torch.empty((w.N, w.H, w.F), dtype=torch.bfloat16, device=device)
     has_b = w.expert_bias is not None
-    b1 = torch.empty((w.N, w.F), dtype=torch.bfloat16, device=device) if has_b else None
+    b1 = torch.empty((w.N, w.w1_rows), dtype=torch.bfloat16, device=device) if has_b else None
     b2 = torch.empty((w.N, w.H), dtype=torch.bfloat16, device=device) if has_b else None
     batch = 32
     with ThreadPoolExecutor(min(32, max(1, w.N))) as ex:

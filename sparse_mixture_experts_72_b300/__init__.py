@@ -24,7 +24,7 @@ __all__ = ["MoEConfig", "MoEWeights", "MoeError", "moe_workspace_size", "moe_max
            "moe_capacity", "moe_forward_num_launches", "moe_route", "moe_permute",
            "moe_permute_static",
            "moe_expert_ffn", "moe_combine", "moe_forward", "moe_workspace_status",
-           "moe_debug_suppress_gemm_producer",
+           "moe_debug_suppress_gemm_producer", "moe_expert_choice", "moe_update_sel_bias",
            "MoEForwardGraph", "alloc_outputs",
            "make_workspace", "library_path", "MOE_TRACE_MAX_EVENTS"]
 
@@ -43,10 +43,25 @@ class MoEConfig:
     capacity_factor: float = 0.0
     F_shared: int = 0
     aux_alpha: float = 0.01
+    routing: str = "token"       # "token" (top-k per token) | "expert" (top-C per expert)
+    activation: str = "gelu"     # "gelu" | "silu" | "swiglu" (W1 [N, 2F, H])
+    min_capacity: int = 0
+    drop_order: str = "token"    # "token" | "slot"
 
     def c(self) -> _lib.MoeConfig:
         return _lib.MoeConfig(self.T, self.H, self.F, self.N, self.k,
-                              float(self.capacity_factor), self.F_shared, float(self.aux_alpha))
+                              float(self.capacity_factor), self.F_shared, float(self.aux_alpha),
+                              _lib.ROUTING[self.routing], _lib.ACTIVATION[self.activation],
+                              int(self.min_capacity), _lib.DROP_ORDER[self.drop_order])
+
+    @property
+    def slots(self) -> int:
+        """Assignments per token: k, or N for expert choice (a = t * slots + j)."""
+        return self.N if self.routing == "expert" else self.k
+
+    @property
+    def w1_rows(self) -> int:
+        return 2 * self.F if self.activation == "swiglu" else self.F
 
 
 @dataclass
@@ -65,16 +80,17 @@ class MoEWeights:
 
     def c(self, cfg: MoEConfig) -> _lib.MoeWeights:
         N, H, F, Fs = cfg.N, cfg.H, cfg.F, cfg.F_shared
+        g = 2 if cfg.activation == "swiglu" else 1   # SwiGLU: gate and up rows
         return _lib.MoeWeights(
             _p(self.Wg, torch.float32, (N, H), "Wg"),
             _p(self.bg, torch.float32, (N,), "bg", True),
             _p(self.sel_bias, torch.float32, (N,), "sel_bias", True),
-            _p(self.W1, torch.bfloat16, (N, F, H), "W1"),
-            _p(self.b1, torch.bfloat16, (N, F), "b1", True),
+            _p(self.W1, torch.bfloat16, (N, g * F, H), "W1"),
+            _p(self.b1, torch.bfloat16, (N, g * F), "b1", True),
             _p(self.W2, torch.bfloat16, (N, H, F), "W2"),
             _p(self.b2, torch.bfloat16, (N, H), "b2", True),
-            _p(self.W1s, torch.bfloat16, (Fs, H), "W1s", Fs == 0),
-            _p(self.b1s, torch.bfloat16, (Fs,), "b1s", True),
+            _p(self.W1s, torch.bfloat16, (g * Fs, H), "W1s", Fs == 0),
+            _p(self.b1s, torch.bfloat16, (g * Fs,), "b1s", True),
             _p(self.W2s, torch.bfloat16, (H, Fs), "W2s", Fs == 0),
             _p(self.b2s, torch.bfloat16, (H,), "b2s", True))
 
@@ -130,14 +146,19 @@ def _ws(cfg, ws, device):
     return ws, C.c_void_p(ws.data_ptr()), C.c_size_t(ws.numel())
 
 
-def moe_route(cfg: MoEConfig, x, Wg, bg=None, sel_bias=None, *, want_probs=False, ws=None,
-              stream=None):
-    """Returns (topk_idx int32 [T,k], topk_w fp32 [T,k], probs fp32 [T,N] or None, p_mean [N])."""
+def moe_route(cfg: MoEConfig, x, Wg, bg=None, sel_bias=None, *, want_probs=False,
+              want_logits=False, want_z=False, ws=None, stream=None):
+    """Returns (topk_idx int32 [T,k], topk_w fp32 [T,k], probs fp32 [T,N] or None, p_mean [N]);
+    with want_logits / want_z also logits fp32 [T,N] and z_loss fp32 [1] (in that order).
+    For expert choice topk_idx and topk_w are None."""
     dev = x.device
     T, N, k = cfg.T, cfg.N, cfg.k
-    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
-    w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    ec = cfg.routing == "expert"
+    idx = None if ec else torch.empty((T, k), dtype=torch.int32, device=dev)
+    w = None if ec else torch.empty((T, k), dtype=torch.float32, device=dev)
     probs = torch.empty((T, N), dtype=torch.float32, device=dev) if want_probs else None
+    logits = torch.empty((T, N), dtype=torch.float32, device=dev) if want_logits else None
+    z = torch.empty(1, dtype=torch.float32, device=dev) if want_z else None
     p_mean = torch.empty(N, dtype=torch.float32, device=dev)
     ws, wsp, wsn = _ws(cfg, ws, dev)
     st = _L.moe_route(C.byref(cfg.c()), _p(x, torch.bfloat16, (T, cfg.H), "x", T == 0),
@@ -146,9 +167,49 @@ def moe_route(cfg: MoEConfig, x, Wg, bg=None, sel_bias=None, *, want_probs=False
                       _p(sel_bias, torch.float32, (N,), "sel_bias", True),
                       _p(idx, torch.int32, None, "idx", True), _p(w, torch.float32, None, "w", True),
                       _p(probs, torch.float32, None, "probs", True),
-                      _p(p_mean, torch.float32, None, "p_mean"), wsp, wsn, _stream(stream))
+                      _p(logits, torch.float32, None, "logits", True),
+                      _p(p_mean, torch.float32, None, "p_mean"),
+                      _p(z, torch.float32, None, "z_loss", True), wsp, wsn, _stream(stream))
     check(st, "moe_route")
-    return idx, w, probs, p_mean
+    res = (idx, w, probs, p_mean)
+    if want_logits:
+        res += (logits,)
+    if want_z:
+        res += (z,)
+    return res
+
+
+def moe_expert_choice(cfg: MoEConfig, logits, p_mean=None, *, stream=None) -> dict:
+    """Expert-choice dispatch.  Returns dict(counts, offsets, perm, inv [T*N], f, l_aux)."""
+    dev = logits.device
+    T, N = cfg.T, cfg.N
+    R = moe_max_rows(cfg)
+    out = dict(counts=torch.empty(N, dtype=torch.int32, device=dev),
+               offsets=torch.empty(N + 1, dtype=torch.int32, device=dev),
+               perm=torch.empty(max(R, 0), dtype=torch.int32, device=dev),
+               inv=torch.empty(T * N, dtype=torch.int32, device=dev),
+               f=torch.empty(N, dtype=torch.float32, device=dev),
+               l_aux=torch.empty(1, dtype=torch.float32, device=dev) if p_mean is not None else None)
+    st = _L.moe_expert_choice(C.byref(cfg.c()), _p(logits, torch.float32, (T, N), "logits", True),
+                              _p(p_mean, torch.float32, (N,), "p_mean", True),
+                              _p(out["counts"], torch.int32, None, "counts"),
+                              _p(out["offsets"], torch.int32, None, "offsets"),
+                              _p(out["perm"], torch.int32, None, "perm", True),
+                              _p(out["inv"], torch.int32, None, "inv", True),
+                              _p(out["f"], torch.float32, None, "f"),
+                              _p(out["l_aux"], torch.float32, None, "l_aux", True),
+                              _stream(stream))
+    check(st, "moe_expert_choice")
+    return out
+
+
+def moe_update_sel_bias(cfg: MoEConfig, counts, sel_bias, gamma: float, *, stream=None):
+    """In place: sel_bias[e] += gamma * sign(counts[e] - mean(counts))."""
+    st = _L.moe_update_sel_bias(C.byref(cfg.c()), _p(counts, torch.int32, (cfg.N,), "counts"),
+                                _p(sel_bias, torch.float32, (cfg.N,), "sel_bias"),
+                                C.c_float(gamma), _stream(stream))
+    check(st, "moe_update_sel_bias")
+    return sel_bias
 
 
 def moe_permute(cfg: MoEConfig, topk_idx, p_mean=None, *, ws=None, stream=None) -> dict:
@@ -218,7 +279,7 @@ def moe_expert_ffn(cfg: MoEConfig, x, perm, offsets, topk_w, weights: MoEWeights
     st = _L.moe_expert_ffn(C.byref(cfg.c()), _p(x, torch.bfloat16, (cfg.T, cfg.H), "x", True),
                            _p(perm, torch.int32, None, "perm", True),
                            _p(offsets, torch.int32, (cfg.N + 1,), "offsets"),
-                           _p(topk_w, torch.float32, (cfg.T, cfg.k), "topk_w", True),
+                           _p(topk_w, torch.float32, (cfg.T, cfg.slots), "topk_w", True),
                            C.byref(wc), _p(y, torch.bfloat16, None, "y", True),
                            _p(ys, torch.bfloat16, None, "y_shared", True), wsp, wsn,
                            _stream(stream))
@@ -230,7 +291,7 @@ def moe_combine(cfg: MoEConfig, y, inv, y_shared=None, *, stream=None):
     dev = inv.device
     out = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=dev)
     st = _L.moe_combine(C.byref(cfg.c()), _p(y, torch.bfloat16, None, "y", True),
-                        _p(inv, torch.int32, (cfg.T * cfg.k,), "inv", True),
+                        _p(inv, torch.int32, (cfg.T * cfg.slots,), "inv", True),
                         _p(y_shared, torch.bfloat16, (cfg.T, cfg.H), "y_shared", True),
                         _p(out, torch.bfloat16, None, "out", True), _stream(stream))
     check(st, "moe_combine")
@@ -238,22 +299,25 @@ def moe_combine(cfg: MoEConfig, y, inv, y_shared=None, *, stream=None):
 
 
 _OUT_FIELDS = ("topk_idx", "topk_w", "probs", "p_mean", "counts", "offsets", "perm", "inv", "f",
-               "l_aux")
+               "l_aux", "z_loss", "logits")
 
 
-def alloc_outputs(cfg: MoEConfig, device, want_probs=False) -> dict:
+def alloc_outputs(cfg: MoEConfig, device, want_probs=False, want_logits=False) -> dict:
     T, N, k = cfg.T, cfg.N, cfg.k
     i32, f32 = torch.int32, torch.float32
-    return dict(topk_idx=torch.empty((T, k), dtype=i32, device=device),
-                topk_w=torch.empty((T, k), dtype=f32, device=device),
+    ec = cfg.routing == "expert"
+    return dict(topk_idx=None if ec else torch.empty((T, k), dtype=i32, device=device),
+                topk_w=None if ec else torch.empty((T, k), dtype=f32, device=device),
                 probs=torch.empty((T, N), dtype=f32, device=device) if want_probs else None,
                 p_mean=torch.empty(N, dtype=f32, device=device),
                 counts=torch.empty(N, dtype=i32, device=device),
                 offsets=torch.empty(N + 1, dtype=i32, device=device),
                 perm=torch.empty(max(moe_max_rows(cfg), 0), dtype=i32, device=device),
-                inv=torch.empty(T * k, dtype=i32, device=device),
+                inv=torch.empty(T * cfg.slots, dtype=i32, device=device),
                 f=torch.empty(N, dtype=f32, device=device),
-                l_aux=torch.empty(1, dtype=f32, device=device))
+                l_aux=torch.empty(1, dtype=f32, device=device),
+                z_loss=torch.empty(1, dtype=f32, device=device),
+                logits=torch.empty((T, N), dtype=f32, device=device) if want_logits else None)
 
 
 def moe_forward(cfg: MoEConfig, weights: MoEWeights, x, *, out=None, outputs: Optional[dict] = None,

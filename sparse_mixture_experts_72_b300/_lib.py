@@ -15,17 +15,24 @@ MOE_TRACE_MAX_EVENTS = 32
 
 # every symbol include/moe.h declares
 EXPORTED = ["moe_workspace_size", "moe_max_rows", "moe_capacity", "moe_forward_num_launches",
-            "moe_route", "moe_permute", "moe_expert_ffn", "moe_combine", "moe_forward",
+            "moe_route", "moe_expert_choice", "moe_update_sel_bias", "moe_permute",
+            "moe_expert_ffn", "moe_combine", "moe_forward",
             "moe_permute_static", "moe_workspace_status", "moe_debug_suppress_gemm_producer",
             "moe_status_string", "moe_version"]
 MOE_STATIC_MAX_ASSIGNMENTS = 65536
 MOE_STATIC_MAX_EXPERTS = 256
 
 
+ROUTING = {"token": 0, "expert": 1}
+ACTIVATION = {"gelu": 0, "silu": 1, "swiglu": 2}
+DROP_ORDER = {"token": 0, "slot": 1}
+
+
 class MoeConfig(C.Structure):
     _fields_ = [("T", C.c_int32), ("H", C.c_int32), ("F", C.c_int32), ("N", C.c_int32),
                 ("k", C.c_int32), ("capacity_factor", C.c_float), ("F_shared", C.c_int32),
-                ("aux_alpha", C.c_float)]
+                ("aux_alpha", C.c_float), ("routing", C.c_int32), ("activation", C.c_int32),
+                ("min_capacity", C.c_int32), ("drop_order", C.c_int32)]
 
 
 class MoeWeights(C.Structure):
@@ -36,7 +43,7 @@ class MoeWeights(C.Structure):
 class MoeOutputs(C.Structure):
     _fields_ = [(n, C.c_void_p) for n in
                 ("topk_idx", "topk_w", "probs", "p_mean", "counts", "offsets", "perm", "inv",
-                 "f", "l_aux")]
+                 "f", "l_aux", "z_loss", "logits")]
 
 
 _lib = None
@@ -61,8 +68,12 @@ def load() -> C.CDLL:
     lib.moe_capacity.restype = C.c_int64
     lib.moe_forward_num_launches.argtypes = [cfgp]
     lib.moe_forward_num_launches.restype = C.c_int32
-    lib.moe_route.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, C.c_size_t, P]
+    lib.moe_route.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, P, P, C.c_size_t, P]
     lib.moe_route.restype = C.c_int
+    lib.moe_expert_choice.argtypes = [cfgp, P, P, P, P, P, P, P, P, P]
+    lib.moe_expert_choice.restype = C.c_int
+    lib.moe_update_sel_bias.argtypes = [cfgp, P, P, C.c_float, P]
+    lib.moe_update_sel_bias.restype = C.c_int
     lib.moe_permute.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, C.c_size_t, P]
     lib.moe_permute.restype = C.c_int
     lib.moe_expert_ffn.argtypes = [cfgp, P, P, P, P, C.POINTER(MoeWeights), P, P, P, C.c_size_t, P]

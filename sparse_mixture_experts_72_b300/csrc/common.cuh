@@ -357,4 +357,8 @@ __device__ __forceinline__ float gelu_erf(float z) {
   return 0.5f * z * (1.0f + erf_as7126(z * 0.70710678118654752440f));
 }
 
+// SiLU, z * sigmoid(z) = z / (1 + e^-z), with the fast intrinsics: for very
+// negative z the denominator overflows and __fdividef returns 0 (the limit).
+__device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+
 }  // namespace moe

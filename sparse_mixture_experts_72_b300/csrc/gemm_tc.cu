@@ -1,8 +1,11 @@
 // Grouped bf16 GEMM on the 5th-generation tensor cores (tcgen05 + TMEM),
 // fed by TMA, with the expert FFN epilogues fused:
 //
-//   EPI_GELU :  out[r, n] = bf16( GELU_erf(acc[r, n] + bias_g[n]) )        (Linear -> GELU)
-//   EPI_SCALE:  out[r, n] = bf16( w_r * (acc[r, n] + bias_g[n]) )          (Linear, gate weight)
+//   EPI_GELU  : out[r, n] = bf16( GELU_erf(acc[r, n] + bias_g[n]) )        (Linear -> GELU)
+//   EPI_SILU  : out[r, n] = bf16( SiLU(acc[r, n] + bias_g[n]) )            (Linear -> SiLU)
+//   EPI_SWIGLU: out[r, n] = bf16( SiLU(gate[r, n]) * up[r, n] )            (gated Linear)
+//               gate / up = acc against B rows n and n_out + n (+ bias)
+//   EPI_SCALE : out[r, n] = bf16( w_r * (acc[r, n] + bias_g[n]) )          (Linear, gate weight)
 //
 // acc[r, :] = A[r, :] . B_g[:, :]^T over the K dimension, where group g (an
 // expert) owns the A rows [offsets[g], offsets[g+1]) and the B rows
@@ -161,8 +164,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   const int units = PAIR == 2 ? (int)num_clusters_x() : (int)gridDim.x;
   const int G = args.num_groups;
   const bool two = args.num_phases == 2;
-  const int nt0 = (args.ph[0].n_out + BN - 1) / BN;
-  const int nt1 = two ? (args.ph[1].n_out + BN - 1) / BN : 0;
+  // output columns per tile: 256, or 128 for SwiGLU (gate + up fill the 256
+  // accumulator columns)
+  const int bno0 = args.ph[0].mode == EPI_SWIGLU ? BN / 2 : BN;
+  const int bno1 = two && args.ph[1].mode == EPI_SWIGLU ? BN / 2 : BN;
+  const int nt0 = (args.ph[0].n_out + bno0 - 1) / bno0;
+  const int nt1 = two ? (args.ph[1].n_out + bno1 - 1) / bno1 : 0;
   const int nkb0 = (args.ph[0].K + BK - 1) / BK;
   const int nkb1 = two ? (args.ph[1].K + BK - 1) / BK : 0;
   // phase-0 epilogue arrivals that complete one row block (every warp of
@@ -271,7 +278,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           if (!ok) break;
           fence_proxy_async_global();  // the TMA reads below see those plain stores
         }
-        const int b_row = cur.g * n_out + n * BN + (int)rank * S::B_ROWS;
+        const bool glu = (ph ? args.ph[1].mode : args.ph[0].mode) == EPI_SWIGLU;
+        // B rows of the tile: n_out-row blocks per group, or for SwiGLU 128
+        // gate rows and the 128 matching up rows (the odd CTA of a pair, or
+        // the second half of a single CTA's B tile, takes the up rows)
+        const int b_row = glu ? cur.g * 2 * n_out + (int)rank * n_out + n * (BN / 2)
+                              : cur.g * n_out + n * BN + (int)rank * S::B_ROWS;
         const int a_row_cta = a_row + (int)rank * 128;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, status)) {
@@ -287,7 +299,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           } else {
             mbar_arrive_expect_tx(full_bar(stage), S::STAGE_BYTES);
             tma_load_2d(sA + stage * A_BYTES, mA, full_bar(stage), kb * BK, a_row_cta);
-            tma_load_2d(sB + stage * S::B_BYTES, mB, full_bar(stage), kb * BK, b_row);
+            if (glu) {
+              // two 128-row boxes: gate rows, then up rows (128 * BK * 2 bytes further)
+              tma_load_2d(sB + stage * S::B_BYTES, mB, full_bar(stage), kb * BK, b_row);
+              tma_load_2d(sB + stage * S::B_BYTES + 128 * BK * 2, mB, full_bar(stage), kb * BK,
+                          b_row + n_out);
+            } else {
+              tma_load_2d(sB + stage * S::B_BYTES, mB, full_bar(stage), kb * BK, b_row);
+            }
           }
           ++issued;
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -356,17 +375,27 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       const int r_in = warp_row0 + lane;
       const bool row_ok = r_in < rows_left;
       const int64_t out_row = (int64_t)a_row + r_in;
-      const int col0 = n * BN + cpart * EPI_COLS;     // first column of this warp's slice
+      const bool glu = P.mode == EPI_SWIGLU;
+      // this warp's output columns: 64 of a 256-wide tile, or 32 of a
+      // 128-wide SwiGLU tile (whose accumulator holds 128 gate + 128 up)
+      const int wcols = glu ? EPI_COLS / 2 : EPI_COLS;
+      const int col0 = n * (glu ? BN / 2 : BN) + cpart * wcols;
       // everything that does not need the accumulator is fetched before waiting
       float wscale = 1.0f;
       if (P.mode == EPI_SCALE && P.topk_w != nullptr && row_ok)
         wscale = P.topk_w[P.perm[out_row]];
       const bool has_bias = P.bias != nullptr;
       if (has_bias) {
-        // EPI_COLS (64) columns: 2 per lane
-        const int c2 = col0 + lane * 2;
+        // 64 staged values, 2 per lane: the slice's bias, or for SwiGLU its
+        // 32 gate biases followed by its 32 up biases
+        int c2 = col0 + lane * 2;
+        size_t boff = (size_t)cur.g * n_out + c2;
+        if (glu) {
+          c2 = col0 + (lane & 15) * 2;
+          boff = (size_t)cur.g * 2 * n_out + (lane >= 16 ? n_out : 0) + c2;
+        }
         uint32_t b = 0u;
-        if (c2 < n_out) b = __ldg(reinterpret_cast<const uint32_t*>(P.bias + (size_t)cur.g * n_out + c2));
+        if (c2 < n_out) b = __ldg(reinterpret_cast<const uint32_t*>(P.bias + boff));
         *reinterpret_cast<uint32_t*>(my_bias + lane * 2) = b;
         __syncwarp();
       }
@@ -377,8 +406,44 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       tc_fence_after();
       __nv_bfloat16* orow = P.out + out_row * P.ld_out;
       const bool warp_has_rows = warp_row0 < rows_left;     // warp-uniform
-      const bool full_cols = col0 + EPI_COLS <= n_out;      // warp-uniform
-      if (warp_has_rows && col0 < n_out) {
+      const bool full_cols = col0 + wcols <= n_out;         // warp-uniform
+      if (warp_has_rows && col0 < n_out && glu) {
+        // 32 output columns in two halves of 16: gate and up accumulators
+        const uint32_t tg = tmem_base + lane_addr + acc * BN + cpart * wcols;
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+          uint32_t rg[16], ru[16];
+          tmem_ld_32x32b_x16(tg + h * 16, rg);
+          tmem_ld_32x32b_x16(tg + BN / 2 + h * 16, ru);
+          tmem_ld_wait();
+          float v[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float g = __uint_as_float(rg[i]), u = __uint_as_float(ru[i]);
+            if (has_bias) {
+              const uint16_t bgate = my_bias[h * 16 + i], bup = my_bias[32 + h * 16 + i];
+              g += __uint_as_float((uint32_t)bgate << 16);
+              u += __uint_as_float((uint32_t)bup << 16);
+            }
+            v[i] = silu_f(g) * u;
+          }
+          uint4 o[2];
+#pragma unroll
+          for (int j8 = 0; j8 < 2; ++j8) {
+            o[j8].x = pack_bf16x2(v[8 * j8 + 0], v[8 * j8 + 1]);
+            o[j8].y = pack_bf16x2(v[8 * j8 + 2], v[8 * j8 + 3]);
+            o[j8].z = pack_bf16x2(v[8 * j8 + 4], v[8 * j8 + 5]);
+            o[j8].w = pack_bf16x2(v[8 * j8 + 6], v[8 * j8 + 7]);
+          }
+          const int col = col0 + h * 16;
+          uint4* dst = reinterpret_cast<uint4*>(orow + col);
+          if (row_ok) {
+#pragma unroll
+            for (int j8 = 0; j8 < 2; ++j8)
+              if (full_cols || col + 8 * j8 < n_out) dst[j8] = o[j8];
+          }
+        }
+      } else if (warp_has_rows && col0 < n_out) {
         const uint32_t taddr = tmem_base + lane_addr + acc * BN + cpart * EPI_COLS;
 #pragma unroll 1
         for (int c = 0; c < 2; ++c) {
@@ -401,6 +466,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           if (P.mode == EPI_GELU) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
+          } else if (P.mode == EPI_SILU) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = silu_f(v[i]);
           } else {
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] *= wscale;
@@ -547,7 +615,9 @@ cudaError_t make_gemm_plan(GemmPlan* plan, const GemmArgs& args, const __nv_bflo
     const __nv_bfloat16* a = p == 0 ? A : args.ph[0].out;
     if (!encode_tensor_map_bf16(&plan->tmA[p], a, a_rows, args.ph[p].K, BK, 128))
       return cudaErrorInvalidValue;
-    if (!encode_tensor_map_bf16(&plan->tmB[p], B[p], b_rows[p], args.ph[p].K, BK, BN / pair))
+    // SwiGLU tiles load 128 gate and 128 up rows: two 128-row boxes
+    const int box_b = args.ph[p].mode == EPI_SWIGLU ? BN / 2 : BN / pair;
+    if (!encode_tensor_map_bf16(&plan->tmB[p], B[p], b_rows[p], args.ph[p].K, BK, box_b))
       return cudaErrorInvalidValue;
   }
   if (np == 1) {
@@ -558,7 +628,10 @@ cudaError_t make_gemm_plan(GemmPlan* plan, const GemmArgs& args, const __nv_bflo
   plan->pair = pair;
   const int64_t tile_m = 128 * pair;
   int64_t n_tiles = 0;
-  for (int p = 0; p < np; ++p) n_tiles += (args.ph[p].n_out + BN - 1) / BN;
+  for (int p = 0; p < np; ++p) {
+    const int bno = args.ph[p].mode == EPI_SWIGLU ? BN / 2 : BN;
+    n_tiles += (args.ph[p].n_out + bno - 1) / bno;
+  }
   const int64_t max_tiles = ((a_rows + tile_m - 1) / tile_m + args.num_groups) * n_tiles;
   const int64_t max_units = num_sms / pair;
   const int64_t units = max_tiles < max_units ? max_tiles : max_units;

@@ -39,14 +39,20 @@ struct RouterLaunch {
   float* topk_w;
   float* probs;     // nullable
   float* p_mean;
-  float* logits;    // scratch [T, N]
-  float* p_part;    // scratch [router_num_select_blocks(T), N]
-  int T, H, N, k;
+  float* logits;    // [T, N]: scratch of the SIMT router; written by the
+                    // tensor-core router only when logits_out is set
+  float* p_part;    // scratch [blocks, N + 1]: per-block column sums of P,
+                    // then the block's sum of logsumexp(l_t)^2
+  float* z_loss;    // nullable: mean over tokens of logsumexp(l_t)^2
+  float* logits_out;  // nullable [T, N] (tensor-core router)
+  int T, H, N, k;   // topk_idx == nullptr: no selection (expert choice)
 };
 int router_num_select_blocks(int T);
 int router_num_launches(int T, int N);
 // fp32 SIMT router (any N <= MOE_MAX_EXPERTS)
 cudaError_t launch_router(const RouterLaunch& a, cudaStream_t st, LaunchTrace* tr);
+// p_mean[0..N) = 0 and *z_loss = 0 (nullable) in one launch (an empty batch)
+cudaError_t launch_router_stats_zero(float* p_mean, float* z_loss, int N, cudaStream_t st);
 
 // tensor-core router (N <= kRouterTcMaxExperts): split kernel + fused kernel
 constexpr int kRouterTcMaxExperts = 256;
@@ -56,7 +62,9 @@ struct RouterTcArgs {
   int32_t* topk_idx;
   float* topk_w;
   float* probs;     // nullable
-  float* p_part;    // [m_tiles * splits, N] per-CTA column sums of P
+  float* logits_out;  // nullable [T, N]
+  float* z_loss;    // nullable
+  float* p_part;    // [m_tiles * splits, N + 1] per-CTA column sums of P, then sum of lse^2
   float* p_mean;
   int* ticket;      // CTAs done; zero on entry
   int* status;
@@ -104,6 +112,7 @@ struct PermuteLaunch {
   int T, N, k;
   int64_t capacity;     // < 0: no limit
   float alpha;
+  int slot_major = 0;   // claim order: 0 a = t*k + j; 1 j-major, then t
   // optional fused gather: xp[row] = x[perm[row] / k] for every kept row
   const __nv_bfloat16* x = nullptr;
   __nv_bfloat16* xp = nullptr;
@@ -122,16 +131,31 @@ cudaError_t launch_combine(const __nv_bfloat16* y, const int32_t* inv,
                            const __nv_bfloat16* y_shared, __nv_bfloat16* out, int T, int k,
                            int H, cudaStream_t st, LaunchTrace* tr);
 
+// ---------------------------------------------------------------- expert choice
+constexpr int kExpertChoiceMaxTokens = 51200;  // one expert's column in shared memory
+// One CTA per expert: counts, offsets, perm, inv [T*N], f, l_aux (nullable).
+cudaError_t launch_expert_choice(const float* logits, const float* p_mean, int T, int N, int C,
+                                 float alpha, int32_t* counts, int32_t* offsets, int32_t* perm,
+                                 int32_t* inv, float* f, float* l_aux, cudaStream_t st,
+                                 LaunchTrace* tr);
+// sel_bias[e] += gamma * sign(counts[e] - mean(counts)), one launch
+cudaError_t launch_update_sel_bias(const int32_t* counts, float* sel_bias, int N, float gamma,
+                                   cudaStream_t st);
+
 // ---------------------------------------------------------------- grouped tcgen05 GEMM
-enum EpilogueMode : int32_t { EPI_GELU = 0, EPI_SCALE = 1 };
+// EPI_SWIGLU: B holds 2*n_out rows per group (gate rows, then up rows); a
+// tile covers 128 output columns, its accumulator the 128 gate and the 128
+// up columns, and the output is SiLU(gate) * up.
+enum EpilogueMode : int32_t { EPI_GELU = 0, EPI_SCALE = 1, EPI_SILU = 2, EPI_SWIGLU = 3 };
 
 // One GEMM of a launch: out = epilogue(A_rows . B_g^T) for every group g.
 struct GemmPhase {
-  int32_t n_out;                 // output columns per group (= B rows per group)
+  int32_t n_out;                 // output columns per group (B rows per group: n_out, or
+                                 // 2 * n_out for EPI_SWIGLU)
   int32_t K;                     // reduction length
   int32_t mode;                  // EpilogueMode
   int32_t ld_out;
-  const __nv_bfloat16* bias;     // [G, n_out] or nullptr
+  const __nv_bfloat16* bias;     // [G, n_out] ([G, 2 * n_out] for EPI_SWIGLU) or nullptr
   const float* topk_w;           // EPI_SCALE: weight per assignment, or nullptr (weight 1)
   const int32_t* perm;           // EPI_SCALE: row -> assignment (with topk_w)
   __nv_bfloat16* out;            // [rows, ld_out]

@@ -23,12 +23,26 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 int64_t capacity_of(const moe_config_t& c) {
   if (!(c.capacity_factor > 0.0f)) return -1;
-  // floor(T / N * cf), in double, in that order
+  // floor(T / N * cf), in double, in that order; then the min_capacity floor
   const double v = std::floor((double)c.T / (double)c.N * (double)c.capacity_factor);
-  return v < 0 ? 0 : (int64_t)v;
+  const int64_t C = v < 0 ? 0 : (int64_t)v;
+  return C < c.min_capacity ? (int64_t)c.min_capacity : C;
+}
+
+bool expert_choice(const moe_config_t& c) { return c.routing == MOE_ROUTING_EXPERT_CHOICE; }
+
+// Slots per token S: assignment a = t*S + j (j the slot, or the expert for
+// expert choice).
+int slots_of(const moe_config_t& c) { return expert_choice(c) ? c.N : c.k; }
+
+// Tokens each expert takes under expert choice: the capacity, at most T.
+int64_t ec_tokens(const moe_config_t& c) {
+  const int64_t C = capacity_of(c);
+  return C < 0 ? 0 : (C < c.T ? C : (int64_t)c.T);
 }
 
 int64_t max_rows_of(const moe_config_t& c) {
+  if (expert_choice(c)) return ec_tokens(c) * c.N;
   const int64_t A = (int64_t)c.T * c.k;
   const int64_t C = capacity_of(c);
   if (C < 0) return A;
@@ -36,17 +50,21 @@ int64_t max_rows_of(const moe_config_t& c) {
   return cap < A ? cap : A;
 }
 
+// Rows of W1 per expert: F, or 2F (gate and up) for SwiGLU.
+int64_t w1_rows(const moe_config_t& c, int64_t F) { return c.activation == MOE_ACT_SWIGLU ? 2 * F : F; }
+
 struct WsLayout {
   size_t status, status_bytes, rows_done, rows_done_s, w3, logits, p_part, local_rank, blk_hist,
       blk_base;
-  size_t topk_idx, topk_w, p_mean, counts, offsets, perm, inv, f, l_aux;
+  size_t topk_idx, topk_w, p_mean, counts, offsets, perm, inv, f, l_aux, z_loss, probs;
   size_t xp, hid, y, hid_s, y_s;
   size_t total;
 };
 
 WsLayout layout_of(const moe_config_t& c) {
   WsLayout L;
-  const int64_t T = c.T, N = c.N, A = T * c.k, R = max_rows_of(c);
+  const int64_t T = c.T, N = c.N, A = T * slots_of(c), R = max_rows_of(c);
+  const int64_t Ak = expert_choice(c) ? 0 : T * c.k;   // top-k outputs (token choice)
   const int64_t nsel = router_num_select_blocks(c.T);
   const int64_t nblk = permute_num_blocks(A);
   size_t o = 0;
@@ -62,14 +80,17 @@ WsLayout layout_of(const moe_config_t& c) {
   L.rows_done_s = L.rows_done + sizeof(int32_t) * nrd;
   const bool tc = c.N <= kRouterTcMaxExperts;
   L.w3 = take(tc ? router_w3_bytes(c.N, c.H) : 0);
-  L.logits = take(tc ? 0 : sizeof(float) * T * N);
+  // logits: the SIMT router's scratch; expert choice selects on them
+  L.logits = take((tc && !expert_choice(c)) ? 0 : sizeof(float) * T * N);
   const int64_t pblocks = tc ? router_tc_num_ctas(c.T, c.N, c.H) : nsel;
-  L.p_part = take(sizeof(float) * (pblocks > 0 ? pblocks : 1) * N);
+  L.p_part = take(sizeof(float) * (pblocks > 0 ? pblocks : 1) * (N + 1));
   L.local_rank = take(sizeof(int32_t) * A);
   L.blk_hist = take(sizeof(int32_t) * (nblk > 0 ? nblk : 1) * N);
   L.blk_base = take(sizeof(int32_t) * (nblk > 0 ? nblk : 1) * N);
-  L.topk_idx = take(sizeof(int32_t) * A);
-  L.topk_w = take(sizeof(float) * A);
+  L.topk_idx = take(sizeof(int32_t) * Ak);
+  L.topk_w = take(sizeof(float) * Ak);
+  // expert choice weights its rows by the softmax itself
+  L.probs = take(expert_choice(c) ? sizeof(float) * T * N : 0);
   L.p_mean = take(sizeof(float) * N);
   L.counts = take(sizeof(int32_t) * N);
   L.offsets = take(sizeof(int32_t) * (N + 1));
@@ -77,8 +98,9 @@ WsLayout layout_of(const moe_config_t& c) {
   L.inv = take(sizeof(int32_t) * A);
   L.f = take(sizeof(float) * N);
   L.l_aux = take(sizeof(float));
+  L.z_loss = take(sizeof(float));
   L.xp = take(2 * (size_t)R * c.H);
-  L.hid = take(2 * (size_t)R * c.F);
+  L.hid = take(2 * (size_t)R * c.F);   // the activation's output: F columns
   L.y = take(2 * (size_t)R * c.H);
   L.hid_s = take(c.F_shared > 0 ? 2 * (size_t)T * c.F_shared : 0);
   L.y_s = take(c.F_shared > 0 ? 2 * (size_t)T * c.H : 0);
@@ -91,6 +113,19 @@ moe_status_t check_config(const moe_config_t* c) {
   if (c->T < 0 || c->H <= 0 || c->F <= 0 || c->N <= 0 || c->k <= 0 || c->F_shared < 0)
     return MOE_ERR_INVALID_ARG;
   if (c->k > c->N) return MOE_ERR_INVALID_ARG;
+  if (c->routing != MOE_ROUTING_TOKEN_CHOICE && c->routing != MOE_ROUTING_EXPERT_CHOICE)
+    return MOE_ERR_INVALID_ARG;
+  if (c->activation != MOE_ACT_GELU && c->activation != MOE_ACT_SILU &&
+      c->activation != MOE_ACT_SWIGLU)
+    return MOE_ERR_INVALID_ARG;
+  if (c->drop_order != MOE_DROP_TOKEN_MAJOR && c->drop_order != MOE_DROP_SLOT_MAJOR)
+    return MOE_ERR_INVALID_ARG;
+  if (c->min_capacity < 0) return MOE_ERR_INVALID_ARG;
+  if (c->routing == MOE_ROUTING_EXPERT_CHOICE) {
+    if (!(c->capacity_factor > 0.0f)) return MOE_ERR_INVALID_ARG;
+    if (c->T > kExpertChoiceMaxTokens) return MOE_ERR_UNSUPPORTED;
+    if ((int64_t)c->T * c->N > INT32_MAX / 2) return MOE_ERR_UNSUPPORTED;
+  }
   if (c->N > MOE_MAX_EXPERTS || c->k > MOE_MAX_TOP_K) return MOE_ERR_UNSUPPORTED;
   if (c->H % 8 || c->F % 8 || c->F_shared % 8) return MOE_ERR_UNSUPPORTED;
   if ((int64_t)c->T * c->k > INT32_MAX / 2) return MOE_ERR_UNSUPPORTED;
@@ -179,9 +214,11 @@ moe_status_t begin_call(const moe_config_t& c, void* ws, const WsLayout& L, cuda
   return clear_status(ws, L, st, tr);
 }
 
+// idx / w nullptr: no per-token selection (expert choice).
 moe_status_t do_route(const moe_config_t& c, const uint16_t* x, const float* Wg, const float* bg,
-                      const float* sel, int32_t* idx, float* w, float* probs, float* p_mean,
-                      void* ws, const WsLayout& L, cudaStream_t st, LaunchTrace* tr) {
+                      const float* sel, int32_t* idx, float* w, float* probs, float* logits,
+                      float* p_mean, float* z_loss, void* ws, const WsLayout& L, cudaStream_t st,
+                      LaunchTrace* tr) {
   RouterLaunch a;
   a.x = reinterpret_cast<const __nv_bfloat16*>(x);
   a.Wg = Wg;
@@ -192,11 +229,13 @@ moe_status_t do_route(const moe_config_t& c, const uint16_t* x, const float* Wg,
   a.probs = probs;
   a.p_mean = p_mean;
   a.logits = at<float>(ws, L.logits);
+  a.logits_out = logits;
+  a.z_loss = z_loss;
   a.p_part = at<float>(ws, L.p_part);
   a.T = c.T;
   a.H = c.H;
   a.N = c.N;
-  a.k = c.k;
+  a.k = idx ? c.k : 1;
   if (c.N <= kRouterTcMaxExperts)
     return cuda_status(launch_router_tc(
         a, at<__nv_bfloat16>(ws, L.w3), at<int>(ws, L.status) + 1, at<int>(ws, L.status),
@@ -226,6 +265,7 @@ moe_status_t do_permute(const moe_config_t& c, const int32_t* idx, const float* 
   a.k = c.k;
   a.capacity = capacity_of(c);
   a.alpha = c.aux_alpha;
+  a.slot_major = c.drop_order == MOE_DROP_SLOT_MAJOR ? 1 : 0;
   if (gather_x && max_rows_of(c) > 0) {
     a.x = reinterpret_cast<const __nv_bfloat16*>(gather_x);
     a.xp = at<__nv_bfloat16>(ws, L.xp);
@@ -252,13 +292,16 @@ moe_status_t do_ffn(const moe_config_t& c, const uint16_t* x, const int32_t* per
   using bf = __nv_bfloat16;
   const int64_t R = max_rows_of(c);
   int* status = at<int>(ws, L.status);
+  const int32_t act_mode = c.activation == MOE_ACT_SWIGLU ? EPI_SWIGLU
+                           : c.activation == MOE_ACT_SILU ? EPI_SILU
+                                                          : EPI_GELU;
   if (R > 0) {
     bf* xp = at<bf>(ws, L.xp);
     bf* hid = at<bf>(ws, L.hid);
     if (!gathered)
-      MOE_CUDA(launch_gather(reinterpret_cast<const bf*>(x), perm, offsets, c.N, c.k, R, c.H, xp,
-                             st, tr));
-    // one persistent launch: Hid = GELU(X_perm W1_e^T + b1_e), then
+      MOE_CUDA(launch_gather(reinterpret_cast<const bf*>(x), perm, offsets, c.N, slots_of(c), R,
+                             c.H, xp, st, tr));
+    // one persistent launch: Hid = act(X_perm W1_e^T + b1_e), then
     // y = w * (Hid W2_e^T + b2_e), row block by row block
     GemmArgs g{};
     g.offsets = offsets;
@@ -266,7 +309,7 @@ moe_status_t do_ffn(const moe_config_t& c, const uint16_t* x, const int32_t* per
     g.num_phases = 2;
     g.ph[0].n_out = c.F;
     g.ph[0].K = c.H;
-    g.ph[0].mode = EPI_GELU;
+    g.ph[0].mode = act_mode;
     g.ph[0].bias = reinterpret_cast<const bf*>(W.b1);
     g.ph[0].out = hid;
     g.ph[0].ld_out = c.F;
@@ -282,7 +325,7 @@ moe_status_t do_ffn(const moe_config_t& c, const uint16_t* x, const int32_t* per
     g.status = status;
     g.skip_producer = take_suppress_producer();
     const bf* B[2] = {reinterpret_cast<const bf*>(W.W1), reinterpret_cast<const bf*>(W.W2)};
-    const int64_t b_rows[2] = {(int64_t)c.N * c.F, (int64_t)c.N * c.H};
+    const int64_t b_rows[2] = {(int64_t)c.N * w1_rows(c, c.F), (int64_t)c.N * c.H};
     GemmPlan p;
     MOE_CUDA(make_gemm_plan(&p, g, xp, R, B, b_rows, sms));
     MOE_CUDA(launch_gemm(p, st, tr));
@@ -295,7 +338,7 @@ moe_status_t do_ffn(const moe_config_t& c, const uint16_t* x, const int32_t* per
     g.num_phases = 2;
     g.ph[0].n_out = c.F_shared;
     g.ph[0].K = c.H;
-    g.ph[0].mode = EPI_GELU;
+    g.ph[0].mode = act_mode;
     g.ph[0].bias = reinterpret_cast<const bf*>(W.b1s);
     g.ph[0].out = at<bf>(ws, L.hid_s);
     g.ph[0].ld_out = c.F_shared;
@@ -309,7 +352,7 @@ moe_status_t do_ffn(const moe_config_t& c, const uint16_t* x, const int32_t* per
     g.status = status;
     g.skip_producer = take_suppress_producer();
     const bf* B[2] = {reinterpret_cast<const bf*>(W.W1s), reinterpret_cast<const bf*>(W.W2s)};
-    const int64_t b_rows[2] = {(int64_t)c.F_shared, (int64_t)c.H};
+    const int64_t b_rows[2] = {w1_rows(c, c.F_shared), (int64_t)c.H};
     GemmPlan p;
     MOE_CUDA(make_gemm_plan(&p, g, reinterpret_cast<const bf*>(x), c.T, B, b_rows, sms));
     MOE_CUDA(launch_gemm(p, st, tr));
@@ -367,29 +410,72 @@ MOE_API int32_t moe_forward_num_launches(const moe_config_t* cfg) {
   const moe_config_t& c = *cfg;
   int n = router_clears_status(c) ? 0 : 1;  // status clear
   n += router_num_launches(c.T, c.N);
-  n += permute_num_launches(c.T, c.k);      // the scatter also gathers the rows
-  n += ffn_num_launches(c, true);
+  if (expert_choice(c)) {
+    n += 1;                                 // expert-choice selection
+    n += ffn_num_launches(c, false);        // gather + expert FFN (+ shared)
+  } else {
+    n += permute_num_launches(c.T, c.k);    // the scatter also gathers the rows
+    n += ffn_num_launches(c, true);
+  }
   if (c.T > 0) n += 1;  // combine
   return n;
 }
 
 MOE_API moe_status_t moe_route(const moe_config_t* cfg, const uint16_t* x, const float* Wg,
                                const float* bg, const float* sel_bias, int32_t* topk_idx,
-                               float* topk_w, float* probs, float* p_mean, void* ws,
-                               size_t ws_bytes, void* stream) {
+                               float* topk_w, float* probs, float* logits, float* p_mean,
+                               float* z_loss, void* ws, size_t ws_bytes, void* stream) {
   MOE_TRY(check_config(cfg));
   const moe_config_t& c = *cfg;
   const bool has_t = c.T > 0;
   MOE_TRY(check_ptrs(true, Wg, p_mean));
-  if (has_t) MOE_TRY(check_ptrs(true, x, topk_idx, topk_w));
-  MOE_TRY(check_ptrs(false, bg, sel_bias, probs));
+  if (expert_choice(c)) {
+    topk_idx = nullptr;
+    topk_w = nullptr;
+  } else if (has_t) {
+    MOE_TRY(check_ptrs(true, x, topk_idx, topk_w));
+  }
+  if (has_t) MOE_TRY(check_ptrs(true, x));
+  MOE_TRY(check_ptrs(false, bg, sel_bias, probs, logits, z_loss));
   MOE_TRY(check_ws(c, ws, ws_bytes));
   DeviceInfo d;
   MOE_TRY(device_info(&d));
   const WsLayout L = layout_of(c);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   MOE_TRY(begin_call(c, ws, L, st, nullptr));
-  return do_route(c, x, Wg, bg, sel_bias, topk_idx, topk_w, probs, p_mean, ws, L, st, nullptr);
+  return do_route(c, x, Wg, bg, sel_bias, topk_idx, topk_w, probs, logits, p_mean, z_loss, ws, L,
+                  st, nullptr);
+}
+
+MOE_API moe_status_t moe_expert_choice(const moe_config_t* cfg, const float* logits,
+                                       const float* p_mean, int32_t* counts, int32_t* offsets,
+                                       int32_t* perm, int32_t* inv, float* f, float* l_aux,
+                                       void* stream) {
+  MOE_TRY(check_config(cfg));
+  const moe_config_t& c = *cfg;
+  if (!expert_choice(c)) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_ptrs(true, counts, offsets));
+  if (c.T > 0) MOE_TRY(check_ptrs(true, logits, inv));
+  if (max_rows_of(c) > 0) MOE_TRY(check_ptrs(true, perm));
+  if (l_aux) MOE_TRY(check_ptrs(true, p_mean));
+  MOE_TRY(check_ptrs(false, logits, p_mean, perm, inv, f, l_aux));
+  DeviceInfo d;
+  MOE_TRY(device_info(&d));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return cuda_status(launch_expert_choice(logits, p_mean, c.T, c.N, (int)ec_tokens(c),
+                                          c.aux_alpha, counts, offsets, perm, inv, f, l_aux, st,
+                                          nullptr));
+}
+
+MOE_API moe_status_t moe_update_sel_bias(const moe_config_t* cfg, const int32_t* counts,
+                                         float* sel_bias, float gamma, void* stream) {
+  MOE_TRY(check_config(cfg));
+  if (std::isnan(gamma)) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_ptrs(true, counts, sel_bias));
+  DeviceInfo d;
+  MOE_TRY(device_info(&d));
+  return cuda_status(
+      launch_update_sel_bias(counts, sel_bias, cfg->N, gamma, static_cast<cudaStream_t>(stream)));
 }
 
 MOE_API moe_status_t moe_permute(const moe_config_t* cfg, const int32_t* topk_idx,
@@ -398,6 +484,7 @@ MOE_API moe_status_t moe_permute(const moe_config_t* cfg, const int32_t* topk_id
                                  size_t ws_bytes, void* stream) {
   MOE_TRY(check_config(cfg));
   const moe_config_t& c = *cfg;
+  if (expert_choice(c)) return MOE_ERR_INVALID_ARG;  // moe_expert_choice dispatches those
   MOE_TRY(check_ptrs(true, counts, offsets));
   if ((int64_t)c.T * c.k > 0) MOE_TRY(check_ptrs(true, topk_idx, inv));
   if (max_rows_of(c) > 0) MOE_TRY(check_ptrs(true, perm));
@@ -448,7 +535,8 @@ MOE_API moe_status_t moe_combine(const moe_config_t* cfg, const uint16_t* y, con
   using bf = __nv_bfloat16;
   return cuda_status(launch_combine(reinterpret_cast<const bf*>(y), inv,
                                     c.F_shared > 0 ? reinterpret_cast<const bf*>(y_shared) : nullptr,
-                                    reinterpret_cast<bf*>(out), c.T, c.k, c.H, st, nullptr));
+                                    reinterpret_cast<bf*>(out), c.T, slots_of(c), c.H, st,
+                                    nullptr));
 }
 
 MOE_API moe_status_t moe_forward(const moe_config_t* cfg, const moe_weights_t* weights,
@@ -463,7 +551,7 @@ MOE_API moe_status_t moe_forward(const moe_config_t* cfg, const moe_weights_t* w
   std::memset(&o, 0, sizeof(o));
   if (outputs) o = *outputs;
   MOE_TRY(check_ptrs(false, o.topk_idx, o.topk_w, o.probs, o.p_mean, o.counts, o.offsets, o.perm,
-                     o.inv, o.f, o.l_aux));
+                     o.inv, o.f, o.l_aux, o.z_loss, o.logits));
   MOE_TRY(check_ws(c, ws, ws_bytes));
   DeviceInfo d;
   MOE_TRY(device_info(&d));
@@ -482,18 +570,31 @@ MOE_API moe_status_t moe_forward(const moe_config_t* cfg, const moe_weights_t* w
   int32_t* inv = o.inv ? o.inv : at<int32_t>(ws, L.inv);
   float* f = o.f ? o.f : at<float>(ws, L.f);
   float* l_aux = o.l_aux ? o.l_aux : at<float>(ws, L.l_aux);
+  float* z_loss = o.z_loss ? o.z_loss : at<float>(ws, L.z_loss);
   uint16_t* y = at<uint16_t>(ws, L.y);
   uint16_t* ys = c.F_shared > 0 ? at<uint16_t>(ws, L.y_s) : nullptr;
 
   MOE_TRY(begin_call(c, ws, L, st, tr));
-  MOE_TRY(do_route(c, x, weights->Wg, weights->bg, weights->sel_bias, idx, w, o.probs, p_mean, ws,
-                   L, st, tr));
-  MOE_TRY(do_permute(c, idx, p_mean, counts, offsets, perm, inv, f, l_aux, ws, L, st, tr, x));
-  MOE_TRY(do_ffn(c, x, perm, offsets, w, *weights, y, ys, ws, L, d.sms, st, tr, true));
+  if (expert_choice(c)) {
+    // route (logits + softmax) -> each expert takes its top-C tokens ->
+    // gather -> expert FFN weighted by P[t, e] -> combine over the N experts
+    float* logits = o.logits ? o.logits : at<float>(ws, L.logits);
+    float* probs = o.probs ? o.probs : at<float>(ws, L.probs);
+    MOE_TRY(do_route(c, x, weights->Wg, weights->bg, nullptr, nullptr, nullptr, probs, logits,
+                     p_mean, z_loss, ws, L, st, tr));
+    MOE_CUDA(launch_expert_choice(logits, p_mean, c.T, c.N, (int)ec_tokens(c), c.aux_alpha,
+                                  counts, offsets, perm, inv, f, l_aux, st, tr));
+    MOE_TRY(do_ffn(c, x, perm, offsets, probs, *weights, y, ys, ws, L, d.sms, st, tr, false));
+  } else {
+    MOE_TRY(do_route(c, x, weights->Wg, weights->bg, weights->sel_bias, idx, w, o.probs, o.logits,
+                     p_mean, z_loss, ws, L, st, tr));
+    MOE_TRY(do_permute(c, idx, p_mean, counts, offsets, perm, inv, f, l_aux, ws, L, st, tr, x));
+    MOE_TRY(do_ffn(c, x, perm, offsets, w, *weights, y, ys, ws, L, d.sms, st, tr, true));
+  }
   if (c.T > 0) {
     using bf = __nv_bfloat16;
     MOE_CUDA(launch_combine(reinterpret_cast<const bf*>(y), inv, reinterpret_cast<const bf*>(ys),
-                            reinterpret_cast<bf*>(out), c.T, c.k, c.H, st, tr));
+                            reinterpret_cast<bf*>(out), c.T, slots_of(c), c.H, st, tr));
   }
   trace_mark(tr, st);
   return MOE_OK;

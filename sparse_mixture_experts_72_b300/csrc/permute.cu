@@ -6,8 +6,10 @@
 // (L_aux = alpha * N * sum f_i p_i); "AI-Research-SKILLs MoE 训练实战" §4.3
 // (f from bincount of the top-k indices over their count), §4.4 (drop_tokens).
 //
-// Assignments a = t*k + j are ranked within their expert in increasing a
-// (a stable scatter), so the first C assignments of each expert keep a row.
+// Assignments claim slots in a fixed order of positions p: p = a = t*k + j
+// (token-major) or p = j*T + t (slot-major: every token's first choice
+// first).  Each is ranked within its expert in increasing p (a stable
+// scatter), so the first C claimants of each expert keep a row.
 // Three launches, all integer work and no atomics on values:
 //   1. rank:    per 256-assignment chunk, rank of each assignment among the
 //               chunk's assignments to the same expert + chunk histogram
@@ -22,15 +24,24 @@ namespace moe {
 constexpr int PR_THREADS = kPermuteChunk;
 constexpr int PR_WARPS = PR_THREADS / 32;
 
+// position p of assignment a (and back): the claim order
+__device__ __forceinline__ int64_t claim_pos(int64_t a, int T, int k, int slot_major) {
+  return slot_major ? (a % k) * T + a / k : a;
+}
+__device__ __forceinline__ int64_t claim_assignment(int64_t p, int T, int k, int slot_major) {
+  return slot_major ? (p % T) * k + p / T : p;
+}
+
+// local_rank and the chunk histograms are indexed by claim position p.
 __global__ void __launch_bounds__(PR_THREADS) permute_rank_kernel(
     const int32_t* __restrict__ idx, int32_t* __restrict__ local_rank,
-    int32_t* __restrict__ blk_hist, int64_t A, int N) {
+    int32_t* __restrict__ blk_hist, int64_t A, int N, int T, int k, int slot_major) {
   extern __shared__ int32_t wcnt[];  // [PR_WARPS][N]
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   for (int i = tid; i < PR_WARPS * N; i += PR_THREADS) wcnt[i] = 0;
   __syncthreads();
-  const int64_t a = (int64_t)blockIdx.x * PR_THREADS + tid;
-  int e = (a < A) ? idx[a] : -1;
+  const int64_t a = (int64_t)blockIdx.x * PR_THREADS + tid;   // claim position p
+  int e = (a < A) ? idx[claim_assignment(a, T, k, slot_major)] : -1;
   if (e < 0 || e >= N) e = -1;  // out-of-range indices take no slot
   const uint32_t peers = __match_any_sync(0xffffffffu, e);
   const int wrank = __popc(peers & ((1u << lane) - 1u));
@@ -100,12 +111,14 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(
 __global__ void __launch_bounds__(256) permute_scatter_kernel(
     const int32_t* __restrict__ idx, const int32_t* __restrict__ local_rank,
     const int32_t* __restrict__ blk_base, const int32_t* __restrict__ offsets,
-    int32_t* __restrict__ perm, int32_t* __restrict__ inv, int64_t A, int N, int64_t capacity) {
+    int32_t* __restrict__ perm, int32_t* __restrict__ inv, int64_t A, int N, int64_t capacity,
+    int T, int k, int slot_major) {
   const int64_t a = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (a >= A) return;
   const int e = idx[a];
   if (e < 0 || e >= N) { inv[a] = -1; return; }
-  const int64_t pos = (int64_t)blk_base[(a / kPermuteChunk) * N + e] + local_rank[a];
+  const int64_t p = claim_pos(a, T, k, slot_major);
+  const int64_t pos = (int64_t)blk_base[(p / kPermuteChunk) * N + e] + local_rank[p];
   if (capacity >= 0 && pos >= capacity) { inv[a] = -1; return; }
   const int32_t row = offsets[e] + (int32_t)pos;
   perm[row] = (int32_t)a;
@@ -120,7 +133,8 @@ __global__ void __launch_bounds__(256) permute_scatter_gather_kernel(
     const int32_t* __restrict__ idx, const int32_t* __restrict__ local_rank,
     const int32_t* __restrict__ blk_base, const int32_t* __restrict__ offsets,
     int32_t* __restrict__ perm, int32_t* __restrict__ inv, int T, int N, int k,
-    int64_t capacity, const __nv_bfloat16* __restrict__ x, __nv_bfloat16* __restrict__ xp, int H) {
+    int64_t capacity, const __nv_bfloat16* __restrict__ x, __nv_bfloat16* __restrict__ xp, int H,
+    int slot_major) {
   const int lane = threadIdx.x % 32;
   const int64_t nvec = H / 8;
   for (int64_t t = (int64_t)blockIdx.x * 8 + threadIdx.x / 32; t < T; t += (int64_t)gridDim.x * 8) {
@@ -130,7 +144,8 @@ __global__ void __launch_bounds__(256) permute_scatter_gather_kernel(
       const int64_t a = t * k + lane;
       const int e = idx[a];
       if (e >= 0 && e < N) {
-        const int64_t pos = (int64_t)blk_base[(a / kPermuteChunk) * N + e] + local_rank[a];
+        const int64_t p = slot_major ? (int64_t)lane * T + t : a;
+        const int64_t pos = (int64_t)blk_base[(p / kPermuteChunk) * N + e] + local_rank[p];
         if (capacity < 0 || pos < capacity) row = offsets[e] + (int32_t)pos;
       }
       inv[a] = row;
@@ -160,7 +175,7 @@ cudaError_t launch_permute(const PermuteLaunch& a, cudaStream_t st, LaunchTrace*
   if (A > 0) {
     trace_mark(tr, st);
     permute_rank_kernel<<<nblk, PR_THREADS, PR_WARPS * a.N * sizeof(int32_t), st>>>(
-        a.topk_idx, a.local_rank, a.blk_hist, A, a.N);
+        a.topk_idx, a.local_rank, a.blk_hist, A, a.N, a.T, a.k, a.slot_major);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
   }
@@ -178,10 +193,11 @@ cudaError_t launch_permute(const PermuteLaunch& a, cudaStream_t st, LaunchTrace*
     if (blocks > 148 * 16) blocks = 148 * 16;
     permute_scatter_gather_kernel<<<(unsigned)blocks, 256, 0, st>>>(
         a.topk_idx, a.local_rank, a.blk_base, a.offsets, a.perm, a.inv, a.T, a.N, a.k,
-        a.capacity, a.x, a.xp, a.H);
+        a.capacity, a.x, a.xp, a.H, a.slot_major);
   } else {
     permute_scatter_kernel<<<(unsigned)((A + 255) / 256), 256, 0, st>>>(
-        a.topk_idx, a.local_rank, a.blk_base, a.offsets, a.perm, a.inv, A, a.N, a.capacity);
+        a.topk_idx, a.local_rank, a.blk_base, a.offsets, a.perm, a.inv, A, a.N, a.capacity, a.T,
+        a.k, a.slot_major);
   }
   return cudaGetLastError();
 }

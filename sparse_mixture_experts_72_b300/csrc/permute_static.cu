@@ -72,7 +72,9 @@ MOE_API moe_status_t moe_permute_static(const moe_config_t* cfg, const int32_t* 
   if (!cfg) return MOE_ERR_INVALID_ARG;
   const moe_config_t& c = *cfg;
   if (c.T < 0 || c.H <= 0 || c.F <= 0 || c.N <= 0 || c.k <= 0 || c.k > c.N || c.F_shared < 0 ||
-      std::isnan(c.capacity_factor) || std::isnan(c.aux_alpha))
+      std::isnan(c.capacity_factor) || std::isnan(c.aux_alpha) ||
+      c.routing != MOE_ROUTING_TOKEN_CHOICE || c.min_capacity < 0 ||
+      (c.drop_order != MOE_DROP_TOKEN_MAJOR && c.drop_order != MOE_DROP_SLOT_MAJOR))
     return MOE_ERR_INVALID_ARG;
   const int64_t A = (int64_t)c.T * c.k;
   // the fixed scratch bounds the problem size
@@ -81,6 +83,7 @@ MOE_API moe_status_t moe_permute_static(const moe_config_t* cfg, const int32_t* 
   if (c.capacity_factor > 0.0f) {
     const double v = std::floor((double)c.T / (double)c.N * (double)c.capacity_factor);
     C = v < 0 ? 0 : (int64_t)v;
+    if (C < c.min_capacity) C = c.min_capacity;
   }
   const int64_t R = C < 0 ? A : (C * c.N < A ? C * c.N : A);
   if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
@@ -115,6 +118,7 @@ MOE_API moe_status_t moe_permute_static(const moe_config_t* cfg, const int32_t* 
   a.k = c.k;
   a.capacity = C;
   a.alpha = c.aux_alpha;
+  a.slot_major = c.drop_order == MOE_DROP_SLOT_MAJOR ? 1 : 0;
   return launch_permute(a, static_cast<cudaStream_t>(stream), nullptr) == cudaSuccess
              ? MOE_OK
              : MOE_ERR_CUDA;

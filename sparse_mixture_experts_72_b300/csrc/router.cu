@@ -98,7 +98,9 @@ __global__ void __launch_bounds__(RS_WARPS * 32) router_select_kernel(
     int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, float* __restrict__ probs,
     float* __restrict__ p_part, int T, int N, int k) {
   __shared__ float psum[RS_WARPS][NPL * 32];
+  __shared__ float zsum[RS_WARPS];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  float zacc = 0.0f;  // this warp's sum of logsumexp(l_t)^2 (router z-loss)
   float pacc[NPL];
 #pragma unroll
   for (int i = 0; i < NPL; ++i) pacc[i] = 0.0f;
@@ -124,6 +126,10 @@ __global__ void __launch_bounds__(RS_WARPS * 32) router_select_kernel(
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+    {
+      const float lse = m + logf(z);
+      zacc += lse * lse;
+    }
     const float inv_z = 1.0f / z;
 #pragma unroll
     for (int i = 0; i < NPL; ++i) {
@@ -132,6 +138,7 @@ __global__ void __launch_bounds__(RS_WARPS * 32) router_select_kernel(
       const int e = lane + 32 * i;
       if (probs && e < N) probs[(size_t)t * N + e] = l[i];
     }
+    if (topk_idx == nullptr) continue;  // expert choice: no per-token selection
     // k rounds of warp arg-max on s; ties go to the lower expert index
     float selp[MOE_MAX_TOP_K > 32 ? 32 : MOE_MAX_TOP_K];
     int seli[MOE_MAX_TOP_K > 32 ? 32 : MOE_MAX_TOP_K];
@@ -170,23 +177,32 @@ __global__ void __launch_bounds__(RS_WARPS * 32) router_select_kernel(
   }
 #pragma unroll
   for (int i = 0; i < NPL; ++i) psum[warp][lane + 32 * i] = pacc[i];
+  if (lane == 0) zsum[warp] = zacc;
   __syncthreads();
-  for (int e = threadIdx.x; e < N; e += blockDim.x) {
+  for (int e = threadIdx.x; e <= N; e += blockDim.x) {
     float acc = 0.0f;
 #pragma unroll
-    for (int w = 0; w < RS_WARPS; ++w) acc += psum[w][e];
-    p_part[(size_t)blockIdx.x * N + e] = acc;
+    for (int w = 0; w < RS_WARPS; ++w) acc += e < N ? psum[w][e] : zsum[w];
+    p_part[(size_t)blockIdx.x * (N + 1) + e] = acc;
   }
 }
 
-// p_mean[e] = (sum over blocks, in block order) / T
+// p_mean[e] = (sum over blocks, in block order) / T; column N of the block
+// sums is the router z-loss numerator.  With nblocks = 0 it zeroes both.
 __global__ void router_pmean_kernel(const float* __restrict__ p_part, float* __restrict__ p_mean,
-                                    int nblocks, int N, int T) {
+                                    float* __restrict__ z_loss, int nblocks, int N, int T) {
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
-  if (e >= N) return;
+  if (e > N) return;
   float acc = 0.0f;
-  for (int b = 0; b < nblocks; ++b) acc += p_part[(size_t)b * N + e];
-  p_mean[e] = T > 0 ? acc / (float)T : 0.0f;
+  for (int b = 0; b < nblocks; ++b) acc += p_part[(size_t)b * (N + 1) + e];
+  const float mean = T > 0 ? acc / (float)T : 0.0f;
+  if (e < N) p_mean[e] = mean;
+  else if (z_loss) *z_loss = mean;
+}
+
+cudaError_t launch_router_stats_zero(float* p_mean, float* z_loss, int N, cudaStream_t st) {
+  router_pmean_kernel<<<(N + 1 + 255) / 256, 256, 0, st>>>(nullptr, p_mean, z_loss, 0, N, 0);
+  return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------
@@ -200,13 +216,14 @@ cudaError_t launch_router(const RouterLaunch& a, cudaStream_t st, LaunchTrace* t
   if (T > 0) {
     dim3 grid((T + RL_BT - 1) / RL_BT, (N + RL_BE - 1) / RL_BE);
     trace_mark(tr, st);
-    router_logits_kernel<<<grid, 256, 0, st>>>(a.x, a.Wg, a.bg, a.logits, T, a.H, N);
+    float* lg = a.logits_out ? a.logits_out : a.logits;
+    router_logits_kernel<<<grid, 256, 0, st>>>(a.x, a.Wg, a.bg, lg, T, a.H, N);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     const int npl = (N + 31) / 32;
     trace_mark(tr, st);
 #define MOE_SEL(NPLV)                                                                      \
-  router_select_kernel<NPLV><<<nsel, RS_WARPS * 32, 0, st>>>(a.logits, a.sel_bias, a.topk_idx, \
+  router_select_kernel<NPLV><<<nsel, RS_WARPS * 32, 0, st>>>(lg, a.sel_bias, a.topk_idx,        \
                                                              a.topk_w, a.probs, a.p_part, T, N, a.k)
     if (npl <= 1) MOE_SEL(1);
     else if (npl <= 2) MOE_SEL(2);
@@ -219,7 +236,8 @@ cudaError_t launch_router(const RouterLaunch& a, cudaStream_t st, LaunchTrace* t
     if (err != cudaSuccess) return err;
   }
   trace_mark(tr, st);
-  router_pmean_kernel<<<(N + 255) / 256, 256, 0, st>>>(a.p_part, a.p_mean, nsel, N, T);
+  router_pmean_kernel<<<(N + 1 + 255) / 256, 256, 0, st>>>(a.p_part, a.p_mean, a.z_loss, nsel,
+                                                           N, T);
   return cudaGetLastError();
 }
 

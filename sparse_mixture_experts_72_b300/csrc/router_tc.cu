@@ -123,6 +123,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* flags = reinterpret_cast<int*>(tmem_holder + 2);      // [0] last CTA
   float* psum = reinterpret_cast<float*>(tmem_holder + 4);   // [4][N_pad]
+  float* zsum = psum + 4 * N_pad;                            // [4]
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int S = args.splits;                                 // cluster size
@@ -270,6 +271,15 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
   }
 
   if (warp >= 2) {
+    if (args.logits_out && !*abort_flag) {
+      // the finished logits of this CTA's rows, row-contiguous stores
+      for (int i = threadIdx.x - 64; i < rows_per * N; i += 128) {
+        const int r = row_lo + i / N, e = i % N;
+        if (t0 + r < args.T)
+          args.logits_out[(size_t)(t0 + r) * N + e] =
+              ltile[(size_t)r * ld + e] + (args.bg ? args.bg[e] : 0.0f);
+      }
+    }
     // ---- E3: one token per thread for this CTA's rows
     const int q = warp & 3;
     const int row = q * 32 + lane;
@@ -308,18 +318,31 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
         }
       }
       // renormalised weights of the k chosen experts (unbiased softmax)
-      float wsum = 0.0f;
+      if (args.topk_idx) {
+        float wsum = 0.0f;
 #pragma unroll
-      for (int j = 0; j < KMAX; ++j)
-        if (j < k) wsum += expf(tl[j] - m);
-      const float inv = 1.0f / wsum;
+        for (int j = 0; j < KMAX; ++j)
+          if (j < k) wsum += expf(tl[j] - m);
+        const float inv = 1.0f / wsum;
 #pragma unroll
-      for (int j = 0; j < KMAX; ++j) {
-        if (j < k) {
-          args.topk_idx[(size_t)t * k + j] = ti[j];
-          args.topk_w[(size_t)t * k + j] = expf(tl[j] - m) * inv;
+        for (int j = 0; j < KMAX; ++j) {
+          if (j < k) {
+            args.topk_idx[(size_t)t * k + j] = ti[j];
+            args.topk_w[(size_t)t * k + j] = expf(tl[j] - m) * inv;
+          }
         }
       }
+    }
+    // router z-loss term of the token: logsumexp(l_t)^2
+    {
+      float zt = 0.0f;
+      if (valid) {
+        const float lse = m + logf(z);
+        zt = lse * lse;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) zt += __shfl_xor_sync(0xffffffffu, zt, o);
+      if (lane == 0) zsum[q] = zt;
     }
     // pass 2: P = exp(l - m) / z for the probs output and the column sums
     // (every lane takes part in the shuffles; rows not finished here add 0)
@@ -348,9 +371,11 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
     named_barrier(1, 128);
     if (!*abort_flag) {
       for (int e = threadIdx.x - 64; e < N; e += 128)
-        args.p_part[(size_t)blockIdx.x * N + e] =
+        args.p_part[(size_t)blockIdx.x * (N + 1) + e] =
             ((psum[0 * N_pad + e] + psum[1 * N_pad + e]) + psum[2 * N_pad + e]) +
             psum[3 * N_pad + e];
+      if (threadIdx.x == 64)
+        args.p_part[(size_t)blockIdx.x * (N + 1) + N] = ((zsum[0] + zsum[1]) + zsum[2]) + zsum[3];
     }
     __threadfence();
     named_barrier(1, 128);
@@ -359,17 +384,20 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
     if (flags[0]) {
       __threadfence();
       const int nb = gridDim.x;
-      for (int e = threadIdx.x - 64; e < N; e += 128) {
+      const int W = N + 1;
+      for (int e = threadIdx.x - 64; e <= N; e += 128) {
         // fixed association: 8 interleaved partial sums, then a fixed tree
         float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
         int b = 0;
         for (; b + 8 <= nb; b += 8) {
 #pragma unroll
-          for (int u = 0; u < 8; ++u) acc[u] += __ldcg(args.p_part + (size_t)(b + u) * N + e);
+          for (int u = 0; u < 8; ++u) acc[u] += __ldcg(args.p_part + (size_t)(b + u) * W + e);
         }
-        for (int u = 0; b < nb; ++b, ++u) acc[u] += __ldcg(args.p_part + (size_t)b * N + e);
+        for (int u = 0; b < nb; ++b, ++u) acc[u] += __ldcg(args.p_part + (size_t)b * W + e);
         const float s2 = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
-        args.p_mean[e] = args.T > 0 ? s2 / (float)args.T : 0.0f;
+        const float mean = args.T > 0 ? s2 / (float)args.T : 0.0f;
+        if (e < N) args.p_mean[e] = mean;
+        else if (args.z_loss) *args.z_loss = mean;
       }
     }
   }
@@ -430,7 +458,7 @@ RouterTcPlan router_tc_plan(int T, int N, int H) {
   const int ring = p.stages * p.stage_bytes;
   const int tile = RT_BM * (p.N_pad + 4) * 4;
   p.work_bytes = ((ring > tile ? ring : tile) + 1023) / 1024 * 1024;
-  p.smem = 1024 + p.work_bytes + (2 * RT_MAX_STAGES + 2) * 8 + 16 + 4 * p.N_pad * 4;
+  p.smem = 1024 + p.work_bytes + (2 * RT_MAX_STAGES + 2) * 8 + 16 + 4 * p.N_pad * 4 + 16;
   return p;
 }
 
@@ -444,7 +472,7 @@ cudaError_t launch_router_tc(const RouterLaunch& a, __nv_bfloat16* W3, int* tick
   const RouterTcPlan P = router_tc_plan(a.T, a.N, a.H);
   if (a.T == 0) {
     trace_mark(tr, st);
-    return cudaMemsetAsync(a.p_mean, 0, sizeof(float) * a.N, st);
+    return launch_router_stats_zero(a.p_mean, a.z_loss, a.N, st);  // p_mean = 0, z_loss = 0
   }
   {
     const int64_t total = (int64_t)P.N_pad * P.H_pad;
@@ -471,6 +499,8 @@ cudaError_t launch_router_tc(const RouterLaunch& a, __nv_bfloat16* W3, int* tick
   args.topk_idx = a.topk_idx;
   args.topk_w = a.topk_w;
   args.probs = a.probs;
+  args.logits_out = a.logits_out;
+  args.z_loss = a.z_loss;
   args.p_part = a.p_part;
   args.p_mean = a.p_mean;
   args.ticket = ticket;

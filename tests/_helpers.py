@@ -35,8 +35,7 @@ def bf16_host(t: torch.Tensor) -> np.ndarray:
 
 def config_of(w: wl.Workload):
     import sparse_mixture_experts_72_b300 as m
-    return m.MoEConfig(T=w.T, H=w.H, F=w.F, N=w.N, k=w.k, capacity_factor=w.capacity_factor,
-                       F_shared=w.F_shared, aux_alpha=w.aux_alpha)
+    return m.MoEConfig(**w.config_kwargs())
 
 
 def upload(w: wl.Workload, seed: int = 0, device="cuda"):
@@ -53,7 +52,8 @@ def oracle_forward(w: wl.Workload, x_bits, router, seed=0, tokens=None):
     Wg, bg, sel = router
     return O.forward(wl.bf16_bits_to_f64(x_bits), Wg, bg, sel, w.k, w.capacity_factor,
                      w.aux_alpha, wl.expert_getter_f64(w, seed), wl.shared_f64(w, seed),
-                     tokens=tokens)
+                     tokens=tokens, routing=w.routing, activation=w.activation,
+                     min_capacity=w.min_capacity, drop_order=w.drop_order)
 
 
 # A GPU choice that differs from the oracle's at a near tie must still be a

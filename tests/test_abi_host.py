@@ -64,14 +64,30 @@ def test_host_shape_functions(lib):
     assert lib.moe_workspace_size(C.byref(c)) > 0
     assert lib.moe_workspace_size(C.byref(_cfg(k=5))) == 0  # k > N is invalid
     assert lib.moe_workspace_size(None) == 0
+    # min_capacity raises a smaller capacity, only when a factor is given
+    for T, N, cf, mc in [(40, 16, 0.1, 4), (32768, 64, 1.25, 4), (64, 4, 1.0, 20), (64, 4, 0.0, 4)]:
+        want = O.capacity(T, N, cf, mc)
+        c = _cfg(T=T, N=N, capacity_factor=cf, k=1, min_capacity=mc)
+        assert lib.moe_capacity(C.byref(c)) == (-1 if want is None else want)
+    # expert choice: N * min(C, T) rows; needs a capacity factor
+    c = _cfg(T=300, N=6, capacity_factor=1.5, k=1, routing=1)
+    assert lib.moe_max_rows(C.byref(c)) == 6 * 75
+    c = _cfg(T=64, N=4, capacity_factor=8.0, k=1, routing=1)
+    assert lib.moe_max_rows(C.byref(c)) == 4 * 64
+    assert lib.moe_workspace_size(C.byref(_cfg(routing=1, capacity_factor=0.0))) == 0
+    for bad in (dict(routing=2), dict(activation=3), dict(drop_order=2), dict(min_capacity=-1)):
+        assert lib.moe_workspace_size(C.byref(_cfg(**bad))) == 0, bad
 
 
 def test_launch_count_matches_bench_names(lib):
     import bench
     import moe_workloads as wl
     for w in list(wl.WORKLOADS.values()) + list(wl.TEST_WORKLOADS.values()):
+        from sparse_mixture_experts_72_b300 import _lib
         c = _cfg(T=w.T, H=w.H, F=w.F, N=w.N, k=w.k, capacity_factor=w.capacity_factor,
-                 F_shared=w.F_shared)
+                 F_shared=w.F_shared, routing=_lib.ROUTING[w.routing],
+                 activation=_lib.ACTIVATION[w.activation], min_capacity=w.min_capacity,
+                 drop_order=_lib.DROP_ORDER[w.drop_order])
         n = lib.moe_forward_num_launches(C.byref(c))
         assert n == len(bench.launch_names(w, lib.moe_max_rows(C.byref(c)) > 0)), w.name
 
@@ -113,6 +129,19 @@ def test_rejects_bad_arguments_before_any_launch(lib):
     if not torch.cuda.is_available():
         assert _forward(lib, ok, _weights()) == 6
     assert lib.moe_status_string(3) == b"workspace missing, misaligned or too small"
+    # widened entry points validate on the host as well
+    ec = _cfg(routing=1, capacity_factor=1.0)
+    assert lib.moe_expert_choice(C.byref(ok), FAKE, None, FAKE, FAKE, FAKE, FAKE, None, None,
+                                 None) == 1   # token-choice config
+    assert lib.moe_expert_choice(C.byref(ec), FAKE + 4, None, FAKE, FAKE, FAKE, FAKE, None, None,
+                                 None) == 2   # misaligned logits
+    assert lib.moe_expert_choice(C.byref(ec), FAKE, None, FAKE, FAKE, FAKE, FAKE, None, FAKE,
+                                 None) == 1   # l_aux without p_mean
+    assert lib.moe_expert_choice(C.byref(_cfg(routing=1, capacity_factor=1.0, T=60000)), FAKE,
+                                 None, FAKE, FAKE, FAKE, FAKE, None, None, None) == 2  # T too large
+    assert lib.moe_update_sel_bias(C.byref(ok), None, FAKE, C.c_float(0.1), None) == 1
+    assert lib.moe_permute(C.byref(ec), FAKE, None, FAKE, FAKE, FAKE, FAKE, None, None, FAKE * 16,
+                           1 << 30, None) == 1   # expert choice has its own dispatch
 
 
 def test_failure_injection_hook_validates_its_count(lib):
