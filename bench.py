@@ -17,6 +17,7 @@ import json
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -97,9 +98,9 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int, interval_ms: int = 50):
+    def __init__(self, gpu_index: int, out_dir: str, interval_ms: int = 50):
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        self.path = os.path.join(out_dir, f"clocks_rank{gpu_index}.csv")
         os.makedirs(os.path.dirname(self.path), exist_ok=True)
         try:
             self.fh = open(self.path, "w")
@@ -157,6 +158,17 @@ def algorithmic_work(w: wl.Workload, counts: np.ndarray, R: int):
         out["shared_ffn"] = dict(flops=2.0 * m * w.T * w.H * Fs,
                                  bytes=2.0 * (m * Fs * w.H + 2 * w.T * w.H))
     return out
+
+
+def bench_config(w: wl.Workload, world: int) -> dict:
+    """The workload description both arms print (shapes, options, protocol)."""
+    return {"workload": w.name, "T": w.T, "H": w.H, "F": w.F, "N": w.N, "k": w.k,
+            "capacity_factor": w.capacity_factor, "F_shared": w.F_shared,
+            "routing": w.routing, "activation": w.activation,
+            "l2": "flushed between steps (256 MiB write, untimed)",
+            "launch": "CUDA graph replay of moe_forward; every 10th step replays a copy with an "
+                      "event node before each launch",
+            "parallelism": f"replicas x{world}"}
 
 
 def launch_names(w: wl.Workload, has_rows: bool):
@@ -271,8 +283,7 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": S / tps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference",
-            "config": {"workload": w.name, "T": w.T, "H": w.H, "F": w.F, "N": w.N, "k": w.k,
-                       "capacity_factor": w.capacity_factor, "F_shared": w.F_shared},
+            "config": bench_config(w, args.gpus),
             "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -335,7 +346,7 @@ def run_ours(args):
     traced_steps = set(range(0, K, TRACE_EVERY))
     per = {n: [] for n in names}
 
-    clocks = ClockSampler(device.index or 0)
+    clocks = ClockSampler(device.index or 0, args.clocks_dir)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -393,25 +404,60 @@ def run_ours(args):
         roof["launch_ms"] = per_ms[dom]
         roof["peak_source"] = f"{peak_src} (burst)"
 
-    # end to end through the C ABI with host buffers: H2D of x, forward, D2H of out
-    x_pin = torch.from_numpy(np.ascontiguousarray(x_bits_host).view(np.int16)).pin_memory()
-    out_pin = torch.empty((w.T, w.H), dtype=torch.int16).pin_memory()
-    x_dev16 = x.view(torch.int16)
-    E = max(10, min(K, 200))
-    e_s = [torch.cuda.Event(enable_timing=True) for _ in range(E)]
-    e_e = [torch.cuda.Event(enable_timing=True) for _ in range(E)]
-    for i in range(E):
-        flush.zero_()
-        e_s[i].record()
-        x_dev16.copy_(x_pin, non_blocking=True)
-        fwd.replay()
-        out_pin.copy_(out.view(torch.int16), non_blocking=True)
-        e_e[i].record()
+    # End to end through the C ABI with host buffers (moe_forward_host: H2D
+    # of x from pinned memory, the forward, D2H of out), pipelined over three
+    # streams (input copies, layers, output copies) and three buffer sets,
+    # so batch i+1's input copy and batch i-1's output copy overlap batch i's
+    # layer.  No flush here: the batches alternate between two weight
+    # replicas, so each step's weights were last read two steps earlier with
+    # the other replica's weights (2x the expert bytes) read in between.
+    wrep = [weights, m.MoEWeights(**{k: (None if v is None else v.clone())
+                                     for k, v in weights.__dict__.items()})]
+    SL = 3
+    x_pin = [torch.from_numpy(np.ascontiguousarray(x_bits_host).view(np.int16)).pin_memory()
+             .view(torch.bfloat16) for _ in range(SL)]
+    out_pin = [torch.empty((w.T, w.H), dtype=torch.bfloat16).pin_memory() for _ in range(SL)]
+    x_st = [torch.empty_like(x) for _ in range(SL)]
+    out_st = [torch.empty_like(out) for _ in range(SL)]
+    h2d_s, k_s, d2h_s = (torch.cuda.Stream(device) for _ in range(3))
+    done = [torch.cuda.Event() for _ in range(SL)]
+    wcs = [wr.c(cfg) for wr in wrep]
+
+    def e2e_step(i):
+        b = i % SL
+        h2d_s.wait_event(done[b])   # slot b's previous output copy has finished
+        m.moe_forward_host(cfg, None, x_pin[b], out_pin[b], x_st[b], out_st[b], ws=ws,
+                           h2d_stream=h2d_s, compute_stream=k_s, d2h_stream=d2h_s,
+                           weights_c=wcs[i % 2])
+        done[b].record(d2h_s)
+
+    E = max(20, min(K, 200))
     torch.cuda.synchronize()
-    e2e_ms = reduce_max(float(np.mean([e_s[i].elapsed_time(e_e[i]) for i in range(E)])), world,
-                        device)
+    for i in range(4):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    if m.moe_workspace_status(ws) != 0:
+        raise RuntimeError("device status after the end-to-end warm-up is not OK")
+    cur = torch.cuda.current_stream(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(cur)
+    for s_ in (h2d_s, k_s, d2h_s):
+        s_.wait_stream(cur)
+    for i in range(E):
+        e2e_step(i)
+    for s_ in (h2d_s, k_s, d2h_s):
+        cur.wait_stream(s_)
+    e1.record(cur)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(e0.elapsed_time(e1) / E, world, device)
+    if not all(torch.equal(out_pin[0].view(torch.int16), o.view(torch.int16)) for o in out_pin):
+        raise RuntimeError("the end-to-end batches disagree")
     e2e = {"value": aggregate(w.T, world, e2e_ms), "unit": "tokens/s",
-           "h2d_bytes_per_step": int(x_pin.numel() * 2), "d2h_bytes_per_step": int(out_pin.numel() * 2)}
+           "h2d_bytes_per_step": int(x_pin[0].numel() * 2),
+           "d2h_bytes_per_step": int(out_pin[0].numel() * 2),
+           "ms_per_step": e2e_ms,
+           "how": "moe_forward_host (C ABI, pinned host buffers) pipelined on H2D, compute "
+                  "and D2H streams with three buffer sets; two weight replicas alternate"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -425,15 +471,10 @@ def run_ours(args):
                 "steps": K, "warmup": max(args.warmup, 3), "ms_per_step": ms_max,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
                 "data": "synthetic",
-                "config": {"workload": w.name, "T": w.T, "H": w.H, "F": w.F, "N": w.N, "k": w.k,
-                           "capacity_factor": w.capacity_factor, "F_shared": w.F_shared,
-                           "routing": w.routing, "activation": w.activation,
-                           "kept_rows": R, "experts_hit": int((counts > 0).sum()),
-                           "l2": "flushed between steps (256 MiB write, untimed)",
-                           "launch": "CUDA graph replay of moe_forward; every 10th step replays a copy with an event node before each launch",
-                           "parallelism": f"replicas x{world}"},
+                "config": bench_config(w, world),
+                "work": {"kept_rows": R, "experts_hit": int((counts > 0).sum())},
                 "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": int(K * (n_launch - 1)),
+                "gpu_launches": int(K * sum(1 for n in names if "memset" not in n)),
                 "step_ms": {"graph_replay": graph_ms, "graph_replay_traced": traced_ms,
                             "traced_steps": len(traced_steps)},
                 "clocks": clk,
@@ -454,6 +495,8 @@ def main(argv=None):
                     choices=sorted(wl.WORKLOADS) + sorted(wl.TEST_WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clocks-dir", default=os.path.join(tempfile.gettempdir(), "moe_bench"),
+                    help="where the nvidia-smi clock samples of the timed region are kept")
     args = ap.parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)

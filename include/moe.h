@@ -228,6 +228,12 @@ moe_status_t moe_permute(const moe_config_t* cfg, const int32_t* topk_idx, const
  *   probs [T, N] for expert choice)
  *   y [moe_max_rows, H] bf16 out; y_shared [T, H] bf16 out (NULL iff F_shared == 0)
  * bf16 x bf16 products accumulate in fp32 on the tensor cores.
+ * Both Linears run in one persistent launch whose second-Linear tiles wait
+ * (bounded) for the first Linear's rows; it sizes its grid to the CTAs that
+ * fit on the GPU at once, so two such launches running at the same time on
+ * different streams can starve each other: keep the layers of concurrent
+ * batches on one stream (moe_forward_host shows the pattern); if they do
+ * overlap, the waits run out and MOE_ERR_TIMEOUT is recorded, nothing hangs.
  */
 moe_status_t moe_expert_ffn(const moe_config_t* cfg, const uint16_t* x, const int32_t* perm,
                             const int32_t* offsets, const float* topk_w,
@@ -260,6 +266,32 @@ moe_status_t moe_combine(const moe_config_t* cfg, const uint16_t* y, const int32
 moe_status_t moe_forward(const moe_config_t* cfg, const moe_weights_t* weights,
                          const uint16_t* x, uint16_t* out, const moe_outputs_t* outputs,
                          void* ws, size_t ws_bytes, void* stream, void* const* trace_events);
+
+/*
+ * moe_forward_host - moe_forward for a batch that lives in host memory:
+ * copies x_host into x_dev, runs the layer, copies out_dev back into
+ * out_host, with cudaMemcpyAsync and no host synchronisation.  The input
+ * copy goes on h2d_stream, the layer on compute_stream and the output copy
+ * on d2h_stream (any of them may be the same stream); the layer waits for
+ * the input copy and the output copy for the layer through events the
+ * library keeps per device.  x_host / out_host should be page-locked
+ * (pinned) for the copies to be asynchronous; pageable memory works but
+ * each copy then waits.
+ * Pipelining: successive calls with three streams overlap batch i+1's input
+ * copy and batch i-1's output copy with batch i's layer; the layers stay in
+ * order on the one compute stream (the expert-FFN launch assumes it is the
+ * only one of its kind on the GPU at a time).  The caller owns buffer reuse:
+ * x_dev / out_dev / out_host of a call must not be reused before its output
+ * copy has completed (three sets of staging buffers keep all three engines
+ * busy).
+ *   x_host [T, H] bf16 (host), out_host [T, H] bf16 (host)
+ *   x_dev, out_dev [T, H] bf16 (device staging), the rest as moe_forward.
+ */
+moe_status_t moe_forward_host(const moe_config_t* cfg, const moe_weights_t* weights,
+                              const uint16_t* x_host, uint16_t* x_dev, uint16_t* out_dev,
+                              uint16_t* out_host, const moe_outputs_t* outputs, void* ws,
+                              size_t ws_bytes, void* h2d_stream, void* compute_stream,
+                              void* d2h_stream);
 
 /*
  * moe_permute_static - moe_permute for callers that cannot allocate device

@@ -25,6 +25,7 @@ __all__ = ["MoEConfig", "MoEWeights", "MoeError", "moe_workspace_size", "moe_max
            "moe_permute_static",
            "moe_expert_ffn", "moe_combine", "moe_forward", "moe_workspace_status",
            "moe_debug_suppress_gemm_producer", "moe_expert_choice", "moe_update_sel_bias",
+           "moe_forward_host",
            "MoEForwardGraph", "alloc_outputs",
            "make_workspace", "library_path", "MOE_TRACE_MAX_EVENTS"]
 
@@ -353,6 +354,35 @@ def moe_forward(cfg: MoEConfig, weights: MoEWeights, x, *, out=None, outputs: Op
                         C.byref(oc) if oc is not None else None, wsp, wsn, _stream(stream), ev)
     check(st, "moe_forward")
     return out
+
+
+def moe_forward_host(cfg: MoEConfig, weights: MoEWeights, x_host, out_host, x_dev, out_dev, *,
+                     outputs: Optional[dict] = None, ws=None, h2d_stream=None,
+                     compute_stream=None, d2h_stream=None, weights_c=None):
+    """The whole layer on a batch in host memory: H2D of x_host into x_dev
+    (h2d_stream), the forward (compute_stream), D2H of out_dev into out_host
+    (d2h_stream); the streams default to the current one.  Pin x_host /
+    out_host for asynchronous copies.  Returns out_host."""
+    for t, n in ((x_host, "x_host"), (out_host, "out_host")):
+        if t.is_cuda or t.dtype != torch.bfloat16 or tuple(t.shape) != (cfg.T, cfg.H) or \
+                not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous host bf16 tensor of shape {(cfg.T, cfg.H)}")
+    oc = None
+    if outputs is not None:
+        oc = _lib.MoeOutputs(*[(C.c_void_p(outputs[n].data_ptr())
+                                if outputs.get(n) is not None and outputs[n].numel() > 0 else None)
+                               for n in _OUT_FIELDS])
+    ws, wsp, wsn = _ws(cfg, ws, x_dev.device)
+    wc = weights_c if weights_c is not None else weights.c(cfg)
+    hp = lambda t: C.c_void_p(t.data_ptr()) if t.numel() > 0 else None  # noqa: E731
+    st = _L.moe_forward_host(C.byref(cfg.c()), C.byref(wc), hp(x_host),
+                             _p(x_dev, torch.bfloat16, (cfg.T, cfg.H), "x_dev", True),
+                             _p(out_dev, torch.bfloat16, (cfg.T, cfg.H), "out_dev", True),
+                             hp(out_host), C.byref(oc) if oc is not None else None, wsp, wsn,
+                             _stream(h2d_stream), _stream(compute_stream),
+                             _stream(d2h_stream))
+    check(st, "moe_forward_host")
+    return out_host
 
 
 class MoEForwardGraph:

@@ -16,7 +16,7 @@ MOE_TRACE_MAX_EVENTS = 32
 # every symbol include/moe.h declares
 EXPORTED = ["moe_workspace_size", "moe_max_rows", "moe_capacity", "moe_forward_num_launches",
             "moe_route", "moe_expert_choice", "moe_update_sel_bias", "moe_permute",
-            "moe_expert_ffn", "moe_combine", "moe_forward",
+            "moe_expert_ffn", "moe_combine", "moe_forward", "moe_forward_host",
             "moe_permute_static", "moe_workspace_status", "moe_debug_suppress_gemm_producer",
             "moe_status_string", "moe_version"]
 MOE_STATIC_MAX_ASSIGNMENTS = 65536
@@ -83,6 +83,9 @@ def load() -> C.CDLL:
     lib.moe_forward.argtypes = [cfgp, C.POINTER(MoeWeights), P, P, C.POINTER(MoeOutputs), P,
                                 C.c_size_t, P, P]
     lib.moe_forward.restype = C.c_int
+    lib.moe_forward_host.argtypes = [cfgp, C.POINTER(MoeWeights), P, P, P, P,
+                                     C.POINTER(MoeOutputs), P, C.c_size_t, P, P, P]
+    lib.moe_forward_host.restype = C.c_int
     lib.moe_permute_static.argtypes = [cfgp, P, P, P, P, P, P, P, P, P]
     lib.moe_permute_static.restype = C.c_int
     lib.moe_workspace_status.argtypes = [P, P]

@@ -17,6 +17,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16* _
                                                           const int32_t* __restrict__ offsets,
                                                           int N, int k, int64_t max_rows, int H,
                                                           __nv_bfloat16* __restrict__ xp) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int64_t R = offsets[N];
   const int lane = threadIdx.x % 32;
   const int64_t nvec = H / 8;
@@ -35,6 +37,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __res
                                                       const __nv_bfloat16* __restrict__ ys,
                                                       __nv_bfloat16* __restrict__ out, int T,
                                                       int k, int H) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int nvec = H / 8;
   const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (gid >= (int64_t)T * nvec) return;
@@ -68,8 +72,8 @@ cudaError_t launch_gather(const __nv_bfloat16* x, const int32_t* perm, const int
   if (blocks > 148 * 16) blocks = 148 * 16;
   if (blocks < 1) blocks = 1;
   trace_mark(tr, st);
-  gather_rows_kernel<<<(unsigned)blocks, 256, 0, st>>>(x, perm, offsets, N, k, max_rows, H, xp);
-  return cudaGetLastError();
+  return launch_pdl(gather_rows_kernel, dim3((unsigned)blocks), dim3(256), 0, st, 1, x, perm,
+                    offsets, N, k, max_rows, H, xp);
 }
 
 cudaError_t launch_combine(const __nv_bfloat16* y, const int32_t* inv,
@@ -78,8 +82,8 @@ cudaError_t launch_combine(const __nv_bfloat16* y, const int32_t* inv,
   const int64_t n = (int64_t)T * (H / 8);
   if (n == 0) return cudaSuccess;
   trace_mark(tr, st);
-  combine_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(y, inv, y_shared, out, T, k, H);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, 1, y, inv,
+                    y_shared, out, T, k, H);
 }
 
 }  // namespace moe

@@ -76,6 +76,18 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch: every kernel of the library lets the next
+// kernel in the stream be scheduled right away, and waits for the previous
+// one to complete (with its writes visible) before touching global memory.
+// Only CTA-local set-up (shared memory, barriers, TMEM) precedes the wait.
+
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
 // cross-CTA signalling inside one grid (release / acquire at GPU scope)
 
 __device__ __forceinline__ int ld_acquire_gpu(const int* p) {

@@ -69,6 +69,8 @@ __global__ void __launch_bounds__(EC_THREADS) expert_choice_kernel(
   __shared__ int s_remaining;
   const int e = blockIdx.x;
   const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
+  pdl_launch_dependents();
+  pdl_wait();
 
   if (tid == 0) {
     counts[e] = C;
@@ -183,9 +185,8 @@ cudaError_t launch_expert_choice(const float* logits, const float* p_mean, int T
     attr_set = true;
   }
   trace_mark(tr, st);
-  expert_choice_kernel<<<N, EC_THREADS, smem, st>>>(logits, p_mean, T, N, C, alpha, counts,
-                                                    offsets, perm, inv, f, l_aux);
-  return cudaGetLastError();
+  return launch_pdl(expert_choice_kernel, dim3(N), dim3(EC_THREADS), smem, st, 1, logits, p_mean,
+                    T, N, C, alpha, counts, offsets, perm, inv, f, l_aux);
 }
 
 // ---------------------------------------------------------------------------
@@ -196,6 +197,8 @@ __global__ void __launch_bounds__(1024) update_sel_bias_kernel(const int32_t* __
                                                                float* __restrict__ sel_bias, int N,
                                                                float gamma) {
   __shared__ long long part[32];
+  pdl_launch_dependents();
+  pdl_wait();
   long long s = 0;
   for (int e = threadIdx.x; e < N; e += blockDim.x) s += counts[e];
 #pragma unroll
@@ -213,8 +216,8 @@ __global__ void __launch_bounds__(1024) update_sel_bias_kernel(const int32_t* __
 
 cudaError_t launch_update_sel_bias(const int32_t* counts, float* sel_bias, int N, float gamma,
                                    cudaStream_t st) {
-  update_sel_bias_kernel<<<1, 1024, 0, st>>>(counts, sel_bias, N, gamma);
-  return cudaGetLastError();
+  return launch_pdl(update_sel_bias_kernel, dim3(1), dim3(1024), 0, st, 1, counts, sel_bias, N,
+                    gamma);
 }
 
 }  // namespace moe

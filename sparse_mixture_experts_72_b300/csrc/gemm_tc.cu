@@ -177,9 +177,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   const int rows_done_target = nt0 * EPI_WARPS * PAIR;
   int* status = args.status;
 
-  // ---- set-up: group table, barriers, TMEM
-  for (int i = threadIdx.x; i <= G; i += GEMM_THREADS)
-    seg[i] = args.offsets ? args.offsets[i] : (i == 0 ? 0 : args.rows_single);
+  // ---- set-up: barriers, TMEM (CTA-local, may overlap the previous kernel),
+  // then the group table
+  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
@@ -210,6 +210,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       tmem_relinquish();
     }
   }
+  pdl_wait();  // offsets, the A rows and the row-block counters come from earlier launches
+  for (int i = threadIdx.x; i <= G; i += GEMM_THREADS)
+    seg[i] = args.offsets ? args.offsets[i] : (i == 0 ? 0 : args.rows_single);
   __syncthreads();  // seg[] visible
   if (warp == 2) {
     // mt_pre = exclusive prefix over groups of their row blocks
@@ -655,13 +658,15 @@ static cudaError_t launch_gemm_t(const GemmPlan& plan, cudaStream_t st) {
   cfg.blockDim = dim3(GEMM_THREADS);
   cfg.dynamicSmemBytes = S::SMEM_BYTES;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = PAIR;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_wait()
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   // A persistent grid must be co-resident: phase-1 tiles wait for phase-0
   // tiles owned by other CTAs.  No more CTAs (pairs) than fit at once.
   static int max_units = -1;

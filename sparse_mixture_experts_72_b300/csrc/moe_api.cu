@@ -6,6 +6,7 @@
 #include <cstring>
 
 #include <atomic>
+#include <mutex>
 
 #include "common.cuh"
 #include "kernels.cuh"
@@ -272,6 +273,23 @@ moe_status_t do_permute(const moe_config_t& c, const int32_t* idx, const float* 
     a.H = c.H;
   }
   return cuda_status(launch_permute(a, st, tr));
+}
+
+// Two events per device for moe_forward_host's stream hand-overs.  A wait
+// takes the state of the event's latest record at the time it is enqueued,
+// so one pair serves every call.
+moe_status_t host_events(cudaEvent_t* in, cudaEvent_t* out) {
+  static std::mutex mu;
+  static cudaEvent_t evs[64][2] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_NO_DEVICE;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < 2; ++i)
+    if (!evs[dev][i] && cudaEventCreateWithFlags(&evs[dev][i], cudaEventDisableTiming) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  *in = evs[dev][0];
+  *out = evs[dev][1];
+  return MOE_OK;
 }
 
 // Failure-injection count (moe_debug_suppress_gemm_producer): each GEMM
@@ -597,6 +615,40 @@ MOE_API moe_status_t moe_forward(const moe_config_t* cfg, const moe_weights_t* w
                             reinterpret_cast<bf*>(out), c.T, slots_of(c), c.H, st, tr));
   }
   trace_mark(tr, st);
+  return MOE_OK;
+}
+
+MOE_API moe_status_t moe_forward_host(const moe_config_t* cfg, const moe_weights_t* weights,
+                                      const uint16_t* x_host, uint16_t* x_dev, uint16_t* out_dev,
+                                      uint16_t* out_host, const moe_outputs_t* outputs, void* ws,
+                                      size_t ws_bytes, void* h2d_stream, void* compute_stream,
+                                      void* d2h_stream) {
+  MOE_TRY(check_config(cfg));
+  const moe_config_t& c = *cfg;
+  if (c.T > 0 && (!x_host || !out_host)) return MOE_ERR_INVALID_ARG;
+  // validate everything the forward checks before the first copy is enqueued
+  MOE_TRY(check_weights(c, weights, true, true));
+  if (c.T > 0) MOE_TRY(check_ptrs(true, x_dev, out_dev));
+  MOE_TRY(check_ws(c, ws, ws_bytes));
+  DeviceInfo d;
+  MOE_TRY(device_info(&d));
+  cudaStream_t is = static_cast<cudaStream_t>(h2d_stream);
+  cudaStream_t ks = static_cast<cudaStream_t>(compute_stream);
+  cudaStream_t os = static_cast<cudaStream_t>(d2h_stream);
+  cudaEvent_t ev_in = nullptr, ev_out = nullptr;
+  if (is != ks || os != ks) MOE_TRY(host_events(&ev_in, &ev_out));
+  const size_t bytes = sizeof(uint16_t) * (size_t)c.T * c.H;
+  if (bytes > 0) MOE_CUDA(cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyHostToDevice, is));
+  if (is != ks) {
+    MOE_CUDA(cudaEventRecord(ev_in, is));
+    MOE_CUDA(cudaStreamWaitEvent(ks, ev_in, 0));
+  }
+  MOE_TRY(moe_forward(cfg, weights, x_dev, out_dev, outputs, ws, ws_bytes, ks, nullptr));
+  if (os != ks) {
+    MOE_CUDA(cudaEventRecord(ev_out, ks));
+    MOE_CUDA(cudaStreamWaitEvent(os, ev_out, 0));
+  }
+  if (bytes > 0) MOE_CUDA(cudaMemcpyAsync(out_host, out_dev, bytes, cudaMemcpyDeviceToHost, os));
   return MOE_OK;
 }
 

@@ -38,7 +38,9 @@ __global__ void __launch_bounds__(PR_THREADS) permute_rank_kernel(
     int32_t* __restrict__ blk_hist, int64_t A, int N, int T, int k, int slot_major) {
   extern __shared__ int32_t wcnt[];  // [PR_WARPS][N]
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  pdl_launch_dependents();
   for (int i = tid; i < PR_WARPS * N; i += PR_THREADS) wcnt[i] = 0;
+  pdl_wait();
   __syncthreads();
   const int64_t a = (int64_t)blockIdx.x * PR_THREADS + tid;   // claim position p
   int e = (a < A) ? idx[claim_assignment(a, T, k, slot_major)] : -1;
@@ -71,6 +73,8 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(
   __shared__ int32_t sc[1024];
   __shared__ double red[1024];
   const int e = threadIdx.x;
+  pdl_launch_dependents();
+  pdl_wait();
   int run = 0;
   if (e < N) {
     for (int b = 0; b < nblk; ++b) {
@@ -113,6 +117,8 @@ __global__ void __launch_bounds__(256) permute_scatter_kernel(
     const int32_t* __restrict__ blk_base, const int32_t* __restrict__ offsets,
     int32_t* __restrict__ perm, int32_t* __restrict__ inv, int64_t A, int N, int64_t capacity,
     int T, int k, int slot_major) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int64_t a = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (a >= A) return;
   const int e = idx[a];
@@ -135,6 +141,8 @@ __global__ void __launch_bounds__(256) permute_scatter_gather_kernel(
     int32_t* __restrict__ perm, int32_t* __restrict__ inv, int T, int N, int k,
     int64_t capacity, const __nv_bfloat16* __restrict__ x, __nv_bfloat16* __restrict__ xp, int H,
     int slot_major) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int lane = threadIdx.x % 32;
   const int64_t nvec = H / 8;
   for (int64_t t = (int64_t)blockIdx.x * 8 + threadIdx.x / 32; t < T; t += (int64_t)gridDim.x * 8) {
@@ -174,30 +182,29 @@ cudaError_t launch_permute(const PermuteLaunch& a, cudaStream_t st, LaunchTrace*
   const int nblk = permute_num_blocks(A);
   if (A > 0) {
     trace_mark(tr, st);
-    permute_rank_kernel<<<nblk, PR_THREADS, PR_WARPS * a.N * sizeof(int32_t), st>>>(
-        a.topk_idx, a.local_rank, a.blk_hist, A, a.N, a.T, a.k, a.slot_major);
-    cudaError_t err = cudaGetLastError();
+    cudaError_t err = launch_pdl(permute_rank_kernel, dim3(nblk), dim3(PR_THREADS),
+                                 PR_WARPS * a.N * sizeof(int32_t), st, 1, a.topk_idx, a.local_rank,
+                                 a.blk_hist, A, a.N, a.T, a.k, a.slot_major);
     if (err != cudaSuccess) return err;
   }
   int threads = 32;
   while (threads < a.N) threads <<= 1;
   trace_mark(tr, st);
-  permute_scan_kernel<<<1, threads, 0, st>>>(a.blk_hist, a.blk_base, a.counts, a.offsets,
-                                             a.p_mean, a.f, a.l_aux, nblk, a.N, A, a.capacity,
-                                             a.alpha);
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err = launch_pdl(permute_scan_kernel, dim3(1), dim3(threads), 0, st, 1, a.blk_hist,
+                               a.blk_base, a.counts, a.offsets, a.p_mean, a.f, a.l_aux, nblk, a.N,
+                               A, a.capacity, a.alpha);
   if (err != cudaSuccess || A == 0) return err;
   trace_mark(tr, st);
   if (a.x != nullptr) {
     int64_t blocks = ((int64_t)a.T + 7) / 8;
     if (blocks > 148 * 16) blocks = 148 * 16;
-    permute_scatter_gather_kernel<<<(unsigned)blocks, 256, 0, st>>>(
-        a.topk_idx, a.local_rank, a.blk_base, a.offsets, a.perm, a.inv, a.T, a.N, a.k,
-        a.capacity, a.x, a.xp, a.H, a.slot_major);
+    return launch_pdl(permute_scatter_gather_kernel, dim3((unsigned)blocks), dim3(256), 0, st, 1,
+                      a.topk_idx, a.local_rank, a.blk_base, a.offsets, a.perm, a.inv, a.T, a.N,
+                      a.k, a.capacity, a.x, a.xp, a.H, a.slot_major);
   } else {
-    permute_scatter_kernel<<<(unsigned)((A + 255) / 256), 256, 0, st>>>(
-        a.topk_idx, a.local_rank, a.blk_base, a.offsets, a.perm, a.inv, A, a.N, a.capacity, a.T,
-        a.k, a.slot_major);
+    return launch_pdl(permute_scatter_kernel, dim3((unsigned)((A + 255) / 256)), dim3(256), 0, st,
+                      1, a.topk_idx, a.local_rank, a.blk_base, a.offsets, a.perm, a.inv, A, a.N,
+                      a.capacity, a.T, a.k, a.slot_major);
   }
   return cudaGetLastError();
 }

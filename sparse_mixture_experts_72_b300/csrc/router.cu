@@ -26,6 +26,8 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const __nv_bfloat16*
                                                             int H, int N) {
   __shared__ float xs[RL_BK][RL_BT + 4];
   __shared__ float wsm[RL_BK][RL_BE + 4];
+  pdl_launch_dependents();
+  pdl_wait();
   const int tid = threadIdx.x;
   const int t0 = blockIdx.x * RL_BT;
   const int e0 = blockIdx.y * RL_BE;
@@ -99,6 +101,8 @@ __global__ void __launch_bounds__(RS_WARPS * 32) router_select_kernel(
     float* __restrict__ p_part, int T, int N, int k) {
   __shared__ float psum[RS_WARPS][NPL * 32];
   __shared__ float zsum[RS_WARPS];
+  pdl_launch_dependents();
+  pdl_wait();
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   float zacc = 0.0f;  // this warp's sum of logsumexp(l_t)^2 (router z-loss)
   float pacc[NPL];
@@ -191,6 +195,8 @@ __global__ void __launch_bounds__(RS_WARPS * 32) router_select_kernel(
 // sums is the router z-loss numerator.  With nblocks = 0 it zeroes both.
 __global__ void router_pmean_kernel(const float* __restrict__ p_part, float* __restrict__ p_mean,
                                     float* __restrict__ z_loss, int nblocks, int N, int T) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e > N) return;
   float acc = 0.0f;
@@ -201,8 +207,8 @@ __global__ void router_pmean_kernel(const float* __restrict__ p_part, float* __r
 }
 
 cudaError_t launch_router_stats_zero(float* p_mean, float* z_loss, int N, cudaStream_t st) {
-  router_pmean_kernel<<<(N + 1 + 255) / 256, 256, 0, st>>>(nullptr, p_mean, z_loss, 0, N, 0);
-  return cudaGetLastError();
+  return launch_pdl(router_pmean_kernel, dim3((N + 1 + 255) / 256), dim3(256), 0, st, 1,
+                    static_cast<const float*>(nullptr), p_mean, z_loss, 0, N, 0);
 }
 
 // ---------------------------------------------------------------------------
@@ -217,14 +223,15 @@ cudaError_t launch_router(const RouterLaunch& a, cudaStream_t st, LaunchTrace* t
     dim3 grid((T + RL_BT - 1) / RL_BT, (N + RL_BE - 1) / RL_BE);
     trace_mark(tr, st);
     float* lg = a.logits_out ? a.logits_out : a.logits;
-    router_logits_kernel<<<grid, 256, 0, st>>>(a.x, a.Wg, a.bg, lg, T, a.H, N);
-    cudaError_t err = cudaGetLastError();
+    cudaError_t err = launch_pdl(router_logits_kernel, grid, dim3(256), 0, st, 1, a.x, a.Wg, a.bg,
+                                 lg, T, a.H, N);
     if (err != cudaSuccess) return err;
     const int npl = (N + 31) / 32;
     trace_mark(tr, st);
 #define MOE_SEL(NPLV)                                                                      \
-  router_select_kernel<NPLV><<<nsel, RS_WARPS * 32, 0, st>>>(lg, a.sel_bias, a.topk_idx,        \
-                                                             a.topk_w, a.probs, a.p_part, T, N, a.k)
+  err = launch_pdl(router_select_kernel<NPLV>, dim3(nsel), dim3(RS_WARPS * 32), 0, st, 1,        \
+                   static_cast<const float*>(lg), a.sel_bias, a.topk_idx, a.topk_w, a.probs,      \
+                   a.p_part, T, N, a.k)
     if (npl <= 1) MOE_SEL(1);
     else if (npl <= 2) MOE_SEL(2);
     else if (npl <= 4) MOE_SEL(4);
@@ -232,13 +239,11 @@ cudaError_t launch_router(const RouterLaunch& a, cudaStream_t st, LaunchTrace* t
     else if (npl <= 16) MOE_SEL(16);
     else MOE_SEL(32);
 #undef MOE_SEL
-    err = cudaGetLastError();
     if (err != cudaSuccess) return err;
   }
   trace_mark(tr, st);
-  router_pmean_kernel<<<(N + 1 + 255) / 256, 256, 0, st>>>(a.p_part, a.p_mean, a.z_loss, nsel,
-                                                           N, T);
-  return cudaGetLastError();
+  return launch_pdl(router_pmean_kernel, dim3((N + 1 + 255) / 256), dim3(256), 0, st, 1,
+                    static_cast<const float*>(a.p_part), a.p_mean, a.z_loss, nsel, N, T);
 }
 
 int router_num_launches(int T, int N) {

@@ -53,6 +53,8 @@ __global__ void __launch_bounds__(256) router_split_kernel(const float* __restri
                                                            __nv_bfloat16* __restrict__ W3, int N,
                                                            int H, int N_pad, int H_pad,
                                                            int stacked, int* clear, int clear_n) {
+  pdl_launch_dependents();
+  pdl_wait();
   if (clear && blockIdx.x == 0)
     for (int i = threadIdx.x; i < clear_n; i += blockDim.x) clear[i] = 0;
   const int64_t total = (int64_t)N_pad * H_pad;
@@ -126,6 +128,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
   float* zsum = psum + 4 * N_pad;                            // [4]
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  pdl_launch_dependents();
   const int S = args.splits;                                 // cluster size
   const int split = S > 1 ? (int)cluster_ctarank() : 0;      // K split
   const int mt = blockIdx.x / S;                             // token tile
@@ -164,6 +167,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   long long tma_issued = 0;
+  pdl_wait();  // the W_g planes, x and the ticket come from earlier launches
 
   if (warp == 0) {
     if (lane == 0) {
@@ -479,9 +483,8 @@ cudaError_t launch_router_tc(const RouterLaunch& a, __nv_bfloat16* W3, int* tick
     int64_t blocks = (total + 255) / 256;
     if (blocks > 148 * 8) blocks = 148 * 8;
     trace_mark(tr, st);
-    router_split_kernel<<<(unsigned)blocks, 256, 0, st>>>(a.Wg, W3, a.N, a.H, P.N_pad, P.H_pad,
-                                                          P.stacked, clear, clear_n);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(router_split_kernel, dim3((unsigned)blocks), dim3(256), 0, st, 1,
+                               a.Wg, W3, a.N, a.H, P.N_pad, P.H_pad, P.stacked, clear, clear_n);
     if (e != cudaSuccess) return e;
   }
   CUtensorMap tmX, tmW;
@@ -523,13 +526,15 @@ cudaError_t launch_router_tc(const RouterLaunch& a, __nv_bfloat16* W3, int* tick
   cfg.blockDim = dim3(RT_THREADS);
   cfg.dynamicSmemBytes = P.smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = P.splits;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_wait()
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   trace_mark(tr, st);
   // the largest ring needs ~203 KB; the attribute is set once per kernel
 #define MOE_RTC(KM)                                                                            \

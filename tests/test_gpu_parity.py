@@ -212,3 +212,20 @@ def test_trace_events_cover_every_launch(_lib):
     torch.cuda.synchronize()
     times = [ev[i].elapsed_time(ev[i + 1]) for i in range(n)]
     assert all(t >= 0 for t in times)
+
+
+def test_forward_host_buffers_match_device_path(_lib):
+    """moe_forward_host (H2D, layer, D2H in one C call) gives the device
+    path's output bit for bit, on one stream and on three (H2D, layer, D2H)."""
+    m = _lib
+    w, cfg, xb, x, W, router, ref = _case("small_shared")
+    want = m.moe_forward(cfg, W, x).view(torch.int16).cpu()
+    x_pin = x.cpu().pin_memory()
+    for three in (False, True):
+        out_pin = torch.empty((w.T, w.H), dtype=torch.bfloat16).pin_memory()
+        xs, os_ = torch.empty_like(x), torch.empty_like(x)
+        st = [torch.cuda.Stream() if three else None for _ in range(3)]
+        m.moe_forward_host(cfg, W, x_pin, out_pin, xs, os_, h2d_stream=st[0],
+                           compute_stream=st[1], d2h_stream=st[2])
+        torch.cuda.synchronize()
+        assert torch.equal(out_pin.view(torch.int16), want), three
