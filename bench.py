@@ -212,20 +212,30 @@ def blas_threads() -> int:
         return 1
 
 
-def all_host_cores():
-    """Context that lets numpy's BLAS use every host core (the environment
-    may pin it to one thread); yields the thread count in effect."""
-    import contextlib
+def host_cores() -> int:
+    """CPUs this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
 
-    @contextlib.contextmanager
-    def ctx():
-        try:
-            from threadpoolctl import threadpool_limits
-            with threadpool_limits(limits=os.cpu_count() or 1, user_api="blas"):
-                yield blas_threads()
-        except ImportError:
-            yield blas_threads()
-    return ctx()
+
+def oracle_timing_all_cores(w: wl.Workload, steps: int, warmup: int, budget_s: float):
+    """oracle_timing in a child process whose BLAS may use every host core
+    (thread-count variables set before numpy loads: a BLAS started with one
+    thread cannot grow later).  Returns (tokens/s, sample tokens, desc, threads)."""
+    n = host_cores()
+    env = dict(os.environ)
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[v] = str(n)
+    code = ("import json, sys; sys.path.insert(0, %r); import bench, moe_workloads as wl; "
+            "w = wl.get_workload(%r); r = bench.oracle_timing(w, %d, %d, %r); "
+            "print(json.dumps([r[0], r[1], r[2], bench.blas_threads()]))"
+            % (ROOT, w.name, steps, warmup, float(budget_s)))
+    out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                         check=True, cwd=ROOT)
+    tps, S, desc, threads = json.loads(out.stdout.strip().splitlines()[-1])
+    return tps, S, desc, threads
 
 
 def oracle_step(w: wl.Workload, x_bits, router, getter, shared, rows: slice):
@@ -277,8 +287,7 @@ def run_reference(args):
         return 0
     w = wl.get_workload(args.workload)
     budget = 150.0
-    with all_host_cores() as cores:
-        tps, S, desc = oracle_timing(w, args.steps, args.warmup, budget)
+    tps, S, desc, cores = oracle_timing_all_cores(w, args.steps, args.warmup, budget)
     line = {"metric": METRIC, "value": tps, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": S / tps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -461,8 +470,7 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        with all_host_cores() as cores:
-            tps, S, desc = oracle_timing(w, steps=3, warmup=1, budget_s=20.0)
+        tps, S, desc, cores = oracle_timing_all_cores(w, steps=3, warmup=1, budget_s=20.0)
         cpu = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                "sample": desc}
 

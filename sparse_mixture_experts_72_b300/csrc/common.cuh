@@ -100,6 +100,17 @@ __device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
   asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// Shared-memory counter add with acquire-release semantics at CTA scope;
+// returns the previous value.
+__device__ __forceinline__ uint32_t atom_add_acqrel_cta(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;"
+               : "=r"(old)
+               : "r"(smem_u32(p)), "r"(v)
+               : "memory");
+  return old;
+}
+
 // Orders this thread's generic-proxy global accesses with its async-proxy
 // (TMA) ones: used between data written by plain stores and its TMA reads.
 __device__ __forceinline__ void fence_proxy_async_global() {

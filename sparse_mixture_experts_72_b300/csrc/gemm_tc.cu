@@ -16,10 +16,11 @@
 // One launch runs the whole expert FFN as two phases over one persistent
 // grid: phase 0 (Hid = GELU(X W1^T + b1)) and phase 1 (y = w (Hid W2^T +
 // b2)).  The tile list is phase 0's tiles followed by phase 1's; CTAs take
-// tiles round-robin.  Every phase-0 epilogue warp releases a per-row-block
-// counter in global memory after its stores (fence.proxy.async + red.release),
-// and the TMA producer acquires the counter of a phase-1 tile's row block
-// before loading its Hid rows.  The second Linear of an expert therefore
+// tiles round-robin.  When the last of a CTA's epilogue warps has stored a
+// phase-0 tile (a CTA-scope acquire-release count in shared memory), it
+// releases a per-row-block counter in global memory (red.release.gpu), and
+// the TMA producer acquires the counter of a phase-1 tile's row block
+// (ld.acquire.gpu, then fence.proxy.async) before loading its Hid rows.  The second Linear of an expert therefore
 // starts as soon as its rows are ready, with no kernel boundary, and the
 // second Linear's few large tiles fill the gaps of the first's tail instead
 // of forming a partial last wave.
@@ -151,6 +152,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + S::NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  uint32_t* stored_cnt = tmem_holder + 2;  // [2]: epilogue warps done with the tile in acc
   int32_t* seg = reinterpret_cast<int32_t*>(tmem_holder + 4);   // [G+1] row offsets
   int32_t* mt_pre = seg + (MAX_GROUPS + 1);                     // [G+1] row-block prefix
   uint16_t* bias_stage = reinterpret_cast<uint16_t*>(  // [EPI_WARPS][EPI_COLS], 16-B aligned
@@ -172,9 +174,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   const int nt1 = two ? (args.ph[1].n_out + bno1 - 1) / bno1 : 0;
   const int nkb0 = (args.ph[0].K + BK - 1) / BK;
   const int nkb1 = two ? (args.ph[1].K + BK - 1) / BK : 0;
-  // phase-0 epilogue arrivals that complete one row block (every warp of
-  // every CTA of the tile, for every column block)
-  const int rows_done_target = nt0 * EPI_WARPS * PAIR;
+  // releases that complete one row block: one per CTA of the tile for every
+  // column block
+  const int rows_done_target = nt0 * PAIR;
   int* status = args.status;
 
   // ---- set-up: barriers, TMEM (CTA-local, may overlap the previous kernel),
@@ -191,6 +193,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
+    stored_cnt[0] = stored_cnt[1] = 0u;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -498,6 +501,19 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           }
         }
       }
+      if (two && cur.phase == 0) {
+        // Hand the row block's stores to phase 1: the last of this CTA's
+        // epilogue warps to finish the tile (a CTA-scope acquire-release
+        // count) releases them at GPU scope with one red.release.  This
+        // comes before the warp frees the accumulator, so every count of
+        // this tile precedes any count of the next tile on the same buffer.
+        __syncwarp();
+        if (lane == 0 && atom_add_acqrel_cta(&stored_cnt[acc], 1u) == EPI_WARPS - 1) {
+          stored_cnt[acc] = 0u;
+          fence_proxy_async_global();
+          red_release_gpu_add(args.rows_done + rb, 1);
+        }
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -508,13 +524,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           mbar_arrive(tempty_bar(acc));
         }
       }
-      if (two && cur.phase == 0) {
-        // release this warp's stores of the row block to phase 1's TMA reads
-        fence_proxy_async_global();
-        __threadfence();
-        __syncwarp();
-        if (lane == 0) red_release_gpu_add(args.rows_done + rb, 1);
-      }
+
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }
