@@ -173,8 +173,9 @@ def bench_config(w: wl.Workload, world: int) -> dict:
 
 def launch_names(w: wl.Workload, has_rows: bool):
     """Names of the launches moe_forward makes, in order (the status clear is
-    folded into the tensor-core router's first kernel, and the dispatch
-    scatter also gathers the expert rows)."""
+    folded into the tensor-core router's first kernel, the scan into the
+    rank launch's last block, and the dispatch scatter also gathers the
+    expert rows)."""
     names = []
     tc_router = w.N <= 256
     if not (tc_router and w.T > 0):
@@ -188,7 +189,7 @@ def launch_names(w: wl.Workload, has_rows: bool):
         if has_rows:
             names += ["gather_rows"]
     elif w.T * w.k > 0:
-        names += ["permute_rank", "permute_scan", "scatter_gather"]
+        names += ["permute_rank_scan", "scatter_gather"]
     else:
         names += ["permute_scan"]
     if has_rows:

@@ -299,7 +299,7 @@ moe_status_t moe_forward_host(const moe_config_t* cfg, const moe_weights_t* weig
  * an inference engine that owns all device memory and forbids allocation on
  * its execution path, or a service that reserves all memory at start-up.
  * The source pages have no counterpart to this entry point: it computes
- * exactly what moe_permute computes (same kernels, same outputs), but its
+ * exactly what moe_permute computes (same arithmetic, same outputs), but its
  * scratch is one fixed array in device memory that the library holds on
  * every device it is loaded on until the process exits.
  *   Arguments and outputs are those of moe_permute, without ws/ws_bytes.

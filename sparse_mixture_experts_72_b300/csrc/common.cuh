@@ -142,6 +142,14 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// Pulls one tile of a tensor map into L2 (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t c0, int32_t c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1)
+               : "memory");
+}
+
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -378,6 +386,34 @@ __device__ __forceinline__ float erf_as7126(float x) {
 // rounding of the result).
 __device__ __forceinline__ float gelu_erf(float z) {
   return 0.5f * z * (1.0f + erf_as7126(z * 0.70710678118654752440f));
+}
+
+// p_i (and the router z-loss) from per-block partial sums p_part[nblocks][N + 1]
+// (column N: the blocks' sums of logsumexp(l_t)^2), by one block: thread
+// (q, c) sums the blocks q, q + Q, ... of column c in order, then thread c
+// sums the Q partials in order, so the result does not depend on timing.
+// `red` is shared memory of blockDim.x floats.
+__device__ __forceinline__ void reduce_router_partials(const float* __restrict__ p_part,
+                                                       int nblocks, int N, int T,
+                                                       float* __restrict__ p_mean,
+                                                       float* __restrict__ z_loss, float* red) {
+  const int W = N + 1;
+  const int Q = (int)blockDim.x / W > 0 ? (int)blockDim.x / W : 1;
+  const int c = threadIdx.x % W, q = threadIdx.x / W;
+  if (q < Q) {
+    float s = 0.0f;
+    for (int b = q; b < nblocks; b += Q) s += __ldcg(p_part + (size_t)b * W + c);
+    red[q * W + c] = s;
+  }
+  __syncthreads();
+  for (int col = threadIdx.x; col < W; col += blockDim.x) {
+    float s = 0.0f;
+    for (int qq = 0; qq < Q; ++qq) s += red[qq * W + col];
+    const float mean = T > 0 ? s / (float)T : 0.0f;
+    if (col < N) p_mean[col] = mean;
+    else if (z_loss) *z_loss = mean;
+  }
+  __syncthreads();
 }
 
 // SiLU, z * sigmoid(z) = z / (1 + e^-z), with the fast intrinsics: for very

@@ -140,6 +140,7 @@ struct PermuteLaunch {
   int64_t capacity;     // < 0: no limit
   float alpha;
   int slot_major = 0;   // claim order: 0 a = t*k + j; 1 j-major, then t
+  int* ticket = nullptr;  // zeroed int: the rank launch's last block also scans
   // optional fused gather: xp[row] = x[perm[row] / k] for every kept row
   const __nv_bfloat16* x = nullptr;
   __nv_bfloat16* xp = nullptr;
@@ -147,7 +148,7 @@ struct PermuteLaunch {
 };
 constexpr int kPermuteChunk = 256;  // assignments per block
 inline int permute_num_blocks(int64_t A) { return (int)((A + kPermuteChunk - 1) / kPermuteChunk); }
-int permute_num_launches(int T, int k);
+int permute_num_launches(int T, int k, bool fused_scan);
 cudaError_t launch_permute(const PermuteLaunch& a, cudaStream_t st, LaunchTrace* tr);
 
 // ---------------------------------------------------------------- gather / combine

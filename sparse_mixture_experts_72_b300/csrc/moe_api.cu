@@ -71,7 +71,7 @@ WsLayout layout_of(const moe_config_t& c) {
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o += align_up(bytes > 0 ? bytes : 1); return at; };
   // The header every call zeroes first: [0] status word, [1] router ticket,
-  // then the row-block counters of the routed and the shared expert FFN
+  // [2] permute ticket, then the row-block counters of the routed and the shared expert FFN
   // launches (phase 0 -> phase 1 hand-over).
   const int64_t nrd = R > 0 ? gemm_rows_done_len(R, (int)N) : 0;
   const int64_t nrd_s = (c.F_shared > 0 && T > 0) ? gemm_rows_done_len(T, 1) : 0;
@@ -267,6 +267,7 @@ moe_status_t do_permute(const moe_config_t& c, const int32_t* idx, const float* 
   a.capacity = capacity_of(c);
   a.alpha = c.aux_alpha;
   a.slot_major = c.drop_order == MOE_DROP_SLOT_MAJOR ? 1 : 0;
+  a.ticket = at<int>(ws, L.status) + 2;  // zeroed with the status word
   if (gather_x && max_rows_of(c) > 0) {
     a.x = reinterpret_cast<const __nv_bfloat16*>(gather_x);
     a.xp = at<__nv_bfloat16>(ws, L.xp);
@@ -432,7 +433,7 @@ MOE_API int32_t moe_forward_num_launches(const moe_config_t* cfg) {
     n += 1;                                 // expert-choice selection
     n += ffn_num_launches(c, false);        // gather + expert FFN (+ shared)
   } else {
-    n += permute_num_launches(c.T, c.k);    // the scatter also gathers the rows
+    n += permute_num_launches(c.T, c.k, true);  // the scatter also gathers the rows
     n += ffn_num_launches(c, true);
   }
   if (c.T > 0) n += 1;  // combine

@@ -10,12 +10,15 @@
 // (token-major) or p = j*T + t (slot-major: every token's first choice
 // first).  Each is ranked within its expert in increasing p (a stable
 // scatter), so the first C claimants of each expert keep a row.
-// Three launches, all integer work and no atomics on values:
-//   1. rank:    per 256-assignment chunk, rank of each assignment among the
-//               chunk's assignments to the same expert + chunk histogram
-//   2. scan:    chunk bases per expert (in chunk order), counts, capacity,
-//               row offsets, f and L_aux (one block)
-//   3. scatter: row = offsets[e] + base + local rank, or dropped
+// Two launches, all integer work and no atomics on values:
+//   1. rank + scan: per 256-assignment chunk, rank of each assignment among
+//               the chunk's assignments to the same expert + the chunk
+//               histogram; the last block to finish (integer ticket) then
+//               scans: chunk bases per expert (in chunk order), counts,
+//               capacity, row offsets, f and L_aux
+//   2. scatter: row = offsets[e] + base + local rank, or dropped
+// (Without a ticket, e.g. for the workspace-free entry point, the scan is a
+// launch of its own.)
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -32,11 +35,82 @@ __device__ __forceinline__ int64_t claim_assignment(int64_t p, int T, int k, int
   return slot_major ? (p % T) * k + p / T : p;
 }
 
+// The scan over the chunk histograms, by one block of any multiple of 32
+// threads.  Thread e takes experts e, e + blockDim, ... and walks the chunks
+// in order (loads coalesced across the experts, eight in flight), so the
+// bases come out in chunk order.  Then warp 0 turns the kept counts into row
+// offsets and reduces L_aux in a fixed order.  `s_kept` holds N ints of
+// shared memory.
+__device__ void scan_experts_block(const int32_t* __restrict__ blk_hist,
+                                   int32_t* __restrict__ blk_base, int32_t* __restrict__ counts,
+                                   int32_t* __restrict__ offsets,
+                                   const float* __restrict__ p_mean, float* __restrict__ f,
+                                   float* __restrict__ l_aux, int nblk, int N, int64_t A,
+                                   int64_t capacity, float alpha, int32_t* s_kept) {
+  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+  constexpr int U = 8;
+  for (int e = threadIdx.x; e < N; e += blockDim.x) {
+    int run = 0;
+    int b = 0;
+    for (; b + U <= nblk; b += U) {
+      int c[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) c[u] = __ldcg(blk_hist + (size_t)(b + u) * N + e);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        blk_base[(size_t)(b + u) * N + e] = run;
+        run += c[u];
+      }
+    }
+    for (; b < nblk; ++b) {
+      const int c = __ldcg(blk_hist + (size_t)b * N + e);
+      blk_base[(size_t)b * N + e] = run;
+      run += c;
+    }
+    counts[e] = run;
+    s_kept[e] = (int)((capacity >= 0 && run > capacity) ? capacity : run);
+    if (f) f[e] = A > 0 ? (float)((double)run / (double)A) : 0.0f;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // offsets: exclusive scan of kept over the experts, contiguous per lane
+    const int epl = (N + 31) / 32;
+    const int e0 = min(N, lane * epl), e1 = min(N, e0 + epl);
+    int sum = 0;
+    double term = 0.0;
+    for (int e = e0; e < e1; ++e) {
+      sum += s_kept[e];
+      if (l_aux) term += (A > 0 ? (double)counts[e] / (double)A : 0.0) * (double)p_mean[e];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - sum;
+    for (int e = e0; e < e1; ++e) {
+      offsets[e] = run;
+      run += s_kept[e];
+    }
+    if (lane == 31) offsets[N] = incl;
+    // fixed-order reduction of the per-lane L_aux terms
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) term += __shfl_xor_sync(0xffffffffu, term, o);
+    if (lane == 0 && l_aux) *l_aux = (float)((double)alpha * (double)N * term);
+  }
+}
+
 // local_rank and the chunk histograms are indexed by claim position p.
+// With a ticket, the last block to finish also runs the scan.
 __global__ void __launch_bounds__(PR_THREADS) permute_rank_kernel(
     const int32_t* __restrict__ idx, int32_t* __restrict__ local_rank,
-    int32_t* __restrict__ blk_hist, int64_t A, int N, int T, int k, int slot_major) {
-  extern __shared__ int32_t wcnt[];  // [PR_WARPS][N]
+    int32_t* __restrict__ blk_hist, int64_t A, int N, int T, int k, int slot_major,
+    int* __restrict__ ticket, int32_t* __restrict__ blk_base, int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, const float* __restrict__ p_mean, float* __restrict__ f,
+    float* __restrict__ l_aux, int64_t capacity, float alpha) {
+  extern __shared__ int32_t wcnt[];  // [PR_WARPS][N]; later the scan's kept counts
+  __shared__ int s_last;
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   pdl_launch_dependents();
   for (int i = tid; i < PR_WARPS * N; i += PR_THREADS) wcnt[i] = 0;
@@ -62,54 +136,30 @@ __global__ void __launch_bounds__(PR_THREADS) permute_rank_kernel(
   }
   __syncthreads();
   if (a < A) local_rank[a] = (e >= 0) ? wcnt[warp * N + e] + wrank : -1;
+  if (ticket == nullptr) return;
+  // last block: every histogram is written (release by each block's fence
+  // before its ticket, acquire by the last one after)
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(ticket, 1) == (int)gridDim.x - 1 ? 1 : 0;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  scan_experts_block(blk_hist, blk_base, counts, offsets, p_mean, f, l_aux, (int)gridDim.x, N, A,
+                     capacity, alpha, wcnt);
 }
 
-// One block of up to 1024 threads; thread e owns expert e.
+// The scan as a launch of its own (one block of 1024 threads).
 __global__ void __launch_bounds__(1024) permute_scan_kernel(
     const int32_t* __restrict__ blk_hist, int32_t* __restrict__ blk_base,
     int32_t* __restrict__ counts, int32_t* __restrict__ offsets, const float* __restrict__ p_mean,
     float* __restrict__ f, float* __restrict__ l_aux, int nblk, int N, int64_t A,
     int64_t capacity, float alpha) {
-  __shared__ int32_t sc[1024];
-  __shared__ double red[1024];
-  const int e = threadIdx.x;
+  __shared__ int32_t s_kept[MOE_MAX_EXPERTS];
   pdl_launch_dependents();
   pdl_wait();
-  int run = 0;
-  if (e < N) {
-    for (int b = 0; b < nblk; ++b) {
-      const int c = blk_hist[(size_t)b * N + e];
-      blk_base[(size_t)b * N + e] = run;
-      run += c;
-    }
-    counts[e] = run;
-  }
-  const int kept = (e < N) ? (int)((capacity >= 0 && run > capacity) ? capacity : run) : 0;
-  // inclusive Hillis-Steele scan of kept over the experts
-  sc[e] = kept;
-  __syncthreads();
-  for (int o = 1; o < blockDim.x; o <<= 1) {
-    const int v = (e >= o) ? sc[e - o] : 0;
-    __syncthreads();
-    sc[e] += v;
-    __syncthreads();
-  }
-  if (e < N) offsets[e] = sc[e] - kept;
-  if (e == N - 1) offsets[N] = sc[e];
-  // f_i and L_aux (fixed-order tree reduction in double)
-  double term = 0.0;
-  if (e < N) {
-    const double fe = A > 0 ? (double)run / (double)A : 0.0;
-    if (f) f[e] = (float)fe;
-    if (l_aux) term = fe * (double)p_mean[e];
-  }
-  red[e] = term;
-  __syncthreads();
-  for (int s = blockDim.x / 2; s > 0; s >>= 1) {
-    if (e < s) red[e] += red[e + s];
-    __syncthreads();
-  }
-  if (e == 0 && l_aux) *l_aux = (float)((double)alpha * (double)N * red[0]);
+  scan_experts_block(blk_hist, blk_base, counts, offsets, p_mean, f, l_aux, nblk, N, A, capacity,
+                     alpha, s_kept);
 }
 
 __global__ void __launch_bounds__(256) permute_scatter_kernel(
@@ -175,25 +225,32 @@ __global__ void __launch_bounds__(256) permute_scatter_gather_kernel(
   }
 }
 
-int permute_num_launches(int T, int k) { return (int64_t)T * k > 0 ? 3 : 1; }
+int permute_num_launches(int T, int k, bool fused_scan) {
+  if ((int64_t)T * k == 0) return 1;  // the scan alone
+  return fused_scan ? 2 : 3;
+}
 
 cudaError_t launch_permute(const PermuteLaunch& a, cudaStream_t st, LaunchTrace* tr) {
   const int64_t A = (int64_t)a.T * a.k;
   const int nblk = permute_num_blocks(A);
+  const bool fused = a.ticket != nullptr && A > 0;
+  const size_t rank_smem = sizeof(int32_t) * (size_t)PR_WARPS * a.N;
   if (A > 0) {
     trace_mark(tr, st);
-    cudaError_t err = launch_pdl(permute_rank_kernel, dim3(nblk), dim3(PR_THREADS),
-                                 PR_WARPS * a.N * sizeof(int32_t), st, 1, a.topk_idx, a.local_rank,
-                                 a.blk_hist, A, a.N, a.T, a.k, a.slot_major);
+    cudaError_t err = launch_pdl(permute_rank_kernel, dim3(nblk), dim3(PR_THREADS), rank_smem, st,
+                                 1, a.topk_idx, a.local_rank, a.blk_hist, A, a.N, a.T, a.k,
+                                 a.slot_major, fused ? a.ticket : static_cast<int*>(nullptr),
+                                 a.blk_base, a.counts, a.offsets, a.p_mean, a.f, a.l_aux,
+                                 a.capacity, a.alpha);
     if (err != cudaSuccess) return err;
   }
-  int threads = 32;
-  while (threads < a.N) threads <<= 1;
-  trace_mark(tr, st);
-  cudaError_t err = launch_pdl(permute_scan_kernel, dim3(1), dim3(threads), 0, st, 1, a.blk_hist,
-                               a.blk_base, a.counts, a.offsets, a.p_mean, a.f, a.l_aux, nblk, a.N,
-                               A, a.capacity, a.alpha);
-  if (err != cudaSuccess || A == 0) return err;
+  if (!fused) {
+    trace_mark(tr, st);
+    cudaError_t err = launch_pdl(permute_scan_kernel, dim3(1), dim3(1024), 0, st, 1, a.blk_hist,
+                                 a.blk_base, a.counts, a.offsets, a.p_mean, a.f, a.l_aux, nblk,
+                                 a.N, A, a.capacity, a.alpha);
+    if (err != cudaSuccess || A == 0) return err;
+  }
   trace_mark(tr, st);
   if (a.x != nullptr) {
     int64_t blocks = ((int64_t)a.T + 7) / 8;

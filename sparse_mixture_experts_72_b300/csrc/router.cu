@@ -191,23 +191,30 @@ __global__ void __launch_bounds__(RS_WARPS * 32) router_select_kernel(
   }
 }
 
-// p_mean[e] = (sum over blocks, in block order) / T; column N of the block
-// sums is the router z-loss numerator.  With nblocks = 0 it zeroes both.
-__global__ void router_pmean_kernel(const float* __restrict__ p_part, float* __restrict__ p_mean,
-                                    float* __restrict__ z_loss, int nblocks, int N, int T) {
+// p_mean[e] = column sum over the blocks / T; column N of the block sums is
+// the router z-loss numerator.  One block; with nblocks = 0 it zeroes both.
+__global__ void __launch_bounds__(256) router_pmean_kernel(const float* __restrict__ p_part,
+                                                           float* __restrict__ p_mean,
+                                                           float* __restrict__ z_loss, int nblocks,
+                                                           int N, int T) {
+  __shared__ float red[256];
   pdl_launch_dependents();
   pdl_wait();
-  const int e = blockIdx.x * blockDim.x + threadIdx.x;
-  if (e > N) return;
-  float acc = 0.0f;
-  for (int b = 0; b < nblocks; ++b) acc += p_part[(size_t)b * (N + 1) + e];
-  const float mean = T > 0 ? acc / (float)T : 0.0f;
-  if (e < N) p_mean[e] = mean;
-  else if (z_loss) *z_loss = mean;
+  if (N + 1 <= 256) {
+    reduce_router_partials(p_part, nblocks, N, T, p_mean, z_loss, red);
+    return;
+  }
+  for (int e = threadIdx.x; e <= N; e += blockDim.x) {  // many experts: one thread per column
+    float acc = 0.0f;
+    for (int b = 0; b < nblocks; ++b) acc += p_part[(size_t)b * (N + 1) + e];
+    const float mean = T > 0 ? acc / (float)T : 0.0f;
+    if (e < N) p_mean[e] = mean;
+    else if (z_loss) *z_loss = mean;
+  }
 }
 
 cudaError_t launch_router_stats_zero(float* p_mean, float* z_loss, int N, cudaStream_t st) {
-  return launch_pdl(router_pmean_kernel, dim3((N + 1 + 255) / 256), dim3(256), 0, st, 1,
+  return launch_pdl(router_pmean_kernel, dim3(1), dim3(256), 0, st, 1,
                     static_cast<const float*>(nullptr), p_mean, z_loss, 0, N, 0);
 }
 
@@ -242,7 +249,7 @@ cudaError_t launch_router(const RouterLaunch& a, cudaStream_t st, LaunchTrace* t
     if (err != cudaSuccess) return err;
   }
   trace_mark(tr, st);
-  return launch_pdl(router_pmean_kernel, dim3((N + 1 + 255) / 256), dim3(256), 0, st, 1,
+  return launch_pdl(router_pmean_kernel, dim3(1), dim3(256), 0, st, 1,
                     static_cast<const float*>(a.p_part), a.p_mean, a.z_loss, nsel, N, T);
 }
 
