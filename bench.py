@@ -255,10 +255,27 @@ def oracle_timing(w: wl.Workload, steps: int, warmup: int, budget_s: float, seed
     """Times the oracle on bounded token samples; returns (tokens/s, sample tokens, desc)."""
     x_bits = wl.gen_x(w, seed)
     router = wl.gen_router(w, seed)
-    getter = wl.expert_getter_f64(w, seed)
+    if w.weight_dtype == "e4m3":
+        from oracle import moe_oracle as O
+        cache = {}
+
+        def getter(e):
+            if e not in cache:
+                q1, s1, b1, q2, s2, b2 = wl.gen_expert_e4m3(w, seed, e)
+                cache[e] = (O.dequantize_rows(q1, s1),
+                            None if b1 is None else wl.bf16_bits_to_f64(b1),
+                            O.dequantize_rows(q2, s2),
+                            None if b2 is None else wl.bf16_bits_to_f64(b2))
+            return cache[e]
+        sh = wl.gen_shared_e4m3(w, seed)
+        shared = None if sh is None else (
+            O.dequantize_rows(sh[0], sh[1]), None if sh[2] is None else wl.bf16_bits_to_f64(sh[2]),
+            O.dequantize_rows(sh[3], sh[4]), None if sh[5] is None else wl.bf16_bits_to_f64(sh[5]))
+    else:
+        getter = wl.expert_getter_f64(w, seed)
+        shared = wl.shared_f64(w, seed)
     for e in range(w.N):
         getter(e)  # draw and widen the weights before timing
-    shared = wl.shared_f64(w, seed)
     # size the sample so that warmup + steps fit in the budget
     probe = min(w.T, 64)
     t0 = time.perf_counter()

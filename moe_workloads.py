@@ -58,6 +58,7 @@ class Workload:
     activation: str = "gelu"          # "gelu" | "silu" | "swiglu" (W1 holds gate + up rows)
     min_capacity: int = 0
     drop_order: str = "token"         # "token" | "slot"
+    weight_dtype: str = "bf16"        # "bf16" | "e4m3" (FP8 codes + one fp32 scale per row)
 
     @property
     def w1_rows(self) -> int:
@@ -70,7 +71,8 @@ class Workload:
         return dict(T=self.T, H=self.H, F=self.F, N=self.N, k=self.k,
                     capacity_factor=self.capacity_factor, F_shared=self.F_shared,
                     aux_alpha=self.aux_alpha, routing=self.routing, activation=self.activation,
-                    min_capacity=self.min_capacity, drop_order=self.drop_order)
+                    min_capacity=self.min_capacity, drop_order=self.drop_order,
+                    weight_dtype=self.weight_dtype)
 
     def with_tokens(self, T: int, name: Optional[str] = None) -> "Workload":
         return replace(self, T=T, name=name or f"{self.name}_T{T}")
@@ -101,6 +103,12 @@ WORKLOADS: Dict[str, Workload] = {w.name: w for w in [
     Workload("mixtral_swiglu_prefill", T=16384, H=4096, F=14336, N=8, k=2, activation="swiglu"),
     Workload("mixtral_swiglu_decode", T=64, H=4096, F=14336, N=8, k=2, activation="swiglu",
              phase="decode"),
+    # FP8 (E4M3) expert weights with one fp32 scale per output row: half the
+    # weight bytes of the HBM-bound decode step
+    Workload("mixtral_decode_fp8", T=64, H=4096, F=14336, N=8, k=2, phase="decode",
+             weight_dtype="e4m3"),
+    Workload("mixtral_swiglu_decode_fp8", T=64, H=4096, F=14336, N=8, k=2, activation="swiglu",
+             phase="decode", weight_dtype="e4m3"),
 ]}
 
 # Extra small cases for tests (not benchmark lines).
@@ -142,6 +150,11 @@ TEST_WORKLOADS: Dict[str, Workload] = {w.name: w for w in [
              gate_bias="zipf1.1", drop_order="slot"),
     Workload("min_capacity", T=40, H=64, F=64, N=16, k=2, capacity_factor=0.1, min_capacity=4,
              F_shared=64),
+    Workload("small_fp8", T=300, H=256, F=384, N=8, k=2, expert_bias="normal", F_shared=256,
+             weight_dtype="e4m3"),
+    Workload("fp8_pairs", T=4096, H=256, F=384, N=4, k=2, weight_dtype="e4m3"),
+    Workload("swiglu_fp8", T=600, H=192, F=320, N=8, k=2, activation="swiglu", F_shared=144,
+             expert_bias="normal", weight_dtype="e4m3"),
 ]}
 
 
@@ -169,6 +182,30 @@ def bf16_bits_to_f64(b: np.ndarray) -> np.ndarray:
     """Exact widening of bf16 bit patterns to float64."""
     return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(
         np.float32).astype(np.float64)
+
+
+def f32_to_e4m3_bits(a: np.ndarray) -> np.ndarray:
+    """Round float32 values (|a| <= 448) to FP8 E4M3 (1 sign, 4 exponent bits
+    with bias 7, 3 mantissa bits, subnormals below 2^-6) with
+    round-to-nearest-even; returns the uint8 codes.  Input data generation
+    only (the quantised weights are inputs of the layer)."""
+    v = np.asarray(a, dtype=np.float64)
+    sign = (np.signbit(v)).astype(np.uint8) << 7
+    m = np.abs(v)
+    out = np.zeros(v.shape, dtype=np.uint8)
+    # exponent of the binade, clamped to the normal range [-6, 8]
+    e = np.floor(np.log2(np.where(m > 0, m, 1.0))).astype(np.int64)
+    e = np.clip(e, -6, 8)
+    quantum = np.ldexp(1.0, e - 3)             # spacing of codes in this binade (2^-9 below 2^-6)
+    q = np.round(m / quantum) * quantum        # numpy rounds half to even
+    # rounding up can carry into the next binade: recompute its fields
+    e2 = np.floor(np.log2(np.where(q > 0, q, 1.0))).astype(np.int64)
+    normal = q >= 2.0 ** -6
+    exp_field = np.where(normal, e2 + 7, 0)
+    man_field = np.where(normal, np.round(q / np.ldexp(1.0, e2 - 3)) - 8, np.round(q / 2.0 ** -9))
+    code = (exp_field << 3) | man_field.astype(np.int64)
+    out[...] = np.where(q > 0, code, 0).astype(np.uint8)
+    return out | sign
 
 
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
@@ -253,6 +290,39 @@ def gen_expert(w: Workload, seed: int, e: int):
     elif w.expert_bias is not None:
         raise ValueError(w.expert_bias)
     return W1, b1, W2, b2
+
+
+def _quantise_rows(W: np.ndarray):
+    """Per-row FP8: scale = max |row| / 448 (1 for an all-zero row), codes =
+    E4M3(row / scale).  Returns (uint8 codes, float32 scales)."""
+    amax = np.abs(W).max(axis=1)
+    scale = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+    return f32_to_e4m3_bits(W / scale[:, None]), scale
+
+
+def gen_expert_e4m3(w: Workload, seed: int, e: int):
+    """FP8 routed expert e: (W1 codes, s1, b1 bits|None, W2 codes, s2, b2 bits|None); the
+    fp32 draws are those of gen_expert, then quantised per output row."""
+    W1 = _normal(seed, "W1", e, (w.w1_rows, w.H), 1.0 / math.sqrt(w.H))
+    W2 = _normal(seed, "W2", e, (w.H, w.F), 1.0 / math.sqrt(w.F))
+    q1, s1 = _quantise_rows(W1)
+    q2, s2 = _quantise_rows(W2)
+    _, b1, _, b2 = gen_expert(replace(w, weight_dtype="bf16"), seed, e)
+    return q1, s1, b1, q2, s2, b2
+
+
+def gen_shared_e4m3(w: Workload, seed: int = 0):
+    """FP8 shared expert (codes, scales, biases) or None."""
+    if w.F_shared <= 0:
+        return None
+    Fs = w.F_shared
+    Fs1 = 2 * Fs if w.activation == "swiglu" else Fs
+    W1s = _normal(seed, "W1s", 0, (Fs1, w.H), 1.0 / math.sqrt(w.H))
+    W2s = _normal(seed, "W2s", 0, (w.H, Fs), 1.0 / math.sqrt(Fs))
+    q1, s1 = _quantise_rows(W1s)
+    q2, s2 = _quantise_rows(W2s)
+    sh = gen_shared(replace(w, weight_dtype="bf16"), seed)
+    return q1, s1, sh[1], q2, s2, sh[3]
 
 
 def gen_shared(w: Workload, seed: int = 0):

@@ -61,6 +61,10 @@ Widened rows (the pages name them; each reading is a choice):
 * router z-loss ([SKILLS] §4.3): the raw mean of logsumexp(l_t)^2.
 * auxiliary-loss-free bias step ([ARCH] §2.4): b_i += gamma * sign(count_i -
   mean count); the pages give no rate, so gamma is an input.
+* FP8 weights (the inference guide's "FP8 量化"): the pages name FP8 and its
+  gains, not a format; read as E4M3 codes with one fp32 scale per output
+  row of each weight matrix, dequantised exactly before the Linears;
+  activations stay as they are.
 
 Parity pins for every function live in the tests (closed forms, brute force,
 textbook routines, hand-worked fixtures); none is "parity unpinned".
@@ -276,6 +280,28 @@ def expert_choice(l: np.ndarray, C: int) -> dict:
             inv[t * N + e] = e * C + r
     return dict(offsets=offsets, perm=perm, inv=inv, counts=np.full(N, C, np.int64),
                 kept=np.full(N, C, np.int64), ec_margin=margin)
+
+
+# ---------------------------------------------------------------------------
+# FP8 expert weights ([SKILLS] §9.2, "FP8 量化" of the inference guide):
+# E4M3 codes with one fp32 scale per output row
+
+def e4m3_decode(bits: np.ndarray) -> np.ndarray:
+    """Value of FP8 E4M3 codes: sign bit, 4 exponent bits with bias 7, 3
+    mantissa bits; exponent field 0 holds the subnormals m * 2^-9; there is no
+    infinity and the all-ones pattern is NaN."""
+    b = np.asarray(bits, dtype=np.uint8).astype(np.int64)
+    sign = np.where(b & 0x80, -1.0, 1.0)
+    e = (b >> 3) & 0xF
+    m = b & 0x7
+    val = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    val = np.where((e == 0xF) & (m == 0x7), np.nan, val)
+    return sign * val
+
+
+def dequantize_rows(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """W[r, :] = scale[r] * decode(codes[r, :]), exactly in float64."""
+    return e4m3_decode(codes) * np.asarray(scales, np.float64).reshape(-1, 1)
 
 
 # ---------------------------------------------------------------------------

@@ -48,10 +48,37 @@ def upload(w: wl.Workload, seed: int = 0, device="cuda"):
     return d["x_bits"], weights, wl.gen_router(w, seed)
 
 
+def expert_getter(w: wl.Workload, seed=0):
+    """float64 weights of routed expert e for the oracle: the bf16 bits
+    widened, or for FP8 workloads the oracle's own dequantisation of the codes."""
+    if w.weight_dtype != "e4m3":
+        return wl.expert_getter_f64(w, seed)
+    cache = {}
+
+    def get(e):
+        if e not in cache:
+            q1, s1, b1, q2, s2, b2 = wl.gen_expert_e4m3(w, seed, e)
+            cache[e] = (O.dequantize_rows(q1, s1), None if b1 is None else wl.bf16_bits_to_f64(b1),
+                        O.dequantize_rows(q2, s2), None if b2 is None else wl.bf16_bits_to_f64(b2))
+        return cache[e]
+    return get
+
+
+def shared_weights(w: wl.Workload, seed=0):
+    if w.weight_dtype != "e4m3":
+        return wl.shared_f64(w, seed)
+    sh = wl.gen_shared_e4m3(w, seed)
+    if sh is None:
+        return None
+    q1, s1, b1, q2, s2, b2 = sh
+    return (O.dequantize_rows(q1, s1), None if b1 is None else wl.bf16_bits_to_f64(b1),
+            O.dequantize_rows(q2, s2), None if b2 is None else wl.bf16_bits_to_f64(b2))
+
+
 def oracle_forward(w: wl.Workload, x_bits, router, seed=0, tokens=None):
     Wg, bg, sel = router
     return O.forward(wl.bf16_bits_to_f64(x_bits), Wg, bg, sel, w.k, w.capacity_factor,
-                     w.aux_alpha, wl.expert_getter_f64(w, seed), wl.shared_f64(w, seed),
+                     w.aux_alpha, expert_getter(w, seed), shared_weights(w, seed),
                      tokens=tokens, routing=w.routing, activation=w.activation,
                      min_capacity=w.min_capacity, drop_order=w.drop_order)
 

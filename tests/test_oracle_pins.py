@@ -512,6 +512,26 @@ def check_update_sel_bias():
                                [0.0, 0.0, 0.0])
 
 
+def check_e4m3_decode():
+    """E4M3 decode against hand values of the format and against torch's
+    float8_e4m3fn (a library routine), all 256 codes."""
+    hand = {0x00: 0.0, 0x38: 1.0, 0x7E: 448.0, 0x01: 2.0 ** -9, 0x08: 2.0 ** -6,
+            0x3A: 1.25, 0xC0: -2.0, 0x07: 7 * 2.0 ** -9, 0x77: 240.0}
+    for b, v in hand.items():
+        assert O.e4m3_decode(np.array([b]))[0] == v, (hex(b), v)
+    assert np.isnan(O.e4m3_decode(np.array([0x7F, 0xFF]))).all()
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = O.e4m3_decode(codes)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+    # per-row scaling
+    q = np.array([[0x38, 0xC0], [0x7E, 0x00]], dtype=np.uint8)
+    np.testing.assert_array_equal(O.dequantize_rows(q, np.array([0.5, 2.0])),
+                                  [[0.5, -1.0], [896.0, 0.0]])
+
+
 ALL_CHECKS = [
     check_router_worked_example, check_capacity_examples, check_permute_worked_example,
     check_laux_worked_examples, check_gelu_textbook, check_moelayer_worked_example,
@@ -522,7 +542,7 @@ ALL_CHECKS = [
     check_empty_input, check_slot_major_worked_example, check_min_capacity_examples,
     check_slot_major_vs_stable_sort, check_silu_textbook, check_swiglu_structure,
     check_expert_choice_bruteforce, check_expert_choice_invariants,
-    check_expert_choice_full_capacity, check_z_loss, check_update_sel_bias,
+    check_expert_choice_full_capacity, check_z_loss, check_update_sel_bias, check_e4m3_decode,
 ]
 
 
@@ -642,7 +662,15 @@ def _mut_bias_update_sign(b, counts, gamma):
     return O.__dict__["_orig_update_sel_bias"](b, counts, -gamma)
 
 
+def _mut_e4m3_bias8(bits):
+    b = np.asarray(bits, dtype=np.uint8).astype(np.int64)
+    sign = np.where(b & 0x80, -1.0, 1.0)
+    e, m = (b >> 3) & 0xF, b & 0x7
+    return sign * np.where(e == 0, m * 2.0 ** -10, (1.0 + m / 8.0) * np.exp2(e - 8.0))
+
+
 MUTANTS = {
+    "e4m3_exponent_bias_8": ("e4m3_decode", _mut_e4m3_bias8),
     "min_capacity_ignored": ("capacity", _mut_min_capacity_ignored),
     "slot_major_as_token_major": ("claim_order", _mut_slot_order_ignored),
     "silu_as_sigmoid": ("silu", _mut_silu_is_sigmoid),
