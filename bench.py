@@ -145,18 +145,25 @@ def algorithmic_work(w: wl.Workload, counts: np.ndarray, R: int):
 
     Per kept row: 2*H*F FLOPs in each Linear (two, or three for SwiGLU's
     gate, up and down).  Bytes: the weight
-    matrices of every expert that received a row (2*F*H bf16), the token rows
+    matrices of every expert that received a row (F*H weights of 2 bytes
+    (bf16) or 1 byte (E4M3) plus 4 bytes per row scale), the token rows
     read (R*H bf16) and the weighted rows written (R*H bf16); the hidden
     activations between the two Linears are the implementation's own round
     trip and are not counted."""
     hit = int((np.asarray(counts) > 0).sum())
     m = 3 if w.activation == "swiglu" else 2   # weight matrices per expert (gate, up, down)
+    fp8 = w.weight_dtype == "e4m3"
+    wb = 1.0 if fp8 else 2.0                  # bytes per weight
+
+    def mats(F):                               # weight (+ scale) bytes of one expert
+        scales = 4.0 * ((m - 1) * F + w.H) if fp8 else 0.0
+        return wb * m * F * w.H + scales
     out = {"expert_ffn": dict(flops=2.0 * m * R * w.H * w.F,
-                              bytes=2.0 * (m * hit * w.F * w.H + 2 * R * w.H))}
+                              bytes=hit * mats(w.F) + 2.0 * 2 * R * w.H)}
     if w.F_shared:
         Fs = w.F_shared
         out["shared_ffn"] = dict(flops=2.0 * m * w.T * w.H * Fs,
-                                 bytes=2.0 * (m * Fs * w.H + 2 * w.T * w.H))
+                                 bytes=mats(Fs) + 2.0 * 2 * w.T * w.H)
     return out
 
 
@@ -165,6 +172,7 @@ def bench_config(w: wl.Workload, world: int) -> dict:
     return {"workload": w.name, "T": w.T, "H": w.H, "F": w.F, "N": w.N, "k": w.k,
             "capacity_factor": w.capacity_factor, "F_shared": w.F_shared,
             "routing": w.routing, "activation": w.activation,
+            "expert_weights": w.weight_dtype,
             "l2": "flushed between steps (256 MiB write, untimed)",
             "launch": "CUDA graph replay of moe_forward; every 10th step replays a copy with an "
                       "event node before each launch",
@@ -338,9 +346,7 @@ def run_ours(args):
     cfg = m.MoEConfig(**w.config_kwargs())
     # replicas share the weights; each rank draws its own batch
     d = wl.to_device(w, seed=0, device=device, x_seed=None if rank == 0 else 1000 + rank)
-    weights = m.MoEWeights(Wg=d["Wg"], W1=d["W1"], W2=d["W2"], bg=d["bg"], sel_bias=d["sel_bias"],
-                           b1=d["b1"], b2=d["b2"], W1s=d["W1s"], b1s=d["b1s"], W2s=d["W2s"],
-                           b2s=d["b2s"])
+    weights = m.MoEWeights(**{k: d[k] for k in wl.WEIGHT_KEYS})
     x_bits_host, x = d["x_bits"], d["x"]
     ws = m.make_workspace(cfg, device)
     outs = m.alloc_outputs(cfg, device)

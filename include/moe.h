@@ -22,7 +22,8 @@
  *    weights use the nn.Linear [out, in] layout (K contiguous):
  *      W_g [N, H] fp32, W1 [N, F, H], W2 [N, H, F], W1s [Fs, H], W2s [H, Fs].
  *  - Every pointer must be 16-byte aligned; H, F and F_shared must be
- *    multiples of 8.  Violations return MOE_ERR_UNSUPPORTED before any launch.
+ *    multiples of 8 (of 16 with E4M3 weights).  Violations return
+ *    MOE_ERR_UNSUPPORTED before any launch.
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *    default stream).  Arguments are validated on the host before anything
  *    is launched; a non-OK return means nothing was enqueued, except
@@ -75,6 +76,15 @@ typedef enum {
  * token's second choice, ...). */
 #define MOE_DROP_TOKEN_MAJOR 0
 #define MOE_DROP_SLOT_MAJOR 1
+/* storage of the expert weights W1, W2, W1s, W2s: bf16, or FP8 ("AI-Research-
+ * SKILLs MoE 训练实战" §9.2 FP8 quantisation, which names no format: read as
+ * E4M3 codes, 1 sign, 4 exponent bits with bias 7, 3 mantissa bits) with one
+ * fp32 scale per weight row:
+ *   W[r, c] = scale[r] * E4M3(code[r, c])
+ * Activations stay bf16; each weight is widened to bf16 (exactly) on chip and
+ * the products accumulate in fp32, as for bf16 weights. */
+#define MOE_WEIGHTS_BF16 0
+#define MOE_WEIGHTS_E4M3 1
 
 typedef struct {
   int32_t T;                /* tokens (rows of x); 0 is allowed */
@@ -90,21 +100,29 @@ typedef struct {
   int32_t min_capacity;     /* >= 0: C = max(C, min_capacity) when a capacity applies
                                (the DeepSpeed moe block's min_capacity, §5.1) */
   int32_t drop_order;       /* MOE_DROP_* (token choice with a capacity) */
+  int32_t weight_dtype;     /* MOE_WEIGHTS_*; E4M3 needs H, F, F_shared multiples of 16 */
 } moe_config_t;
 
-/* Layer parameters (device pointers). */
+/* Layer parameters (device pointers).  The expert weights W1, W2, W1s, W2s
+ * hold one element per weight of the type weight_dtype names: bf16 bit
+ * patterns (2 bytes) or E4M3 codes (1 byte); with E4M3 each has a row scale
+ * array (fp32, one per row of the [out, in] matrix), required. */
 typedef struct {
   const float* Wg;          /* [N, H] fp32 gate weight, required */
   const float* bg;          /* [N] fp32 gate bias, or NULL (= 0) */
   const float* sel_bias;    /* [N] fp32 selection-only bias b_i, or NULL (= 0) */
-  const uint16_t* W1;       /* [N, F, H] bf16 ([N, 2F, H] for SwiGLU), required */
+  const void* W1;           /* [N, F, H] ([N, 2F, H] for SwiGLU), required */
   const uint16_t* b1;       /* [N, F] ([N, 2F] for SwiGLU) bf16 or NULL */
-  const uint16_t* W2;       /* [N, H, F] bf16, required */
+  const void* W2;           /* [N, H, F], required */
   const uint16_t* b2;       /* [N, H] bf16 or NULL */
-  const uint16_t* W1s;      /* [Fs, H] ([2Fs, H] for SwiGLU) bf16, required iff F_shared > 0 */
+  const void* W1s;          /* [Fs, H] ([2Fs, H] for SwiGLU), required iff F_shared > 0 */
   const uint16_t* b1s;      /* [Fs] ([2Fs] for SwiGLU) bf16 or NULL */
-  const uint16_t* W2s;      /* [H, Fs] bf16, required iff F_shared > 0 */
+  const void* W2s;          /* [H, Fs], required iff F_shared > 0 */
   const uint16_t* b2s;      /* [H] bf16 or NULL */
+  const float* s1;          /* E4M3: [N, F] ([N, 2F] for SwiGLU) row scales of W1 */
+  const float* s2;          /* E4M3: [N, H] row scales of W2 */
+  const float* s1s;         /* E4M3 with F_shared > 0: [Fs] ([2Fs]) row scales of W1s */
+  const float* s2s;         /* E4M3 with F_shared > 0: [H] row scales of W2s */
 } moe_weights_t;
 
 /* Optional device outputs of moe_forward; each may be NULL (kept in ws).
@@ -227,7 +245,9 @@ moe_status_t moe_permute(const moe_config_t* cfg, const int32_t* topk_idx, const
  *   topk_w [T, S] fp32 (the renormalised top-k weights, or the softmax
  *   probs [T, N] for expert choice)
  *   y [moe_max_rows, H] bf16 out; y_shared [T, H] bf16 out (NULL iff F_shared == 0)
- * bf16 x bf16 products accumulate in fp32 on the tensor cores.
+ * bf16 x bf16 products accumulate in fp32 on the tensor cores; E4M3 weights
+ * are widened to bf16 in shared memory and their row scale multiplies the
+ * fp32 sum before the bias.
  * Both Linears run in one persistent launch whose second-Linear tiles wait
  * (bounded) for the first Linear's rows; it sizes its grid to the CTAs that
  * fit on the GPU at once, so two such launches running at the same time on

@@ -408,34 +408,62 @@ def bits_to_torch_bf16(a: np.ndarray, device="cpu"):
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
 
 
+# names of the layer parameters (the fields of the binding's MoEWeights)
+WEIGHT_KEYS = ("Wg", "bg", "sel_bias", "W1", "b1", "W2", "b2", "W1s", "b1s", "W2s", "b2s",
+               "s1", "s2", "s1s", "s2s")
+
+
 def to_device(w: Workload, seed: int = 0, device="cuda", x_seed: Optional[int] = None) -> dict:
     """Draws every input on the host (per-expert blocks in threads) and copies
     it to `device`.  Returns a dict of torch tensors with the layer's names
-    plus ``x_bits`` (the host bf16 bits of x)."""
+    (WEIGHT_KEYS, None where absent) plus ``x`` and ``x_bits`` (the host bf16
+    bits of x).  FP8 workloads hold uint8 E4M3 codes in W1, W2, W1s, W2s and
+    their fp32 row scales in s1, s2, s1s, s2s."""
     import torch
+    fp8 = w.weight_dtype == "e4m3"
     x_bits = gen_x(w, seed if x_seed is None else x_seed)
     Wg, bg, sel = gen_router(w, seed)
-    W1 = torch.empty((w.N, w.w1_rows, w.H), dtype=torch.bfloat16, device=device)
-    W2 = torch.empty((w.N, w.H, w.F), dtype=torch.bfloat16, device=device)
+    wdt = torch.uint8 if fp8 else torch.bfloat16
+    W1 = torch.empty((w.N, w.w1_rows, w.H), dtype=wdt, device=device)
+    W2 = torch.empty((w.N, w.H, w.F), dtype=wdt, device=device)
+    s1 = torch.empty((w.N, w.w1_rows), dtype=torch.float32, device=device) if fp8 else None
+    s2 = torch.empty((w.N, w.H), dtype=torch.float32, device=device) if fp8 else None
     has_b = w.expert_bias is not None
     b1 = torch.empty((w.N, w.w1_rows), dtype=torch.bfloat16, device=device) if has_b else None
     b2 = torch.empty((w.N, w.H), dtype=torch.bfloat16, device=device) if has_b else None
+    f32 = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(device)
+    bf = lambda a: None if a is None else bits_to_torch_bf16(a, device)
+    u8 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.uint8))
     batch = 32
+    gen = (lambda e: gen_expert_e4m3(w, seed, e)) if fp8 else (lambda e: gen_expert(w, seed, e))
     with ThreadPoolExecutor(min(32, max(1, w.N))) as ex:
         for e0 in range(0, w.N, batch):
-            blocks = ex.map(lambda e: gen_expert(w, seed, e), range(e0, min(w.N, e0 + batch)))
-            for j, (a, b, c, d) in enumerate(blocks):
+            blocks = ex.map(gen, range(e0, min(w.N, e0 + batch)))
+            for j, blk in enumerate(blocks):
                 e = e0 + j
-                W1[e].copy_(bits_to_torch_bf16(a))
-                W2[e].copy_(bits_to_torch_bf16(c))
+                if fp8:
+                    q1, sc1, b, q2, sc2, d = blk
+                    W1[e].copy_(u8(q1))
+                    W2[e].copy_(u8(q2))
+                    s1[e].copy_(torch.from_numpy(sc1))
+                    s2[e].copy_(torch.from_numpy(sc2))
+                else:
+                    a, b, c, d = blk
+                    W1[e].copy_(bits_to_torch_bf16(a))
+                    W2[e].copy_(bits_to_torch_bf16(c))
                 if has_b:
                     b1[e].copy_(bits_to_torch_bf16(b))
                     b2[e].copy_(bits_to_torch_bf16(d))
-    f32 = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(device)
-    bf = lambda a: None if a is None else bits_to_torch_bf16(a, device)
     d = dict(x_bits=x_bits, x=bits_to_torch_bf16(x_bits, device), Wg=f32(Wg), bg=f32(bg),
-             sel_bias=f32(sel), W1=W1, b1=b1, W2=W2, b2=b2, W1s=None, b1s=None, W2s=None, b2s=None)
-    sh = gen_shared(w, seed)
-    if sh is not None:
-        d.update(W1s=bf(sh[0]), b1s=bf(sh[1]), W2s=bf(sh[2]), b2s=bf(sh[3]))
+             sel_bias=f32(sel), W1=W1, b1=b1, W2=W2, b2=b2, W1s=None, b1s=None, W2s=None, b2s=None,
+             s1=s1, s2=s2, s1s=None, s2s=None)
+    if fp8:
+        sh = gen_shared_e4m3(w, seed)
+        if sh is not None:
+            d.update(W1s=u8(sh[0]).to(device), s1s=f32(sh[1]), b1s=bf(sh[2]),
+                     W2s=u8(sh[3]).to(device), s2s=f32(sh[4]), b2s=bf(sh[5]))
+    else:
+        sh = gen_shared(w, seed)
+        if sh is not None:
+            d.update(W1s=bf(sh[0]), b1s=bf(sh[1]), W2s=bf(sh[2]), b2s=bf(sh[3]))
     return d

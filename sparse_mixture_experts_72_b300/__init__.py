@@ -48,12 +48,14 @@ class MoEConfig:
     activation: str = "gelu"     # "gelu" | "silu" | "swiglu" (W1 [N, 2F, H])
     min_capacity: int = 0
     drop_order: str = "token"    # "token" | "slot"
+    weight_dtype: str = "bf16"   # expert weights: "bf16" | "e4m3" (codes + fp32 row scales)
 
     def c(self) -> _lib.MoeConfig:
         return _lib.MoeConfig(self.T, self.H, self.F, self.N, self.k,
                               float(self.capacity_factor), self.F_shared, float(self.aux_alpha),
                               _lib.ROUTING[self.routing], _lib.ACTIVATION[self.activation],
-                              int(self.min_capacity), _lib.DROP_ORDER[self.drop_order])
+                              int(self.min_capacity), _lib.DROP_ORDER[self.drop_order],
+                              _lib.WEIGHT_DTYPE[self.weight_dtype])
 
     @property
     def slots(self) -> int:
@@ -67,6 +69,9 @@ class MoEConfig:
 
 @dataclass
 class MoEWeights:
+    """Layer parameters.  The expert matrices W1, W2, W1s, W2s are bf16, or
+    with ``weight_dtype="e4m3"`` E4M3 codes (uint8 or torch.float8_e4m3fn)
+    with one fp32 scale per row in s1, s2, s1s, s2s."""
     Wg: torch.Tensor                     # [N, H] fp32
     W1: torch.Tensor                     # [N, F, H] bf16
     W2: torch.Tensor                     # [N, H, F] bf16
@@ -78,22 +83,34 @@ class MoEWeights:
     b1s: Optional[torch.Tensor] = None   # [Fs] bf16
     W2s: Optional[torch.Tensor] = None   # [H, Fs] bf16
     b2s: Optional[torch.Tensor] = None   # [H] bf16
+    s1: Optional[torch.Tensor] = None    # e4m3: [N, F] ([N, 2F] SwiGLU) fp32 row scales of W1
+    s2: Optional[torch.Tensor] = None    # e4m3: [N, H] fp32 row scales of W2
+    s1s: Optional[torch.Tensor] = None   # e4m3: [Fs] ([2Fs]) fp32 row scales of W1s
+    s2s: Optional[torch.Tensor] = None   # e4m3: [H] fp32 row scales of W2s
 
     def c(self, cfg: MoEConfig) -> _lib.MoeWeights:
         N, H, F, Fs = cfg.N, cfg.H, cfg.F, cfg.F_shared
         g = 2 if cfg.activation == "swiglu" else 1   # SwiGLU: gate and up rows
+        fp8 = cfg.weight_dtype == "e4m3"
+        wt = (torch.uint8, torch.float8_e4m3fn) if fp8 else torch.bfloat16
+        no_scale = not fp8
         return _lib.MoeWeights(
             _p(self.Wg, torch.float32, (N, H), "Wg"),
             _p(self.bg, torch.float32, (N,), "bg", True),
             _p(self.sel_bias, torch.float32, (N,), "sel_bias", True),
-            _p(self.W1, torch.bfloat16, (N, g * F, H), "W1"),
+            _p(self.W1, wt, (N, g * F, H), "W1"),
             _p(self.b1, torch.bfloat16, (N, g * F), "b1", True),
-            _p(self.W2, torch.bfloat16, (N, H, F), "W2"),
+            _p(self.W2, wt, (N, H, F), "W2"),
             _p(self.b2, torch.bfloat16, (N, H), "b2", True),
-            _p(self.W1s, torch.bfloat16, (g * Fs, H), "W1s", Fs == 0),
+            _p(self.W1s, wt, (g * Fs, H), "W1s", Fs == 0),
             _p(self.b1s, torch.bfloat16, (g * Fs,), "b1s", True),
-            _p(self.W2s, torch.bfloat16, (H, Fs), "W2s", Fs == 0),
-            _p(self.b2s, torch.bfloat16, (H,), "b2s", True))
+            _p(self.W2s, wt, (H, Fs), "W2s", Fs == 0),
+            _p(self.b2s, torch.bfloat16, (H,), "b2s", True),
+            _p(None if no_scale else self.s1, torch.float32, (N, g * F), "s1", no_scale),
+            _p(None if no_scale else self.s2, torch.float32, (N, H), "s2", no_scale),
+            _p(None if no_scale else self.s1s, torch.float32, (g * Fs,), "s1s",
+               no_scale or Fs == 0),
+            _p(None if no_scale else self.s2s, torch.float32, (H,), "s2s", no_scale or Fs == 0))
 
 
 def _p(t: Optional[torch.Tensor], dtype, shape, name, optional=False):
@@ -103,8 +120,9 @@ def _p(t: Optional[torch.Tensor], dtype, shape, name, optional=False):
         raise ValueError(f"{name} is required")
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
-    if t.dtype != dtype:
-        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    allowed = dtype if isinstance(dtype, tuple) else (dtype,)
+    if t.dtype not in allowed:
+        raise TypeError(f"{name} must be {' or '.join(map(str, allowed))}, got {t.dtype}")
     if shape is not None and tuple(t.shape) != tuple(shape):
         raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
     if not t.is_contiguous():

@@ -26,18 +26,21 @@ MOE_STATIC_MAX_EXPERTS = 256
 ROUTING = {"token": 0, "expert": 1}
 ACTIVATION = {"gelu": 0, "silu": 1, "swiglu": 2}
 DROP_ORDER = {"token": 0, "slot": 1}
+WEIGHT_DTYPE = {"bf16": 0, "e4m3": 1}
 
 
 class MoeConfig(C.Structure):
     _fields_ = [("T", C.c_int32), ("H", C.c_int32), ("F", C.c_int32), ("N", C.c_int32),
                 ("k", C.c_int32), ("capacity_factor", C.c_float), ("F_shared", C.c_int32),
                 ("aux_alpha", C.c_float), ("routing", C.c_int32), ("activation", C.c_int32),
-                ("min_capacity", C.c_int32), ("drop_order", C.c_int32)]
+                ("min_capacity", C.c_int32), ("drop_order", C.c_int32),
+                ("weight_dtype", C.c_int32)]
 
 
 class MoeWeights(C.Structure):
     _fields_ = [(n, C.c_void_p) for n in
-                ("Wg", "bg", "sel_bias", "W1", "b1", "W2", "b2", "W1s", "b1s", "W2s", "b2s")]
+                ("Wg", "bg", "sel_bias", "W1", "b1", "W2", "b2", "W1s", "b1s", "W2s", "b2s",
+                 "s1", "s2", "s1s", "s2s")]
 
 
 class MoeOutputs(C.Structure):

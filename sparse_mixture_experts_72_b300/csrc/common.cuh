@@ -3,6 +3,7 @@
 #pragma once
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda.h>
 #include <stdint.h>
 
@@ -60,6 +61,34 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // another role of the CTA has already given up (abort flag set) or if the
 // wait itself runs past kWaitLimitCycles; in the latter case it sets the
 // abort flag and records MOE_ERR_TIMEOUT in the status word.
+// Parity wait with cluster-scope acquire: for phases completed by arrivals
+// (release.cluster) from the peer CTA of a pair.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_bounded_cluster(uint32_t bar, uint32_t parity,
+                                                          volatile int* abort_flag, int* status) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait_cluster(bar, parity)) {
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitLimitCycles) {
+      *abort_flag = 1;
+      if (status) atomicExch(status, (int)MOE_ERR_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   volatile int* abort_flag, int* status) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -414,6 +443,25 @@ __device__ __forceinline__ void reduce_router_partials(const float* __restrict__
     else if (z_loss) *z_loss = mean;
   }
   __syncthreads();
+}
+
+// Generic-proxy shared-memory writes made visible to the async proxy (the
+// tensor cores reading an operand tile that threads wrote).
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Two FP8 E4M3 values (low byte first) -> two bf16 (low half first): E4M3
+// -> f16 is exact (cvt.rn.f16x2.e4m3x2), and so are f16 -> f32 -> bf16 for
+// values with 3 mantissa bits.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((unsigned short)(two & 0xffffu)));
+  const float lo = __half2float(__ushort_as_half((unsigned short)(h2 & 0xffffu)));
+  const float hi = __half2float(__ushort_as_half((unsigned short)(h2 >> 16)));
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 // SiLU, z * sigmoid(z) = z / (1 + e^-z), with the fast intrinsics: for very

@@ -55,26 +55,36 @@ namespace moe {
 constexpr int BK = 64, BN = 256;
 constexpr int EPI_WARPS = 16;               // 4 per TMEM lane quarter, 64 columns each
 constexpr int EPI_COLS = BN / (EPI_WARPS / 4);
-constexpr int GEMM_THREADS = 64 + EPI_WARPS * 32;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int MAX_GROUPS = MOE_MAX_EXPERTS;
 constexpr int A_BYTES = 128 * BK * 2;  // 128 rows of A per CTA and stage
 constexpr long long kDrainLimitCycles = 200000000LL;  // ~0.1 s
 
-template <int PAIR>
+template <int PAIR, bool FP8>
 struct GemmShape {
   static constexpr int TILE_M = 128 * PAIR;              // rows per tile (whole pair)
   static constexpr int B_ROWS = BN / PAIR;               // B rows each CTA loads
-  static constexpr int B_BYTES = B_ROWS * BK * 2;
+  static constexpr int B_BYTES = B_ROWS * BK * 2;        // bf16 B tile the MMA reads
+  static constexpr int BQ_BYTES = FP8 ? B_ROWS * BK : 0; // E4M3 B tile as loaded (row-major)
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // per CTA
-  static constexpr int STAGES = PAIR == 2 ? 6 : 4;
-  static constexpr int NUM_BARS = 2 * STAGES + 5;
-  static constexpr int SMEM_TILES = STAGES * STAGE_BYTES;
+  // bytes the full barrier of a stage counts per CTA (the FP8 B tile lands
+  // on its own barrier and reaches the bf16 tile through the converters)
+  static constexpr int TX_BYTES = FP8 ? A_BYTES : STAGE_BYTES;
+  static constexpr int STAGES = FP8 ? (PAIR == 2 ? 5 : 3) : (PAIR == 2 ? 6 : 4);
+  // FP8: warps widening E4M3 to bf16 in shared memory.  A single CTA
+  // converts 256 B rows a stage and its tiles are weight-bound (decode), so
+  // it takes four; a pair's CTA converts 128 rows under a longer MMA step.
+  static constexpr int CONV_WARPS = FP8 ? (PAIR == 2 ? 2 : 4) : 0;
+  static constexpr int THREADS = 64 + EPI_WARPS * 32 + CONV_WARPS * 32;
+  // full, empty, tmem full / empty, drain (+ FP8: B landed, B converted)
+  static constexpr int NUM_BARS = 2 * STAGES + 5 + (FP8 ? 2 * STAGES : 0);
+  static constexpr int SMEM_TILES = STAGES * (STAGE_BYTES + BQ_BYTES);
   // tiles (1024-aligned), barriers, TMEM address / flags, bias staging, then
   // the two group tables of G + 1 ints: sized per launch, the unused
   // shared memory is left to L1 (measured 2-3 % faster than a fixed size)
-  static constexpr int SMEM_FIXED =
-      SMEM_TILES + NUM_BARS * 8 + 16 + 16 + EPI_WARPS * EPI_COLS * 2;  // (+16: alignment)
+  static constexpr int SMEM_FIXED = SMEM_TILES + NUM_BARS * 8 + 16 + 16 +
+                                    EPI_WARPS * EPI_COLS * 2 +              // bias staging
+                                    (FP8 ? EPI_WARPS * EPI_COLS * 4 : 0);   // scale staging
   static constexpr int smem_bytes(int G) { return SMEM_FIXED + 2 * (G + 1) * 4; }
   static_assert(SMEM_FIXED + 2 * (MAX_GROUPS + 1) * 4 <= 232448, "shared memory budget");
 };
@@ -122,6 +132,7 @@ struct PhaseView {
   const float* topk_w;
   const int32_t* perm;
   __nv_bfloat16* out;
+  const float* b_scale;
   __device__ __forceinline__ PhaseView(const GemmArgs& a, int p) {
     n_out = p ? a.ph[1].n_out : a.ph[0].n_out;
     K = p ? a.ph[1].K : a.ph[0].K;
@@ -131,17 +142,19 @@ struct PhaseView {
     topk_w = p ? a.ph[1].topk_w : a.ph[0].topk_w;
     perm = p ? a.ph[1].perm : a.ph[0].perm;
     out = p ? a.ph[1].out : a.ph[0].out;
+    b_scale = p ? a.ph[1].b_scale : a.ph[0].b_scale;
   }
 };
 
-template <int PAIR>
-__global__ void __launch_bounds__(GEMM_THREADS, 1)
+template <int PAIR, bool FP8>
+__global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                         const __grid_constant__ CUtensorMap tmB0,
                         const __grid_constant__ CUtensorMap tmA1,
                         const __grid_constant__ CUtensorMap tmB1, const GemmArgs args) {
-  using S = GemmShape<PAIR>;
+  using S = GemmShape<PAIR, FP8>;
   constexpr int STAGES = S::STAGES;
+  constexpr int GEMM_THREADS = S::THREADS;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (smem_u32(smem_raw) & 1023u) {
     // the 128-byte swizzled tiles need a 1024-byte aligned base; never seen,
@@ -152,6 +165,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   uint8_t* smem = smem_raw;
   const uint32_t sA = smem_u32(smem);
   const uint32_t sB = sA + STAGES * A_BYTES;
+  const uint32_t sBq = sB + STAGES * S::B_BYTES;  // FP8 staging (FP8 only)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::SMEM_TILES);
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -159,12 +173,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
   const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+  auto qfull_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + 5 + s); };       // FP8 B landed
+  auto conv_bar = [&](int s) { return bar0 + 8u * (3 * STAGES + 5 + s); };        // B converted
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + S::NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   uint32_t* stored_cnt = tmem_holder + 2;  // [2]: epilogue warps done with the tile in acc
   uint16_t* bias_stage = reinterpret_cast<uint16_t*>(  // [EPI_WARPS][EPI_COLS], 16-B aligned
       (reinterpret_cast<uintptr_t>(tmem_holder + 4) + 15) & ~static_cast<uintptr_t>(15));
-  int32_t* seg = reinterpret_cast<int32_t*>(bias_stage + EPI_WARPS * EPI_COLS);  // [G+1]
+  float* scale_stage = reinterpret_cast<float*>(bias_stage + EPI_WARPS * EPI_COLS);  // FP8 only
+  int32_t* seg = reinterpret_cast<int32_t*>(
+      reinterpret_cast<uint8_t*>(scale_stage) + (FP8 ? EPI_WARPS * EPI_COLS * 4 : 0));  // [G+1]
   int32_t* mt_pre = seg + (args.num_groups + 1);                          // [G+1]
 
   const int warp = threadIdx.x / 32;
@@ -201,6 +219,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       mbar_init(tempty_bar(a), EPI_WARPS * PAIR);
     }
     mbar_init(drain_bar, 1);
+    if constexpr (FP8) {
+      for (int s2 = 0; s2 < STAGES; ++s2) {
+        mbar_init(qfull_bar(s2), 1);
+        mbar_init(conv_bar(s2), S::CONV_WARPS * PAIR);  // every converter warp of the pair
+      }
+    }
     *abort_flag = 0;
     stored_cnt[0] = stored_cnt[1] = 0u;
     fence_mbar_init();
@@ -305,12 +329,27 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             ok = false;
             break;
           }
+          if constexpr (FP8) {
+            // the E4M3 B rows land on this CTA's own barrier; the converter
+            // warps turn them into the bf16 tile
+            mbar_arrive_expect_tx(qfull_bar(stage), S::BQ_BYTES);
+            const uint32_t dq = sBq + stage * S::BQ_BYTES;
+            if (glu && PAIR == 1) {
+              tma_load_2d(dq, mB, qfull_bar(stage), kb * BK, b_row);
+              tma_load_2d(dq + 128 * BK, mB, qfull_bar(stage), kb * BK, b_row + n_out);
+            } else {
+              tma_load_2d(dq, mB, qfull_bar(stage), kb * BK, b_row);
+            }
+          }
           if constexpr (PAIR == 2) {
             // both CTAs' copies complete on the even CTA's full barrier
             const uint32_t fb = mapa_shared(full_bar(stage), 0);
-            if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * S::STAGE_BYTES);
+            if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * S::TX_BYTES);
             tma_load_2d_pair(sA + stage * A_BYTES, mA, fb, kb * BK, a_row_cta);
-            tma_load_2d_pair(sB + stage * S::B_BYTES, mB, fb, kb * BK, b_row);
+            if constexpr (!FP8) tma_load_2d_pair(sB + stage * S::B_BYTES, mB, fb, kb * BK, b_row);
+          } else if constexpr (FP8) {
+            mbar_arrive_expect_tx(full_bar(stage), S::TX_BYTES);
+            tma_load_2d(sA + stage * A_BYTES, mA, full_bar(stage), kb * BK, a_row_cta);
           } else {
             mbar_arrive_expect_tx(full_bar(stage), S::STAGE_BYTES);
             tma_load_2d(sA + stage * A_BYTES, mA, full_bar(stage), kb * BK, a_row_cta);
@@ -349,6 +388,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             ok = false;
             break;
           }
+          if constexpr (FP8) {
+            // the converted B tiles of both CTAs (the peer's arrivals are
+            // cluster-scope releases)
+            if (!mbar_wait_bounded_cluster(conv_bar(stage), phase, abort_flag, status)) {
+              ok = false;
+              break;
+            }
+          }
           tc_fence_after();
           const uint64_t adesc = sdesc_kmajor_sw128(sA + stage * A_BYTES);
           const uint64_t bdesc = sdesc_kmajor_sw128(sB + stage * S::B_BYTES);
@@ -373,6 +420,51 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       }
     }
     __syncwarp();
+  } else if (FP8 && warp >= 2 + EPI_WARPS) {
+    // ------------------------------------------------------------ E4M3 -> bf16
+    // Each staged B tile [B_ROWS][64] of codes becomes the bf16 tile the MMA
+    // reads, in the 128-byte swizzled K-major layout TMA would have written
+    // (8-row groups of 1024 bytes; 16-byte chunk c of row r at c ^ (r % 8)).
+    const int ct = threadIdx.x - (2 + EPI_WARPS) * 32;
+    uint32_t stage = 0, phase = 0;
+    bool ok = true;
+    TileCursor<S::TILE_M> cur;
+    for (int tile = unit; tile < total && ok; tile += units) {
+      int a_row, rows_left, n, rb;
+      cur.locate(tile, tiles0, nt0, nt1, mt_pre, seg, a_row, rows_left, n, rb);
+      const int nkb = cur.phase ? nkb1 : nkb0;
+      for (int kb = 0; kb < nkb; ++kb) {
+        const bool got = mbar_wait_bounded(qfull_bar(stage), phase, abort_flag, status);
+        if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+        const uint8_t* q = smem + STAGES * (A_BYTES + S::B_BYTES) + stage * S::BQ_BYTES;
+        uint8_t* b = smem + STAGES * A_BYTES + stage * S::B_BYTES;
+#pragma unroll 2
+        for (int i = ct; i < S::B_ROWS * 4; i += S::CONV_WARPS * 32) {
+          // 16 codes of row r (K columns 16*c4 ..) -> bf16 chunks 2*c4, 2*c4 + 1
+          const int r = i >> 2, c4 = i & 3;
+          const uint4 in = *reinterpret_cast<const uint4*>(q + r * BK + c4 * 16);
+          uint8_t* row = b + (r >> 3) * 1024 + (r & 7) * 128;
+          uint4 o0, o1;
+          o0.x = e4m3x2_to_bf16x2(in.x);
+          o0.y = e4m3x2_to_bf16x2(in.x >> 16);
+          o0.z = e4m3x2_to_bf16x2(in.y);
+          o0.w = e4m3x2_to_bf16x2(in.y >> 16);
+          o1.x = e4m3x2_to_bf16x2(in.z);
+          o1.y = e4m3x2_to_bf16x2(in.z >> 16);
+          o1.z = e4m3x2_to_bf16x2(in.w);
+          o1.w = e4m3x2_to_bf16x2(in.w >> 16);
+          *reinterpret_cast<uint4*>(row + (((2 * c4) ^ (r & 7)) << 4)) = o0;
+          *reinterpret_cast<uint4*>(row + (((2 * c4 + 1) ^ (r & 7)) << 4)) = o1;
+        }
+        fence_proxy_async_shared();  // the tensor cores read what the threads wrote
+        __syncwarp();
+        if (lane == 0) {
+          if (PAIR == 2 && !leader) mbar_arrive_cluster(mapa_shared(conv_bar(stage), 0));
+          else mbar_arrive(conv_bar(stage));
+        }
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+    }
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                  // TMEM lane quarter this warp may access
@@ -380,6 +472,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
     const int warp_row0 = (int)rank * 128 + q * 32;  // first tile row of this warp
     uint16_t* my_bias = bias_stage + (warp - 2) * EPI_COLS;
+    float* my_scale = scale_stage + (warp - 2) * EPI_COLS;  // FP8: per output column
     uint32_t acc = 0, acc_phase = 0;
     TileCursor<S::TILE_M> cur;
     for (int tile = unit; tile < total; tile += units) {
@@ -414,6 +507,20 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         *reinterpret_cast<uint32_t*>(my_bias + lane * 2) = b;
         __syncwarp();
       }
+      const bool has_scale = FP8 && P.b_scale != nullptr;
+      if (has_scale) {
+        // the 64 column scales of the slice (SwiGLU: 32 gate, then 32 up)
+        int c2 = col0 + lane * 2;
+        size_t soff = (size_t)cur.g * n_out + c2;
+        if (glu) {
+          c2 = col0 + (lane & 15) * 2;
+          soff = (size_t)cur.g * 2 * n_out + (lane >= 16 ? n_out : 0) + c2;
+        }
+        float2 sc = make_float2(0.0f, 0.0f);
+        if (c2 < n_out) sc = __ldg(reinterpret_cast<const float2*>(P.b_scale + soff));
+        *reinterpret_cast<float2*>(my_scale + lane * 2) = sc;
+        __syncwarp();
+      }
       int ok = 1;
       if (lane == 0) ok = mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, status) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -435,6 +542,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             float g = __uint_as_float(rg[i]), u = __uint_as_float(ru[i]);
+            if (has_scale) {
+              g *= my_scale[h * 16 + i];
+              u *= my_scale[32 + h * 16 + i];
+            }
             if (has_bias) {
               const uint16_t bgate = my_bias[h * 16 + i], bup = my_bias[32 + h * 16 + i];
               g += __uint_as_float((uint32_t)bgate << 16);
@@ -468,6 +579,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           float v[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+          if (has_scale) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] *= my_scale[c * 32 + i];
+          }
           if (has_bias) {
 #pragma unroll
             for (int j8 = 0; j8 < 4; ++j8) {
@@ -547,6 +662,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     // Some role gave up, so copies or MMAs may still be in flight.  Let them
     // land / finish before shared memory and TMEM go away.
     if (warp == 0 && lane == 0) {
+      if constexpr (FP8) {
+        // this CTA's E4M3 copies complete on its own barriers
+        const long long first = tma_issued > STAGES ? tma_issued - STAGES : 0;
+        for (long long j = first; j < tma_issued; ++j)
+          mbar_wait_drain(qfull_bar((int)(j % STAGES)), (uint32_t)((j / STAGES) & 1));
+      }
       if (PAIR == 1 || leader) {
         // the full barriers count every byte issued to this CTA's ring
         const long long first = tma_issued > STAGES ? tma_issued - STAGES : 0;
@@ -618,13 +739,31 @@ bool encode_tensor_map_bf16(CUtensorMap* map, const void* base, int64_t rows, in
   return r == CUDA_SUCCESS;
 }
 
+// E4M3 codes [rows, K] (K bytes per row), unswizzled row-major boxes: the
+// converter warps write the swizzled bf16 tile themselves.
+static bool encode_tensor_map_e4m3(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
+                                   int box_cols, int box_rows) {
+  EncodeTiledFn enc = get_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)K};
+  cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 cudaError_t make_gemm_plan(GemmPlan* plan, const GemmArgs& args, const __nv_bfloat16* A,
-                           int64_t a_rows, const __nv_bfloat16* const B[2],
-                           const int64_t b_rows[2], int num_sms) {
+                           int64_t a_rows, const void* const B[2], const int64_t b_rows[2],
+                           bool fp8, int num_sms) {
   const int np = args.num_phases;
   if (np < 1 || np > 2 || a_rows <= 0) return cudaErrorInvalidValue;
   for (int p = 0; p < np; ++p)
-    if (b_rows[p] <= 0 || args.ph[p].K <= 0 || args.ph[p].n_out <= 0) return cudaErrorInvalidValue;
+    if (b_rows[p] <= 0 || args.ph[p].K <= 0 || args.ph[p].n_out <= 0 ||
+        (fp8 && (args.ph[p].K % 16 != 0 || args.ph[p].b_scale == nullptr)))
+      return cudaErrorInvalidValue;
   if (np == 2 && (args.rows_done == nullptr || args.ph[1].K != args.ph[0].n_out ||
                   args.ph[0].ld_out != args.ph[0].n_out))
     return cudaErrorInvalidValue;
@@ -639,8 +778,11 @@ cudaError_t make_gemm_plan(GemmPlan* plan, const GemmArgs& args, const __nv_bflo
       return cudaErrorInvalidValue;
     // SwiGLU tiles load 128 gate and 128 up rows: two 128-row boxes
     const int box_b = args.ph[p].mode == EPI_SWIGLU ? BN / 2 : BN / pair;
-    if (!encode_tensor_map_bf16(&plan->tmB[p], B[p], b_rows[p], args.ph[p].K, BK, box_b))
-      return cudaErrorInvalidValue;
+    const bool ok = fp8 ? encode_tensor_map_e4m3(&plan->tmB[p], B[p], b_rows[p], args.ph[p].K,
+                                                 BK, box_b)
+                        : encode_tensor_map_bf16(&plan->tmB[p], B[p], b_rows[p], args.ph[p].K,
+                                                 BK, box_b);
+    if (!ok) return cudaErrorInvalidValue;
   }
   if (np == 1) {
     plan->tmA[1] = plan->tmA[0];
@@ -648,6 +790,7 @@ cudaError_t make_gemm_plan(GemmPlan* plan, const GemmArgs& args, const __nv_bflo
   }
   plan->args = args;
   plan->pair = pair;
+  plan->fp8 = fp8;
   const int64_t tile_m = 128 * pair;
   int64_t n_tiles = 0;
   for (int p = 0; p < np; ++p) {
@@ -661,12 +804,12 @@ cudaError_t make_gemm_plan(GemmPlan* plan, const GemmArgs& args, const __nv_bflo
   return cudaSuccess;
 }
 
-template <int PAIR>
+template <int PAIR, bool FP8>
 static cudaError_t launch_gemm_t(const GemmPlan& plan, cudaStream_t st) {
-  using S = GemmShape<PAIR>;
+  using S = GemmShape<PAIR, FP8>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<PAIR>,
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<PAIR, FP8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          S::smem_bytes(MAX_GROUPS));
     if (e != cudaSuccess) return e;
@@ -674,7 +817,7 @@ static cudaError_t launch_gemm_t(const GemmPlan& plan, cudaStream_t st) {
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(plan.grid);
-  cfg.blockDim = dim3(GEMM_THREADS);
+  cfg.blockDim = dim3(S::THREADS);
   cfg.dynamicSmemBytes = S::smem_bytes(plan.args.num_groups);
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
@@ -692,27 +835,31 @@ static cudaError_t launch_gemm_t(const GemmPlan& plan, cudaStream_t st) {
   if (max_units < 0) {
     int n = 0;
     if (PAIR == 2) {
-      if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<PAIR>, &cfg) != cudaSuccess)
+      if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<PAIR, FP8>, &cfg) != cudaSuccess)
         n = 0;
     } else {
       int dev = 0, sms = 0, per_sm = 0;
       if (cudaGetDevice(&dev) == cudaSuccess &&
           cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
-          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, grouped_gemm_kernel<PAIR>,
-                                                        GEMM_THREADS,
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, grouped_gemm_kernel<PAIR, FP8>,
+                                                        S::THREADS,
                                                         S::smem_bytes(MAX_GROUPS)) == cudaSuccess)
         n = sms * per_sm;
     }
     max_units = n > 0 ? n : 1;
   }
   if ((int)cfg.gridDim.x > PAIR * max_units) cfg.gridDim.x = PAIR * max_units;
-  return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<PAIR>, plan.tmA[0], plan.tmB[0],
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<PAIR, FP8>, plan.tmA[0], plan.tmB[0],
                             plan.tmA[1], plan.tmB[1], plan.args);
 }
 
 cudaError_t launch_gemm(const GemmPlan& plan, cudaStream_t st, LaunchTrace* tr) {
   trace_mark(tr, st);
-  cudaError_t e = plan.pair == 2 ? launch_gemm_t<2>(plan, st) : launch_gemm_t<1>(plan, st);
+  cudaError_t e;
+  if (plan.fp8)
+    e = plan.pair == 2 ? launch_gemm_t<2, true>(plan, st) : launch_gemm_t<1, true>(plan, st);
+  else
+    e = plan.pair == 2 ? launch_gemm_t<2, false>(plan, st) : launch_gemm_t<1, false>(plan, st);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -187,6 +187,8 @@ struct GemmPhase {
   const float* topk_w;           // EPI_SCALE: weight per assignment, or nullptr (weight 1)
   const int32_t* perm;           // EPI_SCALE: row -> assignment (with topk_w)
   __nv_bfloat16* out;            // [rows, ld_out]
+  const float* b_scale;          // FP8 B: per B row (output column) scale, same layout as
+                                 // bias but fp32; nullptr for bf16 B
 };
 
 // A launch runs one phase, or two where phase 1 reads phase 0's output rows
@@ -206,10 +208,12 @@ struct GemmArgs {
 
 struct GemmPlan {
   CUtensorMap tmA[2];  // per phase: A [rows, K] bf16, box 64 x 128, 128B swizzle
-  CUtensorMap tmB[2];  // per phase: B [G * n_out, K] bf16, box 64 x (256 / pair)
+  CUtensorMap tmB[2];  // per phase: B [G * n_out, K] bf16, box 64 x (256 / pair), 128B
+                       // swizzle; FP8 B: E4M3 bytes, the same box unswizzled
   GemmArgs args;
   int grid;
   int pair;         // 1: one CTA per 128-row tile; 2: a CTA pair per 256-row tile
+  bool fp8;         // B operands are E4M3 codes with per-row scales (ph[p].b_scale)
 };
 
 // Upper bound of the row blocks (tiles along M) of a launch over a_rows rows
@@ -218,9 +222,11 @@ inline int64_t gemm_rows_done_len(int64_t a_rows, int G) { return (a_rows + 127)
 
 // Encodes the tensor maps (phase 1's A is phase 0's output when num_phases
 // is 2); returns cudaErrorInvalidValue if encoding fails.
+// B[p] points at bf16 weights, or with fp8 set at E4M3 codes (one byte per
+// weight; K a multiple of 16 so that rows start on 16-byte boundaries).
 cudaError_t make_gemm_plan(GemmPlan* plan, const GemmArgs& args, const __nv_bfloat16* A,
-                           int64_t a_rows, const __nv_bfloat16* const B[2],
-                           const int64_t b_rows[2], int num_sms);
+                           int64_t a_rows, const void* const B[2], const int64_t b_rows[2],
+                           bool fp8, int num_sms);
 cudaError_t launch_gemm(const GemmPlan& plan, cudaStream_t st, LaunchTrace* tr);
 bool tensor_map_encoder_available();
 

@@ -122,6 +122,8 @@ moe_status_t check_config(const moe_config_t* c) {
   if (c->drop_order != MOE_DROP_TOKEN_MAJOR && c->drop_order != MOE_DROP_SLOT_MAJOR)
     return MOE_ERR_INVALID_ARG;
   if (c->min_capacity < 0) return MOE_ERR_INVALID_ARG;
+  if (c->weight_dtype != MOE_WEIGHTS_BF16 && c->weight_dtype != MOE_WEIGHTS_E4M3)
+    return MOE_ERR_INVALID_ARG;
   if (c->routing == MOE_ROUTING_EXPERT_CHOICE) {
     if (!(c->capacity_factor > 0.0f)) return MOE_ERR_INVALID_ARG;
     if (c->T > kExpertChoiceMaxTokens) return MOE_ERR_UNSUPPORTED;
@@ -129,6 +131,8 @@ moe_status_t check_config(const moe_config_t* c) {
   }
   if (c->N > MOE_MAX_EXPERTS || c->k > MOE_MAX_TOP_K) return MOE_ERR_UNSUPPORTED;
   if (c->H % 8 || c->F % 8 || c->F_shared % 8) return MOE_ERR_UNSUPPORTED;
+  if (c->weight_dtype == MOE_WEIGHTS_E4M3 && (c->H % 16 || c->F % 16 || c->F_shared % 16))
+    return MOE_ERR_UNSUPPORTED;  // E4M3 rows must start on 16-byte boundaries
   if ((int64_t)c->T * c->k > INT32_MAX / 2) return MOE_ERR_UNSUPPORTED;
   if (std::isnan(c->capacity_factor) || std::isnan(c->aux_alpha)) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
@@ -311,6 +315,7 @@ moe_status_t do_ffn(const moe_config_t& c, const uint16_t* x, const int32_t* per
   using bf = __nv_bfloat16;
   const int64_t R = max_rows_of(c);
   int* status = at<int>(ws, L.status);
+  const bool fp8 = c.weight_dtype == MOE_WEIGHTS_E4M3;
   const int32_t act_mode = c.activation == MOE_ACT_SWIGLU ? EPI_SWIGLU
                            : c.activation == MOE_ACT_SILU ? EPI_SILU
                                                           : EPI_GELU;
@@ -340,13 +345,17 @@ moe_status_t do_ffn(const moe_config_t& c, const uint16_t* x, const int32_t* per
     g.ph[1].perm = perm;
     g.ph[1].out = reinterpret_cast<bf*>(y);
     g.ph[1].ld_out = c.H;
+    if (fp8) {
+      g.ph[0].b_scale = W.s1;
+      g.ph[1].b_scale = W.s2;
+    }
     g.rows_done = at<int32_t>(ws, L.rows_done);
     g.status = status;
     g.skip_producer = take_suppress_producer();
-    const bf* B[2] = {reinterpret_cast<const bf*>(W.W1), reinterpret_cast<const bf*>(W.W2)};
+    const void* B[2] = {W.W1, W.W2};
     const int64_t b_rows[2] = {(int64_t)c.N * w1_rows(c, c.F), (int64_t)c.N * c.H};
     GemmPlan p;
-    MOE_CUDA(make_gemm_plan(&p, g, xp, R, B, b_rows, sms));
+    MOE_CUDA(make_gemm_plan(&p, g, xp, R, B, b_rows, fp8, sms));
     MOE_CUDA(launch_gemm(p, st, tr));
   }
   if (c.F_shared > 0 && c.T > 0) {
@@ -367,13 +376,17 @@ moe_status_t do_ffn(const moe_config_t& c, const uint16_t* x, const int32_t* per
     g.ph[1].bias = reinterpret_cast<const bf*>(W.b2s);
     g.ph[1].out = reinterpret_cast<bf*>(y_shared);
     g.ph[1].ld_out = c.H;
+    if (fp8) {
+      g.ph[0].b_scale = W.s1s;
+      g.ph[1].b_scale = W.s2s;
+    }
     g.rows_done = at<int32_t>(ws, L.rows_done_s);
     g.status = status;
     g.skip_producer = take_suppress_producer();
-    const bf* B[2] = {reinterpret_cast<const bf*>(W.W1s), reinterpret_cast<const bf*>(W.W2s)};
+    const void* B[2] = {W.W1s, W.W2s};
     const int64_t b_rows[2] = {w1_rows(c, c.F_shared), (int64_t)c.H};
     GemmPlan p;
-    MOE_CUDA(make_gemm_plan(&p, g, reinterpret_cast<const bf*>(x), c.T, B, b_rows, sms));
+    MOE_CUDA(make_gemm_plan(&p, g, reinterpret_cast<const bf*>(x), c.T, B, b_rows, fp8, sms));
     MOE_CUDA(launch_gemm(p, st, tr));
   }
   return MOE_OK;
@@ -394,11 +407,14 @@ moe_status_t check_weights(const moe_config_t& c, const moe_weights_t* W, bool n
     MOE_TRY(check_ptrs(false, W->bg, W->sel_bias));
   }
   if (need_experts) {
+    const bool fp8 = c.weight_dtype == MOE_WEIGHTS_E4M3;
     MOE_TRY(check_ptrs(true, W->W1, W->W2));
     MOE_TRY(check_ptrs(false, W->b1, W->b2));
+    MOE_TRY(check_ptrs(fp8, W->s1, W->s2));
     if (c.F_shared > 0) {
       MOE_TRY(check_ptrs(true, W->W1s, W->W2s));
       MOE_TRY(check_ptrs(false, W->b1s, W->b2s));
+      MOE_TRY(check_ptrs(fp8, W->s1s, W->s2s));
     }
   }
   return MOE_OK;

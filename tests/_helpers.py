@@ -42,9 +42,7 @@ def upload(w: wl.Workload, seed: int = 0, device="cuda"):
     """Seeded inputs on the device.  Returns (x_bits_host, weights, router_host)."""
     import sparse_mixture_experts_72_b300 as m
     d = wl.to_device(w, seed, device)
-    weights = m.MoEWeights(Wg=d["Wg"], W1=d["W1"], W2=d["W2"], bg=d["bg"],
-                           sel_bias=d["sel_bias"], b1=d["b1"], b2=d["b2"], W1s=d["W1s"],
-                           b1s=d["b1s"], W2s=d["W2s"], b2s=d["b2s"])
+    weights = m.MoEWeights(**{k: d[k] for k in wl.WEIGHT_KEYS})
     return d["x_bits"], weights, wl.gen_router(w, seed)
 
 

@@ -75,8 +75,14 @@ def test_host_shape_functions(lib):
     c = _cfg(T=64, N=4, capacity_factor=8.0, k=1, routing=1)
     assert lib.moe_max_rows(C.byref(c)) == 4 * 64
     assert lib.moe_workspace_size(C.byref(_cfg(routing=1, capacity_factor=0.0))) == 0
-    for bad in (dict(routing=2), dict(activation=3), dict(drop_order=2), dict(min_capacity=-1)):
+    for bad in (dict(routing=2), dict(activation=3), dict(drop_order=2), dict(min_capacity=-1),
+                dict(weight_dtype=2)):
         assert lib.moe_workspace_size(C.byref(_cfg(**bad))) == 0, bad
+    # E4M3 rows must start on 16-byte boundaries: H, F, F_shared multiples of 16
+    assert lib.moe_workspace_size(C.byref(_cfg(weight_dtype=1))) > 0
+    for bad in (dict(H=40), dict(F=136), dict(F_shared=72)):
+        assert lib.moe_workspace_size(C.byref(_cfg(weight_dtype=1, **bad))) == 0, bad
+        assert lib.moe_workspace_size(C.byref(_cfg(**bad))) > 0, bad
 
 
 def test_launch_count_matches_bench_names(lib):
@@ -98,7 +104,7 @@ FAKE = 0x10000  # 16-byte aligned, never dereferenced: every check fails before 
 def _weights(**kw):
     from sparse_mixture_experts_72_b300._lib import MoeWeights
     d = dict(Wg=FAKE, bg=None, sel_bias=None, W1=FAKE, b1=None, W2=FAKE, b2=None, W1s=None,
-             b1s=None, W2s=None, b2s=None)
+             b1s=None, W2s=None, b2s=None, s1=None, s2=None, s1s=None, s2s=None)
     d.update(kw)
     return MoeWeights(**d)
 
@@ -128,6 +134,16 @@ def test_rejects_bad_arguments_before_any_launch(lib):
     import torch
     if not torch.cuda.is_available():
         assert _forward(lib, ok, _weights()) == 6
+    # E4M3 weights need their row scales (16-byte aligned); bf16 ignores them
+    fp8 = _cfg(weight_dtype=1)
+    assert _forward(lib, fp8, _weights()) == 1
+    assert _forward(lib, fp8, _weights(s1=FAKE)) == 1
+    assert _forward(lib, fp8, _weights(s1=FAKE, s2=FAKE + 4)) == 2
+    assert _forward(lib, _cfg(weight_dtype=1, F_shared=64),
+                    _weights(s1=FAKE, s2=FAKE, W1s=FAKE, W2s=FAKE)) == 1  # shared scales
+    assert _forward(lib, _cfg(weight_dtype=1, H=40), _weights(s1=FAKE, s2=FAKE)) == 2
+    if not torch.cuda.is_available():
+        assert _forward(lib, fp8, _weights(s1=FAKE, s2=FAKE)) == 6
     assert lib.moe_status_string(3) == b"workspace missing, misaligned or too small"
     # widened entry points validate on the host as well
     ec = _cfg(routing=1, capacity_factor=1.0)

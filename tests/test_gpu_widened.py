@@ -1,6 +1,7 @@
 """GPU-vs-oracle parity of the widened rows: SiLU and SwiGLU experts,
-expert-choice routing, slot-major drops, min_capacity, the router z-loss and
-logits outputs, and the auxiliary-loss-free bias step.  Stages are also run
+expert-choice routing, slot-major drops, min_capacity, FP8 (E4M3) expert
+weights, the router z-loss and logits outputs, and the auxiliary-loss-free
+bias step.  Stages are also run
 on the oracle's own upstream results (bit-exact integer dispatch); the whole
 layer is compared element by element on small cases and on sampled tokens at
 the benchmark sizes."""
@@ -16,8 +17,8 @@ pytestmark = pytest.mark.gpu
 
 SMALL = ["small_silu", "small_swiglu", "swiglu_pairs", "small_expert_choice",
          "expert_choice_ragged", "expert_choice_all", "many_experts_choice",
-         "slot_major_capacity", "min_capacity"]
-FULL_EXACT = ["mixtral_swiglu_decode"]
+         "slot_major_capacity", "min_capacity", "small_fp8", "fp8_pairs", "swiglu_fp8"]
+FULL_EXACT = ["mixtral_swiglu_decode", "mixtral_decode_fp8"]
 FULL_SAMPLED = ["moelayer_expert_choice", "mixtral_swiglu_prefill"]
 # logit gap under which the fp32 router and the float64 oracle may order two
 # tokens of one expert's column differently (far above fp32 rounding of the
