@@ -155,6 +155,12 @@ TEST_WORKLOADS: Dict[str, Workload] = {w.name: w for w in [
     Workload("fp8_pairs", T=4096, H=256, F=384, N=4, k=2, weight_dtype="e4m3"),
     Workload("swiglu_fp8", T=600, H=192, F=320, N=8, k=2, activation="swiglu", F_shared=144,
              expert_bias="normal", weight_dtype="e4m3"),
+    # decode-sized FP8 batches: A copies of 48 rows (T = 40) and of 16 rows
+    # (capacity 6), several per A-ring slot of 128 rows
+    Workload("fp8_decode_small", T=40, H=256, F=384, N=8, k=2, F_shared=128,
+             expert_bias="normal", gate_bias="normal", weight_dtype="e4m3"),
+    Workload("fp8_capacity_small", T=100, H=192, F=320, N=8, k=2, capacity_factor=0.5,
+             activation="swiglu", gate_bias="zipf1.1", weight_dtype="e4m3"),
 ]}
 
 

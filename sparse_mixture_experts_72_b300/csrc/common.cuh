@@ -3,7 +3,6 @@
 #pragma once
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
-#include <cuda_fp16.h>
 #include <cuda.h>
 #include <stdint.h>
 
@@ -451,17 +450,26 @@ __device__ __forceinline__ void fence_proxy_async_shared() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Two FP8 E4M3 values (low byte first) -> two bf16 (low half first): E4M3
-// -> f16 is exact (cvt.rn.f16x2.e4m3x2), and so are f16 -> f32 -> bf16 for
-// values with 3 mantissa bits.
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two) {
-  uint32_t h2;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((unsigned short)(two & 0xffffu)));
-  const float lo = __half2float(__ushort_as_half((unsigned short)(h2 & 0xffffu)));
-  const float hi = __half2float(__ushort_as_half((unsigned short)(h2 >> 16)));
-  uint32_t r;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
+// Four FP8 E4M3 codes (low byte first) -> four bf16, exactly, with byte
+// permutes, masks and one bf16 multiply (no conversion instructions):
+// the code's 7 magnitude bits placed at bf16 bits [10:4] (exponent field
+// low 4 bits, then the 3 mantissa bits) and its sign at bit 15 form a bf16
+// whose value is the E4M3 value times 2^-120.  This holds for normal codes
+// (bias 127 against 7) and for subnormal ones (both subnormal ranges scale
+// the same mantissa bits), so multiplying by 2^120 restores the value; bf16
+// arithmetic keeps subnormal inputs.  NaN codes (0x7F, 0xFF) are not
+// weights: they decode as +-480.
+//   lo = bf16 of bytes 0 and 1 (byte 0 in the low half), hi = bytes 2 and 3
+__device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  uint32_t x0, x1;
+  // each byte to the top of a 16-bit half: [b1 0 b0 0], [b3 0 b2 0]
+  asm("prmt.b32 %0, %1, 0, 0x1404;" : "=r"(x0) : "r"(w));
+  asm("prmt.b32 %0, %1, 0, 0x3424;" : "=r"(x1) : "r"(w));
+  x0 = ((x0 & 0x7F007F00u) >> 4) | (x0 & 0x80008000u);
+  x1 = ((x1 & 0x7F007F00u) >> 4) | (x1 & 0x80008000u);
+  const uint32_t two120 = 0x7B807B80u;  // bf16 2^120 in both halves
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(lo) : "r"(x0), "r"(two120));
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(hi) : "r"(x1), "r"(two120));
 }
 
 // SiLU, z * sigmoid(z) = z / (1 + e^-z), with the fast intrinsics: for very

@@ -53,32 +53,50 @@
 namespace moe {
 
 constexpr int BK = 64, BN = 256;
-constexpr int EPI_WARPS = 16;               // 4 per TMEM lane quarter, 64 columns each
-constexpr int EPI_COLS = BN / (EPI_WARPS / 4);
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int MAX_GROUPS = MOE_MAX_EXPERTS;
 constexpr int A_BYTES = 128 * BK * 2;  // 128 rows of A per CTA and stage
 constexpr long long kDrainLimitCycles = 200000000LL;  // ~0.1 s
 
+// Shared-memory rings of one CTA.  bf16 weights: one ring of STAGES k-blocks
+// holding A and B, filled by the TMA producer and freed by the MMA.  FP8
+// weights: three rings, so that the weight bytes in flight do not wait for
+// the MMA:
+//   A ring   STAGES   x A tile                producer TMA -> MMA
+//   Q ring   Q_STAGES x E4M3 B tile, 2 k-blocks  the converter warps' own TMA -> converters
+//   B ring   B_STAGES x bf16 B tile           converters -> MMA
+// A Q slot holds 128 bytes of each weight row (two k-blocks): the copies
+// read whole 128-byte row segments, as the bf16 tiles do.  The Q ring runs
+// up to 2 * Q_STAGES + B_STAGES k-blocks ahead of the MMA, and phase-1
+// weights stream in while the producer still waits for phase-0 rows.
 template <int PAIR, bool FP8>
 struct GemmShape {
   static constexpr int TILE_M = 128 * PAIR;              // rows per tile (whole pair)
   static constexpr int B_ROWS = BN / PAIR;               // B rows each CTA loads
   static constexpr int B_BYTES = B_ROWS * BK * 2;        // bf16 B tile the MMA reads
-  static constexpr int BQ_BYTES = FP8 ? B_ROWS * BK : 0; // E4M3 B tile as loaded (row-major)
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // per CTA
-  // bytes the full barrier of a stage counts per CTA (the FP8 B tile lands
-  // on its own barrier and reaches the bf16 tile through the converters)
-  static constexpr int TX_BYTES = FP8 ? A_BYTES : STAGE_BYTES;
-  static constexpr int STAGES = FP8 ? (PAIR == 2 ? 5 : 3) : (PAIR == 2 ? 6 : 4);
-  // FP8: warps widening E4M3 to bf16 in shared memory.  A single CTA
-  // converts 256 B rows a stage and its tiles are weight-bound (decode), so
-  // it takes four; a pair's CTA converts 128 rows under a longer MMA step.
-  static constexpr int CONV_WARPS = FP8 ? (PAIR == 2 ? 2 : 4) : 0;
+  static constexpr int BKQ = 2 * BK;                     // K columns (bytes) of a Q slot
+  static constexpr int BQ_BYTES = FP8 ? B_ROWS * BKQ : 0; // E4M3 B rows as loaded (row-major)
+  // bytes the full barrier of an A-ring slot counts per CTA
+  static constexpr int TX_BYTES = FP8 ? A_BYTES : A_BYTES + B_BYTES;
+  static constexpr int STAGES = FP8 ? (PAIR == 2 ? 6 : 3) : (PAIR == 2 ? 6 : 4);
+  // FP8, single CTA: the A ring's bytes are cut into slots of the launch's A
+  // copy height (GemmArgs::a_box rows), up to A_SLOTS_MAX of them; elsewhere
+  // STAGES slots of 128 rows
+  static constexpr int A_SLOTS_MAX = FP8 && PAIR == 1 ? 12 : STAGES;
+  static constexpr int B_STAGES = FP8 ? (PAIR == 2 ? 4 : 2) : STAGES;
+  static constexpr int Q_STAGES = FP8 ? 3 : 0;
+  // Epilogue warps: 4 per TMEM lane quarter, EPI_COLS columns each.  FP8:
+  // warps widening E4M3 to bf16 in shared memory.  A single CTA converts 256
+  // B rows a k-block and its tiles are weight-bound (decode, few rows): it
+  // gives half of its epilogue warps to the conversion.  A pair's CTA
+  // converts 128 rows under a longer MMA step.
+  static constexpr int EPI_WARPS = FP8 && PAIR == 1 ? 8 : 16;
+  static constexpr int EPI_COLS = BN / (EPI_WARPS / 4);
+  static constexpr int CONV_WARPS = FP8 ? (PAIR == 2 ? 2 : 8) : 0;
   static constexpr int THREADS = 64 + EPI_WARPS * 32 + CONV_WARPS * 32;
-  // full, empty, tmem full / empty, drain (+ FP8: B landed, B converted)
-  static constexpr int NUM_BARS = 2 * STAGES + 5 + (FP8 ? 2 * STAGES : 0);
-  static constexpr int SMEM_TILES = STAGES * (STAGE_BYTES + BQ_BYTES);
+  // full, empty, tmem full / empty, drain (+ FP8: Q full / empty, B full / empty)
+  static constexpr int NUM_BARS = 2 * A_SLOTS_MAX + 5 + (FP8 ? 2 * Q_STAGES + 2 * B_STAGES : 0);
+  static constexpr int SMEM_TILES = STAGES * A_BYTES + B_STAGES * B_BYTES + Q_STAGES * BQ_BYTES;
   // tiles (1024-aligned), barriers, TMEM address / flags, bias staging, then
   // the two group tables of G + 1 ints: sized per launch, the unused
   // shared memory is left to L1 (measured 2-3 % faster than a fixed size)
@@ -164,20 +182,27 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
   }
   uint8_t* smem = smem_raw;
   const uint32_t sA = smem_u32(smem);
-  const uint32_t sB = sA + STAGES * A_BYTES;
-  const uint32_t sBq = sB + STAGES * S::B_BYTES;  // FP8 staging (FP8 only)
+  const uint32_t sB = sA + STAGES * A_BYTES;               // B ring (bf16)
+  const uint32_t sBq = sB + S::B_STAGES * S::B_BYTES;      // Q ring (FP8 only)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::SMEM_TILES);
   const uint32_t bar0 = smem_u32(bars);
+  constexpr int AS = S::A_SLOTS_MAX;
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
-  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
-  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
-  auto qfull_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + 5 + s); };       // FP8 B landed
-  auto conv_bar = [&](int s) { return bar0 + 8u * (3 * STAGES + 5 + s); };        // B converted
+  auto empty_bar = [&](int s) { return bar0 + 8u * (AS + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * AS + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * AS + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * AS + 4);
+  // FP8: E4M3 tile landed / read by every converter warp; bf16 tile written
+  // by every converter warp of the pair / read by the MMA
+  constexpr int QB = 2 * AS + 5, CB = QB + 2 * S::Q_STAGES;
+  auto qfull_bar = [&](int s) { return bar0 + 8u * (QB + s); };
+  auto qempty_bar = [&](int s) { return bar0 + 8u * (QB + S::Q_STAGES + s); };
+  auto cfull_bar = [&](int s) { return bar0 + 8u * (CB + s); };
+  auto cempty_bar = [&](int s) { return bar0 + 8u * (CB + S::B_STAGES + s); };
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + S::NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   uint32_t* stored_cnt = tmem_holder + 2;  // [2]: epilogue warps done with the tile in acc
+  constexpr int EPI_WARPS = S::EPI_WARPS, EPI_COLS = S::EPI_COLS;
   uint16_t* bias_stage = reinterpret_cast<uint16_t*>(  // [EPI_WARPS][EPI_COLS], 16-B aligned
       (reinterpret_cast<uintptr_t>(tmem_holder + 4) + 15) & ~static_cast<uintptr_t>(15));
   float* scale_stage = reinterpret_cast<float*>(bias_stage + EPI_WARPS * EPI_COLS);  // FP8 only
@@ -204,13 +229,19 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
   // releases that complete one row block: one per CTA of the tile for every
   // column block
   const int rows_done_target = nt0 * PAIR;
+  // A copies: a_box rows each (the 128-row MMA also reads the rows after
+  // them, which belong to no row of the tile and are never stored)
+  constexpr bool SMALL_A = FP8 && PAIR == 1;
+  const int a_box = SMALL_A ? args.a_box : 128;
+  const uint32_t a_slot = (uint32_t)a_box * BK * 2;
+  const int a_slots = SMALL_A ? min(AS, (int)(STAGES * A_BYTES / a_slot)) : STAGES;
   int* status = args.status;
 
   // ---- set-up: barriers, TMEM (CTA-local, may overlap the previous kernel),
   // then the group table
   pdl_launch_dependents();
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < AS; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
     }
@@ -220,9 +251,13 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
     }
     mbar_init(drain_bar, 1);
     if constexpr (FP8) {
-      for (int s2 = 0; s2 < STAGES; ++s2) {
+      for (int s2 = 0; s2 < S::Q_STAGES; ++s2) {
         mbar_init(qfull_bar(s2), 1);
-        mbar_init(conv_bar(s2), S::CONV_WARPS * PAIR);  // every converter warp of the pair
+        mbar_init(qempty_bar(s2), S::CONV_WARPS);
+      }
+      for (int s2 = 0; s2 < S::B_STAGES; ++s2) {
+        mbar_init(cfull_bar(s2), S::CONV_WARPS * PAIR);  // every converter warp of the pair
+        mbar_init(cempty_bar(s2), 1);
       }
     }
     *abort_flag = 0;
@@ -281,6 +316,7 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
   const int tiles0 = mt_pre[G] * nt0;
   const int total = tiles0 + (two ? mt_pre[G] * nt1 : 0);
   long long tma_issued = 0;  // producer thread only
+  long long q_issued = 0;    // FP8: the converters' issuing thread only
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -300,6 +336,11 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
         const CUtensorMap* mB = ph ? &tmB1 : &tmB0;
         const int nkb = ph ? nkb1 : nkb0;
         const int n_out = ph ? args.ph[1].n_out : args.ph[0].n_out;
+        if (SMALL_A && min(rows_left, S::TILE_M) > a_box) {
+          // more rows in a group than the launch was planned for: the rows
+          // past a_box are not loaded; report it (the tile is still run)
+          atomicExch(status, (int)MOE_ERR_INVALID_ARG);
+        }
         if (ph == 1) {
           // the A rows of this tile are phase 0's output: wait until every
           // phase-0 tile of the row block has been stored and released
@@ -329,18 +370,6 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
             ok = false;
             break;
           }
-          if constexpr (FP8) {
-            // the E4M3 B rows land on this CTA's own barrier; the converter
-            // warps turn them into the bf16 tile
-            mbar_arrive_expect_tx(qfull_bar(stage), S::BQ_BYTES);
-            const uint32_t dq = sBq + stage * S::BQ_BYTES;
-            if (glu && PAIR == 1) {
-              tma_load_2d(dq, mB, qfull_bar(stage), kb * BK, b_row);
-              tma_load_2d(dq + 128 * BK, mB, qfull_bar(stage), kb * BK, b_row + n_out);
-            } else {
-              tma_load_2d(dq, mB, qfull_bar(stage), kb * BK, b_row);
-            }
-          }
           if constexpr (PAIR == 2) {
             // both CTAs' copies complete on the even CTA's full barrier
             const uint32_t fb = mapa_shared(full_bar(stage), 0);
@@ -348,10 +377,10 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
             tma_load_2d_pair(sA + stage * A_BYTES, mA, fb, kb * BK, a_row_cta);
             if constexpr (!FP8) tma_load_2d_pair(sB + stage * S::B_BYTES, mB, fb, kb * BK, b_row);
           } else if constexpr (FP8) {
-            mbar_arrive_expect_tx(full_bar(stage), S::TX_BYTES);
-            tma_load_2d(sA + stage * A_BYTES, mA, full_bar(stage), kb * BK, a_row_cta);
+            mbar_arrive_expect_tx(full_bar(stage), a_slot);
+            tma_load_2d(sA + stage * a_slot, mA, full_bar(stage), kb * BK, a_row_cta);
           } else {
-            mbar_arrive_expect_tx(full_bar(stage), S::STAGE_BYTES);
+            mbar_arrive_expect_tx(full_bar(stage), S::TX_BYTES);
             tma_load_2d(sA + stage * A_BYTES, mA, full_bar(stage), kb * BK, a_row_cta);
             if (glu) {
               // two 128-row boxes: gate rows, then up rows (128 * BK * 2 bytes further)
@@ -363,7 +392,7 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
             }
           }
           ++issued;
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          if (++stage == a_slots) { stage = 0; phase ^= 1u; }
         }
       }
       tma_issued = issued;
@@ -374,6 +403,7 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
     if (lane == 0 && leader) {
       constexpr uint32_t idesc = idesc_bf16_f32(128 * PAIR, BN);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      uint32_t cstage = 0, cphase = 0;  // FP8: B ring
       bool ok = true;
       for (int tile = unit; tile < total && ok; tile += units) {
         const int nkb = tile < tiles0 ? nkb0 : nkb1;
@@ -391,14 +421,15 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
           if constexpr (FP8) {
             // the converted B tiles of both CTAs (the peer's arrivals are
             // cluster-scope releases)
-            if (!mbar_wait_bounded_cluster(conv_bar(stage), phase, abort_flag, status)) {
+            if (!mbar_wait_bounded_cluster(cfull_bar(cstage), cphase, abort_flag, status)) {
               ok = false;
               break;
             }
           }
           tc_fence_after();
-          const uint64_t adesc = sdesc_kmajor_sw128(sA + stage * A_BYTES);
-          const uint64_t bdesc = sdesc_kmajor_sw128(sB + stage * S::B_BYTES);
+          const uint64_t adesc = sdesc_kmajor_sw128(sA + stage * a_slot);
+          const uint64_t bdesc =
+              sdesc_kmajor_sw128(sB + (FP8 ? cstage : stage) * S::B_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             // +32 bytes along K per step of 16 bf16 inside the 128-byte swizzle atom
@@ -410,7 +441,12 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
           }
           if constexpr (PAIR == 2) umma_commit_pair_mc(empty_bar(stage), 0x3);
           else umma_commit(empty_bar(stage));
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          if (++stage == a_slots) { stage = 0; phase ^= 1u; }
+          if constexpr (FP8) {
+            if constexpr (PAIR == 2) umma_commit_pair_mc(cempty_bar(cstage), 0x3);
+            else umma_commit(cempty_bar(cstage));
+            if (++cstage == S::B_STAGES) { cstage = 0; cphase ^= 1u; }
+          }
         }
         if (!ok) break;
         if constexpr (PAIR == 2) umma_commit_pair_mc(tfull_bar(acc), 0x3);
@@ -422,47 +458,104 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
     __syncwarp();
   } else if (FP8 && warp >= 2 + EPI_WARPS) {
     // ------------------------------------------------------------ E4M3 -> bf16
-    // Each staged B tile [B_ROWS][64] of codes becomes the bf16 tile the MMA
-    // reads, in the 128-byte swizzled K-major layout TMA would have written
-    // (8-row groups of 1024 bytes; 16-byte chunk c of row r at c ^ (r % 8)).
-    const int ct = threadIdx.x - (2 + EPI_WARPS) * 32;
-    uint32_t stage = 0, phase = 0;
-    bool ok = true;
-    TileCursor<S::TILE_M> cur;
-    for (int tile = unit; tile < total && ok; tile += units) {
+    // The converter warps fetch the E4M3 B rows themselves (lane 0 of the
+    // first one issues the copies, Q_STAGES slots of two k-blocks ahead) and
+    // widen each k-block's [B_ROWS][64] codes into the bf16 tile the MMA
+    // reads.  Both tiles are in the 128-byte swizzled layout (8-row groups of
+    // 1024 bytes, 16-byte chunk c of row r at c ^ (r % 8)): the Q rows as the
+    // copies write them (128 codes a row), the bf16 rows as the MMA reads
+    // them (64 values a row).
+    const int cw = warp - (2 + EPI_WARPS);
+    const bool issuer = cw == 0 && lane == 0;
+    // position of the next copy: tile, k-block and its B rows
+    TileCursor<S::TILE_M> lcur;
+    int l_tile = unit, l_kq = 0, l_nkq = 0, l_brow = 0, l_n_out = 0;
+    bool l_glu = false;
+    const CUtensorMap* l_map = &tmB0;
+    auto l_locate = [&]() {
       int a_row, rows_left, n, rb;
-      cur.locate(tile, tiles0, nt0, nt1, mt_pre, seg, a_row, rows_left, n, rb);
-      const int nkb = cur.phase ? nkb1 : nkb0;
+      lcur.locate(l_tile, tiles0, nt0, nt1, mt_pre, seg, a_row, rows_left, n, rb);
+      const int ph = lcur.phase;
+      l_map = ph ? &tmB1 : &tmB0;
+      l_nkq = ((ph ? nkb1 : nkb0) + 1) / 2;  // Q slots of the tile
+      l_n_out = ph ? args.ph[1].n_out : args.ph[0].n_out;
+      l_glu = (ph ? args.ph[1].mode : args.ph[0].mode) == EPI_SWIGLU;
+      // the B rows the producer of a bf16 tile would load (see above)
+      l_brow = l_glu ? lcur.g * 2 * l_n_out + (int)rank * l_n_out + n * (BN / 2)
+                     : lcur.g * l_n_out + n * BN + (int)rank * S::B_ROWS;
+    };
+    auto issue = [&](int slot) {
+      const uint32_t dq = sBq + slot * S::BQ_BYTES;
+      mbar_arrive_expect_tx(qfull_bar(slot), S::BQ_BYTES);
+      if (l_glu && PAIR == 1) {
+        tma_load_2d(dq, l_map, qfull_bar(slot), l_kq * S::BKQ, l_brow);
+        tma_load_2d(dq + 128 * S::BKQ, l_map, qfull_bar(slot), l_kq * S::BKQ,
+                    l_brow + l_n_out);
+      } else {
+        tma_load_2d(dq, l_map, qfull_bar(slot), l_kq * S::BKQ, l_brow);
+      }
+      ++q_issued;
+      if (++l_kq == l_nkq) {
+        l_kq = 0;
+        l_tile += units;
+        if (l_tile < total) l_locate();
+      }
+    };
+    if (issuer && l_tile < total) {
+      l_locate();
+      for (int s2 = 0; s2 < S::Q_STAGES && l_tile < total; ++s2) issue(s2);
+    }
+    uint32_t qs = 0, qph = 0, cs = 0, cph = 0;
+    bool ok = true;
+    for (int tile = unit; tile < total && ok; tile += units) {
+      const int nkb = tile < tiles0 ? nkb0 : nkb1;
       for (int kb = 0; kb < nkb; ++kb) {
-        const bool got = mbar_wait_bounded(qfull_bar(stage), phase, abort_flag, status);
+        // k-block kb is half kb % 2 of Q slot kb / 2 of the tile
+        bool got = (kb & 1) ? true : mbar_wait_bounded(qfull_bar(qs), qph, abort_flag, status);
+        if (got) got = mbar_wait_bounded(cempty_bar(cs), cph ^ 1u, abort_flag, status);
         if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
-        const uint8_t* q = smem + STAGES * (A_BYTES + S::B_BYTES) + stage * S::BQ_BYTES;
-        uint8_t* b = smem + STAGES * A_BYTES + stage * S::B_BYTES;
+        const uint8_t* q = smem + (sBq - sA) + qs * S::BQ_BYTES;
+        uint8_t* b = smem + (sB - sA) + cs * S::B_BYTES;
+        const int h4 = (kb & 1) * 4;  // first 16-byte chunk of this k-block in a Q row
 #pragma unroll 2
-        for (int i = ct; i < S::B_ROWS * 4; i += S::CONV_WARPS * 32) {
-          // 16 codes of row r (K columns 16*c4 ..) -> bf16 chunks 2*c4, 2*c4 + 1
-          const int r = i >> 2, c4 = i & 3;
-          const uint4 in = *reinterpret_cast<const uint4*>(q + r * BK + c4 * 16);
-          uint8_t* row = b + (r >> 3) * 1024 + (r & 7) * 128;
+        for (int g8 = cw; g8 < S::B_ROWS / 8; g8 += S::CONV_WARPS) {
+          // 8-row group g8; each quarter-warp takes rows rr and rr ^ 5 of it
+          // (they differ in bits 0 and 2, so neither the swizzled Q reads nor
+          // the swizzled bf16 writes of a quarter-warp share a bank), and lane
+          // c4 the 16 codes at K columns 16*c4 .. of the k-block
+          const int rr = (lane & 4) ? ((lane >> 3) ^ 5) : (lane >> 3);
+          const int c4 = lane & 3;
+          const uint4 in = *reinterpret_cast<const uint4*>(
+              q + (g8 * 8 + rr) * S::BKQ + (((h4 + c4) ^ rr) << 4));
+          uint8_t* row = b + g8 * 1024 + rr * 128;
           uint4 o0, o1;
-          o0.x = e4m3x2_to_bf16x2(in.x);
-          o0.y = e4m3x2_to_bf16x2(in.x >> 16);
-          o0.z = e4m3x2_to_bf16x2(in.y);
-          o0.w = e4m3x2_to_bf16x2(in.y >> 16);
-          o1.x = e4m3x2_to_bf16x2(in.z);
-          o1.y = e4m3x2_to_bf16x2(in.z >> 16);
-          o1.z = e4m3x2_to_bf16x2(in.w);
-          o1.w = e4m3x2_to_bf16x2(in.w >> 16);
-          *reinterpret_cast<uint4*>(row + (((2 * c4) ^ (r & 7)) << 4)) = o0;
-          *reinterpret_cast<uint4*>(row + (((2 * c4 + 1) ^ (r & 7)) << 4)) = o1;
+          e4m3x4_to_bf16x4(in.x, o0.x, o0.y);
+          e4m3x4_to_bf16x4(in.y, o0.z, o0.w);
+          e4m3x4_to_bf16x4(in.z, o1.x, o1.y);
+          e4m3x4_to_bf16x4(in.w, o1.z, o1.w);
+          *reinterpret_cast<uint4*>(row + (((2 * c4) ^ rr) << 4)) = o0;
+          *reinterpret_cast<uint4*>(row + (((2 * c4 + 1) ^ rr) << 4)) = o1;
         }
         fence_proxy_async_shared();  // the tensor cores read what the threads wrote
         __syncwarp();
+        const bool slot_done = (kb & 1) || kb == nkb - 1;
         if (lane == 0) {
-          if (PAIR == 2 && !leader) mbar_arrive_cluster(mapa_shared(conv_bar(stage), 0));
-          else mbar_arrive(conv_bar(stage));
+          if (slot_done) mbar_arrive(qempty_bar(qs));
+          if (PAIR == 2 && !leader) mbar_arrive_cluster(mapa_shared(cfull_bar(cs), 0));
+          else mbar_arrive(cfull_bar(cs));
         }
-        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        if (++cs == S::B_STAGES) { cs = 0; cph ^= 1u; }
+        if (!slot_done) continue;
+        if (cw == 0) {
+          // once every converter warp has read slot qs, refill it
+          int refill_ok = 1;
+          if (issuer && l_tile < total) {
+            if (mbar_wait_bounded(qempty_bar(qs), qph, abort_flag, status)) issue((int)qs);
+            else refill_ok = 0;
+          }
+          if (!__shfl_sync(0xffffffffu, refill_ok, 0)) { ok = false; break; }
+        }
+        if (++qs == S::Q_STAGES) { qs = 0; qph ^= 1u; }
       }
     }
   } else {
@@ -484,8 +577,9 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
       const bool row_ok = r_in < rows_left;
       const int64_t out_row = (int64_t)a_row + r_in;
       const bool glu = P.mode == EPI_SWIGLU;
-      // this warp's output columns: 64 of a 256-wide tile, or 32 of a
-      // 128-wide SwiGLU tile (whose accumulator holds 128 gate + 128 up)
+      // this warp's output columns: EPI_COLS of a 256-wide tile, or half as
+      // many of a 128-wide SwiGLU tile (whose accumulator holds 128 gate +
+      // 128 up)
       const int wcols = glu ? EPI_COLS / 2 : EPI_COLS;
       const int col0 = n * (glu ? BN / 2 : BN) + cpart * wcols;
       // everything that does not need the accumulator is fetched before waiting
@@ -493,32 +587,31 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
       if (P.mode == EPI_SCALE && P.topk_w != nullptr && row_ok)
         wscale = P.topk_w[P.perm[out_row]];
       const bool has_bias = P.bias != nullptr;
-      if (has_bias) {
-        // 64 staged values, 2 per lane: the slice's bias, or for SwiGLU its
-        // 32 gate biases followed by its 32 up biases
-        int c2 = col0 + lane * 2;
-        size_t boff = (size_t)cur.g * n_out + c2;
-        if (glu) {
-          c2 = col0 + (lane & 15) * 2;
-          boff = (size_t)cur.g * 2 * n_out + (lane >= 16 ? n_out : 0) + c2;
-        }
-        uint32_t b = 0u;
-        if (c2 < n_out) b = __ldg(reinterpret_cast<const uint32_t*>(P.bias + boff));
-        *reinterpret_cast<uint32_t*>(my_bias + lane * 2) = b;
-        __syncwarp();
-      }
       const bool has_scale = FP8 && P.b_scale != nullptr;
-      if (has_scale) {
-        // the 64 column scales of the slice (SwiGLU: 32 gate, then 32 up)
-        int c2 = col0 + lane * 2;
-        size_t soff = (size_t)cur.g * n_out + c2;
-        if (glu) {
-          c2 = col0 + (lane & 15) * 2;
-          soff = (size_t)cur.g * 2 * n_out + (lane >= 16 ? n_out : 0) + c2;
+      if (has_bias || has_scale) {
+        // EPI_COLS staged values per warp, 2 per lane and pass: the slice's
+        // biases (and FP8 column scales), or for SwiGLU its wcols gate values
+        // followed by its wcols up values
+#pragma unroll
+        for (int j2 = lane * 2; j2 < EPI_COLS; j2 += 64) {
+          int c2 = col0 + j2;
+          size_t off = (size_t)cur.g * n_out + c2;
+          if (glu) {
+            const bool up = j2 >= wcols;
+            c2 = col0 + (up ? j2 - wcols : j2);
+            off = (size_t)cur.g * 2 * n_out + (up ? n_out : 0) + c2;
+          }
+          if (has_bias) {
+            uint32_t b = 0u;
+            if (c2 < n_out) b = __ldg(reinterpret_cast<const uint32_t*>(P.bias + off));
+            *reinterpret_cast<uint32_t*>(my_bias + j2) = b;
+          }
+          if (has_scale) {
+            float2 sc = make_float2(0.0f, 0.0f);
+            if (c2 < n_out) sc = __ldg(reinterpret_cast<const float2*>(P.b_scale + off));
+            *reinterpret_cast<float2*>(my_scale + j2) = sc;
+          }
         }
-        float2 sc = make_float2(0.0f, 0.0f);
-        if (c2 < n_out) sc = __ldg(reinterpret_cast<const float2*>(P.b_scale + soff));
-        *reinterpret_cast<float2*>(my_scale + lane * 2) = sc;
         __syncwarp();
       }
       int ok = 1;
@@ -530,10 +623,10 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
       const bool warp_has_rows = warp_row0 < rows_left;     // warp-uniform
       const bool full_cols = col0 + wcols <= n_out;         // warp-uniform
       if (warp_has_rows && col0 < n_out && glu) {
-        // 32 output columns in two halves of 16: gate and up accumulators
+        // wcols output columns in pieces of 16: gate and up accumulators
         const uint32_t tg = tmem_base + lane_addr + acc * BN + cpart * wcols;
 #pragma unroll 1
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < EPI_COLS / 32; ++h) {
           uint32_t rg[16], ru[16];
           tmem_ld_32x32b_x16(tg + h * 16, rg);
           tmem_ld_32x32b_x16(tg + BN / 2 + h * 16, ru);
@@ -544,10 +637,10 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
             float g = __uint_as_float(rg[i]), u = __uint_as_float(ru[i]);
             if (has_scale) {
               g *= my_scale[h * 16 + i];
-              u *= my_scale[32 + h * 16 + i];
+              u *= my_scale[EPI_COLS / 2 + h * 16 + i];
             }
             if (has_bias) {
-              const uint16_t bgate = my_bias[h * 16 + i], bup = my_bias[32 + h * 16 + i];
+              const uint16_t bgate = my_bias[h * 16 + i], bup = my_bias[EPI_COLS / 2 + h * 16 + i];
               g += __uint_as_float((uint32_t)bgate << 16);
               u += __uint_as_float((uint32_t)bup << 16);
             }
@@ -572,7 +665,7 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
       } else if (warp_has_rows && col0 < n_out) {
         const uint32_t taddr = tmem_base + lane_addr + acc * BN + cpart * EPI_COLS;
 #pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < EPI_COLS / 32; ++c) {
           uint32_t r[32];
           tmem_ld_32x32b_x32(taddr + c * 32, r);
           tmem_ld_wait();
@@ -662,23 +755,26 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
     // Some role gave up, so copies or MMAs may still be in flight.  Let them
     // land / finish before shared memory and TMEM go away.
     if (warp == 0 && lane == 0) {
-      if constexpr (FP8) {
-        // this CTA's E4M3 copies complete on its own barriers
-        const long long first = tma_issued > STAGES ? tma_issued - STAGES : 0;
-        for (long long j = first; j < tma_issued; ++j)
-          mbar_wait_drain(qfull_bar((int)(j % STAGES)), (uint32_t)((j / STAGES) & 1));
-      }
       if (PAIR == 1 || leader) {
         // the full barriers count every byte issued to this CTA's ring
-        const long long first = tma_issued > STAGES ? tma_issued - STAGES : 0;
+        const long long first = tma_issued > a_slots ? tma_issued - a_slots : 0;
         for (long long j = first; j < tma_issued; ++j)
-          mbar_wait_drain(full_bar((int)(j % STAGES)), (uint32_t)((j / STAGES) & 1));
+          mbar_wait_drain(full_bar((int)(j % a_slots)), (uint32_t)((j / a_slots) & 1));
       } else {
         // the odd CTA's copies complete on its peer's barriers: give them a
         // bounded grace period (they land within microseconds)
         const long long t0 = clock64();
         while (clock64() - t0 < 4000000LL) {
         }
+      }
+    }
+    if constexpr (FP8) {
+      if (warp == 2 + EPI_WARPS && lane == 0) {
+        // the converters' E4M3 copies complete on this CTA's Q ring
+        constexpr int QS = S::Q_STAGES;
+        const long long first = q_issued > QS ? q_issued - QS : 0;
+        for (long long j = first; j < q_issued; ++j)
+          mbar_wait_drain(qfull_bar((int)(j % QS)), (uint32_t)((j / QS) & 1));
       }
     }
     if (warp == 1 && lane == 0 && leader) {
@@ -739,8 +835,8 @@ bool encode_tensor_map_bf16(CUtensorMap* map, const void* base, int64_t rows, in
   return r == CUDA_SUCCESS;
 }
 
-// E4M3 codes [rows, K] (K bytes per row), unswizzled row-major boxes: the
-// converter warps write the swizzled bf16 tile themselves.
+// E4M3 codes [rows, K] (K bytes per row), boxes of 128 codes a row in the
+// 128-byte swizzled layout; the converter warps write the bf16 tile.
 static bool encode_tensor_map_e4m3(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
                                    int box_cols, int box_rows) {
   EncodeTiledFn enc = get_encoder();
@@ -750,14 +846,15 @@ static bool encode_tensor_map_e4m3(CUtensorMap* map, const void* base, int64_t r
   cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
-cudaError_t make_gemm_plan(GemmPlan* plan, const GemmArgs& args, const __nv_bfloat16* A,
+cudaError_t make_gemm_plan(GemmPlan* plan, const GemmArgs& args_in, const __nv_bfloat16* A,
                            int64_t a_rows, const void* const B[2], const int64_t b_rows[2],
-                           bool fp8, int num_sms) {
+                           bool fp8, int64_t group_rows_max, int num_sms) {
+  GemmArgs args = args_in;
   const int np = args.num_phases;
   if (np < 1 || np > 2 || a_rows <= 0) return cudaErrorInvalidValue;
   for (int p = 0; p < np; ++p)
@@ -771,15 +868,20 @@ cudaError_t make_gemm_plan(GemmPlan* plan, const GemmArgs& args, const __nv_bflo
   // fill them; single CTAs (128-row tiles) for decode-sized groups.
   const int64_t avg_rows = a_rows / (args.num_groups > 0 ? args.num_groups : 1);
   const int pair = (avg_rows >= 192 && num_sms >= 2) ? 2 : 1;
+  // FP8 single-CTA tiles copy the A rows a group can hold, in steps of 16
+  int a_box = 128;
+  if (fp8 && pair == 1 && group_rows_max > 0 && group_rows_max < 128)
+    a_box = (int)((group_rows_max + 15) / 16 * 16);
+  args.a_box = a_box;
   for (int p = 0; p < np; ++p) {
     // phase 1 reads phase 0's output [a_rows, n_out0] as its A operand
     const __nv_bfloat16* a = p == 0 ? A : args.ph[0].out;
-    if (!encode_tensor_map_bf16(&plan->tmA[p], a, a_rows, args.ph[p].K, BK, 128))
+    if (!encode_tensor_map_bf16(&plan->tmA[p], a, a_rows, args.ph[p].K, BK, a_box))
       return cudaErrorInvalidValue;
     // SwiGLU tiles load 128 gate and 128 up rows: two 128-row boxes
     const int box_b = args.ph[p].mode == EPI_SWIGLU ? BN / 2 : BN / pair;
     const bool ok = fp8 ? encode_tensor_map_e4m3(&plan->tmB[p], B[p], b_rows[p], args.ph[p].K,
-                                                 BK, box_b)
+                                                 2 * BK, box_b)
                         : encode_tensor_map_bf16(&plan->tmB[p], B[p], b_rows[p], args.ph[p].K,
                                                  BK, box_b);
     if (!ok) return cudaErrorInvalidValue;

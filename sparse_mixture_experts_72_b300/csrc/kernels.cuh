@@ -204,6 +204,8 @@ struct GemmArgs {
                                  // (zeroed before the launch; gemm_rows_done_len() entries)
   int* status;                   // device status word
   int32_t skip_producer;         // failure injection: the TMA producer issues nothing
+  int32_t a_box;                 // rows per A copy (set by make_gemm_plan): 128, or for
+                                 // FP8 single-CTA tiles the bound on a group's rows
 };
 
 struct GemmPlan {
@@ -224,9 +226,12 @@ inline int64_t gemm_rows_done_len(int64_t a_rows, int G) { return (a_rows + 127)
 // is 2); returns cudaErrorInvalidValue if encoding fails.
 // B[p] points at bf16 weights, or with fp8 set at E4M3 codes (one byte per
 // weight; K a multiple of 16 so that rows start on 16-byte boundaries).
+// group_rows_max bounds the rows of any one group (tokens per expert); FP8
+// launches of small groups copy only that many A rows per k-block (a group
+// that exceeds it records MOE_ERR_INVALID_ARG in the status word).
 cudaError_t make_gemm_plan(GemmPlan* plan, const GemmArgs& args, const __nv_bfloat16* A,
                            int64_t a_rows, const void* const B[2], const int64_t b_rows[2],
-                           bool fp8, int num_sms);
+                           bool fp8, int64_t group_rows_max, int num_sms);
 cudaError_t launch_gemm(const GemmPlan& plan, cudaStream_t st, LaunchTrace* tr);
 bool tensor_map_encoder_available();
 

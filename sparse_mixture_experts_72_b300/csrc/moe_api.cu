@@ -355,7 +355,10 @@ moe_status_t do_ffn(const moe_config_t& c, const uint16_t* x, const int32_t* per
     const void* B[2] = {W.W1, W.W2};
     const int64_t b_rows[2] = {(int64_t)c.N * w1_rows(c, c.F), (int64_t)c.N * c.H};
     GemmPlan p;
-    MOE_CUDA(make_gemm_plan(&p, g, xp, R, B, b_rows, fp8, sms));
+    // rows one expert can hold: its capacity, at most one per token
+    const int64_t cap = capacity_of(c);
+    const int64_t group_max = expert_choice(c) ? ec_tokens(c) : (cap >= 0 && cap < c.T ? cap : c.T);
+    MOE_CUDA(make_gemm_plan(&p, g, xp, R, B, b_rows, fp8, group_max, sms));
     MOE_CUDA(launch_gemm(p, st, tr));
   }
   if (c.F_shared > 0 && c.T > 0) {
@@ -386,7 +389,8 @@ moe_status_t do_ffn(const moe_config_t& c, const uint16_t* x, const int32_t* per
     const void* B[2] = {W.W1s, W.W2s};
     const int64_t b_rows[2] = {w1_rows(c, c.F_shared), (int64_t)c.H};
     GemmPlan p;
-    MOE_CUDA(make_gemm_plan(&p, g, reinterpret_cast<const bf*>(x), c.T, B, b_rows, fp8, sms));
+    MOE_CUDA(make_gemm_plan(&p, g, reinterpret_cast<const bf*>(x), c.T, B, b_rows, fp8, c.T,
+                            sms));
     MOE_CUDA(launch_gemm(p, st, tr));
   }
   return MOE_OK;

@@ -17,7 +17,8 @@ pytestmark = pytest.mark.gpu
 
 SMALL = ["small_silu", "small_swiglu", "swiglu_pairs", "small_expert_choice",
          "expert_choice_ragged", "expert_choice_all", "many_experts_choice",
-         "slot_major_capacity", "min_capacity", "small_fp8", "fp8_pairs", "swiglu_fp8"]
+         "slot_major_capacity", "min_capacity", "small_fp8", "fp8_pairs", "swiglu_fp8",
+         "fp8_decode_small", "fp8_capacity_small"]
 FULL_EXACT = ["mixtral_swiglu_decode", "mixtral_decode_fp8"]
 FULL_SAMPLED = ["moelayer_expert_choice", "mixtral_swiglu_prefill"]
 # logit gap under which the fp32 router and the float64 oracle may order two
