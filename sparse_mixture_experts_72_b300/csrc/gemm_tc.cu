@@ -25,7 +25,8 @@
 // second Linear's few large tiles fill the gaps of the first's tail instead
 // of forming a partial last wave.
 //
-// Two shapes of the same persistent, warp-specialised kernel (576 threads):
+// Two shapes of the same persistent, warp-specialised kernel, each for bf16
+// or FP8 (E4M3) weights:
 //
 //   PAIR = 1  one CTA per tile of 128 rows x 256 columns: A tile 128 x 64 and
 //             B tile 256 x 64 per stage, 4 stages; tcgen05.mma.cta_group::1,
@@ -40,9 +41,12 @@
 //
 // Roles: warp 0 TMA producer; warp 1 TMEM allocator and single-thread MMA
 // issuer (even CTA only for PAIR = 2) into one of two 256-column fp32
-// accumulators; warps 2..17 epilogue (tcgen05.ld -> bias -> GELU or scale ->
-// bf16 stores; warp w reads TMEM lanes 32*(w%4).. and the 64-column slice
-// (w-2)/4 of the tile).
+// accumulators; then EPI_WARPS epilogue warps (tcgen05.ld -> scale -> bias ->
+// activation or gate weight -> bf16 stores; warp w reads TMEM lanes
+// 32*(w%4).. and the EPI_COLS-wide column slice (w-2)/4 of the tile); with
+// FP8 weights, then CONV_WARPS converter warps that fetch the E4M3 weight
+// rows and widen them to the bf16 B tiles (16 epilogue + 2 converter warps
+// per CTA of a pair, 8 + 8 for a single CTA: 576 or 640 threads).
 // The grid never exceeds the CTAs (pairs) that can be resident at once, so a
 // phase-1 tile only ever waits for tiles that running CTAs will finish.
 // Every wait is bounded: on expiry the CTA records MOE_ERR_TIMEOUT, lets its
