@@ -254,6 +254,12 @@ moe_status_t moe_permute(const moe_config_t* cfg, const int32_t* topk_idx, const
  * different streams can starve each other: keep the layers of concurrent
  * batches on one stream (moe_forward_host shows the pattern); if they do
  * overlap, the waits run out and MOE_ERR_TIMEOUT is recorded, nothing hangs.
+ * offsets must give no expert more rows than the config allows (at most T
+ * for token choice, since a token picks distinct experts, and at most the
+ * capacity when one applies), as moe_permute and moe_expert_choice produce:
+ * FP8 launches of decode-sized batches copy only that many rows per expert;
+ * an expert with more records MOE_ERR_INVALID_ARG in the status word (its
+ * extra rows are not computed; nothing is read or written out of bounds).
  */
 moe_status_t moe_expert_ffn(const moe_config_t* cfg, const uint16_t* x, const int32_t* perm,
                             const int32_t* offsets, const float* topk_w,

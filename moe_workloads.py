@@ -109,6 +109,7 @@ WORKLOADS: Dict[str, Workload] = {w.name: w for w in [
              weight_dtype="e4m3"),
     Workload("mixtral_swiglu_decode_fp8", T=64, H=4096, F=14336, N=8, k=2, activation="swiglu",
              phase="decode", weight_dtype="e4m3"),
+    Workload("mixtral_prefill_fp8", T=16384, H=4096, F=14336, N=8, k=2, weight_dtype="e4m3"),
 ]}
 
 # Extra small cases for tests (not benchmark lines).

@@ -45,8 +45,8 @@
 // activation or gate weight -> bf16 stores; warp w reads TMEM lanes
 // 32*(w%4).. and the EPI_COLS-wide column slice (w-2)/4 of the tile); with
 // FP8 weights, then CONV_WARPS converter warps that fetch the E4M3 weight
-// rows and widen them to the bf16 B tiles (16 epilogue + 2 converter warps
-// per CTA of a pair, 8 + 8 for a single CTA: 576 or 640 threads).
+// rows and widen them to the bf16 B tiles (8 epilogue + 8 converter warps;
+// 576 threads in every shape).
 // The grid never exceeds the CTAs (pairs) that can be resident at once, so a
 // phase-1 tile only ever waits for tiles that running CTAs will finish.
 // Every wait is bounded: on expiry the CTA records MOE_ERR_TIMEOUT, lets its
@@ -90,13 +90,13 @@ struct GemmShape {
   static constexpr int B_STAGES = FP8 ? (PAIR == 2 ? 4 : 2) : STAGES;
   static constexpr int Q_STAGES = FP8 ? 3 : 0;
   // Epilogue warps: 4 per TMEM lane quarter, EPI_COLS columns each.  FP8:
-  // warps widening E4M3 to bf16 in shared memory.  A single CTA converts 256
-  // B rows a k-block and its tiles are weight-bound (decode, few rows): it
-  // gives half of its epilogue warps to the conversion.  A pair's CTA
-  // converts 128 rows under a longer MMA step.
-  static constexpr int EPI_WARPS = FP8 && PAIR == 1 ? 8 : 16;
+  // warps widening E4M3 to bf16 in shared memory.  Widening a k-block takes
+  // a warp longer than the MMA step it feeds unless many warps share it, so
+  // FP8 kernels give half of the epilogue warps to the conversion (8 + 8;
+  // with 2 converter warps a pair's CTA ran 3.5x slower than bf16 weights).
+  static constexpr int EPI_WARPS = FP8 ? 8 : 16;
   static constexpr int EPI_COLS = BN / (EPI_WARPS / 4);
-  static constexpr int CONV_WARPS = FP8 ? (PAIR == 2 ? 2 : 8) : 0;
+  static constexpr int CONV_WARPS = FP8 ? 8 : 0;
   static constexpr int THREADS = 64 + EPI_WARPS * 32 + CONV_WARPS * 32;
   // full, empty, tmem full / empty, drain (+ FP8: Q full / empty, B full / empty)
   static constexpr int NUM_BARS = 2 * A_SLOTS_MAX + 5 + (FP8 ? 2 * Q_STAGES + 2 * B_STAGES : 0);

@@ -20,7 +20,7 @@ SMALL = ["small_silu", "small_swiglu", "swiglu_pairs", "small_expert_choice",
          "slot_major_capacity", "min_capacity", "small_fp8", "fp8_pairs", "swiglu_fp8",
          "fp8_decode_small", "fp8_capacity_small"]
 FULL_EXACT = ["mixtral_swiglu_decode", "mixtral_decode_fp8"]
-FULL_SAMPLED = ["moelayer_expert_choice", "mixtral_swiglu_prefill"]
+FULL_SAMPLED = ["moelayer_expert_choice", "mixtral_swiglu_prefill", "mixtral_prefill_fp8"]
 # logit gap under which the fp32 router and the float64 oracle may order two
 # tokens of one expert's column differently (far above fp32 rounding of the
 # logits, far below the gaps of distinct random logits)
@@ -226,3 +226,29 @@ def test_widened_launch_counts_and_trace(_lib):
         m.moe_forward(cfg, W, x, trace_events=ev)
         torch.cuda.synchronize()
         assert all(ev[i].elapsed_time(ev[i + 1]) >= 0 for i in range(n))
+
+
+def test_fp8_group_above_bound_is_reported(_lib):
+    """FP8 launches of decode-sized batches copy at most the rows one expert
+    can hold (here T = 40, so 48); offsets that give an expert 80 rows (more
+    than a token-choice dispatch can) must be reported in the status word,
+    not computed silently.  A dispatch within the bound leaves the word 0."""
+    m = _lib
+    T, H, F = 40, 64, 64
+    cfg = m.MoEConfig(T=T, H=H, F=F, N=2, k=2, weight_dtype="e4m3")
+    dev = "cuda"
+    g = torch.Generator().manual_seed(3)
+    codes = lambda *s: torch.randint(0, 0x7E, s, generator=g, dtype=torch.uint8).to(dev)
+    weights = m.MoEWeights(Wg=torch.zeros((2, H), device=dev), W1=codes(2, F, H),
+                           W2=codes(2, H, F), s1=torch.full((2, F), 1e-3, device=dev),
+                           s2=torch.full((2, H), 1e-3, device=dev))
+    x = torch.randn((T, H), generator=g).to(torch.bfloat16).to(dev)
+    perm = torch.arange(T * 2, dtype=torch.int32, device=dev)
+    topk_w = torch.full((T, 2), 0.5, dtype=torch.float32, device=dev)
+    ws = m.make_workspace(cfg, dev)
+    ok_offsets = torch.tensor([0, T, 2 * T], dtype=torch.int32, device=dev)
+    m.moe_expert_ffn(cfg, x, perm, ok_offsets, topk_w, weights, ws=ws)
+    assert m.moe_workspace_status(ws) == 0
+    bad_offsets = torch.tensor([0, 2 * T, 2 * T], dtype=torch.int32, device=dev)
+    m.moe_expert_ffn(cfg, x, perm, bad_offsets, topk_w, weights, ws=ws)
+    assert m.moe_workspace_status(ws) == 1   # MOE_ERR_INVALID_ARG
