@@ -63,6 +63,17 @@ def test_algorithmic_work_counts():
     d = wl.WORKLOADS["deepseek_prefill"]
     wk = bench.algorithmic_work(d, np.ones(d.N), d.T * d.k)
     assert "shared_ffn" in wk and wk["shared_ffn"]["flops"] == 4 * d.T * d.F_shared * d.H
+    # SwiGLU: gate, up and down matrices
+    s = wl.WORKLOADS["mixtral_swiglu_decode"]
+    ws = bench.algorithmic_work(s, np.full(s.N, 16), 128)
+    assert ws["expert_ffn"]["flops"] == 6 * 128 * s.H * s.F
+    assert ws["expert_ffn"]["bytes"] == 2 * 3 * 8 * s.F * s.H + 2 * 2 * 128 * s.H
+    # E4M3 weights: one byte per weight plus one fp32 scale per matrix row
+    # (W1: F rows, W2: H rows); activations stay bf16
+    f = wl.WORKLOADS["mixtral_decode_fp8"]
+    wf = bench.algorithmic_work(f, np.array([16] * 7 + [0]), 112)
+    assert wf["expert_ffn"]["flops"] == 4 * 112 * f.H * f.F
+    assert wf["expert_ffn"]["bytes"] == 7 * (2 * f.F * f.H + 4 * (f.F + f.H)) + 2 * 2 * 112 * f.H
 
 
 def test_peaks_and_traffic_lookup():
