@@ -5,20 +5,27 @@
 
 A step is one moe_forward call (router, dispatch, expert GEMMs, combine) over
 one batch of seeded synthetic input already resident in HBM; L2 is flushed
-(a 256 MiB write) between timed steps, outside the timed events.  Prints one
-JSON line on rank 0.  Under torchrun (N > 1) every rank runs an independent
-replica on its own batch (weak scaling) and the slowest rank's time counts.
+(a 256 MiB write) before every step, outside the step's CUDA events.  The
+headline workload is the Mixtral-sized prefill (T = 16384, the largest
+single-GPU configuration with a tensor-core roof).  Rank 0 prints one JSON
+line; with one GPU it also carries a ``per_config`` block that measures every
+other layer configuration of the pages (MoELayer, Mixtral decode, DeepSeek
+prefill / decode, Switch capacity) the same way.  Under torchrun (N > 1)
+every rank runs an independent replica on its own batch (weak scaling) and
+the slowest rank's time counts.
 """
 from __future__ import annotations
 
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
-import tempfile
 import sys
+import tempfile
+import threading
 import time
 
 import numpy as np
@@ -28,10 +35,20 @@ sys.path.insert(0, ROOT)
 
 import moe_workloads as wl  # noqa: E402
 
-DEFAULT_WORKLOAD = "moelayer"
+DEFAULT_WORKLOAD = "mixtral_prefill"
+# every layer configuration of the pages, measured in the same run (the
+# headline is one of them)
+# (in an order that lets consecutive workloads with the same layer share
+# their device weights)
+PER_CONFIG = ("mixtral_prefill", "mixtral_decode", "moelayer", "switch_capacity",
+              "deepseek_prefill", "deepseek_decode")
 METRIC = "MoE-layer fwd tokens/s; % of bf16 TC peak (prefill) or HBM BW (decode)"
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+# timed region of each per-config measurement: at least this long, so that
+# the clock sampler sees it
+PER_CONFIG_MIN_S = 0.4
+CLOCK_INTERVAL_S = 0.005
 
 
 # ---------------------------------------------------------------------------
@@ -92,52 +109,103 @@ def committed_traffic(workload: str, kernel: str):
     return None
 
 
-class ClockSampler:
-    """nvidia-smi clock / throttle-reason sampling during the timed region."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+# clock-event reason bits of NVML (nvmlClocksEventReason*)
+_REASON_BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+                "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80}
 
-    def __init__(self, gpu_index: int, out_dir: str, interval_ms: int = 50):
-        self.proc = None
-        self.path = os.path.join(out_dir, f"clocks_rank{gpu_index}.csv")
-        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+
+def summarise_clocks(samples, source: str) -> dict:
+    """samples: [(sm_mhz, sm_max_mhz, power_w, reasons_bitmask)] -> the line's clocks block."""
+    sm = [s[0] for s in samples]
+    reasons = sorted({n for s in samples for n, b in _REASON_BITS.items() if s[3] & b})
+    return {"sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": max(s[1] for s in samples) if samples else None,
+            "sm_mhz_min": min(sm) if sm else None,
+            "power_w_max": max(s[2] for s in samples) if samples else None,
+            "reasons": reasons, "samples": len(sm), "source": source}
+
+
+class ClockSampler:
+    """SM clock, power and clock-event reasons of this process's GPU, sampled
+    every CLOCK_INTERVAL_S by a thread through NVML (read-only queries) while
+    the timed region runs; nvidia-smi is the fallback.  The GPU is found by
+    its PCI bus id, so CUDA_VISIBLE_DEVICES remapping does not matter."""
+
+    def __init__(self, device, out_dir: str):
+        self.samples, self._stop, self.proc, self.thread = [], threading.Event(), None, None
+        self.source = "nvml"
+        self.handle = None
         try:
+            import pynvml
+            import torch
+            pynvml.nvmlInit()
+            pr = torch.cuda.get_device_properties(device)
+            for bus in (f"{pr.pci_domain_id:08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0",
+                        f"{pr.pci_domain_id:04x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0"):
+                try:
+                    self.handle = pynvml.nvmlDeviceGetHandleByPciBusId(bus.upper())
+                    break
+                except pynvml.NVMLError:
+                    continue
+            if self.handle is None:
+                raise RuntimeError("GPU not found by PCI bus id")
+            self.nv = pynvml
+            self.thread = threading.Thread(target=self._loop, daemon=True)
+            self.thread.start()
+        except Exception:  # noqa: BLE001
+            self.handle = None
+            self._start_smi(device, out_dir)
+
+    def _loop(self):
+        nv, h = self.nv, self.handle
+        smax = nv.nvmlDeviceGetMaxClockInfo(h, nv.NVML_CLOCK_SM)
+        while not self._stop.is_set():
+            try:
+                self.samples.append((float(nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM)),
+                                     float(smax), nv.nvmlDeviceGetPowerUsage(h) / 1000.0,
+                                     int(nv.nvmlDeviceGetCurrentClocksEventReasons(h))))
+            except nv.NVMLError:
+                pass
+            time.sleep(CLOCK_INTERVAL_S)
+
+    def _start_smi(self, device, out_dir):
+        self.source = "nvidia-smi"
+        fields = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active")
+        self.path = os.path.join(out_dir, "clocks.csv")
+        os.makedirs(out_dir, exist_ok=True)
+        try:
+            idx = device.index or 0
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", f"-lms", str(interval_ms)],
+                ["nvidia-smi", f"--id={idx}", f"--query-gpu={fields}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=self.fh, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
 
     def stop(self) -> dict:
+        if self.thread is not None:
+            self._stop.set()
+            self.thread.join(timeout=5)
+            return summarise_clocks(self.samples, "nvml")
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no clock source"],
+                    "samples": 0, "source": "none"}
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.fh.close()
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        samples = []
         with open(self.path) as f:
             for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
-                    continue
+                p = [s.strip() for s in line.split(",")]
                 try:
-                    sm.append(float(parts[1]))
-                    smax.append(float(parts[2]))
-                except ValueError:
+                    samples.append((float(p[0]), float(p[1]), float(p[2]), int(p[3], 16)))
+                except (ValueError, IndexError):
                     continue
-                for n, v in zip(names, parts[5:9]):
-                    if v.lower().startswith("active"):
-                        reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        return summarise_clocks(samples, "nvidia-smi")
 
 
 def algorithmic_work(w: wl.Workload, counts: np.ndarray, R: int):
@@ -167,15 +235,49 @@ def algorithmic_work(w: wl.Workload, counts: np.ndarray, R: int):
     return out
 
 
+def forward_work(w: wl.Workload, counts: np.ndarray, R: int) -> dict:
+    """FLOPs and bytes of the whole forward pass at minimum: the gate GEMM
+    (2*T*N*H), both (SwiGLU: three) Linears of every kept row and of the
+    shared expert; the weights of every expert hit, the shared expert and
+    W_g (fp32) read once, x read once and out written once.  Intermediate
+    tensors (logits, the permuted rows, Hid, the weighted rows) are the
+    implementation's own and are not counted."""
+    m = 3 if w.activation == "swiglu" else 2
+    fp8 = w.weight_dtype == "e4m3"
+    wb = 1.0 if fp8 else 2.0
+    hit = int((np.asarray(counts) > 0).sum())
+
+    def mats(F):
+        return wb * m * F * w.H + (4.0 * ((m - 1) * F + w.H) if fp8 else 0.0)
+    flops = 2.0 * w.T * w.N * w.H + 2.0 * m * R * w.H * w.F
+    nbytes = hit * mats(w.F) + 4.0 * w.N * w.H + 2.0 * 2 * w.T * w.H
+    if w.F_shared:
+        flops += 2.0 * m * w.T * w.H * w.F_shared
+        nbytes += mats(w.F_shared)
+    return {"flops": flops, "bytes": nbytes}
+
+
+def roofline_fraction(flops: float, nbytes: float, seconds: float, peaks: dict,
+                      tc_key: str = "bf16_tflops") -> dict:
+    """Fraction of the slower roof: t_roof / t, t_roof = max(FLOPs / tensor peak,
+    bytes / HBM peak)."""
+    t_tc = flops / (peaks[tc_key] * 1e12)
+    t_bw = nbytes / (peaks["hbm_gbs"] * 1e9)
+    bound = "tensor" if t_tc >= t_bw else "hbm"
+    return {"bound": bound, "frac": max(t_tc, t_bw) / seconds if seconds > 0 else None,
+            "tflops": flops / seconds / 1e12 if seconds > 0 else None,
+            "gbs": nbytes / seconds / 1e9 if seconds > 0 else None}
+
+
 def bench_config(w: wl.Workload, world: int) -> dict:
     """The workload description both arms print (shapes, options, protocol)."""
     return {"workload": w.name, "T": w.T, "H": w.H, "F": w.F, "N": w.N, "k": w.k,
             "capacity_factor": w.capacity_factor, "F_shared": w.F_shared,
             "routing": w.routing, "activation": w.activation,
             "expert_weights": w.weight_dtype,
-            "l2": "flushed between steps (256 MiB write, untimed)",
-            "launch": "CUDA graph replay of moe_forward; every 10th step replays a copy with an "
-                      "event node before each launch",
+            "l2": "flushed before every step (256 MiB write, outside the step's events)",
+            "launch": "CUDA graph replay of moe_forward; per-launch times from replays of a copy "
+                      "with an event node before each launch, interleaved with the timed steps",
             "parallelism": f"replicas x{world}"}
 
 
@@ -209,6 +311,14 @@ def launch_names(w: wl.Workload, has_rows: bool):
     return names
 
 
+def per_config_steps(est_ms: float, k_min: int, min_s: float = PER_CONFIG_MIN_S,
+                     k_max: int = 4000) -> int:
+    """Steps of a per-config measurement: at least k_min, and enough for a
+    timed region of min_s at the estimated step time."""
+    want = int(math.ceil(min_s * 1e3 / max(est_ms, 1e-3)))
+    return max(k_min, min(k_max, want))
+
+
 # ---------------------------------------------------------------------------
 # oracle arm (CPU baseline and --impl reference)
 
@@ -229,42 +339,65 @@ def host_cores() -> int:
         return os.cpu_count() or 1
 
 
+def split_rows(S: int, parts: int):
+    """[start, stop) of `parts` contiguous near-equal slices of range(S) (empty ones dropped)."""
+    b = np.linspace(0, S, parts + 1).round().astype(int)
+    return [(int(b[i]), int(b[i + 1])) for i in range(parts) if b[i + 1] > b[i]]
+
+
 def oracle_timing_all_cores(w: wl.Workload, steps: int, warmup: int, budget_s: float):
-    """oracle_timing in a child process whose BLAS may use every host core
-    (thread-count variables set before numpy loads: a BLAS started with one
-    thread cannot grow later).  Returns (tokens/s, sample tokens, desc, threads)."""
-    n = host_cores()
+    """oracle_timing in a child process that never touches CUDA, with one
+    BLAS thread per process (set before numpy loads) and a pool of worker
+    processes, one per host core, forked from it after the weights are
+    drawn (so they share them).  Returns (tokens/s, sample tokens, desc,
+    workers)."""
     env = dict(os.environ)
     for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
-        env[v] = str(n)
+        env[v] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
     code = ("import json, sys; sys.path.insert(0, %r); import bench, moe_workloads as wl; "
-            "w = wl.get_workload(%r); r = bench.oracle_timing(w, %d, %d, %r); "
-            "print(json.dumps([r[0], r[1], r[2], bench.blas_threads()]))"
-            % (ROOT, w.name, steps, warmup, float(budget_s)))
+            "w = wl.get_workload(%r); r = bench.oracle_timing(w, %d, %d, %r, bench.host_cores()); "
+            "print(json.dumps(list(r)))" % (ROOT, w.name, steps, warmup, float(budget_s)))
     out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
                          check=True, cwd=ROOT)
-    tps, S, desc, threads = json.loads(out.stdout.strip().splitlines()[-1])
-    return tps, S, desc, threads
+    tps, S, desc, workers = json.loads(out.stdout.strip().splitlines()[-1])
+    return tps, S, desc, workers
 
 
 def oracle_step(w: wl.Workload, x_bits, router, getter, shared, rows: slice):
     """One oracle forward over the token rows `rows` (a sub-batch of the
-    workload: with no capacity limit the rows are routed exactly as in the
-    full batch)."""
+    workload).  Without a capacity limit the rows are routed exactly as in
+    the full batch; with one, capacity couples all tokens, so the whole
+    batch is routed and dispatched and the experts are evaluated for `rows`."""
     from oracle import moe_oracle as O
     Wg, bg, sel = router
+    kw = dict(routing=w.routing, activation=w.activation, min_capacity=w.min_capacity,
+              drop_order=w.drop_order)
+    if w.capacity_factor > 0:
+        xs = wl.bf16_bits_to_f64(x_bits)
+        return O.forward(xs, Wg, bg, sel, w.k, w.capacity_factor, w.aux_alpha, getter, shared,
+                         tokens=np.arange(rows.start, rows.stop), **kw)
     xs = wl.bf16_bits_to_f64(x_bits[rows])
-    return O.forward(xs, Wg, bg, sel, w.k, w.capacity_factor, w.aux_alpha, getter, shared,
-                     routing=w.routing, activation=w.activation, min_capacity=w.min_capacity,
-                     drop_order=w.drop_order)
+    return O.forward(xs, Wg, bg, sel, w.k, w.capacity_factor, w.aux_alpha, getter, shared, **kw)
 
 
-def oracle_timing(w: wl.Workload, steps: int, warmup: int, budget_s: float, seed: int = 0):
-    """Times the oracle on bounded token samples; returns (tokens/s, sample tokens, desc)."""
+_POOL_STATE = {}
+
+
+def _pool_slice(span):
+    """Worker body: the oracle over rows [span) of the batch held in _POOL_STATE."""
+    st = _POOL_STATE
+    oracle_step(st["w"], st["x_bits"], st["router"], st["getter"], st["shared"],
+                slice(span[0], span[1]))
+    return span[1] - span[0]
+
+
+def oracle_inputs(w: wl.Workload, seed: int = 0):
+    """x bits, router and float64 expert weights (all drawn now) for the oracle."""
+    from oracle import moe_oracle as O
     x_bits = wl.gen_x(w, seed)
     router = wl.gen_router(w, seed)
     if w.weight_dtype == "e4m3":
-        from oracle import moe_oracle as O
         cache = {}
 
         def getter(e):
@@ -282,29 +415,51 @@ def oracle_timing(w: wl.Workload, steps: int, warmup: int, budget_s: float, seed
     else:
         getter = wl.expert_getter_f64(w, seed)
         shared = wl.shared_f64(w, seed)
-    for e in range(w.N):
-        getter(e)  # draw and widen the weights before timing
+    # draw and widen every expert before timing (threads: the draws release the GIL)
+    wl._pool_map(getter, range(w.N), None)
+    return x_bits, router, getter, shared
+
+
+def oracle_timing(w: wl.Workload, steps: int, warmup: int, budget_s: float, workers: int = 1,
+                  seed: int = 0):
+    """Times the oracle on bounded token samples with `workers` processes
+    (forked after the inputs are drawn; each computes a contiguous slice of
+    the sample).  Returns (tokens/s, sample tokens, desc, workers used)."""
+    x_bits, router, getter, shared = oracle_inputs(w, seed)
+    _POOL_STATE.update(w=w, x_bits=x_bits, router=router, getter=getter, shared=shared)
     # size the sample so that warmup + steps fit in the budget
-    probe = min(w.T, 64)
+    probe = min(w.T, 32)
     t0 = time.perf_counter()
-    oracle_step(w, x_bits, router, getter, shared, slice(0, probe))
+    _pool_slice((0, probe))
     per_tok = (time.perf_counter() - t0) / probe
     total_steps = max(1, steps + warmup)
-    S = int(max(8, min(w.T, budget_s / total_steps / max(per_tok, 1e-9))))
-    if w.capacity_factor > 0:
-        S = w.T  # capacity couples tokens: only the whole batch is exact
-    for i in range(warmup):
-        oracle_step(w, x_bits, router, getter, shared, slice(0, S))
-    times = []
-    for i in range(steps):
-        s0 = (i * S) % max(1, w.T - S + 1)
-        t0 = time.perf_counter()
-        oracle_step(w, x_bits, router, getter, shared, slice(s0, s0 + S))
-        times.append(time.perf_counter() - t0)
+    per_step = budget_s / total_steps
+    S = int(max(8, min(w.T, workers * per_step / max(per_tok, 1e-9))))
+    workers = max(1, min(workers, S))
+    pool = None
+    if workers > 1:
+        import multiprocessing as mp
+        pool = mp.get_context("fork").Pool(workers)
+
+    def one_step(s0):
+        spans = [(s0 + a, s0 + b) for a, b in split_rows(S, workers)]
+        t = time.perf_counter()
+        n = sum(pool.map(_pool_slice, spans, chunksize=1)) if pool else _pool_slice(spans[0])
+        assert n == S
+        return time.perf_counter() - t
+    try:
+        for i in range(warmup):
+            one_step(0)
+        times = [one_step((i * S) % max(1, w.T - S + 1)) for i in range(steps)]
+    finally:
+        if pool:
+            pool.close()
+            pool.join()
     tps = S / statistics.median(times)
-    desc = (f"oracle forward over {S}-token slices of the {w.name} batch "
-            f"(T={w.T}), {steps} timed slices, float64 numpy on host")
-    return tps, S, desc
+    desc = (f"oracle forward over {S}-token slices of the {w.name} batch (T={w.T}), "
+            f"{steps} timed slices, each split over {workers} worker processes with one "
+            f"BLAS thread each, float64 numpy on host")
+    return tps, S, desc, workers
 
 
 def run_reference(args):
@@ -330,39 +485,26 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 # CUDA arm
 
-def run_ours(args):
+def measure(m, w, d, device, steps: int, warmup: int, world: int, flush, peaks, clocks_dir,
+            min_s: float = 0.0):
+    """Times `steps` graph replays of moe_forward on the inputs `d` (with
+    min_s > 0: at least min_s of them, the step count raised from a warm-up
+    estimate).  Returns a dict of results (ms_per_step is this rank's)."""
     import torch
-    rank, world, local_rank = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local_rank)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
-    device = torch.device("cuda", local_rank if world > 1 else 0)
-    torch.cuda.set_device(device)
-
-    import sparse_mixture_experts_72_b300 as m
-
-    w = wl.get_workload(args.workload)
     cfg = m.MoEConfig(**w.config_kwargs())
-    # replicas share the weights; each rank draws its own batch
-    d = wl.to_device(w, seed=0, device=device, x_seed=None if rank == 0 else 1000 + rank)
     weights = m.MoEWeights(**{k: d[k] for k in wl.WEIGHT_KEYS})
-    x_bits_host, x = d["x_bits"], d["x"]
+    x = d["x"]
     ws = m.make_workspace(cfg, device)
     outs = m.alloc_outputs(cfg, device)
     out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=device)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     n_launch = m.moe_forward_num_launches(cfg)
-
-    for _ in range(max(args.warmup, 3)):
+    W = max(warmup, 3)
+    for _ in range(W):
         flush.zero_()
         m.moe_forward(cfg, weights, x, out=out, outputs=outs, ws=ws)
     torch.cuda.synchronize()
     if m.moe_workspace_status(ws) != 0:
-        raise RuntimeError("device status after warm-up is not OK")
-    # the timed steps replay the whole forward as one CUDA graph; every
-    # TRACE_EVERY-th step replays a copy of it that also records an event
-    # before each launch (device timestamps, no host gaps)
+        raise RuntimeError(f"{w.name}: device status after warm-up is not OK")
     fwd = m.MoEForwardGraph(cfg, weights, x, out, outputs=outs, ws=ws)
     trace_ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_launch + 1)]
     fwd_traced = m.MoEForwardGraph(cfg, weights, x, out, outputs=outs, ws=ws,
@@ -371,15 +513,24 @@ def run_ours(args):
     R = int(outs["offsets"][-1].item())
     names = launch_names(w, m.moe_max_rows(cfg) > 0)
     assert len(names) == n_launch, (names, n_launch)
-
-    K = args.steps
-    TRACE_EVERY = 10
+    K = steps
+    if min_s > 0:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(3):
+            fwd.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        K = per_config_steps(e0.elapsed_time(e1) / 3, steps, min_s)
+    # per-launch device times: a traced replay after every trace_every-th
+    # step (not a step: its own events are not in the step times)
+    trace_every = max(1, K // 5)
+    traced_after = set(range(0, K, trace_every))
     ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    traced_steps = set(range(0, K, TRACE_EVERY))
     per = {n: [] for n in names}
 
-    clocks = ClockSampler(device.index or 0, args.clocks_dir)
+    clocks = ClockSampler(device, clocks_dir)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -387,63 +538,97 @@ def run_ours(args):
     for i in range(K):
         flush.zero_()
         ev_s[i].record()
-        if i in traced_steps:
+        fwd.replay()
+        ev_e[i].record()
+        if i in traced_after:
+            flush.zero_()
             fwd_traced.replay()
-            ev_e[i].record()
             torch.cuda.synchronize()  # read this replay's stamps before the next overwrites them
             for j, n in enumerate(names):
                 per[n].append(trace_ev[j].elapsed_time(trace_ev[j + 1]))
-        else:
-            fwd.replay()
-            ev_e[i].record()
     torch.cuda.synchronize()
     wall_s = time.perf_counter() - t_wall
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
     if m.moe_workspace_status(ws) != 0:
-        raise RuntimeError("device status after the timed steps is not OK")
+        raise RuntimeError(f"{w.name}: device status after the timed steps is not OK")
 
     step_ms = [ev_s[i].elapsed_time(ev_e[i]) for i in range(K)]
     ms_local = float(np.mean(step_ms))
-    graph_ms = float(np.mean([t for i, t in enumerate(step_ms) if i not in traced_steps] or step_ms))
-    traced_ms = float(np.mean([step_ms[i] for i in traced_steps]))
-    ms_max = reduce_max(ms_local, world, device)
-    value = aggregate(w.T, world, ms_max)
-
-    # per-launch device times from the traced replays
     per_ms = {n: float(np.mean(v)) for n, v in per.items()}
-
-    peaks, peak_src = load_peaks()
     work = algorithmic_work(w, counts, R)
+    fw = forward_work(w, counts, R)
     gemms = [n for n in names if n.endswith("_ffn")]
     dom = max(gemms, key=lambda n: per_ms[n]) if gemms else max(per_ms, key=per_ms.get)
-    t_dom = per_ms[dom] * 1e-3
-    wk = work.get(dom)
-    roof = None
-    if wk is not None and t_dom > 0:
-        t_tc = wk["flops"] / (peaks["bf16_tflops"] * 1e12)
-        t_bw = wk["bytes"] / (peaks["hbm_gbs"] * 1e9)
-        if t_tc >= t_bw:
-            ach = wk["flops"] / t_dom / 1e12
-            roof = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"],
-                    "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"]}
-        else:
-            ach = wk["bytes"] / t_dom / 1e9
-            roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                    "frac": ach / peaks["hbm_gbs"]}
-        roof["traffic"] = committed_traffic(w.name, dom)
-        roof["kernel"] = f"grouped_gemm_kernel ({dom})"
-        roof["launch_ms"] = per_ms[dom]
-        roof["peak_source"] = f"{peak_src} (burst)"
+    res = dict(cfg=cfg, weights=weights, ws=ws, outs=outs, out=out, x=x, names=names,
+               n_launch=n_launch, K=K, W=W, n_traced=len(traced_after), ms_local=ms_local,
+               step_ms_min=float(np.min(step_ms)), step_ms_max=float(np.max(step_ms)),
+               per_ms=per_ms, counts=counts, R=R, work=work, fw=fw, dom=dom, clocks=clk,
+               wall_s=wall_s)
+    return res
 
-    # End to end through the C ABI with host buffers (moe_forward_host: H2D
-    # of x from pinned memory, the forward, D2H of out), pipelined over three
-    # streams (input copies, layers, output copies) and three buffer sets,
-    # so batch i+1's input copy and batch i-1's output copy overlap batch i's
-    # layer.  No flush here: the batches alternate between two weight
-    # replicas, so each step's weights were last read two steps earlier with
-    # the other replica's weights (2x the expert bytes) read in between.
+
+def kernel_roofline(w, res, peaks, peak_src):
+    """The roofline object of the dominant launch (an expert-FFN launch)."""
+    dom = res["dom"]
+    t_dom = res["per_ms"][dom] * 1e-3
+    wk = res["work"].get(dom)
+    if wk is None or t_dom <= 0:
+        return None
+    t_tc = wk["flops"] / (peaks["bf16_tflops"] * 1e12)
+    t_bw = wk["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    if t_tc >= t_bw:
+        ach = wk["flops"] / t_dom / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"]}
+    else:
+        ach = wk["bytes"] / t_dom / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / peaks["hbm_gbs"]}
+    roof["traffic"] = committed_traffic(w.name, dom)
+    roof["algorithmic"] = wk["bytes"] if roof["bound"] == "hbm" else wk["flops"]
+    roof["kernel"] = f"grouped_gemm_kernel ({dom})"
+    roof["launch_ms"] = res["per_ms"][dom]
+    roof["peak_source"] = f"{peak_src} ({'burst' if roof['bound'] == 'tensor' else 'copy'})"
+    return roof
+
+
+def forward_roofline(res, ms, peaks, peak_src):
+    """Whole-step fraction of the slower roof, against the burst and the
+    sustained tensor peak."""
+    fw = res["fw"]
+    s = ms * 1e-3
+    burst = roofline_fraction(fw["flops"], fw["bytes"], s, peaks, "bf16_tflops")
+    sus = roofline_fraction(fw["flops"], fw["bytes"], s, peaks,
+                            "bf16_tflops_sustained" if "bf16_tflops_sustained" in peaks
+                            else "bf16_tflops")
+    return {"bound": burst["bound"], "frac": burst["frac"], "frac_sustained_peak": sus["frac"],
+            "flops": fw["flops"], "bytes": fw["bytes"], "tflops": burst["tflops"],
+            "gbs": burst["gbs"], "peak_source": peak_src}
+
+
+def config_entry(w, res, ms, peaks, peak_src):
+    roof = kernel_roofline(w, res, peaks, peak_src)
+    return {"T": w.T, "ms_per_step": ms, "tokens_per_s": w.T / (ms * 1e-3),
+            "steps": res["K"], "step_ms_min": res["step_ms_min"], "step_ms_max": res["step_ms_max"],
+            "kept_rows": res["R"], "experts_hit": int((res["counts"] > 0).sum()),
+            "ffn": None if roof is None else {k: roof[k] for k in
+                                              ("bound", "achieved", "unit", "frac", "launch_ms")},
+            "forward": forward_roofline(res, ms, peaks, peak_src),
+            "launch_ms": res["per_ms"], "clocks": res["clocks"]}
+
+
+def e2e_measure(m, w, res, x_bits_host, K, world, device):
+    """End to end through the C ABI with host buffers (moe_forward_host: H2D
+    of x from pinned memory, the forward, D2H of out), pipelined over three
+    streams (input copies, layers, output copies) and three buffer sets, so
+    batch i+1's input copy and batch i-1's output copy overlap batch i's
+    layer.  No flush here: the batches alternate between two weight
+    replicas, so each step's weights were last read two steps earlier with
+    the other replica's weights (2x the expert bytes) read in between."""
+    import torch
+    cfg, weights, ws, x, out = res["cfg"], res["weights"], res["ws"], res["x"], res["out"]
     wrep = [weights, m.MoEWeights(**{k: (None if v is None else v.clone())
                                      for k, v in weights.__dict__.items()})]
     SL = 3
@@ -485,33 +670,87 @@ def run_ours(args):
     e2e_ms = reduce_max(e0.elapsed_time(e1) / E, world, device)
     if not all(torch.equal(out_pin[0].view(torch.int16), o.view(torch.int16)) for o in out_pin):
         raise RuntimeError("the end-to-end batches disagree")
-    e2e = {"value": aggregate(w.T, world, e2e_ms), "unit": "tokens/s",
-           "h2d_bytes_per_step": int(x_pin[0].numel() * 2),
-           "d2h_bytes_per_step": int(out_pin[0].numel() * 2),
-           "ms_per_step": e2e_ms,
-           "how": "moe_forward_host (C ABI, pinned host buffers) pipelined on H2D, compute "
-                  "and D2H streams with three buffer sets; two weight replicas alternate"}
+    del wrep
+    return {"value": aggregate(w.T, world, e2e_ms), "unit": "tokens/s",
+            "h2d_bytes_per_step": int(x_pin[0].numel() * 2),
+            "d2h_bytes_per_step": int(out_pin[0].numel() * 2),
+            "ms_per_step": e2e_ms, "steps": E,
+            "how": "moe_forward_host (C ABI, pinned host buffers) pipelined on H2D, compute "
+                   "and D2H streams with three buffer sets; two weight replicas alternate"}
+
+
+def run_ours(args):
+    import torch
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    device = torch.device("cuda", local_rank if world > 1 else 0)
+    torch.cuda.set_device(device)
+
+    import sparse_mixture_experts_72_b300 as m
+
+    peaks, peak_src = load_peaks()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    w = wl.get_workload(args.workload)
+    # replicas share the weights; each rank draws its own batch
+    d = wl.to_device(w, seed=0, device=device, x_seed=None if rank == 0 else 1000 + rank)
+    res = measure(m, w, d, device, args.steps, args.warmup, world, flush, peaks, args.clocks_dir)
+    K = res["K"]
+    ms_max = reduce_max(res["ms_local"], world, device)
+    value = aggregate(w.T, world, ms_max)
+    roof = kernel_roofline(w, res, peaks, peak_src)
+    fwd_roof = forward_roofline(res, ms_max, peaks, peak_src)
+    e2e = e2e_measure(m, w, res, d["x_bits"], K, world, device)
+    launches = (K + res["n_traced"]) * sum(1 for n in res["names"] if "memset" not in n)
+    headline_entry = config_entry(w, res, ms_max, peaks, peak_src)
+
+    per_config = None
+    if world == 1 and not args.no_per_config:
+        per_config = {w.name: headline_entry}
+        cache = {w.name: d}
+        del res
+        for name in PER_CONFIG:
+            if name in per_config:
+                continue
+            wc = wl.get_workload(name)
+            # reuse the device weights of a workload with the same layer
+            src = next((cache[n] for n in cache if wl.same_weights(wl.get_workload(n), wc)), None)
+            for n in list(cache):
+                if cache[n] is not src:
+                    del cache[n]
+            torch.cuda.empty_cache()
+            dc = wl.to_device(wc, seed=0, device=device, reuse=src)
+            cache = {name: dc}
+            rc = measure(m, wc, dc, device, args.steps, args.warmup, 1, flush, peaks,
+                         args.clocks_dir, min_s=PER_CONFIG_MIN_S)
+            per_config[name] = config_entry(wc, rc, rc["ms_local"], peaks, peak_src)
+            del rc
+        cache.clear()
+        torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        tps, S, desc, cores = oracle_timing_all_cores(w, steps=3, warmup=1, budget_s=20.0)
+        tps, S, desc, cores = oracle_timing_all_cores(w, steps=3, warmup=1, budget_s=24.0)
         cpu = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-               "sample": desc}
+               "sample": desc, "host_cores": host_cores()}
 
     if rank == 0:
+        hr = headline_entry
         line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
                 "steps": K, "warmup": max(args.warmup, 3), "ms_per_step": ms_max,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
                 "data": "synthetic",
                 "config": bench_config(w, world),
-                "work": {"kept_rows": R, "experts_hit": int((counts > 0).sum())},
-                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": int(K * sum(1 for n in names if "memset" not in n)),
-                "step_ms": {"graph_replay": graph_ms, "graph_replay_traced": traced_ms,
-                            "traced_steps": len(traced_steps)},
-                "clocks": clk,
-                "launch_ms": per_ms,
-                "wall_s_timed_region": wall_s}
+                "work": {"kept_rows": hr["kept_rows"], "experts_hit": hr["experts_hit"]},
+                "roofline": roof, "forward_roofline": fwd_roof,
+                "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": int(launches),
+                "clocks": hr["clocks"],
+                "launch_ms": hr["launch_ms"],
+                "step_ms": {"mean": ms_max, "min": hr["step_ms_min"], "max": hr["step_ms_max"]},
+                "per_config": per_config}
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
@@ -521,14 +760,16 @@ def run_ours(args):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=500)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=sorted(wl.WORKLOADS) + sorted(wl.TEST_WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="measure only the headline workload")
     ap.add_argument("--clocks-dir", default=os.path.join(tempfile.gettempdir(), "moe_bench"),
-                    help="where the nvidia-smi clock samples of the timed region are kept")
+                    help="where nvidia-smi clock samples go if NVML is unavailable")
     args = ap.parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)

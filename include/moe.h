@@ -333,11 +333,16 @@ moe_status_t moe_forward_host(const moe_config_t* cfg, const moe_weights_t* weig
  *   larger sizes return MOE_ERR_UNSUPPORTED before anything is enqueued.
  *   The call allocates nothing (no cudaMalloc/cudaFree).  Its first call on a
  *   device looks up the array's device address (cudaGetSymbolAddress) with
- *   that device current, so make the first call on each device before any
- *   stream capture.  Every call shares the one array, which keeps the last
- *   call's contents (nothing in it needs clearing: each call writes every
- *   entry it reads); calls that overlap on the GPU - on different streams,
- *   or from different threads - race on it and must be serialised.
+ *   that device current.  Under CUDA's default lazy module loading that
+ *   first call is also when the library's code and this 768 KiB array are
+ *   placed in that device's memory, so it can fail with MOE_ERR_CUDA in a
+ *   process that has already reserved all device memory: make one call on
+ *   each device at start-up, before reserving memory and before any stream
+ *   capture; later calls take no device memory.  Every call shares the one
+ *   array, which keeps the last call's contents (nothing in it needs
+ *   clearing: each call writes every entry it reads); calls that overlap on
+ *   the GPU - on different streams, or from different threads - race on it
+ *   and must be serialised.
  */
 #define MOE_STATIC_MAX_ASSIGNMENTS 65536
 #define MOE_STATIC_MAX_EXPERTS 256

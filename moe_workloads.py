@@ -110,6 +110,9 @@ WORKLOADS: Dict[str, Workload] = {w.name: w for w in [
     Workload("mixtral_swiglu_decode_fp8", T=64, H=4096, F=14336, N=8, k=2, activation="swiglu",
              phase="decode", weight_dtype="e4m3"),
     Workload("mixtral_prefill_fp8", T=16384, H=4096, F=14336, N=8, k=2, weight_dtype="e4m3"),
+    # calibration of the expert GEMM kernel on a dense shape: one expert, so
+    # the layer is two 8192 x 8192 x 8192 GEMMs (the gate is the identity)
+    Workload("dense_ffn_8192", T=8192, H=8192, F=8192, N=1, k=1),
 ]}
 
 # Extra small cases for tests (not benchmark lines).
@@ -420,15 +423,30 @@ WEIGHT_KEYS = ("Wg", "bg", "sel_bias", "W1", "b1", "W2", "b2", "W1s", "b1s", "W2
                "s1", "s2", "s1s", "s2s")
 
 
-def to_device(w: Workload, seed: int = 0, device="cuda", x_seed: Optional[int] = None) -> dict:
+def same_weights(a: Workload, b: Workload) -> bool:
+    """True when the two workloads draw identical layer parameters (they
+    differ at most in the token count and the routing options)."""
+    return (a.H, a.F, a.N, a.F_shared, a.activation, a.weight_dtype, a.expert_bias, a.gate_bias,
+            a.sel_bias) == (b.H, b.F, b.N, b.F_shared, b.activation, b.weight_dtype,
+                            b.expert_bias, b.gate_bias, b.sel_bias)
+
+
+def to_device(w: Workload, seed: int = 0, device="cuda", x_seed: Optional[int] = None,
+              reuse: Optional[dict] = None) -> dict:
     """Draws every input on the host (per-expert blocks in threads) and copies
     it to `device`.  Returns a dict of torch tensors with the layer's names
     (WEIGHT_KEYS, None where absent) plus ``x`` and ``x_bits`` (the host bf16
     bits of x).  FP8 workloads hold uint8 E4M3 codes in W1, W2, W1s, W2s and
-    their fp32 row scales in s1, s2, s1s, s2s."""
+    their fp32 row scales in s1, s2, s1s, s2s.  ``reuse``: the result of an
+    earlier call for a workload with the same parameters (same_weights); its
+    weight tensors are shared and only x is drawn."""
     import torch
     fp8 = w.weight_dtype == "e4m3"
     x_bits = gen_x(w, seed if x_seed is None else x_seed)
+    if reuse is not None:
+        d = {k: reuse[k] for k in WEIGHT_KEYS}
+        d.update(x_bits=x_bits, x=bits_to_torch_bf16(x_bits, device))
+        return d
     Wg, bg, sel = gen_router(w, seed)
     wdt = torch.uint8 if fp8 else torch.bfloat16
     W1 = torch.empty((w.N, w.w1_rows, w.H), dtype=wdt, device=device)

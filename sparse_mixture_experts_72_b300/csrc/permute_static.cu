@@ -7,8 +7,11 @@
 // real-time service that reserves every byte at start-up so that no request
 // can fail on a cudaMalloc.  Such callers still pass their inputs and
 // outputs; the scratch space moe_permute would take from the workspace comes
-// instead from one fixed array in device memory, allocated when the library
-// is loaded on a device and held until the process exits.
+// instead from one fixed array in device memory, placed there when this
+// module is loaded on a device and held until the process exits.  With
+// CUDA's default lazy module loading the module is loaded by the first
+// cudaGetSymbolAddress below, i.e. inside the first call on each device:
+// callers make that call at start-up, before they reserve all memory.
 //
 // The page's method has no counterpart to this entry point; it changes where
 // the scratch lives, not what is computed (the same kernels run).

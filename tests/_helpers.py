@@ -46,19 +46,27 @@ def upload(w: wl.Workload, seed: int = 0, device="cuda"):
     return d["x_bits"], weights, wl.gen_router(w, seed)
 
 
-def expert_getter(w: wl.Workload, seed=0):
+def expert_getter(w: wl.Workload, seed=0, cache: bool = True):
     """float64 weights of routed expert e for the oracle: the bf16 bits
-    widened, or for FP8 workloads the oracle's own dequantisation of the codes."""
+    widened, or for FP8 workloads the oracle's own dequantisation of the codes.
+    cache=False draws an expert again on every call (the oracle's forward
+    asks for each expert once; the DeepSeek-sized experts would hold ~60 GB
+    of float64 if all were kept)."""
     if w.weight_dtype != "e4m3":
-        return wl.expert_getter_f64(w, seed)
-    cache = {}
+        if cache:
+            return wl.expert_getter_f64(w, seed)
+        return lambda e: wl.expert_getter_f64(w, seed)(e)
+    store = {}
 
     def get(e):
-        if e not in cache:
-            q1, s1, b1, q2, s2, b2 = wl.gen_expert_e4m3(w, seed, e)
-            cache[e] = (O.dequantize_rows(q1, s1), None if b1 is None else wl.bf16_bits_to_f64(b1),
-                        O.dequantize_rows(q2, s2), None if b2 is None else wl.bf16_bits_to_f64(b2))
-        return cache[e]
+        if e in store:
+            return store[e]
+        q1, s1, b1, q2, s2, b2 = wl.gen_expert_e4m3(w, seed, e)
+        v = (O.dequantize_rows(q1, s1), None if b1 is None else wl.bf16_bits_to_f64(b1),
+             O.dequantize_rows(q2, s2), None if b2 is None else wl.bf16_bits_to_f64(b2))
+        if cache:
+            store[e] = v
+        return v
     return get
 
 
@@ -76,7 +84,8 @@ def shared_weights(w: wl.Workload, seed=0):
 def oracle_forward(w: wl.Workload, x_bits, router, seed=0, tokens=None):
     Wg, bg, sel = router
     return O.forward(wl.bf16_bits_to_f64(x_bits), Wg, bg, sel, w.k, w.capacity_factor,
-                     w.aux_alpha, expert_getter(w, seed), shared_weights(w, seed),
+                     w.aux_alpha, expert_getter(w, seed, cache=tokens is None),
+                     shared_weights(w, seed),
                      tokens=tokens, routing=w.routing, activation=w.activation,
                      min_capacity=w.min_capacity, drop_order=w.drop_order)
 
@@ -129,6 +138,59 @@ def sample_tokens(T: int, n: int, seed: int = 123) -> np.ndarray:
     picks = set([0, T - 1, T // 2])
     picks.update(rng.choice(T, size=n - len(picks), replace=False).tolist())
     return np.array(sorted(picks)[:n])
+
+
+# Row tiles of the expert GEMMs start at each expert's first row and are 128
+# (single CTA) or 256 (CTA pair) rows high; every 256-row tile is two
+# 128-row blocks, so covering the 128-row blocks covers both.
+TILE_ROWS = 128
+
+
+def tile_rows(offsets: np.ndarray, block: int = TILE_ROWS) -> np.ndarray:
+    """The first and the last row of every `block`-row tile of every
+    expert's row segment (the last tile of a segment is usually ragged)."""
+    rows = []
+    for e in range(len(offsets) - 1):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        for b in range(r0, r1, block):
+            rows += [b, min(b + block, r1) - 1]
+    return np.unique(np.array(rows, dtype=np.int64))
+
+
+def tile_tokens(w: wl.Workload, x_bits, router, n_random: int = 48, seed: int = 123):
+    """Tokens for a sampled full-size check: n_random random ones plus the
+    tokens owning the first and the last row of every row tile of every
+    expert, under the oracle's own routing and dispatch (so that every M-tile
+    of the expert GEMMs, ragged last ones included, has an output row the
+    oracle evaluates).  Returns (tokens, oracle offsets, oracle perm)."""
+    Wg, bg, sel = router
+    x = wl.bf16_bits_to_f64(x_bits)
+    C = O.capacity(w.T, w.N, w.capacity_factor, w.min_capacity)
+    if w.routing == "expert":
+        d = O.expert_choice(O.gate_logits(x, Wg, bg), min(C, w.T))
+        slots = w.N
+    else:
+        r = O.route(x, Wg, bg, sel, w.k)
+        d = O.permute(r["idx"], w.N, C, w.drop_order)
+        slots = w.k
+    rows = tile_rows(d["offsets"])
+    toks = set((d["perm"][rows] // slots).tolist())
+    toks.update(sample_tokens(w.T, n_random, seed).tolist())
+    return np.array(sorted(toks), dtype=np.int64), d["offsets"], d["perm"]
+
+
+def assert_tiles_covered(offsets: np.ndarray, perm: np.ndarray, slots: int, checked) -> int:
+    """Every TILE_ROWS-row tile of every expert segment holds at least one row
+    whose token's output was compared.  Returns the number of tiles."""
+    checked = set(np.asarray(checked).tolist())
+    n = 0
+    for e in range(len(offsets) - 1):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        for b in range(r0, r1, TILE_ROWS):
+            toks = perm[b:min(b + TILE_ROWS, r1)] // slots
+            assert checked.intersection(toks.tolist()), f"expert {e}: tile at row {b} unchecked"
+            n += 1
+    return n
 
 
 def laux_close(gpu: float, ref: float):

@@ -150,9 +150,12 @@ def test_forward(name, _lib):
 
 @pytest.mark.parametrize("name", FULL_SAMPLED)
 def test_forward_full_size_sampled(name, _lib):
+    """Routing, statistics and dispatch on every token; the output on random
+    tokens plus the owners of the first and last row of every row tile of
+    every expert, so that each M-tile of the expert GEMMs is checked."""
     m = _lib
     w = wl.get_workload(name)
-    tokens = h.sample_tokens(w.T, 48)
+    tokens, _, _ = h.tile_tokens(w, wl.gen_x(w, 0), wl.gen_router(w, 0), n_random=48)
     w_, cfg, xb, x, W, router, ref = _case(name, tokens=tokens)
     outs = m.alloc_outputs(cfg, "cuda")
     ws = m.make_workspace(cfg)
@@ -175,6 +178,7 @@ def test_forward_full_size_sampled(name, _lib):
                ((inv_g >= 0) == (ref["inv"].reshape(w.T, w.k)[tokens] >= 0)).all(1)
         assert keep.mean() > 0.9
     h.assert_close_out(got[keep], ref["out"][keep])
+    h.assert_tiles_covered(ref["offsets"], ref["perm"], w.k, tokens[keep])
 
 
 def test_forward_is_deterministic(_lib):

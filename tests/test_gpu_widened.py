@@ -122,6 +122,7 @@ def _check_forward(m, name, tokens=None):
             assert same.mean() > 0.99
             keep = same[toks]
     h.assert_close_out(got[keep], ref["out"][keep])
+    return toks[keep]
 
 
 @pytest.mark.parametrize("name", SMALL + FULL_EXACT)
@@ -131,8 +132,12 @@ def test_forward(name, _lib):
 
 @pytest.mark.parametrize("name", FULL_SAMPLED)
 def test_forward_full_size_sampled(name, _lib):
+    """Random tokens plus the owners of the first and last row of every row
+    tile of every expert: each M-tile of the expert GEMMs is checked."""
     w = wl.get_workload(name)
-    _check_forward(_lib, name, tokens=h.sample_tokens(w.T, 40))
+    tokens, offsets, perm = h.tile_tokens(w, wl.gen_x(w, 0), wl.gen_router(w, 0), n_random=40)
+    checked = _check_forward(_lib, name, tokens=tokens)
+    h.assert_tiles_covered(offsets, perm, w.N if w.routing == "expert" else w.k, checked)
 
 
 @pytest.mark.parametrize("name", ["small_expert_choice", "expert_choice_ragged",

@@ -7,17 +7,21 @@ byte at start-up so no request can fail on an allocation.  moe_permute_static
 serves them: it takes only inputs and outputs and keeps its scratch in a
 fixed device array inside the library.
 
-This test calls it through the C ABI twice in a row (two different shapes,
-the second at the array's size limit, so stale contents of the first call
-would show) and checks each result against moe_permute, the workspace
-version, with the tolerances the other parity tests use.  It lives in a file
-of its own that pytest collects last.
+This test calls it through the C ABI twice in a row: first at the array's
+size limit (256 experts), then a smaller case with another expert count, so
+the second call reads histograms laid out with a different stride over the
+first call's leftovers.  Each result is checked against the CPU oracle's
+dispatch (bit-exact integers, L_aux within 1e-5 relative) and against
+moe_permute, the workspace version.  It lives in a file of its own that
+pytest collects last.
 """
 import ctypes as C
 
 import numpy as np
 import pytest
 import torch
+
+from oracle import moe_oracle as O
 
 pytestmark = pytest.mark.gpu
 
@@ -61,9 +65,10 @@ def test_static_scratch_matches_workspace_version_twice():
     from sparse_mixture_experts_72_b300 import _lib
     lib = _lib.load()
     cases = [
-        # (T, N, k, capacity_factor): a capacity-limited case, then the size limit
-        (1000, 8, 2, 1.0),
+        # (T, N, k, capacity_factor): the size limit, then a smaller
+        # capacity-limited case with fewer experts
         (_lib.MOE_STATIC_MAX_ASSIGNMENTS // 8, _lib.MOE_STATIC_MAX_EXPERTS, 8, 1.25),
+        (1000, 8, 2, 1.0),
     ]
     for i, (T, N, k, cf) in enumerate(cases):
         cfg = _lib.MoeConfig(T=T, H=64, F=64, N=N, k=k, capacity_factor=cf, F_shared=0,
@@ -76,6 +81,16 @@ def test_static_scratch_matches_workspace_version_twice():
         got, R = _run(lib, cfg, lib.moe_permute_static, idx, p_mean)
         want, R_w = _run(lib, cfg, lib.moe_permute, idx, p_mean, ws)
         assert R == R_w
+        # the oracle's dispatch of the same indices
+        idx_h = idx.cpu().numpy()
+        ref = O.permute(idx_h, N, O.capacity(T, N, cf))
+        for name in ("counts", "offsets", "inv"):
+            assert np.array_equal(got[name], ref[name]), name
+        assert np.array_equal(got["perm"][:R], ref["perm"])
+        P = np.tile(p_mean.cpu().numpy().astype(np.float64), (T, 1))   # column means = p_mean
+        lb = O.load_balance(P, ref["counts"], k, 0.01)
+        np.testing.assert_allclose(got["f"], lb["f"], rtol=1e-6, atol=0)
+        assert abs(got["l_aux"][0] - lb["l_aux"]) <= 1e-5 * abs(lb["l_aux"])
         for name in ("counts", "offsets", "inv"):
             assert np.array_equal(got[name], want[name]), name
         assert np.array_equal(got["perm"][:R], want["perm"][:R])
