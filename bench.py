@@ -135,25 +135,27 @@ class ClockSampler:
         self.samples, self._stop, self.proc, self.thread = [], threading.Event(), None, None
         self.source = "nvml"
         self.handle = None
+        self.error = None
         try:
             import pynvml
             import torch
             pynvml.nvmlInit()
             pr = torch.cuda.get_device_properties(device)
-            for bus in (f"{pr.pci_domain_id:08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0",
-                        f"{pr.pci_domain_id:04x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0"):
-                try:
-                    self.handle = pynvml.nvmlDeviceGetHandleByPciBusId(bus.upper())
+            want = (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
+            for i in range(pynvml.nvmlDeviceGetCount()):
+                h = pynvml.nvmlDeviceGetHandleByIndex(i)
+                pci = pynvml.nvmlDeviceGetPciInfo(h)
+                if (pci.domain, pci.bus, pci.device) == want:
+                    self.handle = h
                     break
-                except pynvml.NVMLError:
-                    continue
             if self.handle is None:
-                raise RuntimeError("GPU not found by PCI bus id")
+                raise RuntimeError(f"no NVML device at PCI {want}")
             self.nv = pynvml
             self.thread = threading.Thread(target=self._loop, daemon=True)
             self.thread.start()
-        except Exception:  # noqa: BLE001
+        except Exception as e:  # noqa: BLE001
             self.handle = None
+            self.error = f"{type(e).__name__}: {e}"[:200]
             self._start_smi(device, out_dir)
 
     def _loop(self):
@@ -188,6 +190,12 @@ class ClockSampler:
             self._stop.set()
             self.thread.join(timeout=5)
             return summarise_clocks(self.samples, "nvml")
+        fallback = self._stop_smi()
+        if self.error:
+            fallback["nvml_error"] = self.error
+        return fallback
+
+    def _stop_smi(self) -> dict:
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no clock source"],
                     "samples": 0, "source": "none"}
@@ -232,6 +240,10 @@ def algorithmic_work(w: wl.Workload, counts: np.ndarray, R: int):
         Fs = w.F_shared
         out["shared_ffn"] = dict(flops=2.0 * m * w.T * w.H * Fs,
                                  bytes=mats(Fs) + 2.0 * 2 * w.T * w.H)
+    # the operand-swapped decode launch runs the routed and the shared experts
+    both = [out["expert_ffn"]] + ([out["shared_ffn"]] if w.F_shared else [])
+    out["expert_ffn_decode"] = dict(flops=sum(d["flops"] for d in both),
+                                    bytes=sum(d["bytes"] for d in both))
     return out
 
 
@@ -279,36 +291,6 @@ def bench_config(w: wl.Workload, world: int) -> dict:
             "launch": "CUDA graph replay of moe_forward; per-launch times from replays of a copy "
                       "with an event node before each launch, interleaved with the timed steps",
             "parallelism": f"replicas x{world}"}
-
-
-def launch_names(w: wl.Workload, has_rows: bool):
-    """Names of the launches moe_forward makes, in order (the status clear is
-    folded into the tensor-core router's first kernel, the scan into the
-    rank launch's last block, and the dispatch scatter also gathers the
-    expert rows)."""
-    names = []
-    tc_router = w.N <= 256
-    if not (tc_router and w.T > 0):
-        names += ["status_memset"]
-    if tc_router:  # tensor-core router: W_g split + fused router
-        names += ["router_split", "router_tc"] if w.T > 0 else ["router_pmean"]
-    else:
-        names += ["router_logits", "router_select", "router_pmean"] if w.T > 0 else ["router_pmean"]
-    if w.routing == "expert":
-        names += ["expert_choice"]
-        if has_rows:
-            names += ["gather_rows"]
-    elif w.T * w.k > 0:
-        names += ["permute_rank_scan", "scatter_gather"]
-    else:
-        names += ["permute_scan"]
-    if has_rows:
-        names += ["expert_ffn"]   # both Linears of every expert in one launch
-    if w.F_shared:
-        names += ["shared_ffn"]
-    if w.T > 0:
-        names += ["combine"]
-    return names
 
 
 def per_config_steps(est_ms: float, k_min: int, min_s: float = PER_CONFIG_MIN_S,
@@ -511,8 +493,7 @@ def measure(m, w, d, device, steps: int, warmup: int, world: int, flush, peaks, 
                                    trace_events=trace_ev)
     counts = outs["counts"].cpu().numpy()
     R = int(outs["offsets"][-1].item())
-    names = launch_names(w, m.moe_max_rows(cfg) > 0)
-    assert len(names) == n_launch, (names, n_launch)
+    names = m.moe_forward_launch_names(cfg)
     K = steps
     if min_s > 0:
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -559,7 +540,7 @@ def measure(m, w, d, device, steps: int, warmup: int, world: int, flush, peaks, 
     per_ms = {n: float(np.mean(v)) for n, v in per.items()}
     work = algorithmic_work(w, counts, R)
     fw = forward_work(w, counts, R)
-    gemms = [n for n in names if n.endswith("_ffn")]
+    gemms = [n for n in names if "_ffn" in n]
     dom = max(gemms, key=lambda n: per_ms[n]) if gemms else max(per_ms, key=per_ms.get)
     res = dict(cfg=cfg, weights=weights, ws=ws, outs=outs, out=out, x=x, names=names,
                n_launch=n_launch, K=K, W=W, n_traced=len(traced_after), ms_local=ms_local,
@@ -588,7 +569,8 @@ def kernel_roofline(w, res, peaks, peak_src):
                 "frac": ach / peaks["hbm_gbs"]}
     roof["traffic"] = committed_traffic(w.name, dom)
     roof["algorithmic"] = wk["bytes"] if roof["bound"] == "hbm" else wk["flops"]
-    roof["kernel"] = f"grouped_gemm_kernel ({dom})"
+    roof["kernel"] = ("decode_ffn_kernel" if dom.endswith("_decode") else "grouped_gemm_kernel") + \
+        f" ({dom})"
     roof["launch_ms"] = res["per_ms"][dom]
     roof["peak_source"] = f"{peak_src} ({'burst' if roof['bound'] == 'tensor' else 'copy'})"
     return roof

@@ -158,6 +158,12 @@ int64_t moe_capacity(const moe_config_t* cfg);
 /* Number of kernel launches (and memsets) one moe_forward call enqueues. */
 int32_t moe_forward_num_launches(const moe_config_t* cfg);
 
+/* Name of launch i (0 <= i < moe_forward_num_launches(cfg)) of moe_forward,
+ * e.g. "router_tc", "expert_ffn", "expert_ffn_decode", "combine": the
+ * intervals a trace_events array times.  A static string; NULL for an
+ * invalid configuration or index.  No device access. */
+const char* moe_forward_launch_name(const moe_config_t* cfg, int32_t i);
+
 /*
  * moe_route - gate, softmax, top-k selection and renormalisation.
  * ("混合专家模型 MoE 架构深度解析" §1.2 gate formula, §1.3 top-K steps 1-3,
@@ -254,12 +260,20 @@ moe_status_t moe_permute(const moe_config_t* cfg, const int32_t* topk_idx, const
  * different streams can starve each other: keep the layers of concurrent
  * batches on one stream (moe_forward_host shows the pattern); if they do
  * overlap, the waits run out and MOE_ERR_TIMEOUT is recorded, nothing hangs.
- * offsets must give no expert more rows than the config allows (at most T
- * for token choice, since a token picks distinct experts, and at most the
- * capacity when one applies), as moe_permute and moe_expert_choice produce:
- * FP8 launches of decode-sized batches copy only that many rows per expert;
- * an expert with more records MOE_ERR_INVALID_ARG in the status word (its
- * extra rows are not computed; nothing is read or written out of bounds).
+ * Two kernels serve it.  When the experts hold at most 64 rows on average
+ * (moe_max_rows(cfg) <= 64 N: decode-sized batches) the operands are
+ * swapped: each expert's weights are the 128-row operand of the tensor-core
+ * MMA and its token rows the narrow one, and the shared expert is one more
+ * group of the same launch; any row count per expert is computed.
+ * Otherwise token rows are the 128- or 256-row operand (CTA pairs for groups
+ * of 192 rows or more on average) and the shared expert has a launch of its
+ * own.  There, offsets must give no expert more rows than the config allows
+ * (at most T for token choice, since a token picks distinct experts, and at
+ * most the capacity when one applies), as moe_permute and moe_expert_choice
+ * produce: FP8 launches with groups below 128 rows copy only that many rows
+ * per expert; an expert with more records MOE_ERR_INVALID_ARG in the status
+ * word (its extra rows are not computed; nothing is read or written out of
+ * bounds).
  */
 moe_status_t moe_expert_ffn(const moe_config_t* cfg, const uint16_t* x, const int32_t* perm,
                             const int32_t* offsets, const float* topk_w,

@@ -21,7 +21,8 @@ from ._lib import MOE_TRACE_MAX_EVENTS, MoeError, check
 _L = _lib.load()
 
 __all__ = ["MoEConfig", "MoEWeights", "MoeError", "moe_workspace_size", "moe_max_rows",
-           "moe_capacity", "moe_forward_num_launches", "moe_route", "moe_permute",
+           "moe_capacity", "moe_forward_num_launches", "moe_forward_launch_names", "moe_route",
+           "moe_permute",
            "moe_permute_static",
            "moe_expert_ffn", "moe_combine", "moe_forward", "moe_workspace_status",
            "moe_debug_suppress_gemm_producer", "moe_expert_choice", "moe_update_sel_bias",
@@ -150,6 +151,13 @@ def moe_capacity(cfg: MoEConfig) -> Optional[int]:
 
 def moe_forward_num_launches(cfg: MoEConfig) -> int:
     return int(_L.moe_forward_num_launches(C.byref(cfg.c())))
+
+
+def moe_forward_launch_names(cfg: MoEConfig) -> list:
+    """Names of the launches moe_forward makes, in order (one per trace interval)."""
+    c = cfg.c()
+    n = moe_forward_num_launches(cfg)
+    return [_L.moe_forward_launch_name(C.byref(c), i).decode() for i in range(n)]
 
 
 def make_workspace(cfg: MoEConfig, device=None) -> torch.Tensor:

@@ -15,7 +15,7 @@ MOE_TRACE_MAX_EVENTS = 32
 
 # every symbol include/moe.h declares
 EXPORTED = ["moe_workspace_size", "moe_max_rows", "moe_capacity", "moe_forward_num_launches",
-            "moe_route", "moe_expert_choice", "moe_update_sel_bias", "moe_permute",
+            "moe_forward_launch_name", "moe_route", "moe_expert_choice", "moe_update_sel_bias", "moe_permute",
             "moe_expert_ffn", "moe_combine", "moe_forward", "moe_forward_host",
             "moe_permute_static", "moe_workspace_status", "moe_debug_suppress_gemm_producer",
             "moe_status_string", "moe_version"]
@@ -71,6 +71,8 @@ def load() -> C.CDLL:
     lib.moe_capacity.restype = C.c_int64
     lib.moe_forward_num_launches.argtypes = [cfgp]
     lib.moe_forward_num_launches.restype = C.c_int32
+    lib.moe_forward_launch_name.argtypes = [cfgp, C.c_int32]
+    lib.moe_forward_launch_name.restype = C.c_char_p
     lib.moe_route.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, P, P, C.c_size_t, P]
     lib.moe_route.restype = C.c_int
     lib.moe_expert_choice.argtypes = [cfgp, P, P, P, P, P, P, P, P, P]

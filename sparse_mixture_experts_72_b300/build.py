@@ -24,7 +24,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_b300.so")
 SOURCES = ["moe_api.cu", "router.cu", "router_tc.cu", "permute.cu", "combine.cu", "gemm_tc.cu",
-           "permute_static.cu", "expert_choice.cu"]
+           "permute_static.cu", "expert_choice.cu", "decode_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-fvisibility=hidden", "--expt-relaxed-constexpr",

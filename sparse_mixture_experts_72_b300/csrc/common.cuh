@@ -472,6 +472,28 @@ __device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t w, uint32_t& lo, uint3
   asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(hi) : "r"(x1), "r"(two120));
 }
 
+// Widens one 8-row group of E4M3 codes to bf16 (both tiles 128-byte
+// swizzled: 16-byte chunk c of row r at c ^ (r % 8)).  q: code rows of 128
+// codes (two k-blocks; h4 = 0 or 4 picks the k-block's first chunk); b: the
+// bf16 tile, rows of 64 values.  Each quarter-warp takes rows rr and rr ^ 5
+// of the group (they differ in bits 0 and 2, so neither the swizzled code
+// reads nor the swizzled bf16 writes of a quarter-warp share a bank), and
+// lane c4 the 16 codes at K columns 16*c4 of the k-block.
+__device__ __forceinline__ void widen_e4m3_rows8(const uint8_t* q, uint8_t* b, int g8, int h4,
+                                                 int lane) {
+  const int rr = (lane & 4) ? ((lane >> 3) ^ 5) : (lane >> 3);
+  const int c4 = lane & 3;
+  const uint4 in = *reinterpret_cast<const uint4*>(q + (g8 * 8 + rr) * 128 + (((h4 + c4) ^ rr) << 4));
+  uint8_t* row = b + g8 * 1024 + rr * 128;
+  uint4 o0, o1;
+  e4m3x4_to_bf16x4(in.x, o0.x, o0.y);
+  e4m3x4_to_bf16x4(in.y, o0.z, o0.w);
+  e4m3x4_to_bf16x4(in.z, o1.x, o1.y);
+  e4m3x4_to_bf16x4(in.w, o1.z, o1.w);
+  *reinterpret_cast<uint4*>(row + (((2 * c4) ^ rr) << 4)) = o0;
+  *reinterpret_cast<uint4*>(row + (((2 * c4 + 1) ^ rr) << 4)) = o1;
+}
+
 // SiLU, z * sigmoid(z) = z / (1 + e^-z), with the fast intrinsics: for very
 // negative z the denominator overflows and __fdividef returns 0 (the limit).
 __device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.0f + __expf(-z)); }

@@ -1,0 +1,697 @@
+// Expert FFN for decode-sized batches, operands swapped: the expert weights
+// are the 128-row M operand of tcgen05.mma and the few token rows an expert
+// holds are the narrow N operand, so that the tensor cores do no work on
+// padding rows and the launch streams the weights at the memory rate.
+//
+//   phase 0: Hid^T[f, j] = act( W1_e[f, :] . X_e[j, :] + b1_e[f] )
+//   phase 1: y^T[h, j]   = w_j ( W2_e[h, :] . Hid_e[j, :] + b2_e[h] )
+//
+// for expert e's token rows j ("AI-Research-SKILLs MoE 训练实战" §3.1:
+// Linear(H, 4H) -> GELU -> Linear(4H, H), the output weighted by the
+// renormalised gate score; §6.1 SiLU / SwiGLU).  The always-on shared expert
+// ("混合专家模型 MoE 架构深度解析" §3, Output = Shared(x) + sum_j w_j Routed_j(x))
+// is one more group of the same launch: all T token rows, weight 1, its own
+// weights and outputs.  Decode is bound by the weight bytes (INFER "FP8 量化":
+// weight streaming dominates small batches), so with E4M3 weights converter
+// warps widen the codes to bf16 in shared memory as they stream in.
+//
+// A tile is (phase, group, 128 weight rows, up to NT token rows).  The
+// accumulator holds 128 TMEM lanes (weight rows) x NT columns (tokens), or
+// for SwiGLU the gate rows' NT columns followed by the up rows' NT columns.
+// Tiles are ordered phase 0 before phase 1, then group, weight block and
+// token chunk (fastest); CTAs take them round-robin.  A phase-1 tile reads
+// Hid rows of its group's token chunk, which every phase-0 tile of that
+// chunk writes: each phase-0 tile releases a per-chunk counter in global
+// memory (red.release.gpu after the last epilogue warp's stores), and the
+// producer of a phase-1 tile issues its weight copies for the first ring
+// slots, then acquires the counter (bounded spin) before the Hid copies.
+//
+// Roles: warp 0 TMA producer (weights and activations; activations only with
+// E4M3 weights), warp 1 TMEM allocator and MMA issuer, warps 2-5 epilogue
+// (TMEM lane quarter warp % 4: 32 weight rows each, all token columns; the
+// rows are transposed through shared memory into 16-byte stores along the
+// output row), warps 6-13 E4M3 converters.
+// Every wait is bounded: on expiry the CTA records MOE_ERR_TIMEOUT, lets its
+// copies land, drains its MMAs, frees TMEM and exits.
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int DK = 64;                     // K per k-block: one 128-byte swizzled bf16 row
+constexpr int DM = 128;                    // weight rows per tile (MMA M)
+constexpr int DBOX = 16;                   // token rows per activation copy
+constexpr int D_A_BYTES = DM * DK * 2;     // one bf16 weight tile
+constexpr int D_Q_BYTES = DM * 2 * DK;     // one E4M3 slot: 128 rows x 128 codes (two k-blocks)
+constexpr int D_MAX_STAGES = 8;
+constexpr int D_Q_STAGES_MAX = 3;
+constexpr int D_EPI_WARPS = 4;
+constexpr int D_CONV_WARPS = 8;
+constexpr long long kDecodeDrainCycles = 200000000LL;
+
+template <bool FP8>
+struct DShape {
+  static constexpr int THREADS = 64 + D_EPI_WARPS * 32 + (FP8 ? D_CONV_WARPS * 32 : 0);
+};
+
+__device__ __forceinline__ bool d_wait_drain(uint32_t bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kDecodeDrainCycles) return false;
+  }
+  return true;
+}
+
+// Tile position: phase, group, weight block, token chunk.  Tiles are visited
+// in increasing order by each role, so the group only moves forward.
+struct DCursor {
+  int phase = 0, g = 0;
+  __device__ __forceinline__ void locate(int tile, int tiles0, const int32_t* tp0,
+                                         const int32_t* tp1, const int32_t* nch, int& wb,
+                                         int& tc) {
+    int local = tile;
+    if (tile >= tiles0) {
+      if (phase == 0) { phase = 1; g = 0; }
+      local = tile - tiles0;
+    }
+    const int32_t* tp = phase ? tp1 : tp0;
+    while (local >= tp[g + 1]) ++g;
+    const int lg = local - tp[g];
+    const int c = nch[g];
+    wb = lg / c;
+    tc = lg - wb * c;
+  }
+};
+
+}  // namespace
+
+// Per-group view of one tile's operands and outputs (routed expert g < G,
+// or the shared expert g == G).
+struct DTileView {
+  bool shared;
+  int rows;       // token rows of the group
+  int row0;       // first activation / output row of the chunk
+  int n_valid;    // token rows in this chunk
+  int n_out;      // output columns of the phase (F, Fs or H)
+  int K;          // reduction length of the phase
+  int w_row;      // first weight row of the tile (gate rows for SwiGLU)
+  int w_row_up;   // SwiGLU phase 0: first up row
+};
+
+__device__ __forceinline__ DTileView d_view(const DecodeArgs& a, const int32_t* seg, int phase,
+                                            int g, int wb, int tc, int nt) {
+  DTileView v;
+  v.shared = g == a.num_groups;
+  const int base = v.shared ? 0 : seg[g];
+  v.rows = v.shared ? a.shared_rows : seg[g + 1] - seg[g];
+  v.row0 = base + tc * nt;
+  v.n_valid = min(nt, v.rows - tc * nt);
+  const bool glu = phase == 0 && a.mode0 == EPI_SWIGLU;
+  if (phase == 0) {
+    v.n_out = v.shared ? a.Fs : a.F;
+    v.K = a.H;
+    const int wrows = glu ? 2 * v.n_out : v.n_out;   // weight rows of one expert
+    const int gbase = v.shared ? 0 : g * wrows;
+    v.w_row = gbase + wb * DM;
+    v.w_row_up = gbase + v.n_out + wb * DM;
+  } else {
+    v.n_out = a.H;
+    v.K = v.shared ? a.Fs : a.F;
+    v.w_row = (v.shared ? 0 : g * a.H) + wb * DM;
+    v.w_row_up = 0;
+  }
+  return v;
+}
+
+template <bool FP8>
+__global__ void __launch_bounds__(DShape<FP8>::THREADS, 1)
+    decode_ffn_kernel(const __grid_constant__ DecodeMaps maps, const DecodeArgs args) {
+  constexpr int THREADS = DShape<FP8>::THREADS;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) atomicExch(args.status, (int)MOE_ERR_UNSUPPORTED);
+    return;
+  }
+  const int NT = args.nt;
+  const bool glu = args.mode0 == EPI_SWIGLU;
+  const int STAGES = args.stages;
+  const int QST = args.q_stages;
+  const int a_stage = glu ? 2 * D_A_BYTES : D_A_BYTES;   // weight bytes per ring slot
+  const int b_stage = NT * DK * 2;                       // activation bytes per ring slot
+  const int acc_cols = glu ? 2 * NT : NT;
+  uint8_t* smem = smem_raw;
+  const uint32_t sA = smem_u32(smem);
+  const uint32_t sB = sA + STAGES * a_stage;
+  const uint32_t sQ = sB + STAGES * b_stage;                       // E4M3 slots (FP8)
+  const int q_bytes = FP8 ? QST * (glu ? 2 : 1) * D_Q_BYTES : 0;
+  uint16_t* tbuf = reinterpret_cast<uint16_t*>(smem + (sQ - sA) + q_bytes);  // [4][NT][32]
+  float* wv = reinterpret_cast<float*>(tbuf + D_EPI_WARPS * NT * 32);      // [4][NT]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(wv + D_EPI_WARPS * NT);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (D_MAX_STAGES + s); };
+  auto cfull_bar = [&](int s) { return bar0 + 8u * (2 * D_MAX_STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (3 * D_MAX_STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (3 * D_MAX_STAGES + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (3 * D_MAX_STAGES + 4);
+  auto qfull_bar = [&](int s) { return bar0 + 8u * (3 * D_MAX_STAGES + 5 + s); };
+  auto qempty_bar = [&](int s) { return bar0 + 8u * (3 * D_MAX_STAGES + 5 + D_Q_STAGES_MAX + s); };
+  constexpr int NUM_BARS = 3 * D_MAX_STAGES + 5 + 2 * D_Q_STAGES_MAX;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  uint32_t* stored_cnt = tmem_holder + 2;   // [2]
+  const int G = args.num_groups;
+  const int NG = G + (args.shared_rows > 0 ? 1 : 0);   // groups incl. the shared one
+  int32_t* seg = reinterpret_cast<int32_t*>(tmem_holder + 4);   // [G + 2]
+  int32_t* nch = seg + (G + 2);      // [G + 1] token chunks per group
+  int32_t* cpre = nch + (G + 1);     // [G + 2] first chunk counter of each group
+  int32_t* tp0 = cpre + (G + 2);     // [G + 2] phase-0 tile prefix
+  int32_t* tp1 = tp0 + (G + 2);      // [G + 2] phase-1 tile prefix
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int unit = blockIdx.x, units = gridDim.x;
+  int* status = args.status;
+
+  pdl_launch_dependents();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < D_MAX_STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+      mbar_init(cfull_bar(s), D_CONV_WARPS);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), D_EPI_WARPS);
+    }
+    mbar_init(drain_bar, 1);
+    for (int s = 0; s < D_Q_STAGES_MAX; ++s) {
+      mbar_init(qfull_bar(s), 1);
+      mbar_init(qempty_bar(s), D_CONV_WARPS);
+    }
+    *abort_flag = 0;
+    stored_cnt[0] = stored_cnt[1] = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&maps.wa0);
+    tma_prefetch_desc(&maps.wa1);
+    tma_prefetch_desc(&maps.xa0);
+    tma_prefetch_desc(&maps.xa1);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), args.tmem_cols);
+    tmem_relinquish();
+  }
+  pdl_wait();   // offsets, the token rows and the chunk counters come from earlier launches
+  for (int i = threadIdx.x; i <= G; i += THREADS) seg[i] = args.offsets ? args.offsets[i] : 0;
+  __syncthreads();
+  if (warp == 2) {
+    // per group: token chunks, and prefixes over the groups of the chunks
+    // and of both phases' tiles (one lane per run of groups, then a warp scan)
+    const int nwb0 = (args.F + DM - 1) / DM, nwb0s = (args.Fs + DM - 1) / DM;
+    const int nwb1 = (args.H + DM - 1) / DM;
+    const int per = (NG + 31) / 32;
+    const int g0 = lane * per;
+    int c_loc = 0, t0_loc = 0, t1_loc = 0;
+    for (int g = g0; g < g0 + per && g < NG; ++g) {
+      const int rows = g == G ? args.shared_rows : seg[g + 1] - seg[g];
+      const int c = rows > 0 ? (rows + NT - 1) / NT : 0;
+      nch[g] = c;
+      c_loc += c;
+      t0_loc += c * (g == G ? nwb0s : nwb0);
+      t1_loc += c * nwb1;
+    }
+    int ci = c_loc, ti0 = t0_loc, ti1 = t1_loc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int a = __shfl_up_sync(0xffffffffu, ci, o);
+      const int b = __shfl_up_sync(0xffffffffu, ti0, o);
+      const int c = __shfl_up_sync(0xffffffffu, ti1, o);
+      if (lane >= o) { ci += a; ti0 += b; ti1 += c; }
+    }
+    int rc = ci - c_loc, r0 = ti0 - t0_loc, r1 = ti1 - t1_loc;
+    for (int g = g0; g < g0 + per && g < NG; ++g) {
+      cpre[g] = rc;
+      tp0[g] = r0;
+      tp1[g] = r1;
+      rc += nch[g];
+      r0 += nch[g] * (g == G ? nwb0s : nwb0);
+      r1 += nch[g] * nwb1;
+    }
+    if (lane == 31) {
+      cpre[NG] = ci;
+      tp0[NG] = ti0;
+      tp1[NG] = ti1;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const int tiles0 = tp0[NG], total = tiles0 + tp1[NG];
+  const int nwb0 = (args.F + DM - 1) / DM, nwb0s = (args.Fs + DM - 1) / DM;
+  long long tma_issued = 0, q_issued = 0;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0 && !args.skip_producer) {
+      uint32_t stage = 0, phase = 0;
+      long long issued = 0;
+      bool ok = true;
+      DCursor cur;
+      int pend_stage[D_MAX_STAGES];
+      for (int tile = unit; tile < total && ok; tile += units) {
+        int wb, tc;
+        cur.locate(tile, tiles0, tp0, tp1, nch, wb, tc);
+        const int ph = cur.phase, g = cur.g;
+        const DTileView v = d_view(args, seg, ph, g, wb, tc, NT);
+        const CUtensorMap* mW = v.shared ? (ph ? &maps.ws1 : &maps.ws0) : (ph ? &maps.wa1 : &maps.wa0);
+        const CUtensorMap* mX = v.shared ? (ph ? &maps.xs1 : &maps.xs0) : (ph ? &maps.xa1 : &maps.xa0);
+        const bool tglu = glu && ph == 0;
+        const int nb = (v.n_valid + DBOX - 1) / DBOX;
+        const uint32_t tx = (FP8 ? 0u : (uint32_t)(tglu ? 2 : 1) * D_A_BYTES) +
+                            (uint32_t)nb * DBOX * DK * 2;
+        const int nkb = (v.K + DK - 1) / DK;
+        auto issue_w = [&](uint32_t st, int kb) {
+          if constexpr (!FP8) {
+            tma_load_2d(sA + st * a_stage, mW, full_bar(st), kb * DK, v.w_row);
+            if (tglu) tma_load_2d(sA + st * a_stage + D_A_BYTES, mW, full_bar(st), kb * DK, v.w_row_up);
+          }
+        };
+        auto issue_x = [&](uint32_t st, int kb) {
+          for (int b = 0; b < nb; ++b)
+            tma_load_2d(sB + st * b_stage + b * DBOX * DK * 2, mX, full_bar(st), kb * DK,
+                        v.row0 + b * DBOX);
+        };
+        int kb = 0;
+        if (ph == 1) {
+          // the Hid rows of this chunk come from phase-0 tiles: copy the
+          // first slots' weights now, then wait for the rows
+          const int target = v.shared ? nwb0s : nwb0;
+          const int* cnt = args.rows_done + cpre[g] + tc;
+          if (ld_acquire_gpu(cnt) < target) {
+            int pre = 0;
+            while (pre < nkb && pre < STAGES) {
+              if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, status)) { ok = false; break; }
+              mbar_arrive_expect_tx(full_bar(stage), tx);
+              issue_w(stage, pre);
+              pend_stage[pre] = (int)stage;
+              ++issued;
+              ++pre;
+              if (++stage == (uint32_t)STAGES) { stage = 0; phase ^= 1u; }
+            }
+            if (!ok) break;
+            const long long t0 = clock64();
+            while (ld_acquire_gpu(cnt) < target) {
+              if (*abort_flag) { ok = false; break; }
+              if (clock64() - t0 > kWaitLimitCycles) {
+                *abort_flag = 1;
+                atomicExch(status, (int)MOE_ERR_TIMEOUT);
+                ok = false;
+                break;
+              }
+            }
+            if (!ok) break;
+            fence_proxy_async_global();
+            for (int j = 0; j < pre; ++j) issue_x((uint32_t)pend_stage[j], j);
+            kb = pre;
+          } else {
+            fence_proxy_async_global();
+          }
+        }
+        for (; kb < nkb; ++kb) {
+          if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, status)) { ok = false; break; }
+          mbar_arrive_expect_tx(full_bar(stage), tx);
+          issue_w(stage, kb);
+          issue_x(stage, kb);
+          ++issued;
+          if (++stage == (uint32_t)STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      tma_issued = issued;
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      DCursor cur;
+      for (int tile = unit; tile < total && ok; tile += units) {
+        int wb, tc;
+        cur.locate(tile, tiles0, tp0, tp1, nch, wb, tc);
+        const DTileView v = d_view(args, seg, cur.phase, cur.g, wb, tc, NT);
+        const bool tglu = glu && cur.phase == 0;
+        const int n16 = (v.n_valid + 15) / 16 * 16;
+        const uint32_t idesc = idesc_bf16_f32(DM, n16);
+        const int nkb = (v.K + DK - 1) / DK;
+        if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * acc_cols;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, status)) { ok = false; break; }
+          if constexpr (FP8) {
+            if (!mbar_wait_bounded(cfull_bar(stage), phase, abort_flag, status)) { ok = false; break; }
+          }
+          tc_fence_after();
+          const uint64_t adesc = sdesc_kmajor_sw128(sA + stage * a_stage);
+          const uint64_t bdesc = sdesc_kmajor_sw128(sB + stage * b_stage);
+#pragma unroll
+          for (int kk = 0; kk < DK / 16; ++kk) {
+            const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
+            umma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, accum);
+            if (tglu) {
+              const uint64_t udesc = sdesc_kmajor_sw128(sA + stage * a_stage + D_A_BYTES);
+              umma_bf16(d_tmem + NT, udesc + 2 * kk, bdesc + 2 * kk, idesc, accum);
+            }
+          }
+          umma_commit(empty_bar(stage));
+          if (++stage == (uint32_t)STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        umma_commit(tfull_bar(acc));
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+    }
+    __syncwarp();
+  } else if (FP8 && warp >= 2 + D_EPI_WARPS) {
+    // ------------------------------------------------------------ E4M3 -> bf16
+    // The converter warps copy the E4M3 weight rows themselves (lane 0 of
+    // the first one issues the copies, QST slots of two k-blocks ahead) and
+    // widen each k-block's [128][64] codes (gate and up: [256][64]) into the
+    // bf16 weight tile of the ring slot the MMA reads.
+    const int cw = warp - (2 + D_EPI_WARPS);
+    const bool issuer = cw == 0 && lane == 0;
+    const int qslot = (glu ? 2 : 1) * D_Q_BYTES;
+    DCursor lcur;
+    int l_tile = unit, l_kq = 0, l_nkq = 0, l_row = 0, l_row_up = 0;
+    bool l_glu = false, l_shared = false;
+    int l_ph = 0;
+    auto l_locate = [&]() {
+      int wb, tc;
+      lcur.locate(l_tile, tiles0, tp0, tp1, nch, wb, tc);
+      l_ph = lcur.phase;
+      const DTileView v = d_view(args, seg, l_ph, lcur.g, wb, tc, NT);
+      l_nkq = ((v.K + DK - 1) / DK + 1) / 2;
+      l_row = v.w_row;
+      l_row_up = v.w_row_up;
+      l_glu = glu && l_ph == 0;
+      l_shared = v.shared;
+    };
+    auto issue = [&](int slot) {
+      const uint32_t dq = sQ + slot * qslot;
+      const CUtensorMap* m = l_shared ? (l_ph ? &maps.ws1 : &maps.ws0) : (l_ph ? &maps.wa1 : &maps.wa0);
+      mbar_arrive_expect_tx(qfull_bar(slot), (uint32_t)(l_glu ? 2 : 1) * D_Q_BYTES);
+      tma_load_2d(dq, m, qfull_bar(slot), l_kq * 2 * DK, l_row);
+      if (l_glu) tma_load_2d(dq + D_Q_BYTES, m, qfull_bar(slot), l_kq * 2 * DK, l_row_up);
+      ++q_issued;
+      if (++l_kq == l_nkq) {
+        l_kq = 0;
+        l_tile += units;
+        if (l_tile < total) l_locate();
+      }
+    };
+    if (issuer && l_tile < total) {
+      l_locate();
+      for (int s2 = 0; s2 < QST && l_tile < total; ++s2) issue(s2);
+    }
+    uint32_t qs = 0, qph = 0, stage = 0, phase = 0;
+    bool ok = true;
+    DCursor cur;
+    for (int tile = unit; tile < total && ok; tile += units) {
+      int wb, tc;
+      cur.locate(tile, tiles0, tp0, tp1, nch, wb, tc);
+      const DTileView v = d_view(args, seg, cur.phase, cur.g, wb, tc, NT);
+      const bool tglu = glu && cur.phase == 0;
+      const int nkb = (v.K + DK - 1) / DK;
+      for (int kb = 0; kb < nkb; ++kb) {
+        bool got = (kb & 1) ? true : mbar_wait_bounded(qfull_bar(qs), qph, abort_flag, status);
+        if (got) got = mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, status);
+        if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+        const int h4 = (kb & 1) * 4;   // first 16-byte chunk of this k-block in a code row
+        for (int half = 0; half < (tglu ? 2 : 1); ++half) {
+          const uint8_t* q = smem + (sQ - sA) + qs * qslot + half * D_Q_BYTES;
+          uint8_t* b = smem + stage * a_stage + half * D_A_BYTES;
+#pragma unroll 2
+          for (int g8 = cw; g8 < DM / 8; g8 += D_CONV_WARPS) widen_e4m3_rows8(q, b, g8, h4, lane);
+        }
+        fence_proxy_async_shared();   // the tensor cores read what the threads wrote
+        __syncwarp();
+        const bool slot_done = (kb & 1) || kb == nkb - 1;
+        if (lane == 0) {
+          if (slot_done) mbar_arrive(qempty_bar(qs));
+          mbar_arrive(cfull_bar(stage));
+        }
+        if (++stage == (uint32_t)STAGES) { stage = 0; phase ^= 1u; }
+        if (!slot_done) continue;
+        if (cw == 0) {
+          int refill_ok = 1;
+          if (issuer && l_tile < total) {
+            if (mbar_wait_bounded(qempty_bar(qs), qph, abort_flag, status)) issue((int)qs);
+            else refill_ok = 0;
+          }
+          if (!__shfl_sync(0xffffffffu, refill_ok, 0)) { ok = false; break; }
+        }
+        if (++qs == (uint32_t)QST) { qs = 0; qph ^= 1u; }
+      }
+    }
+  } else if (warp >= 2 && warp < 2 + D_EPI_WARPS) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;                       // TMEM lane quarter
+    const int ew = warp - 2;
+    const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+    uint16_t* tb = tbuf + ew * NT * 32;            // [NT][32] bf16: this warp's rows, transposed
+    float* wj = wv + ew * NT;                      // [NT] gate weight of each token column
+    uint32_t acc = 0, acc_phase = 0;
+    DCursor cur;
+    for (int tile = unit; tile < total; tile += units) {
+      int wb, tc;
+      cur.locate(tile, tiles0, tp0, tp1, nch, wb, tc);
+      const int ph = cur.phase, g = cur.g;
+      const DTileView v = d_view(args, seg, ph, g, wb, tc, NT);
+      const bool tglu = glu && ph == 0;
+      const int mode = ph ? EPI_SCALE : args.mode0;
+      const int col = wb * DM + q * 32 + lane;     // output column of this thread's weight row
+      const bool col_ok = col < v.n_out;
+      // per-row constants: bias and (E4M3) row scale of the gate / plain row and the up row
+      const __nv_bfloat16* bias = v.shared ? (ph ? args.b2s : args.b1s) : (ph ? args.b2 : args.b1);
+      const float* scale = v.shared ? (ph ? args.s2s : args.s1s) : (ph ? args.s2 : args.s1);
+      const int wrows = tglu ? 2 * v.n_out : v.n_out;
+      const int64_t rbase = v.shared ? 0 : (int64_t)g * wrows;
+      float bz = 0.0f, bu = 0.0f, sz = 1.0f, su = 1.0f;
+      if (col_ok) {
+        if (bias) {
+          bz = __bfloat162float(bias[rbase + col]);
+          if (tglu) bu = __bfloat162float(bias[rbase + v.n_out + col]);
+        }
+        if (FP8 && scale) {
+          sz = scale[rbase + col];
+          if (tglu) su = scale[rbase + v.n_out + col];
+        }
+      }
+      if (ph == 1) {
+        for (int j = lane; j < v.n_valid; j += 32)
+          wj[j] = (v.shared || args.topk_w == nullptr) ? 1.0f : args.topk_w[args.perm[v.row0 + j]];
+        __syncwarp();
+      }
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, status) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + lane_addr + acc * acc_cols;
+      const int n16 = (v.n_valid + 15) / 16 * 16;
+      for (int c = 0; c < n16; c += 16) {
+        uint32_t r[16], ru[16];
+        tmem_ld_32x32b_x16(taddr + c, r);
+        if (tglu) tmem_ld_32x32b_x16(taddr + NT + c, ru);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int j = c + i;
+          float z = __uint_as_float(r[i]) * sz + bz;
+          float o;
+          if (mode == EPI_GELU) o = gelu_erf(z);
+          else if (mode == EPI_SILU) o = silu_f(z);
+          else if (mode == EPI_SWIGLU) o = silu_f(z) * (__uint_as_float(ru[i]) * su + bu);
+          else o = (j < v.n_valid ? wj[j] : 0.0f) * z;
+          if (j < v.n_valid) tb[j * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+        }
+      }
+      __syncwarp();
+      // rows of the chunk: 32 consecutive output columns each, 16-byte stores
+      __nv_bfloat16* out = v.shared ? (ph ? args.out1s : args.out0s) : (ph ? args.out1 : args.out0);
+      const int ld = v.n_out;
+      const int col0 = wb * DM + q * 32;
+      for (int i = lane; i < v.n_valid * 4; i += 32) {
+        const int j = i >> 2, c8 = (i & 3) * 8;
+        if (col0 + c8 < v.n_out) {
+          const uint4 val = *reinterpret_cast<const uint4*>(tb + j * 32 + c8);
+          *reinterpret_cast<uint4*>(out + (int64_t)(v.row0 + j) * ld + col0 + c8) = val;
+        }
+      }
+      __syncwarp();
+      if (ph == 0) {
+        // the last epilogue warp of the tile releases the chunk's counter
+        if (lane == 0 && atom_add_acqrel_cta(&stored_cnt[acc], 1u) == D_EPI_WARPS - 1) {
+          stored_cnt[acc] = 0u;
+          fence_proxy_async_global();
+          red_release_gpu_add(args.rows_done + cpre[g] + tc, 1);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(acc));
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  // ---- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {
+    if (warp == 0 && lane == 0) {
+      const long long first = tma_issued > STAGES ? tma_issued - STAGES : 0;
+      for (long long j = first; j < tma_issued; ++j)
+        d_wait_drain(full_bar((int)(j % STAGES)), (uint32_t)((j / STAGES) & 1));
+    }
+    if (FP8 && warp == 2 + D_EPI_WARPS && lane == 0) {
+      const long long first = q_issued > QST ? q_issued - QST : 0;
+      for (long long j = first; j < q_issued; ++j)
+        d_wait_drain(qfull_bar((int)(j % QST)), (uint32_t)((j / QST) & 1));
+    }
+    if (warp == 1 && lane == 0) {
+      umma_commit(drain_bar);
+      d_wait_drain(drain_bar, 0);
+    }
+    __syncwarp();
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, args.tmem_cols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+
+namespace {
+
+bool encode_e4m3(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int box_rows) {
+  return encode_tensor_map_u8(map, base, rows, K, 2 * DK, box_rows);
+}
+
+}  // namespace
+
+int decode_token_tile(int64_t group_rows_max) {
+  int64_t nt = (group_rows_max + 15) / 16 * 16;
+  if (nt < 16) nt = 16;
+  if (nt > 128) nt = 128;
+  return (int)nt;
+}
+
+cudaError_t make_decode_plan(DecodePlan* plan, const DecodeArgs& args_in, const DecodeTensors& t,
+                             bool fp8, int64_t group_rows_max, int num_sms) {
+  DecodeArgs a = args_in;
+  const bool glu = a.mode0 == EPI_SWIGLU;
+  a.nt = decode_token_tile(group_rows_max);
+  const int NT = a.nt;
+  const int acc_cols = glu ? 2 * NT : NT;
+  int cols = 32;
+  while (cols < 2 * acc_cols) cols <<= 1;
+  if (cols > 512) return cudaErrorInvalidValue;
+  a.tmem_cols = cols;
+  const bool has_routed = t.R > 0;
+  const bool has_shared = a.shared_rows > 0;
+  if (!has_routed && !has_shared) return cudaErrorInvalidValue;
+  const int w1r = glu ? 2 * a.F : a.F, w1rs = glu ? 2 * a.Fs : a.Fs;
+  DecodeMaps& m = plan->maps;
+  auto wmap = [&](CUtensorMap* mp, const void* base, int64_t rows, int64_t K) {
+    return fp8 ? encode_e4m3(mp, base, rows, K, DM) : encode_tensor_map_bf16(mp, base, rows, K, DK, DM);
+  };
+  auto xmap = [&](CUtensorMap* mp, const void* base, int64_t rows, int64_t K) {
+    return encode_tensor_map_bf16(mp, base, rows, K, DK, DBOX);
+  };
+  bool ok = true;
+  if (has_routed) {
+    ok = ok && wmap(&m.wa0, t.W1, (int64_t)a.num_groups * w1r, a.H);
+    ok = ok && wmap(&m.wa1, t.W2, (int64_t)a.num_groups * a.H, a.F);
+    ok = ok && xmap(&m.xa0, t.xp, t.R, a.H);
+    ok = ok && xmap(&m.xa1, t.hid, t.R, a.F);
+  }
+  if (has_shared) {
+    ok = ok && wmap(&m.ws0, t.W1s, w1rs, a.H);
+    ok = ok && wmap(&m.ws1, t.W2s, a.H, a.Fs);
+    ok = ok && xmap(&m.xs0, t.x, a.shared_rows, a.H);
+    ok = ok && xmap(&m.xs1, t.hid_s, a.shared_rows, a.Fs);
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  if (!has_routed) { m.wa0 = m.ws0; m.wa1 = m.ws1; m.xa0 = m.xs0; m.xa1 = m.xs1; }
+  if (!has_shared) { m.ws0 = m.wa0; m.ws1 = m.wa1; m.xs0 = m.xa0; m.xs1 = m.xa1; }
+  // shared memory: ring slots (weights + activations), E4M3 slots, the
+  // epilogue's transpose buffers and gate weights, barriers, group tables
+  const int a_stage = glu ? 2 * D_A_BYTES : D_A_BYTES;
+  const int b_stage = NT * DK * 2;
+  const int q_stages = fp8 ? (glu ? 2 : 3) : 0;
+  const int q_bytes = q_stages * (glu ? 2 : 1) * D_Q_BYTES;
+  const int G = a.num_groups;
+  const int fixed = D_EPI_WARPS * NT * 32 * 2 + D_EPI_WARPS * NT * 4 +
+                    (3 * D_MAX_STAGES + 5 + 2 * D_Q_STAGES_MAX) * 8 + 16 + 5 * (G + 2) * 4;
+  const int budget = 232448 - 1024;
+  int stages = (budget - fixed - q_bytes) / (a_stage + b_stage);
+  if (stages > D_MAX_STAGES) stages = D_MAX_STAGES;
+  if (stages < 2) return cudaErrorInvalidValue;
+  a.stages = stages;
+  a.q_stages = q_stages;
+  plan->smem = stages * (a_stage + b_stage) + q_bytes + fixed;
+  plan->args = a;
+  plan->fp8 = fp8;
+  plan->grid = num_sms;
+  return cudaSuccess;
+}
+
+template <bool FP8>
+static cudaError_t launch_decode_t(const DecodePlan& plan, cudaStream_t st) {
+  using S = DShape<FP8>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(decode_ffn_kernel<FP8>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(plan.grid);
+  cfg.blockDim = dim3(S::THREADS);
+  cfg.dynamicSmemBytes = plan.smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_wait()
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // phase-1 tiles wait for phase-0 tiles of other CTAs: every CTA must be
+  // resident at once (one per SM with this much shared memory)
+  int per_sm = 0, dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_ffn_kernel<FP8>, S::THREADS,
+                                                    plan.smem) != cudaSuccess ||
+      per_sm < 1)
+    return cudaErrorInvalidConfiguration;
+  if ((int)cfg.gridDim.x > sms * per_sm) cfg.gridDim.x = sms * per_sm;
+  return cudaLaunchKernelEx(&cfg, decode_ffn_kernel<FP8>, plan.maps, plan.args);
+}
+
+cudaError_t launch_decode(const DecodePlan& plan, cudaStream_t st, LaunchTrace* tr) {
+  trace_mark(tr, st);
+  cudaError_t e = plan.fp8 ? launch_decode_t<true>(plan, st) : launch_decode_t<false>(plan, st);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace moe

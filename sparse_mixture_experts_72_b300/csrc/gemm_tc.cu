@@ -841,8 +841,8 @@ bool encode_tensor_map_bf16(CUtensorMap* map, const void* base, int64_t rows, in
 
 // E4M3 codes [rows, K] (K bytes per row), boxes of 128 codes a row in the
 // 128-byte swizzled layout; the converter warps write the bf16 tile.
-static bool encode_tensor_map_e4m3(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
-                                   int box_cols, int box_rows) {
+bool encode_tensor_map_u8(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
+                          int box_cols, int box_rows) {
   EncodeTiledFn enc = get_encoder();
   if (!enc) return false;
   cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
@@ -884,7 +884,7 @@ cudaError_t make_gemm_plan(GemmPlan* plan, const GemmArgs& args_in, const __nv_b
       return cudaErrorInvalidValue;
     // SwiGLU tiles load 128 gate and 128 up rows: two 128-row boxes
     const int box_b = args.ph[p].mode == EPI_SWIGLU ? BN / 2 : BN / pair;
-    const bool ok = fp8 ? encode_tensor_map_e4m3(&plan->tmB[p], B[p], b_rows[p], args.ph[p].K,
+    const bool ok = fp8 ? encode_tensor_map_u8(&plan->tmB[p], B[p], b_rows[p], args.ph[p].K,
                                                  2 * BK, box_b)
                         : encode_tensor_map_bf16(&plan->tmB[p], B[p], b_rows[p], args.ph[p].K,
                                                  BK, box_b);

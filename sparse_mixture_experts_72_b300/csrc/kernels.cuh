@@ -234,5 +234,57 @@ cudaError_t make_gemm_plan(GemmPlan* plan, const GemmArgs& args, const __nv_bflo
                            bool fp8, int64_t group_rows_max, int num_sms);
 cudaError_t launch_gemm(const GemmPlan& plan, cudaStream_t st, LaunchTrace* tr);
 bool tensor_map_encoder_available();
+// TMA map of a row-major byte matrix [rows, K] (E4M3 codes), 128B swizzle
+bool encode_tensor_map_u8(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
+                          int box_cols, int box_rows);
+
+// ---------------------------------------------------------------- decode expert FFN
+// The expert FFN with the operands swapped (weights as the 128-row MMA
+// operand, an expert's few token rows as N), routed experts and the shared
+// expert in one launch.  For batches whose experts hold few rows.
+struct DecodeMaps {
+  CUtensorMap wa0, wa1;   // routed weights: W1 [G * w1_rows, H], W2 [G * H, F]
+  CUtensorMap ws0, ws1;   // shared weights: W1s [w1_rows_s, H], W2s [H, Fs]
+  CUtensorMap xa0, xa1;   // routed activations: X_perm [R, H], Hid [R, F] (boxes of 16 rows)
+  CUtensorMap xs0, xs1;   // shared activations: x [T, H], Hid_s [T, Fs]
+};
+struct DecodeArgs {
+  const int32_t* offsets;        // [G + 1] row segments of the routed experts
+  int32_t num_groups;            // G
+  int32_t shared_rows;           // T with a shared expert, else 0
+  int32_t H, F, Fs;              // hidden, routed and shared inner sizes (output columns of phase 0)
+  int32_t mode0;                 // EPI_GELU / EPI_SILU / EPI_SWIGLU (phase 1 is EPI_SCALE)
+  const __nv_bfloat16 *b1, *b2, *b1s, *b2s;   // biases or nullptr
+  const float *s1, *s2, *s1s, *s2s;           // E4M3 row scales (nullptr for bf16 weights)
+  __nv_bfloat16 *out0, *out1, *out0s, *out1s; // Hid, y, Hid_s, y_s
+  const float* topk_w;           // routed rows' gate weights (through perm)
+  const int32_t* perm;
+  int32_t* rows_done;            // per token chunk: phase-0 tiles stored (zeroed before the launch)
+  int* status;
+  int32_t skip_producer;         // failure injection: the TMA producer issues nothing
+  // set by make_decode_plan
+  int32_t nt, stages, q_stages, tmem_cols;
+};
+struct DecodeTensors {
+  const void *W1, *W2, *W1s, *W2s;            // weights (bf16 or E4M3 codes)
+  const __nv_bfloat16* xp;                    // [R, H] permuted token rows
+  const __nv_bfloat16* hid;                   // [R, F]
+  int64_t R;                                  // rows of xp / hid (0: no routed rows)
+  const __nv_bfloat16* x;                     // [T, H]
+  const __nv_bfloat16* hid_s;                 // [T, Fs]
+};
+struct DecodePlan {
+  DecodeMaps maps;
+  DecodeArgs args;
+  int grid, smem;
+  bool fp8;
+};
+// token rows per tile for groups of at most group_rows_max rows (16..128)
+int decode_token_tile(int64_t group_rows_max);
+// Upper bound of the token chunks (phase-1 counters) of a decode launch.
+inline int64_t decode_rows_done_len(int64_t R, int G, int64_t T) { return (R + 15) / 16 + G + (T + 15) / 16 + 1; }
+cudaError_t make_decode_plan(DecodePlan* plan, const DecodeArgs& args, const DecodeTensors& t,
+                             bool fp8, int64_t group_rows_max, int num_sms);
+cudaError_t launch_decode(const DecodePlan& plan, cudaStream_t st, LaunchTrace* tr);
 
 }  // namespace moe

@@ -54,6 +54,22 @@ int64_t max_rows_of(const moe_config_t& c) {
 // Rows of W1 per expert: F, or 2F (gate and up) for SwiGLU.
 int64_t w1_rows(const moe_config_t& c, int64_t F) { return c.activation == MOE_ACT_SWIGLU ? 2 * F : F; }
 
+// Rows one expert can hold: its capacity, at most one per token.
+int64_t group_rows_max(const moe_config_t& c) {
+  const int64_t cap = capacity_of(c);
+  return expert_choice(c) ? ec_tokens(c) : (cap >= 0 && cap < c.T ? cap : (int64_t)c.T);
+}
+
+// The expert FFN runs with the operands swapped (decode_tc.cu: weights as
+// the MMA's 128-row operand, routed and shared experts in one launch) when
+// the experts hold few rows on average: a 128-row token tile would then be
+// mostly padding.
+constexpr int64_t kDecodeAvgRows = 64;
+bool decode_ffn(const moe_config_t& c) {
+  if (c.T == 0) return false;
+  return max_rows_of(c) <= kDecodeAvgRows * c.N;
+}
+
 struct WsLayout {
   size_t status, status_bytes, rows_done, rows_done_s, w3, logits, p_part, local_rank, blk_hist,
       blk_base;
@@ -73,8 +89,12 @@ WsLayout layout_of(const moe_config_t& c) {
   // The header every call zeroes first: [0] status word, [1] router ticket,
   // [2] permute ticket, then the row-block counters of the routed and the shared expert FFN
   // launches (phase 0 -> phase 1 hand-over).
-  const int64_t nrd = R > 0 ? gemm_rows_done_len(R, (int)N) : 0;
+  int64_t nrd = R > 0 ? gemm_rows_done_len(R, (int)N) : 0;
   const int64_t nrd_s = (c.F_shared > 0 && T > 0) ? gemm_rows_done_len(T, 1) : 0;
+  if (T > 0 && decode_ffn(c)) {
+    const int64_t nd = decode_rows_done_len(R, (int)N, c.F_shared > 0 ? T : 0);
+    if (nd > nrd) nrd = nd;
+  }
   L.status_bytes = align_up(sizeof(int32_t) * (4 + nrd + nrd_s));
   L.status = take(L.status_bytes);
   L.rows_done = L.status + 16;
@@ -319,6 +339,55 @@ moe_status_t do_ffn(const moe_config_t& c, const uint16_t* x, const int32_t* per
   const int32_t act_mode = c.activation == MOE_ACT_SWIGLU ? EPI_SWIGLU
                            : c.activation == MOE_ACT_SILU ? EPI_SILU
                                                           : EPI_GELU;
+  if (decode_ffn(c) && (R > 0 || (c.F_shared > 0 && c.T > 0))) {
+    // routed and shared experts in one operand-swapped launch
+    bf* xp = at<bf>(ws, L.xp);
+    if (!gathered && R > 0)
+      MOE_CUDA(launch_gather(reinterpret_cast<const bf*>(x), perm, offsets, c.N, slots_of(c), R,
+                             c.H, xp, st, tr));
+    const bool sh = c.F_shared > 0;
+    DecodeArgs a{};
+    a.offsets = offsets;
+    a.num_groups = c.N;
+    a.shared_rows = sh ? c.T : 0;
+    a.H = c.H;
+    a.F = c.F;
+    a.Fs = sh ? c.F_shared : 0;
+    a.mode0 = act_mode;
+    a.b1 = reinterpret_cast<const bf*>(W.b1);
+    a.b2 = reinterpret_cast<const bf*>(W.b2);
+    a.b1s = reinterpret_cast<const bf*>(W.b1s);
+    a.b2s = reinterpret_cast<const bf*>(W.b2s);
+    if (fp8) {
+      a.s1 = W.s1;
+      a.s2 = W.s2;
+      a.s1s = W.s1s;
+      a.s2s = W.s2s;
+    }
+    a.out0 = at<bf>(ws, L.hid);
+    a.out1 = reinterpret_cast<bf*>(y);
+    a.out0s = sh ? at<bf>(ws, L.hid_s) : nullptr;
+    a.out1s = reinterpret_cast<bf*>(y_shared);
+    a.topk_w = topk_w;
+    a.perm = perm;
+    a.rows_done = at<int32_t>(ws, L.rows_done);
+    a.status = status;
+    a.skip_producer = take_suppress_producer();
+    DecodeTensors t{};
+    t.W1 = W.W1;
+    t.W2 = W.W2;
+    t.W1s = W.W1s;
+    t.W2s = W.W2s;
+    t.xp = xp;
+    t.hid = at<bf>(ws, L.hid);
+    t.R = R;
+    t.x = reinterpret_cast<const bf*>(x);
+    t.hid_s = sh ? at<bf>(ws, L.hid_s) : nullptr;
+    DecodePlan p;
+    MOE_CUDA(make_decode_plan(&p, a, t, fp8, group_rows_max(c), sms));
+    MOE_CUDA(launch_decode(p, st, tr));
+    return MOE_OK;
+  }
   if (R > 0) {
     bf* xp = at<bf>(ws, L.xp);
     bf* hid = at<bf>(ws, L.hid);
@@ -355,10 +424,7 @@ moe_status_t do_ffn(const moe_config_t& c, const uint16_t* x, const int32_t* per
     const void* B[2] = {W.W1, W.W2};
     const int64_t b_rows[2] = {(int64_t)c.N * w1_rows(c, c.F), (int64_t)c.N * c.H};
     GemmPlan p;
-    // rows one expert can hold: its capacity, at most one per token
-    const int64_t cap = capacity_of(c);
-    const int64_t group_max = expert_choice(c) ? ec_tokens(c) : (cap >= 0 && cap < c.T ? cap : c.T);
-    MOE_CUDA(make_gemm_plan(&p, g, xp, R, B, b_rows, fp8, group_max, sms));
+    MOE_CUDA(make_gemm_plan(&p, g, xp, R, B, b_rows, fp8, group_rows_max(c), sms));
     MOE_CUDA(launch_gemm(p, st, tr));
   }
   if (c.F_shared > 0 && c.T > 0) {
@@ -397,9 +463,46 @@ moe_status_t do_ffn(const moe_config_t& c, const uint16_t* x, const int32_t* per
 }
 
 int ffn_num_launches(const moe_config_t& c, bool gathered) {
+  const bool rows = max_rows_of(c) > 0, sh = c.F_shared > 0 && c.T > 0;
+  if (decode_ffn(c)) return (rows && !gathered ? 1 : 0) + (rows || sh ? 1 : 0);
   int n = 0;
-  if (max_rows_of(c) > 0) n += gathered ? 1 : 2;
-  if (c.F_shared > 0 && c.T > 0) n += 1;
+  if (rows) n += gathered ? 1 : 2;
+  if (sh) n += 1;
+  return n;
+}
+
+// Names of the launches moe_forward makes, in order (moe_forward_launch_name).
+int forward_launch_names(const moe_config_t& c, const char** names, int cap) {
+  int n = 0;
+  auto add = [&](const char* s) {
+    if (n < cap) names[n] = s;
+    ++n;
+  };
+  const bool tc = c.N <= kRouterTcMaxExperts;
+  if (!router_clears_status(c)) add("status_memset");
+  if (c.T == 0) add("router_pmean");
+  else if (tc) { add("router_split"); add("router_tc"); }
+  else { add("router_logits"); add("router_select"); add("router_pmean"); }
+  const bool rows = max_rows_of(c) > 0, sh = c.F_shared > 0 && c.T > 0;
+  bool gathered = true;
+  if (expert_choice(c)) {
+    add("expert_choice");
+    gathered = false;
+  } else if ((int64_t)c.T * c.k > 0) {
+    add("permute_rank_scan");
+    add("scatter_gather");
+  } else {
+    add("permute_scan");
+  }
+  if (decode_ffn(c)) {
+    if (rows && !gathered) add("gather_rows");
+    if (rows || sh) add("expert_ffn_decode");
+  } else {
+    if (rows && !gathered) add("gather_rows");
+    if (rows) add("expert_ffn");
+    if (sh) add("shared_ffn");
+  }
+  if (c.T > 0) add("combine");
   return n;
 }
 
@@ -458,6 +561,13 @@ MOE_API int32_t moe_forward_num_launches(const moe_config_t* cfg) {
   }
   if (c.T > 0) n += 1;  // combine
   return n;
+}
+
+MOE_API const char* moe_forward_launch_name(const moe_config_t* cfg, int32_t i) {
+  if (check_config(cfg) != MOE_OK || i < 0) return nullptr;
+  const char* names[MOE_TRACE_MAX_EVENTS];
+  const int n = forward_launch_names(*cfg, names, MOE_TRACE_MAX_EVENTS);
+  return i < n && i < MOE_TRACE_MAX_EVENTS ? names[i] : nullptr;
 }
 
 MOE_API moe_status_t moe_route(const moe_config_t* cfg, const uint16_t* x, const float* Wg,

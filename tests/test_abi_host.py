@@ -85,17 +85,42 @@ def test_host_shape_functions(lib):
         assert lib.moe_workspace_size(C.byref(_cfg(**bad))) > 0, bad
 
 
-def test_launch_count_matches_bench_names(lib):
-    import bench
+def _wcfg(w):
+    from sparse_mixture_experts_72_b300 import _lib
+    return _cfg(T=w.T, H=w.H, F=w.F, N=w.N, k=w.k, capacity_factor=w.capacity_factor,
+                F_shared=w.F_shared, routing=_lib.ROUTING[w.routing],
+                activation=_lib.ACTIVATION[w.activation], min_capacity=w.min_capacity,
+                drop_order=_lib.DROP_ORDER[w.drop_order],
+                weight_dtype=_lib.WEIGHT_DTYPE[w.weight_dtype])
+
+
+def test_launch_names_cover_every_launch(lib):
+    """One name per launch moe_forward enqueues; the expert FFN runs as the
+    operand-swapped decode launch (shared expert included) exactly when the
+    experts hold at most 64 rows on average."""
     import moe_workloads as wl
     for w in list(wl.WORKLOADS.values()) + list(wl.TEST_WORKLOADS.values()):
-        from sparse_mixture_experts_72_b300 import _lib
-        c = _cfg(T=w.T, H=w.H, F=w.F, N=w.N, k=w.k, capacity_factor=w.capacity_factor,
-                 F_shared=w.F_shared, routing=_lib.ROUTING[w.routing],
-                 activation=_lib.ACTIVATION[w.activation], min_capacity=w.min_capacity,
-                 drop_order=_lib.DROP_ORDER[w.drop_order])
+        c = _wcfg(w)
         n = lib.moe_forward_num_launches(C.byref(c))
-        assert n == len(bench.launch_names(w, lib.moe_max_rows(C.byref(c)) > 0)), w.name
+        names = [lib.moe_forward_launch_name(C.byref(c), i) for i in range(n + 1)]
+        assert all(isinstance(x, bytes) for x in names[:n]) and names[n] is None, w.name
+        names = [x.decode() for x in names[:n]]
+        R = lib.moe_max_rows(C.byref(c))
+        decode = R <= 64 * w.N
+        assert ("expert_ffn_decode" in names) == (decode and (R > 0 or w.F_shared > 0)), w.name
+        assert ("shared_ffn" in names) == (w.F_shared > 0 and not decode), w.name
+        assert names[-1] == "combine", w.name
+    for name in ("mixtral_decode", "deepseek_decode", "mixtral_decode_fp8", "tiny"):
+        c = _wcfg(wl.get_workload(name))
+        n = lib.moe_forward_num_launches(C.byref(c))
+        assert b"expert_ffn_decode" in [lib.moe_forward_launch_name(C.byref(c), i)
+                                        for i in range(n)], name
+    for name in ("moelayer", "mixtral_prefill", "deepseek_prefill", "switch_capacity"):
+        c = _wcfg(wl.get_workload(name))
+        n = lib.moe_forward_num_launches(C.byref(c))
+        assert b"expert_ffn" in [lib.moe_forward_launch_name(C.byref(c), i)
+                                 for i in range(n)], name
+    assert lib.moe_forward_launch_name(C.byref(_cfg()), -1) is None
 
 
 FAKE = 0x10000  # 16-byte aligned, never dereferenced: every check fails before a device call

@@ -234,13 +234,16 @@ def test_widened_launch_counts_and_trace(_lib):
 
 
 def test_fp8_group_above_bound_is_reported(_lib):
-    """FP8 launches of decode-sized batches copy at most the rows one expert
-    can hold (here T = 40, so 48); offsets that give an expert 80 rows (more
-    than a token-choice dispatch can) must be reported in the status word,
-    not computed silently.  A dispatch within the bound leaves the word 0."""
+    """FP8 launches of the token-row kernel with groups below 128 rows copy at
+    most the rows one expert can hold (here T = 100, so 112); offsets that
+    give an expert 200 rows (more than a token-choice dispatch can) must be
+    reported in the status word, not computed silently.  A dispatch within
+    the bound leaves the word 0.  (100 rows per expert on average: not the
+    operand-swapped decode kernel, which takes any row count.)"""
     m = _lib
-    T, H, F = 40, 64, 64
+    T, H, F = 100, 64, 64
     cfg = m.MoEConfig(T=T, H=H, F=F, N=2, k=2, weight_dtype="e4m3")
+    assert "expert_ffn" in m.moe_forward_launch_names(cfg)
     dev = "cuda"
     g = torch.Generator().manual_seed(3)
     codes = lambda *s: torch.randint(0, 0x7E, s, generator=g, dtype=torch.uint8).to(dev)
@@ -257,3 +260,46 @@ def test_fp8_group_above_bound_is_reported(_lib):
     bad_offsets = torch.tensor([0, 2 * T, 2 * T], dtype=torch.int32, device=dev)
     m.moe_expert_ffn(cfg, x, perm, bad_offsets, topk_w, weights, ws=ws)
     assert m.moe_workspace_status(ws) == 1   # MOE_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("weight_dtype", ["bf16", "e4m3"])
+def test_decode_kernel_takes_any_group_size(weight_dtype, _lib):
+    """The operand-swapped decode kernel computes groups of any size, in token
+    chunks: offsets that give one expert every row (80, more than a
+    token-choice dispatch can, so several chunks) and the other none match
+    the oracle row by row."""
+    m = _lib
+    T, H, F, N = 40, 64, 96, 2
+    cfg = m.MoEConfig(T=T, H=H, F=F, N=N, k=2, weight_dtype=weight_dtype)
+    assert "expert_ffn_decode" in m.moe_forward_launch_names(cfg)
+    dev = "cuda"
+    rng = np.random.default_rng(5)
+    if weight_dtype == "e4m3":
+        c1 = rng.integers(0, 0x7E, (N, F, H), dtype=np.uint8) | (rng.integers(0, 2, (N, F, H), dtype=np.uint8) << 7)
+        c2 = rng.integers(0, 0x7E, (N, H, F), dtype=np.uint8) | (rng.integers(0, 2, (N, H, F), dtype=np.uint8) << 7)
+        s1 = np.full((N, F), 2e-3, np.float32)
+        s2 = np.full((N, H), 2e-3, np.float32)
+        W1f = np.stack([O.dequantize_rows(c1[e], s1[e]) for e in range(N)])
+        W2f = np.stack([O.dequantize_rows(c2[e], s2[e]) for e in range(N)])
+        weights = m.MoEWeights(Wg=torch.zeros((N, H), device=dev),
+                               W1=torch.from_numpy(c1).to(dev), W2=torch.from_numpy(c2).to(dev),
+                               s1=torch.from_numpy(s1).to(dev), s2=torch.from_numpy(s2).to(dev))
+    else:
+        W1b = wl.f32_to_bf16_bits(rng.standard_normal((N, F, H)).astype(np.float32) / 8)
+        W2b = wl.f32_to_bf16_bits(rng.standard_normal((N, H, F)).astype(np.float32) / 10)
+        W1f, W2f = wl.bf16_bits_to_f64(W1b), wl.bf16_bits_to_f64(W2b)
+        weights = m.MoEWeights(Wg=torch.zeros((N, H), device=dev),
+                               W1=h.bf16_dev(W1b), W2=h.bf16_dev(W2b))
+    xb = wl.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    x = h.bf16_dev(xb)
+    perm = torch.arange(T * 2, dtype=torch.int32, device=dev)   # row r <- assignment r
+    w_np = rng.random((T, 2)).astype(np.float32)
+    topk_w = torch.from_numpy(w_np).to(dev)
+    offsets = torch.tensor([0, 2 * T, 2 * T], dtype=torch.int32, device=dev)
+    ws = m.make_workspace(cfg, dev)
+    y, _ = m.moe_expert_ffn(cfg, x, perm, offsets, topk_w, weights, ws=ws)
+    assert m.moe_workspace_status(ws) == 0
+    a = np.arange(2 * T)
+    xs = wl.bf16_bits_to_f64(xb)[a // 2]
+    want = w_np.reshape(-1)[a][:, None] * O.expert_ffn(xs, W1f[0], None, W2f[0], None)
+    h.assert_close_out(h.bf16_host(y[:2 * T]), want, "rows of the one expert")
