@@ -37,11 +37,12 @@ import moe_workloads as wl  # noqa: E402
 
 DEFAULT_WORKLOAD = "mixtral_prefill"
 # every layer configuration of the pages, measured in the same run (the
-# headline is one of them)
+# headline is one of them), and the Mixtral-sized decode with E4M3 expert
+# weights
 # (in an order that lets consecutive workloads with the same layer share
 # their device weights)
 PER_CONFIG = ("mixtral_prefill", "mixtral_decode", "moelayer", "switch_capacity",
-              "deepseek_prefill", "deepseek_decode")
+              "deepseek_prefill", "deepseek_decode", "mixtral_decode_fp8")
 METRIC = "MoE-layer fwd tokens/s; % of bf16 TC peak (prefill) or HBM BW (decode)"
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
@@ -125,6 +126,63 @@ def summarise_clocks(samples, source: str) -> dict:
             "reasons": reasons, "samples": len(sm), "source": source}
 
 
+class _Nvml:
+    """The few read-only NVML queries the clock sampler needs, through ctypes
+    on the driver's libnvidia-ml (no Python NVML package required)."""
+    CLOCK_SM = 1
+
+    class PciInfo(__import__("ctypes").Structure):
+        import ctypes as _c
+        _fields_ = [("busIdLegacy", _c.c_char * 16), ("domain", _c.c_uint), ("bus", _c.c_uint),
+                    ("device", _c.c_uint), ("pciDeviceId", _c.c_uint),
+                    ("pciSubSystemId", _c.c_uint), ("busId", _c.c_char * 32)]
+
+    def __init__(self):
+        import ctypes as c
+        self.c = c
+        self.lib = c.CDLL("libnvidia-ml.so.1")
+        self._ok(self.lib.nvmlInit_v2())
+
+    def _ok(self, r):
+        if r != 0:
+            raise RuntimeError(f"NVML error {r}")
+
+    def handle_by_pci(self, domain, bus, device):
+        c = self.c
+        n = c.c_uint(0)
+        self._ok(self.lib.nvmlDeviceGetCount_v2(c.byref(n)))
+        for i in range(n.value):
+            h = c.c_void_p()
+            self._ok(self.lib.nvmlDeviceGetHandleByIndex_v2(c.c_uint(i), c.byref(h)))
+            pci = self.PciInfo()
+            self._ok(self.lib.nvmlDeviceGetPciInfo_v3(h, c.byref(pci)))
+            if (pci.domain, pci.bus, pci.device) == (domain, bus, device):
+                return h
+        raise RuntimeError(f"no NVML device at PCI {(domain, bus, device)}")
+
+    def sm_clock(self, h):
+        v = self.c.c_uint(0)
+        self._ok(self.lib.nvmlDeviceGetClockInfo(h, self.CLOCK_SM, self.c.byref(v)))
+        return v.value
+
+    def sm_max_clock(self, h):
+        v = self.c.c_uint(0)
+        self._ok(self.lib.nvmlDeviceGetMaxClockInfo(h, self.CLOCK_SM, self.c.byref(v)))
+        return v.value
+
+    def power_w(self, h):
+        v = self.c.c_uint(0)
+        self._ok(self.lib.nvmlDeviceGetPowerUsage(h, self.c.byref(v)))
+        return v.value / 1000.0
+
+    def reasons(self, h):
+        v = self.c.c_ulonglong(0)
+        fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self._ok(fn(h, self.c.byref(v)))
+        return v.value
+
+
 class ClockSampler:
     """SM clock, power and clock-event reasons of this process's GPU, sampled
     every CLOCK_INTERVAL_S by a thread through NVML (read-only queries) while
@@ -137,20 +195,11 @@ class ClockSampler:
         self.handle = None
         self.error = None
         try:
-            import pynvml
             import torch
-            pynvml.nvmlInit()
             pr = torch.cuda.get_device_properties(device)
-            want = (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
-            for i in range(pynvml.nvmlDeviceGetCount()):
-                h = pynvml.nvmlDeviceGetHandleByIndex(i)
-                pci = pynvml.nvmlDeviceGetPciInfo(h)
-                if (pci.domain, pci.bus, pci.device) == want:
-                    self.handle = h
-                    break
-            if self.handle is None:
-                raise RuntimeError(f"no NVML device at PCI {want}")
-            self.nv = pynvml
+            self.nv = _Nvml()
+            self.handle = self.nv.handle_by_pci(pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
+            self.smax = float(self.nv.sm_max_clock(self.handle))
             self.thread = threading.Thread(target=self._loop, daemon=True)
             self.thread.start()
         except Exception as e:  # noqa: BLE001
@@ -160,13 +209,11 @@ class ClockSampler:
 
     def _loop(self):
         nv, h = self.nv, self.handle
-        smax = nv.nvmlDeviceGetMaxClockInfo(h, nv.NVML_CLOCK_SM)
         while not self._stop.is_set():
             try:
-                self.samples.append((float(nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM)),
-                                     float(smax), nv.nvmlDeviceGetPowerUsage(h) / 1000.0,
-                                     int(nv.nvmlDeviceGetCurrentClocksEventReasons(h))))
-            except nv.NVMLError:
+                self.samples.append((float(nv.sm_clock(h)), self.smax, nv.power_w(h),
+                                     int(nv.reasons(h))))
+            except Exception:  # noqa: BLE001 - a failed query is a missing sample
                 pass
             time.sleep(CLOCK_INTERVAL_S)
 
@@ -684,7 +731,7 @@ def run_ours(args):
     value = aggregate(w.T, world, ms_max)
     roof = kernel_roofline(w, res, peaks, peak_src)
     fwd_roof = forward_roofline(res, ms_max, peaks, peak_src)
-    e2e = e2e_measure(m, w, res, d["x_bits"], K, world, device)
+    e2e = None if args.no_e2e else e2e_measure(m, w, res, d["x_bits"], K, world, device)
     launches = (K + res["n_traced"]) * sum(1 for n in res["names"] if "memset" not in n)
     headline_entry = config_entry(w, res, ms_max, peaks, peak_src)
 
@@ -750,6 +797,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true",
                     help="measure only the headline workload")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the end-to-end (host buffers) leg, e.g. under a profiler")
     ap.add_argument("--clocks-dir", default=os.path.join(tempfile.gettempdir(), "moe_bench"),
                     help="where nvidia-smi clock samples go if NVML is unavailable")
     args = ap.parse_args(argv)

@@ -104,9 +104,13 @@ struct GemmShape {
   // tiles (1024-aligned), barriers, TMEM address / flags, bias staging, then
   // the two group tables of G + 1 ints: sized per launch, the unused
   // shared memory is left to L1 (measured 2-3 % faster than a fixed size)
+  // CTA pairs: a transpose buffer per epilogue warp for swapped tail tiles
+  // (8 token rows x 32 output columns of bf16)
+  static constexpr int TRANS_BYTES = PAIR == 2 ? EPI_WARPS * 8 * 32 * 2 : 0;
   static constexpr int SMEM_FIXED = SMEM_TILES + NUM_BARS * 8 + 16 + 16 +
                                     EPI_WARPS * EPI_COLS * 2 +              // bias staging
-                                    (FP8 ? EPI_WARPS * EPI_COLS * 4 : 0);   // scale staging
+                                    (FP8 ? EPI_WARPS * EPI_COLS * 4 : 0) +  // scale staging
+                                    TRANS_BYTES;
   static constexpr int smem_bytes(int G) { return SMEM_FIXED + 2 * (G + 1) * 4; }
   static_assert(SMEM_FIXED + 2 * (MAX_GROUPS + 1) * 4 <= 232448, "shared memory budget");
 };
@@ -173,7 +177,9 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                         const __grid_constant__ CUtensorMap tmB0,
                         const __grid_constant__ CUtensorMap tmA1,
-                        const __grid_constant__ CUtensorMap tmB1, const GemmArgs args) {
+                        const __grid_constant__ CUtensorMap tmB1,
+                        const __grid_constant__ CUtensorMap tmA0s,
+                        const __grid_constant__ CUtensorMap tmA1s, const GemmArgs args) {
   using S = GemmShape<PAIR, FP8>;
   constexpr int STAGES = S::STAGES;
   constexpr int GEMM_THREADS = S::THREADS;
@@ -210,8 +216,10 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
   uint16_t* bias_stage = reinterpret_cast<uint16_t*>(  // [EPI_WARPS][EPI_COLS], 16-B aligned
       (reinterpret_cast<uintptr_t>(tmem_holder + 4) + 15) & ~static_cast<uintptr_t>(15));
   float* scale_stage = reinterpret_cast<float*>(bias_stage + EPI_WARPS * EPI_COLS);  // FP8 only
+  uint16_t* trans_stage = reinterpret_cast<uint16_t*>(   // [EPI_WARPS][8][32] (CTA pairs)
+      reinterpret_cast<uint8_t*>(scale_stage) + (FP8 ? EPI_WARPS * EPI_COLS * 4 : 0));
   int32_t* seg = reinterpret_cast<int32_t*>(
-      reinterpret_cast<uint8_t*>(scale_stage) + (FP8 ? EPI_WARPS * EPI_COLS * 4 : 0));  // [G+1]
+      reinterpret_cast<uint8_t*>(trans_stage) + S::TRANS_BYTES);  // [G+1]
   int32_t* mt_pre = seg + (args.num_groups + 1);                          // [G+1]
 
   const int warp = threadIdx.x / 32;
@@ -240,6 +248,18 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
   const uint32_t a_slot = (uint32_t)a_box * BK * 2;
   const int a_slots = SMALL_A ? min(AS, (int)(STAGES * A_BYTES / a_slot)) : STAGES;
   int* status = args.status;
+  // Tail tiles of CTA pairs: the last row block of a group with fewer than
+  // 256 rows runs with the operands swapped - the 256 weight rows of the tile
+  // (the B rows, split 128 per CTA as usual) are the MMA's M operand and the
+  // group's remaining token rows, rounded up to 16 and split in halves
+  // across the pair, its N operand - so the tensor cores skip the padding
+  // rows.  The accumulator then holds output columns in TMEM lanes and tokens
+  // in columns.  Not for SwiGLU first Linears (gate and up rows would land in
+  // different CTAs).
+  auto swapped_tail = [&](int ph, int rows_left) {
+    return PAIR == 2 && args.swap_tail != 0 && rows_left < S::TILE_M &&
+           (ph ? args.ph[1].mode : args.ph[0].mode) != EPI_SWIGLU;
+  };
 
   // ---- set-up: barriers, TMEM (CTA-local, may overlap the previous kernel),
   // then the group table
@@ -274,6 +294,10 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
     if (two) {
       tma_prefetch_desc(&tmA1);
       tma_prefetch_desc(&tmB1);
+    }
+    if (PAIR == 2 && args.swap_tail) {
+      tma_prefetch_desc(&tmA0s);
+      if (two) tma_prefetch_desc(&tmA1s);
     }
   }
   if (warp == 1) {
@@ -369,6 +393,11 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
         const int b_row = glu ? cur.g * 2 * n_out + (int)rank * n_out + n * (BN / 2)
                               : cur.g * n_out + n * BN + (int)rank * S::B_ROWS;
         const int a_row_cta = a_row + (int)rank * 128;
+        // swapped tail tile: the token rows in 8-row copies, half per CTA
+        const bool sw = swapped_tail(ph, rows_left);
+        const int half = sw ? (rows_left + 15) / 16 * 8 : 0;
+        const CUtensorMap* mAs = ph ? &tmA1s : &tmA0s;
+        const uint32_t tx_sw = (uint32_t)((FP8 ? 0 : S::B_BYTES) + half * BK * 2);
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, status)) {
             ok = false;
@@ -377,8 +406,15 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
           if constexpr (PAIR == 2) {
             // both CTAs' copies complete on the even CTA's full barrier
             const uint32_t fb = mapa_shared(full_bar(stage), 0);
-            if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * S::TX_BYTES);
-            tma_load_2d_pair(sA + stage * A_BYTES, mA, fb, kb * BK, a_row_cta);
+            if (sw) {
+              if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * tx_sw);
+              for (int i = 0; i < half / 8; ++i)
+                tma_load_2d_pair(sA + stage * A_BYTES + i * 8 * BK * 2, mAs, fb, kb * BK,
+                                 a_row + (int)rank * half + 8 * i);
+            } else {
+              if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * S::TX_BYTES);
+              tma_load_2d_pair(sA + stage * A_BYTES, mA, fb, kb * BK, a_row_cta);
+            }
             if constexpr (!FP8) tma_load_2d_pair(sB + stage * S::B_BYTES, mB, fb, kb * BK, b_row);
           } else if constexpr (FP8) {
             mbar_arrive_expect_tx(full_bar(stage), a_slot);
@@ -405,12 +441,19 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && leader) {
-      constexpr uint32_t idesc = idesc_bf16_f32(128 * PAIR, BN);
+      constexpr uint32_t idesc_full = idesc_bf16_f32(128 * PAIR, BN);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       uint32_t cstage = 0, cphase = 0;  // FP8: B ring
       bool ok = true;
+      TileCursor<S::TILE_M> cur;
       for (int tile = unit; tile < total && ok; tile += units) {
         const int nkb = tile < tiles0 ? nkb0 : nkb1;
+        int a_row, rows_left, n, rb;
+        cur.locate(tile, tiles0, nt0, nt1, mt_pre, seg, a_row, rows_left, n, rb);
+        // swapped tail tile: M = the 256 weight rows, N = the token rows rounded to 16
+        const bool sw = swapped_tail(cur.phase, rows_left);
+        const uint32_t idesc =
+            sw ? idesc_bf16_f32(128 * PAIR, (rows_left + 15) / 16 * 16) : idesc_full;
         if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, status)) {
           ok = false;
           break;
@@ -431,9 +474,11 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
             }
           }
           tc_fence_after();
-          const uint64_t adesc = sdesc_kmajor_sw128(sA + stage * a_slot);
-          const uint64_t bdesc =
-              sdesc_kmajor_sw128(sB + (FP8 ? cstage : stage) * S::B_BYTES);
+          const uint64_t tdesc = sdesc_kmajor_sw128(sA + stage * a_slot);   // token rows
+          const uint64_t wdesc =
+              sdesc_kmajor_sw128(sB + (FP8 ? cstage : stage) * S::B_BYTES);  // weight rows
+          const uint64_t adesc = sw ? wdesc : tdesc;
+          const uint64_t bdesc = sw ? tdesc : wdesc;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             // +32 bytes along K per step of 16 bf16 inside the 128-byte swizzle atom
@@ -577,6 +622,52 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
       cur.locate(tile, tiles0, nt0, nt1, mt_pre, seg, a_row, rows_left, n, rb);
       const PhaseView P(args, cur.phase);
       const int n_out = P.n_out;
+      if (swapped_tail(cur.phase, rows_left)) {
+        // Swapped tail tile: output columns in TMEM lanes, token rows in
+        // columns.  This warp takes the 32 output columns of its lane quarter
+        // and every (EPI_WARPS / 4)-th 8-token chunk, transposed through its
+        // shared buffer into 16-byte stores along the output rows.
+        const int n16 = (rows_left + 15) / 16 * 16;
+        const int colq = n * BN + (int)rank * S::B_ROWS + q * 32;   // the warp's first column
+        const int colw = colq + lane;
+        float bz = 0.0f, sz = 1.0f;
+        if (colw < n_out) {
+          if (P.bias) bz = __bfloat162float(P.bias[(size_t)cur.g * n_out + colw]);
+          if (FP8 && P.b_scale) sz = P.b_scale[(size_t)cur.g * n_out + colw];
+        }
+        int ok = 1;
+        if (lane == 0) ok = mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, status) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        tc_fence_after();
+        uint16_t* tb = trans_stage + (warp - 2) * 8 * 32;
+        const uint32_t taddr = tmem_base + lane_addr + acc * BN;
+        for (int c = cpart * 8; c < n16; c += 8 * (EPI_WARPS / 4)) {
+          float wv = 1.0f;
+          if (P.mode == EPI_SCALE && P.topk_w != nullptr && lane < 8 && c + lane < rows_left)
+            wv = P.topk_w[P.perm[a_row + c + lane]];
+          uint32_t r[8];
+          tmem_ld_32x32b_x8(taddr + c, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float z = __uint_as_float(r[i]) * sz + bz;
+            float o;
+            if (P.mode == EPI_GELU) o = gelu_erf(z);
+            else if (P.mode == EPI_SILU) o = silu_f(z);
+            else o = __shfl_sync(0xffffffffu, wv, i) * z;
+            tb[i * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+          }
+          __syncwarp();
+          {
+            const int i = lane >> 2, c8 = (lane & 3) * 8;
+            if (c + i < rows_left && colq + c8 < n_out)
+              *reinterpret_cast<uint4*>(P.out + (int64_t)(a_row + c + i) * P.ld_out + colq + c8) =
+                  *reinterpret_cast<const uint4*>(tb + i * 32 + c8);
+          }
+          __syncwarp();
+        }
+      } else {
       const int r_in = warp_row0 + lane;
       const bool row_ok = r_in < rows_left;
       const int64_t out_row = (int64_t)a_row + r_in;
@@ -722,6 +813,7 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
           }
         }
       }
+      }  // normal tile
       if (two && cur.phase == 0) {
         // Hand the row block's stores to phase 1: the last of this CTA's
         // epilogue warps to finish the tile (a CTA-scope acquire-release
@@ -882,6 +974,9 @@ cudaError_t make_gemm_plan(GemmPlan* plan, const GemmArgs& args_in, const __nv_b
     const __nv_bfloat16* a = p == 0 ? A : args.ph[0].out;
     if (!encode_tensor_map_bf16(&plan->tmA[p], a, a_rows, args.ph[p].K, BK, a_box))
       return cudaErrorInvalidValue;
+    // the token rows of swapped tail tiles, in copies of 8 rows (CTA pairs)
+    if (!encode_tensor_map_bf16(&plan->tmAs[p], a, a_rows, args.ph[p].K, BK, 8))
+      return cudaErrorInvalidValue;
     // SwiGLU tiles load 128 gate and 128 up rows: two 128-row boxes
     const int box_b = args.ph[p].mode == EPI_SWIGLU ? BN / 2 : BN / pair;
     const bool ok = fp8 ? encode_tensor_map_u8(&plan->tmB[p], B[p], b_rows[p], args.ph[p].K,
@@ -893,7 +988,9 @@ cudaError_t make_gemm_plan(GemmPlan* plan, const GemmArgs& args_in, const __nv_b
   if (np == 1) {
     plan->tmA[1] = plan->tmA[0];
     plan->tmB[1] = plan->tmB[0];
+    plan->tmAs[1] = plan->tmAs[0];
   }
+  args.swap_tail = pair == 2 ? 1 : 0;
   plan->args = args;
   plan->pair = pair;
   plan->fp8 = fp8;
@@ -956,7 +1053,7 @@ static cudaError_t launch_gemm_t(const GemmPlan& plan, cudaStream_t st) {
   }
   if ((int)cfg.gridDim.x > PAIR * max_units) cfg.gridDim.x = PAIR * max_units;
   return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<PAIR, FP8>, plan.tmA[0], plan.tmB[0],
-                            plan.tmA[1], plan.tmB[1], plan.args);
+                            plan.tmA[1], plan.tmB[1], plan.tmAs[0], plan.tmAs[1], plan.args);
 }
 
 cudaError_t launch_gemm(const GemmPlan& plan, cudaStream_t st, LaunchTrace* tr) {

@@ -103,6 +103,19 @@ struct RouterTcArgs {
   int kb_per_split;      // x tiles (64 wide) per K split
   int splits;            // K splits = cluster size (1, 2, 4 or 8)
   int work_bytes;        // ring / logits-tile shared memory
+  // stacked planes: the epilogue warps split W_g (fp32 [N, H]) into the
+  // three bf16 planes of each ring slot themselves (no W3, no split kernel)
+  const float* Wg;
+  int H;
+  // dispatch fused into the router (moe_forward, token choice, token-major
+  // claims): each CTA writes its chunk's local ranks (local_rank[t*k + j],
+  // the rank of the assignment among the chunk's assignments to the same
+  // expert in token order) and expert histogram (blk_hist[cta][N]) instead
+  // of reducing p_mean; `clear` (clear_n ints) is zeroed by CTA 0 first.
+  int32_t* local_rank;   // nullptr: not fused (the last CTA reduces p_mean)
+  int32_t* blk_hist;
+  int* clear;
+  int clear_n;
 };
 struct RouterTcPlan {
   int N_pad, H_pad, stacked, pp, nacc, tmem_cols, stage_bytes, stages, m_tiles, splits,
@@ -115,9 +128,22 @@ inline size_t router_w3_bytes(int N, int H) {
   return N_pad * 3 * H_pad * 2;
 }
 // `clear` (nullable, clear_n ints) is zeroed by the first kernel of the
-// router, before the router kernel itself runs.
+// router, before the router kernel itself runs (with stacked planes and no
+// split kernel: by the router's CTA 0; the router then uses no ticket, so
+// `clear` must not hold one it needs - see router_stacked()).
+// fused (nullable): the dispatch histogram outputs of a fused router.
+struct RouterFused {
+  int32_t* local_rank;   // [T * k]
+  int32_t* blk_hist;     // [chunks, N]
+};
 cudaError_t launch_router_tc(const RouterLaunch& a, __nv_bfloat16* W3, int* ticket, int* status,
-                             int* clear, int clear_n, cudaStream_t st, LaunchTrace* tr);
+                             int* clear, int clear_n, const RouterFused* fused, cudaStream_t st,
+                             LaunchTrace* tr);
+// whether the tensor-core router splits W_g itself (3 N_pad <= 256)
+bool router_stacked(int N);
+// chunks (router CTAs) and tokens per chunk of a fused router launch
+int router_fused_chunks(int T, int N, int H);
+int router_fused_chunk_tokens(int T, int N, int H);
 
 // TMA map of a row-major bf16 matrix [rows, K], box 64 (K) x box_rows, 128B swizzle
 bool encode_tensor_map_bf16(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
@@ -146,6 +172,34 @@ struct PermuteLaunch {
   __nv_bfloat16* xp = nullptr;
   int H = 0;
 };
+// Dispatch after a fused router (router_tc with RouterFused): the scatter
+// launch's CTA 0 scans the router's chunk histograms (counts, capacity,
+// offsets, chunk bases, f, p_mean from the router's partial sums, z-loss,
+// L_aux) and releases a flag; every CTA then scatters and gathers its tokens.
+struct DispatchFusedLaunch {
+  const int32_t* topk_idx;
+  const int32_t* local_rank;  // [T * k] from the router
+  const int32_t* blk_hist;    // [chunks, N] from the router
+  int32_t* blk_base;          // scratch [chunks, N]
+  const float* p_part;        // [chunks, N + 1] from the router
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* perm;
+  int32_t* inv;
+  float* f;                   // nullable
+  float* p_mean;
+  float* z_loss;              // nullable
+  float* l_aux;               // nullable
+  int* flag;                  // zeroed by the router's CTA 0
+  int* status;
+  const __nv_bfloat16* x;
+  __nv_bfloat16* xp;
+  int T, N, k, H, chunks, chunk_tokens;
+  int64_t capacity;
+  float alpha;
+};
+cudaError_t launch_dispatch_fused(const DispatchFusedLaunch& a, cudaStream_t st, LaunchTrace* tr);
+
 constexpr int kPermuteChunk = 256;  // assignments per block
 inline int permute_num_blocks(int64_t A) { return (int)((A + kPermuteChunk - 1) / kPermuteChunk); }
 int permute_num_launches(int T, int k, bool fused_scan);
@@ -206,10 +260,13 @@ struct GemmArgs {
   int32_t skip_producer;         // failure injection: the TMA producer issues nothing
   int32_t a_box;                 // rows per A copy (set by make_gemm_plan): 128, or for
                                  // FP8 single-CTA tiles the bound on a group's rows
+  int32_t swap_tail;             // CTA pairs: a group's last row block of fewer than 256
+                                 // rows runs operand-swapped (set by make_gemm_plan)
 };
 
 struct GemmPlan {
   CUtensorMap tmA[2];  // per phase: A [rows, K] bf16, box 64 x 128, 128B swizzle
+  CUtensorMap tmAs[2]; // per phase: the same A in boxes of 64 x 8 (swapped tail tiles)
   CUtensorMap tmB[2];  // per phase: B [G * n_out, K] bf16, box 64 x (256 / pair), 128B
                        // swizzle; FP8 B: E4M3 bytes, the same box unswizzled
   GemmArgs args;

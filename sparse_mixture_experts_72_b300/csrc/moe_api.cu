@@ -83,7 +83,12 @@ WsLayout layout_of(const moe_config_t& c) {
   const int64_t T = c.T, N = c.N, A = T * slots_of(c), R = max_rows_of(c);
   const int64_t Ak = expert_choice(c) ? 0 : T * c.k;   // top-k outputs (token choice)
   const int64_t nsel = router_num_select_blocks(c.T);
-  const int64_t nblk = permute_num_blocks(A);
+  int64_t nblk = permute_num_blocks(A);
+  if (T > 0 && c.N <= kRouterTcMaxExperts) {
+    // a fused router's chunks use the same histogram / base arrays
+    const int64_t ch = router_fused_chunks(c.T, c.N, c.H);
+    if (ch > nblk) nblk = ch;
+  }
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o += align_up(bytes > 0 ? bytes : 1); return at; };
   // The header every call zeroes first: [0] status word, [1] router ticket,
@@ -229,13 +234,27 @@ moe_status_t clear_status(void* ws, const WsLayout& L, cudaStream_t st, LaunchTr
 
 // ---------------------------------------------------------------- stages
 // The tensor-core router's first kernel can zero the status header itself.
-bool router_clears_status(const moe_config_t& c) { return c.N <= kRouterTcMaxExperts && c.T > 0; }
+// Token choice with token-major claims on the tensor-core router: the
+// router's CTAs also rank their chunk's assignments per expert and count
+// them, and the scatter launch scans the counts (no rank launch).
+bool fused_dispatch(const moe_config_t& c) {
+  return !expert_choice(c) && c.drop_order == MOE_DROP_TOKEN_MAJOR &&
+         c.N <= kRouterTcMaxExperts && c.T > 0;
+}
+
+// Whether the router's first kernel zeroes the header itself: the W_g split
+// kernel does (planes along K); with stacked planes there is no split kernel
+// and the router's CTA 0 does it, but only when the router uses no ticket
+// (a fused dispatch).
+bool router_clears_status(const moe_config_t& c, bool fused) {
+  return c.N <= kRouterTcMaxExperts && c.T > 0 && (!router_stacked(c.N) || fused);
+}
 
 // Zeroes the status word and router ticket, unless the router's first kernel
 // does it (router_clears_status).
-moe_status_t begin_call(const moe_config_t& c, void* ws, const WsLayout& L, cudaStream_t st,
-                        LaunchTrace* tr) {
-  if (router_clears_status(c)) return MOE_OK;
+moe_status_t begin_call(const moe_config_t& c, bool fused, void* ws, const WsLayout& L,
+                        cudaStream_t st, LaunchTrace* tr) {
+  if (router_clears_status(c, fused)) return MOE_OK;
   return clear_status(ws, L, st, tr);
 }
 
@@ -243,7 +262,7 @@ moe_status_t begin_call(const moe_config_t& c, void* ws, const WsLayout& L, cuda
 moe_status_t do_route(const moe_config_t& c, const uint16_t* x, const float* Wg, const float* bg,
                       const float* sel, int32_t* idx, float* w, float* probs, float* logits,
                       float* p_mean, float* z_loss, void* ws, const WsLayout& L, cudaStream_t st,
-                      LaunchTrace* tr) {
+                      LaunchTrace* tr, bool fused = false) {
   RouterLaunch a;
   a.x = reinterpret_cast<const __nv_bfloat16*>(x);
   a.Wg = Wg;
@@ -261,11 +280,13 @@ moe_status_t do_route(const moe_config_t& c, const uint16_t* x, const float* Wg,
   a.H = c.H;
   a.N = c.N;
   a.k = idx ? c.k : 1;
-  if (c.N <= kRouterTcMaxExperts)
+  if (c.N <= kRouterTcMaxExperts) {
+    RouterFused fz{at<int32_t>(ws, L.local_rank), at<int32_t>(ws, L.blk_hist)};
     return cuda_status(launch_router_tc(
         a, at<__nv_bfloat16>(ws, L.w3), at<int>(ws, L.status) + 1, at<int>(ws, L.status),
-        router_clears_status(c) ? at<int>(ws, L.status) : nullptr, (int)(L.status_bytes / 4), st,
-        tr));
+        router_clears_status(c, fused) ? at<int>(ws, L.status) : nullptr,
+        (int)(L.status_bytes / 4), fused ? &fz : nullptr, st, tr));
+  }
   return cuda_status(launch_router(a, st, tr));
 }
 
@@ -298,6 +319,40 @@ moe_status_t do_permute(const moe_config_t& c, const int32_t* idx, const float* 
     a.H = c.H;
   }
   return cuda_status(launch_permute(a, st, tr));
+}
+
+// The scatter launch after a fused router (fused_dispatch).
+moe_status_t do_dispatch_fused(const moe_config_t& c, const int32_t* idx, float* p_mean,
+                               float* z_loss, int32_t* counts, int32_t* offsets, int32_t* perm,
+                               int32_t* inv, float* f, float* l_aux, const uint16_t* x, void* ws,
+                               const WsLayout& L, cudaStream_t st, LaunchTrace* tr) {
+  DispatchFusedLaunch a{};
+  a.topk_idx = idx;
+  a.local_rank = at<int32_t>(ws, L.local_rank);
+  a.blk_hist = at<int32_t>(ws, L.blk_hist);
+  a.blk_base = at<int32_t>(ws, L.blk_base);
+  a.p_part = at<float>(ws, L.p_part);
+  a.counts = counts;
+  a.offsets = offsets;
+  a.perm = perm;
+  a.inv = inv;
+  a.f = f;
+  a.p_mean = p_mean;
+  a.z_loss = z_loss;
+  a.l_aux = l_aux;
+  a.flag = at<int>(ws, L.status) + 2;   // zeroed with the header by the router
+  a.status = at<int>(ws, L.status);
+  a.x = reinterpret_cast<const __nv_bfloat16*>(x);
+  a.xp = max_rows_of(c) > 0 ? at<__nv_bfloat16>(ws, L.xp) : nullptr;
+  a.T = c.T;
+  a.N = c.N;
+  a.k = c.k;
+  a.H = c.H;
+  a.chunks = router_fused_chunks(c.T, c.N, c.H);
+  a.chunk_tokens = router_fused_chunk_tokens(c.T, c.N, c.H);
+  a.capacity = capacity_of(c);
+  a.alpha = c.aux_alpha;
+  return cuda_status(launch_dispatch_fused(a, st, tr));
 }
 
 // Two events per device for moe_forward_host's stream hand-overs.  A wait
@@ -479,15 +534,20 @@ int forward_launch_names(const moe_config_t& c, const char** names, int cap) {
     ++n;
   };
   const bool tc = c.N <= kRouterTcMaxExperts;
-  if (!router_clears_status(c)) add("status_memset");
+  const bool fz = fused_dispatch(c);
+  if (!router_clears_status(c, fz)) add("status_memset");
   if (c.T == 0) add("router_pmean");
-  else if (tc) { add("router_split"); add("router_tc"); }
-  else { add("router_logits"); add("router_select"); add("router_pmean"); }
+  else if (tc) {
+    if (!router_stacked(c.N)) add("router_split");
+    add("router_tc");
+  } else { add("router_logits"); add("router_select"); add("router_pmean"); }
   const bool rows = max_rows_of(c) > 0, sh = c.F_shared > 0 && c.T > 0;
   bool gathered = true;
   if (expert_choice(c)) {
     add("expert_choice");
     gathered = false;
+  } else if (fz) {
+    add("dispatch_scatter");
   } else if ((int64_t)c.T * c.k > 0) {
     add("permute_rank_scan");
     add("scatter_gather");
@@ -550,11 +610,15 @@ MOE_API int64_t moe_capacity(const moe_config_t* cfg) {
 MOE_API int32_t moe_forward_num_launches(const moe_config_t* cfg) {
   if (check_config(cfg) != MOE_OK) return -1;
   const moe_config_t& c = *cfg;
-  int n = router_clears_status(c) ? 0 : 1;  // status clear
+  const bool fz = fused_dispatch(c);
+  int n = router_clears_status(c, fz) ? 0 : 1;  // status clear
   n += router_num_launches(c.T, c.N);
   if (expert_choice(c)) {
     n += 1;                                 // expert-choice selection
     n += ffn_num_launches(c, false);        // gather + expert FFN (+ shared)
+  } else if (fz) {
+    n += 1;                                 // scan + scatter + gather
+    n += ffn_num_launches(c, true);
   } else {
     n += permute_num_launches(c.T, c.k, true);  // the scatter also gathers the rows
     n += ffn_num_launches(c, true);
@@ -591,7 +655,7 @@ MOE_API moe_status_t moe_route(const moe_config_t* cfg, const uint16_t* x, const
   MOE_TRY(device_info(&d));
   const WsLayout L = layout_of(c);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  MOE_TRY(begin_call(c, ws, L, st, nullptr));
+  MOE_TRY(begin_call(c, false, ws, L, st, nullptr));
   return do_route(c, x, Wg, bg, sel_bias, topk_idx, topk_w, probs, logits, p_mean, z_loss, ws, L,
                   st, nullptr);
 }
@@ -723,7 +787,8 @@ MOE_API moe_status_t moe_forward(const moe_config_t* cfg, const moe_weights_t* w
   uint16_t* y = at<uint16_t>(ws, L.y);
   uint16_t* ys = c.F_shared > 0 ? at<uint16_t>(ws, L.y_s) : nullptr;
 
-  MOE_TRY(begin_call(c, ws, L, st, tr));
+  const bool fz = fused_dispatch(c);
+  MOE_TRY(begin_call(c, fz, ws, L, st, tr));
   if (expert_choice(c)) {
     // route (logits + softmax) -> each expert takes its top-C tokens ->
     // gather -> expert FFN weighted by P[t, e] -> combine over the N experts
@@ -736,8 +801,12 @@ MOE_API moe_status_t moe_forward(const moe_config_t* cfg, const moe_weights_t* w
     MOE_TRY(do_ffn(c, x, perm, offsets, probs, *weights, y, ys, ws, L, d.sms, st, tr, false));
   } else {
     MOE_TRY(do_route(c, x, weights->Wg, weights->bg, weights->sel_bias, idx, w, o.probs, o.logits,
-                     p_mean, z_loss, ws, L, st, tr));
-    MOE_TRY(do_permute(c, idx, p_mean, counts, offsets, perm, inv, f, l_aux, ws, L, st, tr, x));
+                     p_mean, z_loss, ws, L, st, tr, fz));
+    if (fz)
+      MOE_TRY(do_dispatch_fused(c, idx, p_mean, z_loss, counts, offsets, perm, inv, f, l_aux, x,
+                                ws, L, st, tr));
+    else
+      MOE_TRY(do_permute(c, idx, p_mean, counts, offsets, perm, inv, f, l_aux, ws, L, st, tr, x));
     MOE_TRY(do_ffn(c, x, perm, offsets, w, *weights, y, ys, ws, L, d.sms, st, tr, true));
   }
   if (c.T > 0) {

@@ -18,7 +18,9 @@
 //               capacity, row offsets, f and L_aux
 //   2. scatter: row = offsets[e] + base + local rank, or dropped
 // (Without a ticket, e.g. for the workspace-free entry point, the scan is a
-// launch of its own.)
+// launch of its own.)  In a forward pass with token-major claims the router
+// ranks and counts the assignments of its chunks instead, and one launch
+// (dispatch_fused_kernel) scans and scatters.
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -223,6 +225,152 @@ __global__ void __launch_bounds__(256) permute_scatter_gather_kernel(
       }
     }
   }
+}
+
+// ---------------------------------------------------------------------------
+// Dispatch after a fused router (token choice, token-major claims).  The
+// router's CTAs each wrote, for their chunk of consecutive tokens, the
+// local rank of every assignment and the chunk's expert histogram.  CTA 0
+// of this launch scans them: per expert the chunk bases (prefix over chunks,
+// in chunk order), the counts, the capacity, the row offsets, f_i; p_i and
+// the z-loss from the router's per-chunk partial sums (fixed order); L_aux.
+// It then releases a flag (zeroed by the router), and every CTA - which
+// waits for the flag, bounded - scatters its tokens: row = offsets[e] +
+// base[chunk][e] + local rank, or dropped past the capacity, with the token's
+// x row copied into each kept row.  The grid never exceeds the CTAs that fit
+// at once, so CTA 0 always runs.
+constexpr int DF_THREADS = 512;
+
+__device__ __forceinline__ void st_release_gpu(int* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__global__ void __launch_bounds__(DF_THREADS) dispatch_fused_kernel(const DispatchFusedLaunch a) {
+  __shared__ int32_t s_part[DF_THREADS];
+  __shared__ int32_t s_cnt[kRouterTcMaxExperts];
+  __shared__ float s_red[DF_THREADS];
+  __shared__ int s_ok;
+  const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
+  const int N = a.N, C = a.chunks;
+  const int64_t A = (int64_t)a.T * a.k;
+  pdl_launch_dependents();
+  pdl_wait();
+  if (blockIdx.x == 0) {
+    // chunk bases: P threads per expert, each over a run of chunks
+    const int P = DF_THREADS / N > 0 ? DF_THREADS / N : 1;
+    const int cp = (C + P - 1) / P;
+    const int e = tid / P, part = tid % P;
+    const bool act = e < N;
+    const int c0 = part * cp, c1 = min(C, c0 + cp);
+    int sum = 0;
+    if (act)
+      for (int c = c0; c < c1; ++c) sum += __ldcg(a.blk_hist + (size_t)c * N + e);
+    s_part[tid] = sum;
+    __syncthreads();
+    if (act) {
+      int base = 0;
+      for (int p2 = 0; p2 < part; ++p2) base += s_part[e * P + p2];
+      for (int c = c0; c < c1; ++c) {
+        a.blk_base[(size_t)c * N + e] = base;
+        base += __ldcg(a.blk_hist + (size_t)c * N + e);
+      }
+      if (part == P - 1) s_cnt[e] = base;   // every chunk: the expert's count
+    }
+    __syncthreads();
+    // p_i and the z-loss from the router's per-chunk sums (fixed order)
+    reduce_router_partials(a.p_part, C, N, a.T, a.p_mean, a.z_loss, s_red);
+    if (warp == 0) {
+      // counts, f, capacity, offsets (exclusive scan of the kept counts,
+      // contiguous runs of experts per lane) and L_aux (fixed order, double)
+      const int epl = (N + 31) / 32;
+      const int e0 = min(N, lane * epl), e1 = min(N, e0 + epl);
+      int run_k = 0;
+      double term = 0.0;
+      for (int e2 = e0; e2 < e1; ++e2) {
+        const int cnt = s_cnt[e2];
+        a.counts[e2] = cnt;
+        const double fe = A > 0 ? (double)cnt / (double)A : 0.0;
+        if (a.f) a.f[e2] = (float)fe;
+        term += fe * (double)a.p_mean[e2];
+        run_k += (int)((a.capacity >= 0 && cnt > a.capacity) ? a.capacity : cnt);
+      }
+      int incl = run_k;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      int run = incl - run_k;
+      for (int e2 = e0; e2 < e1; ++e2) {
+        a.offsets[e2] = run;
+        const int cnt = s_cnt[e2];
+        run += (int)((a.capacity >= 0 && cnt > a.capacity) ? a.capacity : cnt);
+      }
+      if (lane == 31) a.offsets[N] = incl;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) term += __shfl_xor_sync(0xffffffffu, term, o);
+      if (lane == 0 && a.l_aux) *a.l_aux = (float)((double)a.alpha * (double)N * term);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence();
+      st_release_gpu(a.flag, 1);
+    }
+  } else {
+    if (tid == 0) {
+      int ok = 1;
+      const long long t0 = clock64();
+      while (ld_acquire_gpu(a.flag) == 0) {
+        if (clock64() - t0 > kWaitLimitCycles) {
+          atomicExch(a.status, (int)MOE_ERR_TIMEOUT);
+          ok = 0;
+          break;
+        }
+      }
+      s_ok = ok;
+    }
+    __syncthreads();
+    if (!s_ok) return;
+  }
+  // scatter and gather: one warp per token, lane j < k for slot j
+  const int64_t nvec = a.H / 8;
+  constexpr int WPB = DF_THREADS / 32;
+  for (int64_t t = (int64_t)blockIdx.x * WPB + warp; t < a.T; t += (int64_t)gridDim.x * WPB) {
+    int32_t row = -1;
+    if (lane < a.k) {
+      const int64_t as = t * a.k + lane;
+      const int e = a.topk_idx[as];
+      if (e >= 0 && e < N) {
+        const int64_t pos = (int64_t)__ldcg(a.blk_base + (t / a.chunk_tokens) * N + e) +
+                            a.local_rank[as];
+        if (a.capacity < 0 || pos < a.capacity) row = __ldcg(a.offsets + e) + (int32_t)pos;
+      }
+      a.inv[as] = row;
+      if (row >= 0) a.perm[row] = (int32_t)as;
+    }
+    const unsigned kept_mask = __ballot_sync(0xffffffffu, row >= 0);
+    if (kept_mask == 0u || a.xp == nullptr) continue;
+    const uint4* src = reinterpret_cast<const uint4*>(a.x + t * a.H);
+    for (int64_t v = lane; v < nvec; v += 32) {
+      const uint4 val = __ldg(src + v);
+      unsigned mk = kept_mask;
+      while (mk) {
+        const int j = __ffs(mk) - 1;
+        mk &= mk - 1;
+        const int32_t r = __shfl_sync(0xffffffffu, row, j);
+        reinterpret_cast<uint4*>(a.xp + (int64_t)r * a.H)[v] = val;
+      }
+    }
+  }
+}
+
+cudaError_t launch_dispatch_fused(const DispatchFusedLaunch& a, cudaStream_t st, LaunchTrace* tr) {
+  // at most two CTAs per SM: every CTA is resident while CTA 0 scans
+  int64_t blocks = ((int64_t)a.T + DF_THREADS / 32 - 1) / (DF_THREADS / 32);
+  if (blocks > 148 * 2) blocks = 148 * 2;
+  if (blocks < 1) blocks = 1;
+  trace_mark(tr, st);
+  return launch_pdl(dispatch_fused_kernel, dim3((unsigned)blocks), dim3(DF_THREADS), 0, st, 1, a);
 }
 
 int permute_num_launches(int T, int k, bool fused_scan) {

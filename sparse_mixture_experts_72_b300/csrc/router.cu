@@ -254,7 +254,8 @@ cudaError_t launch_router(const RouterLaunch& a, cudaStream_t st, LaunchTrace* t
 }
 
 int router_num_launches(int T, int N) {
-  if (N <= kRouterTcMaxExperts) return T > 0 ? 2 : 1;
+  // tensor-core router: [W_g split kernel, unless the planes are stacked] + router
+  if (N <= kRouterTcMaxExperts) return T > 0 ? (router_stacked(N) ? 1 : 2) : 1;
   return T > 0 ? 3 : 1;
 }
 

@@ -14,10 +14,13 @@
 // an fp32-accumulated sum of exact products: the same accuracy class as an
 // fp32 FFMA dot product.
 //
-// Layout of the three planes (W3, written by router_split_kernel):
-//   stacked (3 N_pad <= 256): rows p*N_pad + e of a [3 N_pad, H_pad] matrix,
-//            so one MMA with N = 3 N_pad covers all planes;
-//   along K (wider routers): W3[e, p*H_pad + h], one plane per MMA.
+// Layout of the three planes:
+//   stacked (3 N_pad <= 256): rows p*N_pad + e of each ring slot's B tile, so
+//            one MMA with N = 3 N_pad covers all planes; the epilogue warps,
+//            idle during the main loop, split W_g's slice of every slot
+//            into shared memory themselves (no split kernel, no W3);
+//   along K (wider routers): W3[e, p*H_pad + h] written by
+//            router_split_kernel, one plane per MMA.
 // Consecutive k-steps go round-robin to `nacc` independent TMEM accumulators
 // so that the MMAs of a stage do not wait on one another; the epilogue adds
 // accumulators and planes back up in a fixed order.
@@ -34,7 +37,11 @@
 // keeps an online max/sum for the softmax and a sorted top-k of l - b_sel in
 // registers and pass 2 forms P for the optional probs output and the CTA's
 // column sums.  The last CTA to finish (integer ticket) reduces the per-CTA
-// column sums in CTA order into p_mean.
+// column sums in CTA order into p_mean.  In a forward pass with token-major
+// claims the router also starts the dispatch ("混合专家模型 MoE 架构深度解析"
+// §2.3): each CTA ranks its chunk's assignments per expert from per-expert
+// token bitmasks and writes the chunk's histogram, and the scatter launch
+// (dispatch_fused_kernel) reduces p_mean, so no ticket is needed.
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -115,11 +122,16 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
   auto empty_bar = [&](int s) { return bar0 + 8u * (RT_MAX_STAGES + s); };
   const uint32_t tfull_bar = bar0 + 8u * (2 * RT_MAX_STAGES);
   const uint32_t drain_bar = bar0 + 8u * (2 * RT_MAX_STAGES + 1);
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * RT_MAX_STAGES + 2);
+  // W_g planes of a ring slot written by the epilogue warps (in-kernel split)
+  auto bfull_bar = [&](int s) { return bar0 + 8u * (2 * RT_MAX_STAGES + 2 + s); };
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 3 * RT_MAX_STAGES + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* flags = reinterpret_cast<int*>(tmem_holder + 2);      // [0] last CTA
   float* psum = reinterpret_cast<float*>(tmem_holder + 4);   // [4][N_pad]
   float* zsum = psum + 4 * N_pad;                            // [4]
+  uint32_t* tmask = reinterpret_cast<uint32_t*>(zsum + 4);   // [N_pad][4]: tokens per expert
+  const bool own_split = args.Wg != nullptr;                 // stacked planes split here
+  const bool fused = args.local_rank != nullptr;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   pdl_launch_dependents();
@@ -142,6 +154,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
+      mbar_init(bfull_bar(s), 4);   // the four epilogue warps
     }
     mbar_init(tfull_bar, 1);
     mbar_init(drain_bar, 1);
@@ -150,7 +163,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmX);
-    tma_prefetch_desc(&tmW);
+    if (!own_split) tma_prefetch_desc(&tmW);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_holder), args.tmem_cols);
@@ -162,6 +175,11 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
   const uint32_t tmem_base = *tmem_holder;
   long long tma_issued = 0;
   pdl_wait();  // the W_g planes, x and the ticket come from earlier launches
+  if (args.clear && blockIdx.x == 0 && warp >= 2) {
+    // the forward pass's header (status word, dispatch flag, the expert
+    // FFN's counters): no kernel before this one in the call clears it
+    for (int i = threadIdx.x - 64; i < args.clear_n; i += RT_THREADS - 64) args.clear[i] = 0;
+  }
 
   if (warp == 0) {
     if (lane == 0) {
@@ -173,9 +191,9 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
         if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, status)) break;
         const int kx = kx0 + st / per_x;
         const uint32_t sa = s0 + stage * stage_bytes;
-        mbar_arrive_expect_tx(full_bar(stage), stage_bytes);
+        mbar_arrive_expect_tx(full_bar(stage), own_split ? RT_A_BYTES : stage_bytes);
         tma_load_2d(sa, &tmX, full_bar(stage), kx * RT_BK, t0);
-        for (int pp = 0; pp < PP; ++pp) {
+        for (int pp = 0; pp < (own_split ? 0 : PP); ++pp) {
           // stacked: all planes in one tile at column kx*64;
           // along K: plane p's tile at column p*H_pad + kx*64
           const int p = PP == 3 ? pp : st % per_x;
@@ -195,6 +213,10 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
       bool ok = true;
       for (int st = 0; st < nst; ++st) {
         if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, status)) { ok = false; break; }
+        if (own_split && !mbar_wait_bounded(bfull_bar(stage), phase, abort_flag, status)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const uint32_t sa = s0 + stage * stage_bytes;
         const uint64_t adesc = sdesc_kmajor_sw128(sa);
@@ -214,6 +236,58 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
     }
     __syncwarp();
   } else {
+    if (own_split) {
+      // ---- E0: the three bf16 planes of W_g for each ring slot, written in
+      // the 128-byte swizzled layout the MMA reads (rows p * N_pad + e of 64
+      // values; 16-byte chunk c of row r at c ^ (r % 8)).  hi = bf16(w),
+      // mid = bf16(w - hi), lo = bf16(w - hi - mid): hi + mid + lo = w
+      // exactly, so x . W_g^T accumulates exact products in fp32.
+      const int et = threadIdx.x - 64;
+      uint32_t stage = 0, phase = 0;
+      for (int st = 0; st < nst; ++st) {
+        int ok = 1;
+        if (lane == 0) ok = mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, status) ? 1 : 0;
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        const int col0 = (kx0 + st) * RT_BK;
+        uint8_t* bt = smem + stage * stage_bytes + RT_A_BYTES;
+        for (int it = et; it < N_pad * 8; it += 128) {
+          const int e = it >> 3, c = it & 7;
+          const int col = col0 + c * 8;
+          float w[8];
+          if (e < N && col < args.H) {
+            const float4 a = __ldg(reinterpret_cast<const float4*>(args.Wg + (size_t)e * args.H + col));
+            const float4 b = __ldg(reinterpret_cast<const float4*>(args.Wg + (size_t)e * args.H + col + 4));
+            w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w; w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) w[i] = 0.0f;
+          }
+          uint32_t ph[3][4];
+#pragma unroll
+          for (int i = 0; i < 8; i += 2) {
+            float r0 = w[i], r1 = w[i + 1];
+#pragma unroll
+            for (int pl = 0; pl < 3; ++pl) {
+              const __nv_bfloat16 h0 = __float2bfloat16_rn(r0), h1 = __float2bfloat16_rn(r1);
+              ph[pl][i / 2] = (uint32_t)__bfloat16_as_ushort(h0) |
+                              ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+              r0 -= __bfloat162float(h0);
+              r1 -= __bfloat162float(h1);
+            }
+          }
+#pragma unroll
+          for (int pl = 0; pl < 3; ++pl) {
+            const int r = pl * N_pad + e;
+            *reinterpret_cast<uint4*>(bt + (r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4)) =
+                make_uint4(ph[pl][0], ph[pl][1], ph[pl][2], ph[pl][3]);
+          }
+        }
+        fence_proxy_async_shared();   // the tensor cores read what the threads wrote
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bfull_bar(stage));
+        if (++stage == (uint32_t)STAGES) { stage = 0; phase ^= 1u; }
+      }
+    }
     // ---- E1: this CTA's (partial) logits, TMEM -> shared-memory tile.  The
     // ring is idle once every MMA has completed (tmem_full), so the tile
     // reuses its space.  Accumulators and planes are added in a fixed order.
@@ -331,6 +405,37 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
         }
       }
     }
+    if (fused) {
+      // dispatch ranks of this CTA's chunk (its rows, in token order): the
+      // rank of (t, j) among the chunk's assignments to expert e is the
+      // number of earlier chunk tokens that chose e (a token's k experts
+      // are distinct), read from a per-expert token bitmask
+      const int et = threadIdx.x - 64;
+      for (int i = et; i < N_pad * 4; i += 128) tmask[i] = 0u;
+      named_barrier(1, 128);
+      const int lr = row - row_lo;   // token index inside the chunk (< 128)
+      if (valid) {
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j)
+          if (j < k) atomicOr(&tmask[ti[j] * 4 + (lr >> 5)], 1u << (lr & 31));
+      }
+      named_barrier(1, 128);
+      if (valid) {
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+          if (j < k) {
+            const uint32_t* mk = tmask + ti[j] * 4;
+            int rank = __popc(mk[lr >> 5] & ((1u << (lr & 31)) - 1u));
+            for (int wd = 0; wd < (lr >> 5); ++wd) rank += __popc(mk[wd]);
+            args.local_rank[(size_t)t * k + j] = rank;
+          }
+        }
+      }
+      for (int e = et; e < N; e += 128)
+        args.blk_hist[(size_t)blockIdx.x * N + e] =
+            __popc(tmask[e * 4]) + __popc(tmask[e * 4 + 1]) + __popc(tmask[e * 4 + 2]) +
+            __popc(tmask[e * 4 + 3]);
+    }
     // router z-loss term of the token: logsumexp(l_t)^2
     {
       float zt = 0.0f;
@@ -375,6 +480,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
       if (threadIdx.x == 64)
         args.p_part[(size_t)blockIdx.x * (N + 1) + N] = ((zsum[0] + zsum[1]) + zsum[2]) + zsum[3];
     }
+    if (!fused) {
     __threadfence();
     named_barrier(1, 128);
     if (threadIdx.x == 64) flags[0] = (atomicAdd(args.ticket, 1) == (int)gridDim.x - 1) ? 1 : 0;
@@ -398,6 +504,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
         else if (args.z_loss) *args.z_loss = mean;
       }
     }
+    }  // !fused
   }
 
   tc_fence_before();
@@ -456,7 +563,8 @@ RouterTcPlan router_tc_plan(int T, int N, int H) {
   const int ring = p.stages * p.stage_bytes;
   const int tile = RT_BM * (p.N_pad + 4) * 4;
   p.work_bytes = ((ring > tile ? ring : tile) + 1023) / 1024 * 1024;
-  p.smem = 1024 + p.work_bytes + (2 * RT_MAX_STAGES + 2) * 8 + 16 + 4 * p.N_pad * 4 + 16;
+  p.smem = 1024 + p.work_bytes + (3 * RT_MAX_STAGES + 2) * 8 + 16 + 4 * p.N_pad * 4 + 16 +
+           p.N_pad * 16;
   return p;
 }
 
@@ -465,14 +573,25 @@ int router_tc_num_ctas(int T, int N, int H) {
   return p.m_tiles * p.splits;
 }
 
+bool router_stacked(int N) { return 3 * ((N + 15) / 16 * 16) <= 256; }
+
+int router_fused_chunks(int T, int N, int H) { return router_tc_num_ctas(T, N, H); }
+
+int router_fused_chunk_tokens(int T, int N, int H) {
+  return RT_BM / router_tc_plan(T, N, H).splits;
+}
+
 cudaError_t launch_router_tc(const RouterLaunch& a, __nv_bfloat16* W3, int* ticket, int* status,
-                             int* clear, int clear_n, cudaStream_t st, LaunchTrace* tr) {
+                             int* clear, int clear_n, const RouterFused* fused, cudaStream_t st,
+                             LaunchTrace* tr) {
   const RouterTcPlan P = router_tc_plan(a.T, a.N, a.H);
   if (a.T == 0) {
     trace_mark(tr, st);
     return launch_router_stats_zero(a.p_mean, a.z_loss, a.N, st);  // p_mean = 0, z_loss = 0
   }
-  {
+  // stacked planes: the router's epilogue warps split W_g per ring slot and
+  // (fused only, where it uses no ticket) its CTA 0 clears the header
+  if (!P.stacked) {
     const int64_t total = (int64_t)P.N_pad * P.H_pad;
     int64_t blocks = (total + 255) / 256;
     if (blocks > 148 * 8) blocks = 148 * 8;
@@ -484,8 +603,7 @@ cudaError_t launch_router_tc(const RouterLaunch& a, __nv_bfloat16* W3, int* tick
   CUtensorMap tmX, tmW;
   if (!encode_tensor_map_bf16(&tmX, a.x, a.T, a.H, RT_BK, RT_BM)) return cudaErrorInvalidValue;
   if (P.stacked) {
-    if (!encode_tensor_map_bf16(&tmW, W3, 3 * P.N_pad, P.H_pad, RT_BK, 3 * P.N_pad))
-      return cudaErrorInvalidValue;
+    tmW = tmX;   // not read: the planes are written in shared memory
   } else {
     if (!encode_tensor_map_bf16(&tmW, W3, P.N_pad, 3 * P.H_pad, RT_BK, P.N_pad))
       return cudaErrorInvalidValue;
@@ -515,6 +633,12 @@ cudaError_t launch_router_tc(const RouterLaunch& a, __nv_bfloat16* W3, int* tick
   args.kb_per_split = P.kb_per_split;
   args.splits = P.splits;
   args.work_bytes = P.work_bytes;
+  args.Wg = P.stacked ? a.Wg : nullptr;
+  args.H = a.H;
+  args.local_rank = fused ? fused->local_rank : nullptr;
+  args.blk_hist = fused ? fused->blk_hist : nullptr;
+  args.clear = (P.stacked && fused) ? clear : nullptr;
+  args.clear_n = clear_n;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(P.m_tiles * P.splits);
   cfg.blockDim = dim3(RT_THREADS);

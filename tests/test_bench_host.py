@@ -146,4 +146,5 @@ def test_weight_reuse_between_workloads():
 def test_bench_defaults_to_the_largest_prefill_config():
     assert bench.DEFAULT_WORKLOAD == "mixtral_prefill"
     assert set(bench.PER_CONFIG) == {"moelayer", "mixtral_prefill", "mixtral_decode",
-                                     "deepseek_prefill", "deepseek_decode", "switch_capacity"}
+                                     "deepseek_prefill", "deepseek_decode", "switch_capacity",
+                                     "mixtral_decode_fp8"}
