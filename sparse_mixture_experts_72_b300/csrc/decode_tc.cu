@@ -23,14 +23,23 @@
 // Hid rows of its group's token chunk, which every phase-0 tile of that
 // chunk writes: each phase-0 tile releases a per-chunk counter in global
 // memory (red.release.gpu after the last epilogue warp's stores), and the
-// producer of a phase-1 tile issues its weight copies for the first ring
-// slots, then acquires the counter (bounded spin) before the Hid copies.
+// token producer of a phase-1 tile acquires it (bounded spin) before its
+// Hid copies.
 //
-// Roles: warp 0 TMA producer (weights and activations; activations only with
-// E4M3 weights), warp 1 TMEM allocator and MMA issuer, warps 2-5 epilogue
-// (TMEM lane quarter warp % 4: 32 weight rows each, all token columns; the
-// rows are transposed through shared memory into 16-byte stores along the
-// output row), warps 6-13 E4M3 converters.
+// Decode streams every expert weight once; at a loaded memory latency of
+// about 4 us each SM must keep ~170 KB of weights in flight to reach the
+// HBM rate.  So the weights have a ring of their own, as deep as shared
+// memory allows and filled by a producer that does not wait for the
+// phase-1 hand-over (bf16: up to 12 slots of 16 KB; E4M3: up to 12 slots
+// of 16 KB of codes feeding a short bf16 ring), and the token rows a short
+// ring of their own.
+//
+// Roles: warp 0 token producer (TMA), warp 1 TMEM allocator and MMA issuer,
+// warps 2-5 epilogue (TMEM lane quarter warp % 4: 32 weight rows each, all
+// token columns, transposed through shared memory 16 tokens at a time into
+// 16-byte stores along the output rows), then the weight producer: warp 6
+// (TMA) with bf16 weights, or warps 6-13 with E4M3 weights, which copy the
+// codes and widen them to bf16.
 // Every wait is bounded: on expiry the CTA records MOE_ERR_TIMEOUT, lets its
 // copies land, drains its MMAs, frees TMEM and exits.
 #include "common.cuh"
@@ -45,15 +54,20 @@ constexpr int DM = 128;                    // weight rows per tile (MMA M)
 constexpr int DBOX = 16;                   // token rows per activation copy
 constexpr int D_A_BYTES = DM * DK * 2;     // one bf16 weight tile
 constexpr int D_Q_BYTES = DM * 2 * DK;     // one E4M3 slot: 128 rows x 128 codes (two k-blocks)
-constexpr int D_MAX_STAGES = 8;
-constexpr int D_Q_STAGES_MAX = 3;
+constexpr int D_W_MAX = 12;                // weight ring slots (bf16 tiles)
+constexpr int D_X_MAX = 4;                 // token ring slots
+constexpr int D_Q_MAX = 12;                // E4M3 ring slots
 constexpr int D_EPI_WARPS = 4;
 constexpr int D_CONV_WARPS = 8;
+constexpr int D_NT_MAX = 64;               // token rows per tile
 constexpr long long kDecodeDrainCycles = 200000000LL;
 
+// warps: 0 token producer, 1 MMA, 2-5 epilogue, then the weight producer
+// (one warp with bf16 weights, the E4M3 converters otherwise)
 template <bool FP8>
 struct DShape {
-  static constexpr int THREADS = 64 + D_EPI_WARPS * 32 + (FP8 ? D_CONV_WARPS * 32 : 0);
+  static constexpr int W_WARPS = FP8 ? D_CONV_WARPS : 1;
+  static constexpr int THREADS = (2 + D_EPI_WARPS + W_WARPS) * 32;
 };
 
 __device__ __forceinline__ bool d_wait_drain(uint32_t bar, uint32_t parity) {
@@ -136,29 +150,30 @@ __global__ void __launch_bounds__(DShape<FP8>::THREADS, 1)
   }
   const int NT = args.nt;
   const bool glu = args.mode0 == EPI_SWIGLU;
-  const int STAGES = args.stages;
-  const int QST = args.q_stages;
-  const int a_stage = glu ? 2 * D_A_BYTES : D_A_BYTES;   // weight bytes per ring slot
-  const int b_stage = NT * DK * 2;                       // activation bytes per ring slot
+  const int WST = args.w_stages, XST = args.x_stages, QST = args.q_stages;
+  const int a_stage = glu ? 2 * D_A_BYTES : D_A_BYTES;   // bf16 weight bytes per ring slot
+  const int x_stage = NT * DK * 2;                       // token bytes per ring slot
+  const int qslot = (glu ? 2 : 1) * D_Q_BYTES;           // E4M3 bytes per ring slot
   const int acc_cols = glu ? 2 * NT : NT;
   uint8_t* smem = smem_raw;
-  const uint32_t sA = smem_u32(smem);
-  const uint32_t sB = sA + STAGES * a_stage;
-  const uint32_t sQ = sB + STAGES * b_stage;                       // E4M3 slots (FP8)
-  const int q_bytes = FP8 ? QST * (glu ? 2 : 1) * D_Q_BYTES : 0;
-  uint16_t* tbuf = reinterpret_cast<uint16_t*>(smem + (sQ - sA) + q_bytes);  // [4][NT][32]
-  float* wv = reinterpret_cast<float*>(tbuf + D_EPI_WARPS * NT * 32);      // [4][NT]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(wv + D_EPI_WARPS * NT);
+  const uint32_t sW = smem_u32(smem);
+  const uint32_t sQ = sW + WST * a_stage;                // E4M3 slots (FP8)
+  const uint32_t sX = sQ + (FP8 ? QST * qslot : 0);
+  uint16_t* tbuf = reinterpret_cast<uint16_t*>(smem + (sX - sW) + XST * x_stage);  // [4][16][32]
+  float* wv = reinterpret_cast<float*>(tbuf + D_EPI_WARPS * 16 * 32);              // [4][NT]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(wv + D_EPI_WARPS * D_NT_MAX);
   const uint32_t bar0 = smem_u32(bars);
-  auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (D_MAX_STAGES + s); };
-  auto cfull_bar = [&](int s) { return bar0 + 8u * (2 * D_MAX_STAGES + s); };
-  auto tfull_bar = [&](int a) { return bar0 + 8u * (3 * D_MAX_STAGES + a); };
-  auto tempty_bar = [&](int a) { return bar0 + 8u * (3 * D_MAX_STAGES + 2 + a); };
-  const uint32_t drain_bar = bar0 + 8u * (3 * D_MAX_STAGES + 4);
-  auto qfull_bar = [&](int s) { return bar0 + 8u * (3 * D_MAX_STAGES + 5 + s); };
-  auto qempty_bar = [&](int s) { return bar0 + 8u * (3 * D_MAX_STAGES + 5 + D_Q_STAGES_MAX + s); };
-  constexpr int NUM_BARS = 3 * D_MAX_STAGES + 5 + 2 * D_Q_STAGES_MAX;
+  auto wfull_bar = [&](int s) { return bar0 + 8u * s; };
+  auto wempty_bar = [&](int s) { return bar0 + 8u * (D_W_MAX + s); };
+  auto xfull_bar = [&](int s) { return bar0 + 8u * (2 * D_W_MAX + s); };
+  auto xempty_bar = [&](int s) { return bar0 + 8u * (2 * D_W_MAX + D_X_MAX + s); };
+  auto qfull_bar = [&](int s) { return bar0 + 8u * (2 * D_W_MAX + 2 * D_X_MAX + s); };
+  auto qempty_bar = [&](int s) { return bar0 + 8u * (2 * D_W_MAX + 2 * D_X_MAX + D_Q_MAX + s); };
+  constexpr int TB = 2 * D_W_MAX + 2 * D_X_MAX + 2 * D_Q_MAX;
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (TB + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (TB + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (TB + 4);
+  constexpr int NUM_BARS = TB + 5;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   uint32_t* stored_cnt = tmem_holder + 2;   // [2]
@@ -172,24 +187,28 @@ __global__ void __launch_bounds__(DShape<FP8>::THREADS, 1)
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int unit = blockIdx.x, units = gridDim.x;
+  constexpr int WW0 = 2 + D_EPI_WARPS;   // first weight-producer warp
   int* status = args.status;
 
   pdl_launch_dependents();
   if (threadIdx.x == 0) {
-    for (int s = 0; s < D_MAX_STAGES; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
-      mbar_init(cfull_bar(s), D_CONV_WARPS);
+    for (int s = 0; s < D_W_MAX; ++s) {
+      mbar_init(wfull_bar(s), FP8 ? D_CONV_WARPS : 1);
+      mbar_init(wempty_bar(s), 1);
+    }
+    for (int s = 0; s < D_X_MAX; ++s) {
+      mbar_init(xfull_bar(s), 1);
+      mbar_init(xempty_bar(s), 1);
+    }
+    for (int s = 0; s < D_Q_MAX; ++s) {
+      mbar_init(qfull_bar(s), 1);
+      mbar_init(qempty_bar(s), D_CONV_WARPS);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
       mbar_init(tempty_bar(a), D_EPI_WARPS);
     }
     mbar_init(drain_bar, 1);
-    for (int s = 0; s < D_Q_STAGES_MAX; ++s) {
-      mbar_init(qfull_bar(s), 1);
-      mbar_init(qempty_bar(s), D_CONV_WARPS);
-    }
     *abort_flag = 0;
     stored_cnt[0] = stored_cnt[1] = 0u;
     fence_mbar_init();
@@ -252,91 +271,59 @@ __global__ void __launch_bounds__(DShape<FP8>::THREADS, 1)
   const uint32_t tmem_base = *tmem_holder;
   const int tiles0 = tp0[NG], total = tiles0 + tp1[NG];
   const int nwb0 = (args.F + DM - 1) / DM, nwb0s = (args.Fs + DM - 1) / DM;
-  long long tma_issued = 0, q_issued = 0;
+  long long x_issued = 0, w_issued = 0, q_issued = 0;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ token producer
+    // (with skip_producer set nothing is issued: the consumers' bounded waits
+    // run out and the abort path drains nothing)
     if (lane == 0 && !args.skip_producer) {
       uint32_t stage = 0, phase = 0;
-      long long issued = 0;
       bool ok = true;
       DCursor cur;
-      int pend_stage[D_MAX_STAGES];
       for (int tile = unit; tile < total && ok; tile += units) {
         int wb, tc;
         cur.locate(tile, tiles0, tp0, tp1, nch, wb, tc);
         const int ph = cur.phase, g = cur.g;
         const DTileView v = d_view(args, seg, ph, g, wb, tc, NT);
-        const CUtensorMap* mW = v.shared ? (ph ? &maps.ws1 : &maps.ws0) : (ph ? &maps.wa1 : &maps.wa0);
         const CUtensorMap* mX = v.shared ? (ph ? &maps.xs1 : &maps.xs0) : (ph ? &maps.xa1 : &maps.xa0);
-        const bool tglu = glu && ph == 0;
         const int nb = (v.n_valid + DBOX - 1) / DBOX;
-        const uint32_t tx = (FP8 ? 0u : (uint32_t)(tglu ? 2 : 1) * D_A_BYTES) +
-                            (uint32_t)nb * DBOX * DK * 2;
+        const uint32_t tx = (uint32_t)nb * DBOX * DK * 2;
         const int nkb = (v.K + DK - 1) / DK;
-        auto issue_w = [&](uint32_t st, int kb) {
-          if constexpr (!FP8) {
-            tma_load_2d(sA + st * a_stage, mW, full_bar(st), kb * DK, v.w_row);
-            if (tglu) tma_load_2d(sA + st * a_stage + D_A_BYTES, mW, full_bar(st), kb * DK, v.w_row_up);
-          }
-        };
-        auto issue_x = [&](uint32_t st, int kb) {
-          for (int b = 0; b < nb; ++b)
-            tma_load_2d(sB + st * b_stage + b * DBOX * DK * 2, mX, full_bar(st), kb * DK,
-                        v.row0 + b * DBOX);
-        };
-        int kb = 0;
         if (ph == 1) {
-          // the Hid rows of this chunk come from phase-0 tiles: copy the
-          // first slots' weights now, then wait for the rows
+          // the Hid rows of this chunk come from phase-0 tiles: wait until
+          // each of them has stored and released its part
           const int target = v.shared ? nwb0s : nwb0;
           const int* cnt = args.rows_done + cpre[g] + tc;
-          if (ld_acquire_gpu(cnt) < target) {
-            int pre = 0;
-            while (pre < nkb && pre < STAGES) {
-              if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, status)) { ok = false; break; }
-              mbar_arrive_expect_tx(full_bar(stage), tx);
-              issue_w(stage, pre);
-              pend_stage[pre] = (int)stage;
-              ++issued;
-              ++pre;
-              if (++stage == (uint32_t)STAGES) { stage = 0; phase ^= 1u; }
+          const long long t0 = clock64();
+          while (ld_acquire_gpu(cnt) < target) {
+            if (*abort_flag) { ok = false; break; }
+            if (clock64() - t0 > kWaitLimitCycles) {
+              *abort_flag = 1;
+              atomicExch(status, (int)MOE_ERR_TIMEOUT);
+              ok = false;
+              break;
             }
-            if (!ok) break;
-            const long long t0 = clock64();
-            while (ld_acquire_gpu(cnt) < target) {
-              if (*abort_flag) { ok = false; break; }
-              if (clock64() - t0 > kWaitLimitCycles) {
-                *abort_flag = 1;
-                atomicExch(status, (int)MOE_ERR_TIMEOUT);
-                ok = false;
-                break;
-              }
-            }
-            if (!ok) break;
-            fence_proxy_async_global();
-            for (int j = 0; j < pre; ++j) issue_x((uint32_t)pend_stage[j], j);
-            kb = pre;
-          } else {
-            fence_proxy_async_global();
           }
+          if (!ok) break;
+          fence_proxy_async_global();   // the TMA reads below see those plain stores
         }
-        for (; kb < nkb; ++kb) {
-          if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, status)) { ok = false; break; }
-          mbar_arrive_expect_tx(full_bar(stage), tx);
-          issue_w(stage, kb);
-          issue_x(stage, kb);
-          ++issued;
-          if (++stage == (uint32_t)STAGES) { stage = 0; phase ^= 1u; }
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait_bounded(xempty_bar(stage), phase ^ 1u, abort_flag, status)) { ok = false; break; }
+          mbar_arrive_expect_tx(xfull_bar(stage), tx);
+          for (int b = 0; b < nb; ++b)
+            tma_load_2d(sX + stage * x_stage + b * DBOX * DK * 2, mX, xfull_bar(stage), kb * DK,
+                        v.row0 + b * DBOX);
+          ++x_issued;
+          if (++stage == (uint32_t)XST) { stage = 0; phase ^= 1u; }
         }
       }
-      tma_issued = issued;
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      uint32_t ws = 0, wph = 0, xs = 0, xph = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       DCursor cur;
       for (int tile = unit; tile < total && ok; tile += units) {
@@ -351,24 +338,27 @@ __global__ void __launch_bounds__(DShape<FP8>::THREADS, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * acc_cols;
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, status)) { ok = false; break; }
-          if constexpr (FP8) {
-            if (!mbar_wait_bounded(cfull_bar(stage), phase, abort_flag, status)) { ok = false; break; }
+          if (!mbar_wait_bounded(wfull_bar(ws), wph, abort_flag, status) ||
+              !mbar_wait_bounded(xfull_bar(xs), xph, abort_flag, status)) {
+            ok = false;
+            break;
           }
           tc_fence_after();
-          const uint64_t adesc = sdesc_kmajor_sw128(sA + stage * a_stage);
-          const uint64_t bdesc = sdesc_kmajor_sw128(sB + stage * b_stage);
+          const uint64_t adesc = sdesc_kmajor_sw128(sW + ws * a_stage);
+          const uint64_t bdesc = sdesc_kmajor_sw128(sX + xs * x_stage);
 #pragma unroll
           for (int kk = 0; kk < DK / 16; ++kk) {
             const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
             umma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, accum);
             if (tglu) {
-              const uint64_t udesc = sdesc_kmajor_sw128(sA + stage * a_stage + D_A_BYTES);
+              const uint64_t udesc = sdesc_kmajor_sw128(sW + ws * a_stage + D_A_BYTES);
               umma_bf16(d_tmem + NT, udesc + 2 * kk, bdesc + 2 * kk, idesc, accum);
             }
           }
-          umma_commit(empty_bar(stage));
-          if (++stage == (uint32_t)STAGES) { stage = 0; phase ^= 1u; }
+          umma_commit(wempty_bar(ws));
+          umma_commit(xempty_bar(xs));
+          if (++ws == (uint32_t)WST) { ws = 0; wph ^= 1u; }
+          if (++xs == (uint32_t)XST) { xs = 0; xph ^= 1u; }
         }
         if (!ok) break;
         umma_commit(tfull_bar(acc));
@@ -377,15 +367,42 @@ __global__ void __launch_bounds__(DShape<FP8>::THREADS, 1)
       }
     }
     __syncwarp();
-  } else if (FP8 && warp >= 2 + D_EPI_WARPS) {
+  } else if (!FP8 && warp == WW0) {
+    // ------------------------------------------------------------ weight producer
+    // independent of the phase-1 hand-over, so the weight copies of the
+    // next tiles stream in while the token producer waits for Hid rows
+    if (lane == 0 && !args.skip_producer) {
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      DCursor cur;
+      for (int tile = unit; tile < total && ok; tile += units) {
+        int wb, tc;
+        cur.locate(tile, tiles0, tp0, tp1, nch, wb, tc);
+        const int ph = cur.phase;
+        const DTileView v = d_view(args, seg, ph, cur.g, wb, tc, NT);
+        const CUtensorMap* mW = v.shared ? (ph ? &maps.ws1 : &maps.ws0) : (ph ? &maps.wa1 : &maps.wa0);
+        const bool tglu = glu && ph == 0;
+        const int nkb = (v.K + DK - 1) / DK;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait_bounded(wempty_bar(stage), phase ^ 1u, abort_flag, status)) { ok = false; break; }
+          mbar_arrive_expect_tx(wfull_bar(stage), (uint32_t)(tglu ? 2 : 1) * D_A_BYTES);
+          tma_load_2d(sW + stage * a_stage, mW, wfull_bar(stage), kb * DK, v.w_row);
+          if (tglu) tma_load_2d(sW + stage * a_stage + D_A_BYTES, mW, wfull_bar(stage), kb * DK, v.w_row_up);
+          ++w_issued;
+          if (++stage == (uint32_t)WST) { stage = 0; phase ^= 1u; }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (FP8 && warp >= WW0) {
     // ------------------------------------------------------------ E4M3 -> bf16
     // The converter warps copy the E4M3 weight rows themselves (lane 0 of
-    // the first one issues the copies, QST slots of two k-blocks ahead) and
-    // widen each k-block's [128][64] codes (gate and up: [256][64]) into the
-    // bf16 weight tile of the ring slot the MMA reads.
-    const int cw = warp - (2 + D_EPI_WARPS);
+    // the first one issues the copies, QST slots of two k-blocks ahead: the
+    // bytes in flight from memory) and widen each k-block's [128][64] codes
+    // (gate and up: [256][64]) into the bf16 weight tile of the ring slot
+    // the MMA reads.
+    const int cw = warp - WW0;
     const bool issuer = cw == 0 && lane == 0;
-    const int qslot = (glu ? 2 : 1) * D_Q_BYTES;
     DCursor lcur;
     int l_tile = unit, l_kq = 0, l_nkq = 0, l_row = 0, l_row_up = 0;
     bool l_glu = false, l_shared = false;
@@ -414,7 +431,7 @@ __global__ void __launch_bounds__(DShape<FP8>::THREADS, 1)
         if (l_tile < total) l_locate();
       }
     };
-    if (issuer && l_tile < total) {
+    if (issuer && !args.skip_producer && l_tile < total) {
       l_locate();
       for (int s2 = 0; s2 < QST && l_tile < total; ++s2) issue(s2);
     }
@@ -429,11 +446,11 @@ __global__ void __launch_bounds__(DShape<FP8>::THREADS, 1)
       const int nkb = (v.K + DK - 1) / DK;
       for (int kb = 0; kb < nkb; ++kb) {
         bool got = (kb & 1) ? true : mbar_wait_bounded(qfull_bar(qs), qph, abort_flag, status);
-        if (got) got = mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, status);
+        if (got) got = mbar_wait_bounded(wempty_bar(stage), phase ^ 1u, abort_flag, status);
         if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
         const int h4 = (kb & 1) * 4;   // first 16-byte chunk of this k-block in a code row
         for (int half = 0; half < (tglu ? 2 : 1); ++half) {
-          const uint8_t* q = smem + (sQ - sA) + qs * qslot + half * D_Q_BYTES;
+          const uint8_t* q = smem + (sQ - sW) + qs * qslot + half * D_Q_BYTES;
           uint8_t* b = smem + stage * a_stage + half * D_A_BYTES;
 #pragma unroll 2
           for (int g8 = cw; g8 < DM / 8; g8 += D_CONV_WARPS) widen_e4m3_rows8(q, b, g8, h4, lane);
@@ -443,13 +460,13 @@ __global__ void __launch_bounds__(DShape<FP8>::THREADS, 1)
         const bool slot_done = (kb & 1) || kb == nkb - 1;
         if (lane == 0) {
           if (slot_done) mbar_arrive(qempty_bar(qs));
-          mbar_arrive(cfull_bar(stage));
+          mbar_arrive(wfull_bar(stage));
         }
-        if (++stage == (uint32_t)STAGES) { stage = 0; phase ^= 1u; }
+        if (++stage == (uint32_t)WST) { stage = 0; phase ^= 1u; }
         if (!slot_done) continue;
         if (cw == 0) {
           int refill_ok = 1;
-          if (issuer && l_tile < total) {
+          if (issuer && !args.skip_producer && l_tile < total) {
             if (mbar_wait_bounded(qempty_bar(qs), qph, abort_flag, status)) issue((int)qs);
             else refill_ok = 0;
           }
@@ -463,8 +480,8 @@ __global__ void __launch_bounds__(DShape<FP8>::THREADS, 1)
     const int q = warp & 3;                       // TMEM lane quarter
     const int ew = warp - 2;
     const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
-    uint16_t* tb = tbuf + ew * NT * 32;            // [NT][32] bf16: this warp's rows, transposed
-    float* wj = wv + ew * NT;                      // [NT] gate weight of each token column
+    uint16_t* tb = tbuf + ew * 16 * 32;            // [16][32] bf16: 16 tokens x this warp's rows
+    float* wj = wv + ew * D_NT_MAX;                // [NT] gate weight of each token column
     uint32_t acc = 0, acc_phase = 0;
     DCursor cur;
     for (int tile = unit; tile < total; tile += units) {
@@ -504,6 +521,9 @@ __global__ void __launch_bounds__(DShape<FP8>::THREADS, 1)
       tc_fence_after();
       const uint32_t taddr = tmem_base + lane_addr + acc * acc_cols;
       const int n16 = (v.n_valid + 15) / 16 * 16;
+      __nv_bfloat16* out = v.shared ? (ph ? args.out1s : args.out0s) : (ph ? args.out1 : args.out0);
+      const int ld = v.n_out;
+      const int col0 = wb * DM + q * 32;
       for (int c = 0; c < n16; c += 16) {
         uint32_t r[16], ru[16];
         tmem_ld_32x32b_x16(taddr + c, r);
@@ -512,28 +532,25 @@ __global__ void __launch_bounds__(DShape<FP8>::THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int j = c + i;
-          float z = __uint_as_float(r[i]) * sz + bz;
+          const float z = __uint_as_float(r[i]) * sz + bz;
           float o;
           if (mode == EPI_GELU) o = gelu_erf(z);
           else if (mode == EPI_SILU) o = silu_f(z);
           else if (mode == EPI_SWIGLU) o = silu_f(z) * (__uint_as_float(ru[i]) * su + bu);
           else o = (j < v.n_valid ? wj[j] : 0.0f) * z;
-          if (j < v.n_valid) tb[j * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+          tb[i * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
         }
-      }
-      __syncwarp();
-      // rows of the chunk: 32 consecutive output columns each, 16-byte stores
-      __nv_bfloat16* out = v.shared ? (ph ? args.out1s : args.out0s) : (ph ? args.out1 : args.out0);
-      const int ld = v.n_out;
-      const int col0 = wb * DM + q * 32;
-      for (int i = lane; i < v.n_valid * 4; i += 32) {
-        const int j = i >> 2, c8 = (i & 3) * 8;
-        if (col0 + c8 < v.n_out) {
-          const uint4 val = *reinterpret_cast<const uint4*>(tb + j * 32 + c8);
-          *reinterpret_cast<uint4*>(out + (int64_t)(v.row0 + j) * ld + col0 + c8) = val;
+        __syncwarp();
+        // 16 token rows of 32 consecutive output columns: 16-byte stores
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const int i = (lane >> 2) + 8 * h2, c8 = (lane & 3) * 8;
+          if (c + i < v.n_valid && col0 + c8 < v.n_out)
+            *reinterpret_cast<uint4*>(out + (int64_t)(v.row0 + c + i) * ld + col0 + c8) =
+                *reinterpret_cast<const uint4*>(tb + i * 32 + c8);
         }
+        __syncwarp();
       }
-      __syncwarp();
       if (ph == 0) {
         // the last epilogue warp of the tile releases the chunk's counter
         if (lane == 0 && atom_add_acqrel_cta(&stored_cnt[acc], 1u) == D_EPI_WARPS - 1) {
@@ -554,12 +571,18 @@ __global__ void __launch_bounds__(DShape<FP8>::THREADS, 1)
   tc_fence_before();
   __syncthreads();
   if (*abort_flag) {
+    // let every copy still in flight land before shared memory goes away
     if (warp == 0 && lane == 0) {
-      const long long first = tma_issued > STAGES ? tma_issued - STAGES : 0;
-      for (long long j = first; j < tma_issued; ++j)
-        d_wait_drain(full_bar((int)(j % STAGES)), (uint32_t)((j / STAGES) & 1));
+      const long long first = x_issued > XST ? x_issued - XST : 0;
+      for (long long j = first; j < x_issued; ++j)
+        d_wait_drain(xfull_bar((int)(j % XST)), (uint32_t)((j / XST) & 1));
     }
-    if (FP8 && warp == 2 + D_EPI_WARPS && lane == 0) {
+    if (!FP8 && warp == WW0 && lane == 0) {
+      const long long first = w_issued > WST ? w_issued - WST : 0;
+      for (long long j = first; j < w_issued; ++j)
+        d_wait_drain(wfull_bar((int)(j % WST)), (uint32_t)((j / WST) & 1));
+    }
+    if (FP8 && warp == WW0 && lane == 0) {
       const long long first = q_issued > QST ? q_issued - QST : 0;
       for (long long j = first; j < q_issued; ++j)
         d_wait_drain(qfull_bar((int)(j % QST)), (uint32_t)((j / QST) & 1));
@@ -579,18 +602,10 @@ __global__ void __launch_bounds__(DShape<FP8>::THREADS, 1)
 // ---------------------------------------------------------------------------
 // host side
 
-namespace {
-
-bool encode_e4m3(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int box_rows) {
-  return encode_tensor_map_u8(map, base, rows, K, 2 * DK, box_rows);
-}
-
-}  // namespace
-
 int decode_token_tile(int64_t group_rows_max) {
   int64_t nt = (group_rows_max + 15) / 16 * 16;
   if (nt < 16) nt = 16;
-  if (nt > 128) nt = 128;
+  if (nt > D_NT_MAX) nt = D_NT_MAX;
   return (int)nt;
 }
 
@@ -611,7 +626,8 @@ cudaError_t make_decode_plan(DecodePlan* plan, const DecodeArgs& args_in, const 
   const int w1r = glu ? 2 * a.F : a.F, w1rs = glu ? 2 * a.Fs : a.Fs;
   DecodeMaps& m = plan->maps;
   auto wmap = [&](CUtensorMap* mp, const void* base, int64_t rows, int64_t K) {
-    return fp8 ? encode_e4m3(mp, base, rows, K, DM) : encode_tensor_map_bf16(mp, base, rows, K, DK, DM);
+    return fp8 ? encode_tensor_map_u8(mp, base, rows, K, 2 * DK, DM)
+               : encode_tensor_map_bf16(mp, base, rows, K, DK, DM);
   };
   auto xmap = [&](CUtensorMap* mp, const void* base, int64_t rows, int64_t K) {
     return encode_tensor_map_bf16(mp, base, rows, K, DK, DBOX);
@@ -632,22 +648,34 @@ cudaError_t make_decode_plan(DecodePlan* plan, const DecodeArgs& args_in, const 
   if (!ok) return cudaErrorInvalidValue;
   if (!has_routed) { m.wa0 = m.ws0; m.wa1 = m.ws1; m.xa0 = m.xs0; m.xa1 = m.xs1; }
   if (!has_shared) { m.ws0 = m.wa0; m.ws1 = m.wa1; m.xs0 = m.xa0; m.xs1 = m.xa1; }
-  // shared memory: ring slots (weights + activations), E4M3 slots, the
-  // epilogue's transpose buffers and gate weights, barriers, group tables
+  // shared memory: the token ring, the weight ring (bf16: as deep as fits;
+  // E4M3: a short bf16 ring and as many code slots as fit, since those are
+  // the bytes in flight from memory), the transpose buffers, gate weights,
+  // barriers and group tables
   const int a_stage = glu ? 2 * D_A_BYTES : D_A_BYTES;
-  const int b_stage = NT * DK * 2;
-  const int q_stages = fp8 ? (glu ? 2 : 3) : 0;
-  const int q_bytes = q_stages * (glu ? 2 : 1) * D_Q_BYTES;
+  const int x_stage = NT * DK * 2;
+  const int qslot = (glu ? 2 : 1) * D_Q_BYTES;
   const int G = a.num_groups;
-  const int fixed = D_EPI_WARPS * NT * 32 * 2 + D_EPI_WARPS * NT * 4 +
-                    (3 * D_MAX_STAGES + 5 + 2 * D_Q_STAGES_MAX) * 8 + 16 + 5 * (G + 2) * 4;
-  const int budget = 232448 - 1024;
-  int stages = (budget - fixed - q_bytes) / (a_stage + b_stage);
-  if (stages > D_MAX_STAGES) stages = D_MAX_STAGES;
-  if (stages < 2) return cudaErrorInvalidValue;
-  a.stages = stages;
+  const int n_bars = 2 * D_W_MAX + 2 * D_X_MAX + 2 * D_Q_MAX + 5;
+  const int fixed = D_EPI_WARPS * 16 * 32 * 2 + D_EPI_WARPS * D_NT_MAX * 4 + n_bars * 8 + 16 +
+                    5 * (G + 2) * 4;
+  const int budget = 232448 - 1024 - fixed;
+  const int x_stages = D_X_MAX;
+  int w_stages, q_stages = 0;
+  if (fp8) {
+    w_stages = glu ? 2 : 3;
+    q_stages = (budget - x_stages * x_stage - w_stages * a_stage) / qslot;
+    if (q_stages > D_Q_MAX) q_stages = D_Q_MAX;
+    if (q_stages < 2) return cudaErrorInvalidValue;
+  } else {
+    w_stages = (budget - x_stages * x_stage) / a_stage;
+    if (w_stages > D_W_MAX) w_stages = D_W_MAX;
+    if (w_stages < 2) return cudaErrorInvalidValue;
+  }
+  a.w_stages = w_stages;
+  a.x_stages = x_stages;
   a.q_stages = q_stages;
-  plan->smem = stages * (a_stage + b_stage) + q_bytes + fixed;
+  plan->smem = w_stages * a_stage + q_stages * qslot + x_stages * x_stage + fixed;
   plan->args = a;
   plan->fp8 = fp8;
   plan->grid = num_sms;

@@ -177,9 +177,7 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                         const __grid_constant__ CUtensorMap tmB0,
                         const __grid_constant__ CUtensorMap tmA1,
-                        const __grid_constant__ CUtensorMap tmB1,
-                        const __grid_constant__ CUtensorMap tmA0s,
-                        const __grid_constant__ CUtensorMap tmA1s, const GemmArgs args) {
+                        const __grid_constant__ CUtensorMap tmB1, const GemmArgs args) {
   using S = GemmShape<PAIR, FP8>;
   constexpr int STAGES = S::STAGES;
   constexpr int GEMM_THREADS = S::THREADS;
@@ -295,10 +293,7 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
       tma_prefetch_desc(&tmA1);
       tma_prefetch_desc(&tmB1);
     }
-    if (PAIR == 2 && args.swap_tail) {
-      tma_prefetch_desc(&tmA0s);
-      if (two) tma_prefetch_desc(&tmA1s);
-    }
+
   }
   if (warp == 1) {
     if constexpr (PAIR == 2) {
@@ -393,11 +388,10 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
         const int b_row = glu ? cur.g * 2 * n_out + (int)rank * n_out + n * (BN / 2)
                               : cur.g * n_out + n * BN + (int)rank * S::B_ROWS;
         const int a_row_cta = a_row + (int)rank * 128;
-        // swapped tail tile: the token rows in 8-row copies, half per CTA
+        // swapped tail tile: each CTA copies the usual 128-row token box,
+        // starting at its half of the rows (the MMA's N reads only that half)
         const bool sw = swapped_tail(ph, rows_left);
         const int half = sw ? (rows_left + 15) / 16 * 8 : 0;
-        const CUtensorMap* mAs = ph ? &tmA1s : &tmA0s;
-        const uint32_t tx_sw = (uint32_t)((FP8 ? 0 : S::B_BYTES) + half * BK * 2);
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, status)) {
             ok = false;
@@ -406,15 +400,9 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
           if constexpr (PAIR == 2) {
             // both CTAs' copies complete on the even CTA's full barrier
             const uint32_t fb = mapa_shared(full_bar(stage), 0);
-            if (sw) {
-              if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * tx_sw);
-              for (int i = 0; i < half / 8; ++i)
-                tma_load_2d_pair(sA + stage * A_BYTES + i * 8 * BK * 2, mAs, fb, kb * BK,
-                                 a_row + (int)rank * half + 8 * i);
-            } else {
-              if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * S::TX_BYTES);
-              tma_load_2d_pair(sA + stage * A_BYTES, mA, fb, kb * BK, a_row_cta);
-            }
+            if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * S::TX_BYTES);
+            tma_load_2d_pair(sA + stage * A_BYTES, mA, fb, kb * BK,
+                             sw ? a_row + (int)rank * half : a_row_cta);
             if constexpr (!FP8) tma_load_2d_pair(sB + stage * S::B_BYTES, mB, fb, kb * BK, b_row);
           } else if constexpr (FP8) {
             mbar_arrive_expect_tx(full_bar(stage), a_slot);
@@ -974,9 +962,7 @@ cudaError_t make_gemm_plan(GemmPlan* plan, const GemmArgs& args_in, const __nv_b
     const __nv_bfloat16* a = p == 0 ? A : args.ph[0].out;
     if (!encode_tensor_map_bf16(&plan->tmA[p], a, a_rows, args.ph[p].K, BK, a_box))
       return cudaErrorInvalidValue;
-    // the token rows of swapped tail tiles, in copies of 8 rows (CTA pairs)
-    if (!encode_tensor_map_bf16(&plan->tmAs[p], a, a_rows, args.ph[p].K, BK, 8))
-      return cudaErrorInvalidValue;
+
     // SwiGLU tiles load 128 gate and 128 up rows: two 128-row boxes
     const int box_b = args.ph[p].mode == EPI_SWIGLU ? BN / 2 : BN / pair;
     const bool ok = fp8 ? encode_tensor_map_u8(&plan->tmB[p], B[p], b_rows[p], args.ph[p].K,
@@ -988,7 +974,7 @@ cudaError_t make_gemm_plan(GemmPlan* plan, const GemmArgs& args_in, const __nv_b
   if (np == 1) {
     plan->tmA[1] = plan->tmA[0];
     plan->tmB[1] = plan->tmB[0];
-    plan->tmAs[1] = plan->tmAs[0];
+
   }
   args.swap_tail = pair == 2 ? 1 : 0;
   plan->args = args;
@@ -1053,7 +1039,7 @@ static cudaError_t launch_gemm_t(const GemmPlan& plan, cudaStream_t st) {
   }
   if ((int)cfg.gridDim.x > PAIR * max_units) cfg.gridDim.x = PAIR * max_units;
   return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<PAIR, FP8>, plan.tmA[0], plan.tmB[0],
-                            plan.tmA[1], plan.tmB[1], plan.tmAs[0], plan.tmAs[1], plan.args);
+                            plan.tmA[1], plan.tmB[1], plan.args);
 }
 
 cudaError_t launch_gemm(const GemmPlan& plan, cudaStream_t st, LaunchTrace* tr) {

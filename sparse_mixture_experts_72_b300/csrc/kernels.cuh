@@ -75,7 +75,7 @@ struct RouterLaunch {
   int T, H, N, k;   // topk_idx == nullptr: no selection (expert choice)
 };
 int router_num_select_blocks(int T);
-int router_num_launches(int T, int N);
+int router_num_launches(int T, int N, int H);
 // fp32 SIMT router (any N <= MOE_MAX_EXPERTS)
 cudaError_t launch_router(const RouterLaunch& a, cudaStream_t st, LaunchTrace* tr);
 // p_mean[0..N) = 0 and *z_loss = 0 (nullable) in one launch (an empty batch)
@@ -139,8 +139,9 @@ struct RouterFused {
 cudaError_t launch_router_tc(const RouterLaunch& a, __nv_bfloat16* W3, int* ticket, int* status,
                              int* clear, int clear_n, const RouterFused* fused, cudaStream_t st,
                              LaunchTrace* tr);
-// whether the tensor-core router splits W_g itself (3 N_pad <= 256)
-bool router_stacked(int N);
+// whether the tensor-core router splits W_g itself (stacked planes, few x
+// tiles per CTA): no split kernel then
+bool router_own_split(int T, int N, int H);
 // chunks (router CTAs) and tokens per chunk of a fused router launch
 int router_fused_chunks(int T, int N, int H);
 int router_fused_chunk_tokens(int T, int N, int H);
@@ -266,7 +267,6 @@ struct GemmArgs {
 
 struct GemmPlan {
   CUtensorMap tmA[2];  // per phase: A [rows, K] bf16, box 64 x 128, 128B swizzle
-  CUtensorMap tmAs[2]; // per phase: the same A in boxes of 64 x 8 (swapped tail tiles)
   CUtensorMap tmB[2];  // per phase: B [G * n_out, K] bf16, box 64 x (256 / pair), 128B
                        // swizzle; FP8 B: E4M3 bytes, the same box unswizzled
   GemmArgs args;
@@ -320,7 +320,7 @@ struct DecodeArgs {
   int* status;
   int32_t skip_producer;         // failure injection: the TMA producer issues nothing
   // set by make_decode_plan
-  int32_t nt, stages, q_stages, tmem_cols;
+  int32_t nt, w_stages, x_stages, q_stages, tmem_cols;
 };
 struct DecodeTensors {
   const void *W1, *W2, *W1s, *W2s;            // weights (bf16 or E4M3 codes)
@@ -336,7 +336,7 @@ struct DecodePlan {
   int grid, smem;
   bool fp8;
 };
-// token rows per tile for groups of at most group_rows_max rows (16..128)
+// token rows per tile for groups of at most group_rows_max rows (16..64)
 int decode_token_tile(int64_t group_rows_max);
 // Upper bound of the token chunks (phase-1 counters) of a decode launch.
 inline int64_t decode_rows_done_len(int64_t R, int G, int64_t T) { return (R + 15) / 16 + G + (T + 15) / 16 + 1; }

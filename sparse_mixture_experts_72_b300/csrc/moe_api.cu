@@ -247,7 +247,7 @@ bool fused_dispatch(const moe_config_t& c) {
 // and the router's CTA 0 does it, but only when the router uses no ticket
 // (a fused dispatch).
 bool router_clears_status(const moe_config_t& c, bool fused) {
-  return c.N <= kRouterTcMaxExperts && c.T > 0 && (!router_stacked(c.N) || fused);
+  return c.N <= kRouterTcMaxExperts && c.T > 0 && (!router_own_split(c.T, c.N, c.H) || fused);
 }
 
 // Zeroes the status word and router ticket, unless the router's first kernel
@@ -538,7 +538,7 @@ int forward_launch_names(const moe_config_t& c, const char** names, int cap) {
   if (!router_clears_status(c, fz)) add("status_memset");
   if (c.T == 0) add("router_pmean");
   else if (tc) {
-    if (!router_stacked(c.N)) add("router_split");
+    if (!router_own_split(c.T, c.N, c.H)) add("router_split");
     add("router_tc");
   } else { add("router_logits"); add("router_select"); add("router_pmean"); }
   const bool rows = max_rows_of(c) > 0, sh = c.F_shared > 0 && c.T > 0;
@@ -612,7 +612,7 @@ MOE_API int32_t moe_forward_num_launches(const moe_config_t* cfg) {
   const moe_config_t& c = *cfg;
   const bool fz = fused_dispatch(c);
   int n = router_clears_status(c, fz) ? 0 : 1;  // status clear
-  n += router_num_launches(c.T, c.N);
+  n += router_num_launches(c.T, c.N, c.H);
   if (expert_choice(c)) {
     n += 1;                                 // expert-choice selection
     n += ffn_num_launches(c, false);        // gather + expert FFN (+ shared)

@@ -351,21 +351,29 @@ __global__ void __launch_bounds__(DF_THREADS) dispatch_fused_kernel(const Dispat
     const unsigned kept_mask = __ballot_sync(0xffffffffu, row >= 0);
     if (kept_mask == 0u || a.xp == nullptr) continue;
     const uint4* src = reinterpret_cast<const uint4*>(a.x + t * a.H);
-    for (int64_t v = lane; v < nvec; v += 32) {
-      const uint4 val = __ldg(src + v);
+    // four 16-byte loads in flight per lane, then their copies into every kept row
+    for (int64_t v0 = lane; v0 < nvec; v0 += 4 * 32) {
+      uint4 val[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (v0 + u * 32 < nvec) val[u] = __ldg(src + v0 + u * 32);
       unsigned mk = kept_mask;
       while (mk) {
         const int j = __ffs(mk) - 1;
         mk &= mk - 1;
         const int32_t r = __shfl_sync(0xffffffffu, row, j);
-        reinterpret_cast<uint4*>(a.xp + (int64_t)r * a.H)[v] = val;
+        uint4* dst = reinterpret_cast<uint4*>(a.xp + (int64_t)r * a.H);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (v0 + u * 32 < nvec) dst[v0 + u * 32] = val[u];
       }
     }
   }
 }
 
 cudaError_t launch_dispatch_fused(const DispatchFusedLaunch& a, cudaStream_t st, LaunchTrace* tr) {
-  // at most two CTAs per SM: every CTA is resident while CTA 0 scans
+  // at most two CTAs per SM (the kernel's registers allow that many):
+  // every CTA is resident while CTA 0 scans
   int64_t blocks = ((int64_t)a.T + DF_THREADS / 32 - 1) / (DF_THREADS / 32);
   if (blocks > 148 * 2) blocks = 148 * 2;
   if (blocks < 1) blocks = 1;

@@ -253,9 +253,9 @@ cudaError_t launch_router(const RouterLaunch& a, cudaStream_t st, LaunchTrace* t
                     static_cast<const float*>(a.p_part), a.p_mean, a.z_loss, nsel, N, T);
 }
 
-int router_num_launches(int T, int N) {
-  // tensor-core router: [W_g split kernel, unless the planes are stacked] + router
-  if (N <= kRouterTcMaxExperts) return T > 0 ? (router_stacked(N) ? 1 : 2) : 1;
+int router_num_launches(int T, int N, int H) {
+  // tensor-core router: [W_g split kernel, unless the router splits itself] + router
+  if (N <= kRouterTcMaxExperts) return T > 0 ? (router_own_split(T, N, H) ? 1 : 2) : 1;
   return T > 0 ? 3 : 1;
 }
 

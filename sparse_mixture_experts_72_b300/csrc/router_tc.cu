@@ -16,9 +16,11 @@
 //
 // Layout of the three planes:
 //   stacked (3 N_pad <= 256): rows p*N_pad + e of each ring slot's B tile, so
-//            one MMA with N = 3 N_pad covers all planes; the epilogue warps,
-//            idle during the main loop, split W_g's slice of every slot
-//            into shared memory themselves (no split kernel, no W3);
+//            one MMA with N = 3 N_pad covers all planes; when a CTA streams
+//            at most 16 x tiles the epilogue warps, idle during the main
+//            loop, split W_g's slice of every slot into shared memory
+//            themselves (no split kernel, no W3), else router_split_kernel
+//            writes W3 as a [3 N_pad, H_pad] matrix;
 //   along K (wider routers): W3[e, p*H_pad + h] written by
 //            router_split_kernel, one plane per MMA.
 // Consecutive k-steps go round-robin to `nacc` independent TMEM accumulators
@@ -573,7 +575,15 @@ int router_tc_num_ctas(int T, int N, int H) {
   return p.m_tiles * p.splits;
 }
 
-bool router_stacked(int N) { return 3 * ((N + 15) / 16 * 16) <= 256; }
+// The epilogue warps split W_g for each ring slot with a dependent L2 round
+// trip per slot; that pays off against a separate split launch only while a
+// CTA streams few x tiles.
+constexpr int kOwnSplitMaxTiles = 16;
+
+bool router_own_split(int T, int N, int H) {
+  const RouterTcPlan p = router_tc_plan(T, N, H);
+  return p.stacked && p.kb_per_split <= kOwnSplitMaxTiles;
+}
 
 int router_fused_chunks(int T, int N, int H) { return router_tc_num_ctas(T, N, H); }
 
@@ -589,9 +599,11 @@ cudaError_t launch_router_tc(const RouterLaunch& a, __nv_bfloat16* W3, int* tick
     trace_mark(tr, st);
     return launch_router_stats_zero(a.p_mean, a.z_loss, a.N, st);  // p_mean = 0, z_loss = 0
   }
-  // stacked planes: the router's epilogue warps split W_g per ring slot and
-  // (fused only, where it uses no ticket) its CTA 0 clears the header
-  if (!P.stacked) {
+  // stacked planes over few x tiles per CTA: the router's epilogue warps
+  // split W_g per ring slot and (fused only, where it uses no ticket) its
+  // CTA 0 clears the header; otherwise a split kernel writes W3 first
+  const bool own = router_own_split(a.T, a.N, a.H);
+  if (!own) {
     const int64_t total = (int64_t)P.N_pad * P.H_pad;
     int64_t blocks = (total + 255) / 256;
     if (blocks > 148 * 8) blocks = 148 * 8;
@@ -602,8 +614,11 @@ cudaError_t launch_router_tc(const RouterLaunch& a, __nv_bfloat16* W3, int* tick
   }
   CUtensorMap tmX, tmW;
   if (!encode_tensor_map_bf16(&tmX, a.x, a.T, a.H, RT_BK, RT_BM)) return cudaErrorInvalidValue;
-  if (P.stacked) {
+  if (own) {
     tmW = tmX;   // not read: the planes are written in shared memory
+  } else if (P.stacked) {
+    if (!encode_tensor_map_bf16(&tmW, W3, 3 * P.N_pad, P.H_pad, RT_BK, 3 * P.N_pad))
+      return cudaErrorInvalidValue;
   } else {
     if (!encode_tensor_map_bf16(&tmW, W3, P.N_pad, 3 * P.H_pad, RT_BK, P.N_pad))
       return cudaErrorInvalidValue;
@@ -633,11 +648,11 @@ cudaError_t launch_router_tc(const RouterLaunch& a, __nv_bfloat16* W3, int* tick
   args.kb_per_split = P.kb_per_split;
   args.splits = P.splits;
   args.work_bytes = P.work_bytes;
-  args.Wg = P.stacked ? a.Wg : nullptr;
+  args.Wg = own ? a.Wg : nullptr;
   args.H = a.H;
   args.local_rank = fused ? fused->local_rank : nullptr;
   args.blk_hist = fused ? fused->blk_hist : nullptr;
-  args.clear = (P.stacked && fused) ? clear : nullptr;
+  args.clear = (own && fused) ? clear : nullptr;
   args.clear_n = clear_n;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(P.m_tiles * P.splits);
