@@ -15,9 +15,14 @@
 // weight streaming dominates small batches), so with E4M3 weights converter
 // warps widen the codes to bf16 in shared memory as they stream in.
 //
-// A tile is (phase, group, 128 weight rows, up to NT token rows).  The
-// accumulator holds 128 TMEM lanes (weight rows) x NT columns (tokens), or
-// for SwiGLU the gate rows' NT columns followed by the up rows' NT columns.
+// A tile is (phase, group, 256 weight rows, up to NT token rows): two M=128
+// MMAs per k-step, half 0 into accumulator columns [0, NT) and half 1 into
+// [NT, 2 NT), TMEM lanes holding weight rows.  The halves are 256
+// consecutive weight rows (256 output columns, one copy of 32 KB per
+// k-block), or for SwiGLU's first Linear the 128 gate rows and the 128
+// matching up rows of 128 output columns.  Each copy instruction carries
+// 16-32 KB of weights: the per-copy cost, not the bytes in flight, bounded
+// an earlier 128-row version at 4.2 TB/s.
 // Tiles are ordered phase 0 before phase 1, then group, weight block and
 // token chunk (fastest); CTAs take them round-robin.  A phase-1 tile reads
 // Hid rows of its group's token chunk, which every phase-0 tile of that
@@ -26,13 +31,10 @@
 // token producer of a phase-1 tile acquires it (bounded spin) before its
 // Hid copies.
 //
-// Decode streams every expert weight once; at a loaded memory latency of
-// about 4 us each SM must keep ~170 KB of weights in flight to reach the
-// HBM rate.  So the weights have a ring of their own, as deep as shared
-// memory allows and filled by a producer that does not wait for the
-// phase-1 hand-over (bf16: up to 12 slots of 16 KB; E4M3: up to 12 slots
-// of 16 KB of codes feeding a short bf16 ring), and the token rows a short
-// ring of their own.
+// Decode streams every expert weight once.  The weights have a ring of
+// their own, filled by a producer that does not wait for the phase-1
+// hand-over (bf16: 32 KB slots; E4M3: 32 KB slots of codes feeding a short
+// bf16 ring), and the token rows a ring of small slots of their own.
 //
 // Roles: warp 0 token producer (TMA), warp 1 TMEM allocator and MMA issuer,
 // warps 2-5 epilogue (TMEM lane quarter warp % 4: 32 weight rows each, all
@@ -50,16 +52,16 @@ namespace moe {
 namespace {
 
 constexpr int DK = 64;                     // K per k-block: one 128-byte swizzled bf16 row
-constexpr int DM = 128;                    // weight rows per tile (MMA M)
+constexpr int DM = 128;                    // weight rows per MMA (M); a tile has two halves
 constexpr int DBOX = 16;                   // token rows per activation copy
 constexpr int D_A_BYTES = DM * DK * 2;     // one bf16 weight tile
-constexpr int D_Q_BYTES = DM * 2 * DK;     // one E4M3 slot: 128 rows x 128 codes (two k-blocks)
-constexpr int D_W_MAX = 12;                // weight ring slots (bf16 tiles)
-constexpr int D_X_MAX = 4;                 // token ring slots
-constexpr int D_Q_MAX = 12;                // E4M3 ring slots
+constexpr int D_Q_BYTES = DM * 2 * DK;     // E4M3 codes of one half: 128 rows x 128 codes (two k-blocks)
+constexpr int D_W_MAX = 8;                 // weight ring slots (bf16 tiles of both halves)
+constexpr int D_X_MAX = 16;                // token ring slots
+constexpr int D_Q_MAX = 8;                 // E4M3 ring slots (both halves)
 constexpr int D_EPI_WARPS = 4;
 constexpr int D_CONV_WARPS = 8;
-constexpr int D_NT_MAX = 64;               // token rows per tile
+constexpr int D_NT_MAX = 32;               // token rows per tile
 constexpr long long kDecodeDrainCycles = 200000000LL;
 
 // warps: 0 token producer, 1 MMA, 2-5 epilogue, then the weight producer
@@ -110,8 +112,10 @@ struct DTileView {
   int n_valid;    // token rows in this chunk
   int n_out;      // output columns of the phase (F, Fs or H)
   int K;          // reduction length of the phase
-  int w_row;      // first weight row of the tile (gate rows for SwiGLU)
-  int w_row_up;   // SwiGLU phase 0: first up row
+  int w_row;      // first weight row of half 0 (256 rows, or SwiGLU's 128 gate rows)
+  int w_row_up;   // SwiGLU phase 0: first of half 1's 128 up rows
+  int cols;       // output columns of the tile: 256, or 128 for SwiGLU
+  int col0;       // first output column
 };
 
 __device__ __forceinline__ DTileView d_view(const DecodeArgs& a, const int32_t* seg, int phase,
@@ -123,17 +127,19 @@ __device__ __forceinline__ DTileView d_view(const DecodeArgs& a, const int32_t* 
   v.row0 = base + tc * nt;
   v.n_valid = min(nt, v.rows - tc * nt);
   const bool glu = phase == 0 && a.mode0 == EPI_SWIGLU;
+  v.cols = glu ? DM : 2 * DM;
+  v.col0 = wb * v.cols;
   if (phase == 0) {
     v.n_out = v.shared ? a.Fs : a.F;
     v.K = a.H;
     const int wrows = glu ? 2 * v.n_out : v.n_out;   // weight rows of one expert
     const int gbase = v.shared ? 0 : g * wrows;
-    v.w_row = gbase + wb * DM;
-    v.w_row_up = gbase + v.n_out + wb * DM;
+    v.w_row = gbase + v.col0;
+    v.w_row_up = gbase + v.n_out + v.col0;
   } else {
     v.n_out = a.H;
     v.K = v.shared ? a.Fs : a.F;
-    v.w_row = (v.shared ? 0 : g * a.H) + wb * DM;
+    v.w_row = (v.shared ? 0 : g * a.H) + v.col0;
     v.w_row_up = 0;
   }
   return v;
@@ -151,10 +157,10 @@ __global__ void __launch_bounds__(DShape<FP8>::THREADS, 1)
   const int NT = args.nt;
   const bool glu = args.mode0 == EPI_SWIGLU;
   const int WST = args.w_stages, XST = args.x_stages, QST = args.q_stages;
-  const int a_stage = glu ? 2 * D_A_BYTES : D_A_BYTES;   // bf16 weight bytes per ring slot
+  constexpr int a_stage = 2 * D_A_BYTES;                 // bf16 weights of both halves
   const int x_stage = NT * DK * 2;                       // token bytes per ring slot
-  const int qslot = (glu ? 2 : 1) * D_Q_BYTES;           // E4M3 bytes per ring slot
-  const int acc_cols = glu ? 2 * NT : NT;
+  constexpr int qslot = 2 * D_Q_BYTES;                   // E4M3 codes of both halves
+  const int acc_cols = 2 * NT;                           // half 0's NT columns, then half 1's
   uint8_t* smem = smem_raw;
   const uint32_t sW = smem_u32(smem);
   const uint32_t sQ = sW + WST * a_stage;                // E4M3 slots (FP8)
@@ -229,8 +235,9 @@ __global__ void __launch_bounds__(DShape<FP8>::THREADS, 1)
   if (warp == 2) {
     // per group: token chunks, and prefixes over the groups of the chunks
     // and of both phases' tiles (one lane per run of groups, then a warp scan)
-    const int nwb0 = (args.F + DM - 1) / DM, nwb0s = (args.Fs + DM - 1) / DM;
-    const int nwb1 = (args.H + DM - 1) / DM;
+    const int cw0 = glu ? DM : 2 * DM;   // output columns per phase-0 tile
+    const int nwb0 = (args.F + cw0 - 1) / cw0, nwb0s = (args.Fs + cw0 - 1) / cw0;
+    const int nwb1 = (args.H + 2 * DM - 1) / (2 * DM);
     const int per = (NG + 31) / 32;
     const int g0 = lane * per;
     int c_loc = 0, t0_loc = 0, t1_loc = 0;
@@ -270,7 +277,8 @@ __global__ void __launch_bounds__(DShape<FP8>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   const int tiles0 = tp0[NG], total = tiles0 + tp1[NG];
-  const int nwb0 = (args.F + DM - 1) / DM, nwb0s = (args.Fs + DM - 1) / DM;
+  const int cw0 = glu ? DM : 2 * DM;
+  const int nwb0 = (args.F + cw0 - 1) / cw0, nwb0s = (args.Fs + cw0 - 1) / cw0;
   long long x_issued = 0, w_issued = 0, q_issued = 0;
 
   if (warp == 0) {
@@ -330,7 +338,6 @@ __global__ void __launch_bounds__(DShape<FP8>::THREADS, 1)
         int wb, tc;
         cur.locate(tile, tiles0, tp0, tp1, nch, wb, tc);
         const DTileView v = d_view(args, seg, cur.phase, cur.g, wb, tc, NT);
-        const bool tglu = glu && cur.phase == 0;
         const int n16 = (v.n_valid + 15) / 16 * 16;
         const uint32_t idesc = idesc_bf16_f32(DM, n16);
         const int nkb = (v.K + DK - 1) / DK;
@@ -349,11 +356,11 @@ __global__ void __launch_bounds__(DShape<FP8>::THREADS, 1)
 #pragma unroll
           for (int kk = 0; kk < DK / 16; ++kk) {
             const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
+            // half 0 (weight rows 0-127 / gate rows) into columns [0, NT),
+            // half 1 (rows 128-255 / up rows) into [NT, 2 NT)
+            const uint64_t udesc = sdesc_kmajor_sw128(sW + ws * a_stage + D_A_BYTES);
             umma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, accum);
-            if (tglu) {
-              const uint64_t udesc = sdesc_kmajor_sw128(sW + ws * a_stage + D_A_BYTES);
-              umma_bf16(d_tmem + NT, udesc + 2 * kk, bdesc + 2 * kk, idesc, accum);
-            }
+            umma_bf16(d_tmem + NT, udesc + 2 * kk, bdesc + 2 * kk, idesc, accum);
           }
           umma_commit(wempty_bar(ws));
           umma_commit(xempty_bar(xs));
@@ -385,7 +392,9 @@ __global__ void __launch_bounds__(DShape<FP8>::THREADS, 1)
         const int nkb = (v.K + DK - 1) / DK;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait_bounded(wempty_bar(stage), phase ^ 1u, abort_flag, status)) { ok = false; break; }
-          mbar_arrive_expect_tx(wfull_bar(stage), (uint32_t)(tglu ? 2 : 1) * D_A_BYTES);
+          mbar_arrive_expect_tx(wfull_bar(stage), (uint32_t)a_stage);
+          // 256 consecutive weight rows in one copy (the map's box), or
+          // SwiGLU's gate and up rows in two 128-row copies
           tma_load_2d(sW + stage * a_stage, mW, wfull_bar(stage), kb * DK, v.w_row);
           if (tglu) tma_load_2d(sW + stage * a_stage + D_A_BYTES, mW, wfull_bar(stage), kb * DK, v.w_row_up);
           ++w_issued;
@@ -421,7 +430,7 @@ __global__ void __launch_bounds__(DShape<FP8>::THREADS, 1)
     auto issue = [&](int slot) {
       const uint32_t dq = sQ + slot * qslot;
       const CUtensorMap* m = l_shared ? (l_ph ? &maps.ws1 : &maps.ws0) : (l_ph ? &maps.wa1 : &maps.wa0);
-      mbar_arrive_expect_tx(qfull_bar(slot), (uint32_t)(l_glu ? 2 : 1) * D_Q_BYTES);
+      mbar_arrive_expect_tx(qfull_bar(slot), (uint32_t)qslot);
       tma_load_2d(dq, m, qfull_bar(slot), l_kq * 2 * DK, l_row);
       if (l_glu) tma_load_2d(dq + D_Q_BYTES, m, qfull_bar(slot), l_kq * 2 * DK, l_row_up);
       ++q_issued;
@@ -442,14 +451,13 @@ __global__ void __launch_bounds__(DShape<FP8>::THREADS, 1)
       int wb, tc;
       cur.locate(tile, tiles0, tp0, tp1, nch, wb, tc);
       const DTileView v = d_view(args, seg, cur.phase, cur.g, wb, tc, NT);
-      const bool tglu = glu && cur.phase == 0;
       const int nkb = (v.K + DK - 1) / DK;
       for (int kb = 0; kb < nkb; ++kb) {
         bool got = (kb & 1) ? true : mbar_wait_bounded(qfull_bar(qs), qph, abort_flag, status);
         if (got) got = mbar_wait_bounded(wempty_bar(stage), phase ^ 1u, abort_flag, status);
         if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
         const int h4 = (kb & 1) * 4;   // first 16-byte chunk of this k-block in a code row
-        for (int half = 0; half < (tglu ? 2 : 1); ++half) {
+        for (int half = 0; half < 2; ++half) {
           const uint8_t* q = smem + (sQ - sW) + qs * qslot + half * D_Q_BYTES;
           uint8_t* b = smem + stage * a_stage + half * D_A_BYTES;
 #pragma unroll 2
@@ -491,22 +499,21 @@ __global__ void __launch_bounds__(DShape<FP8>::THREADS, 1)
       const DTileView v = d_view(args, seg, ph, g, wb, tc, NT);
       const bool tglu = glu && ph == 0;
       const int mode = ph ? EPI_SCALE : args.mode0;
-      const int col = wb * DM + q * 32 + lane;     // output column of this thread's weight row
-      const bool col_ok = col < v.n_out;
-      // per-row constants: bias and (E4M3) row scale of the gate / plain row and the up row
+      // per-row constants of this thread's two weight rows (half 0 and half
+      // 1: rows q*32 + lane of each, or for SwiGLU the gate and up rows of
+      // one output column): bias and E4M3 row scale
       const __nv_bfloat16* bias = v.shared ? (ph ? args.b2s : args.b1s) : (ph ? args.b2 : args.b1);
       const float* scale = v.shared ? (ph ? args.s2s : args.s1s) : (ph ? args.s2 : args.s1);
       const int wrows = tglu ? 2 * v.n_out : v.n_out;
       const int64_t rbase = v.shared ? 0 : (int64_t)g * wrows;
-      float bz = 0.0f, bu = 0.0f, sz = 1.0f, su = 1.0f;
-      if (col_ok) {
-        if (bias) {
-          bz = __bfloat162float(bias[rbase + col]);
-          if (tglu) bu = __bfloat162float(bias[rbase + v.n_out + col]);
-        }
-        if (FP8 && scale) {
-          sz = scale[rbase + col];
-          if (tglu) su = scale[rbase + v.n_out + col];
+      float bh[2] = {0.0f, 0.0f}, sh[2] = {1.0f, 1.0f};
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int c = tglu ? v.col0 + q * 32 + lane : v.col0 + h * DM + q * 32 + lane;
+        const int64_t r = tglu ? rbase + h * v.n_out + c : rbase + c;
+        if (c < v.n_out) {
+          if (bias) bh[h] = __bfloat162float(bias[r]);
+          if (FP8 && scale) sh[h] = scale[r];
         }
       }
       if (ph == 1) {
@@ -523,33 +530,37 @@ __global__ void __launch_bounds__(DShape<FP8>::THREADS, 1)
       const int n16 = (v.n_valid + 15) / 16 * 16;
       __nv_bfloat16* out = v.shared ? (ph ? args.out1s : args.out0s) : (ph ? args.out1 : args.out0);
       const int ld = v.n_out;
-      const int col0 = wb * DM + q * 32;
-      for (int c = 0; c < n16; c += 16) {
-        uint32_t r[16], ru[16];
-        tmem_ld_32x32b_x16(taddr + c, r);
-        if (tglu) tmem_ld_32x32b_x16(taddr + NT + c, ru);
-        tmem_ld_wait();
+      // SwiGLU combines the halves into one set of 32 output columns; other
+      // tiles store each half's 32 columns
+      for (int h = 0; h < (tglu ? 1 : 2); ++h) {
+        const int colw = v.col0 + h * DM + q * 32;   // this warp's first output column
+        for (int c = 0; c < n16; c += 16) {
+          uint32_t r[16], ru[16];
+          tmem_ld_32x32b_x16(taddr + h * NT + c, r);
+          if (tglu) tmem_ld_32x32b_x16(taddr + NT + c, ru);
+          tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int j = c + i;
-          const float z = __uint_as_float(r[i]) * sz + bz;
-          float o;
-          if (mode == EPI_GELU) o = gelu_erf(z);
-          else if (mode == EPI_SILU) o = silu_f(z);
-          else if (mode == EPI_SWIGLU) o = silu_f(z) * (__uint_as_float(ru[i]) * su + bu);
-          else o = (j < v.n_valid ? wj[j] : 0.0f) * z;
-          tb[i * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
-        }
-        __syncwarp();
-        // 16 token rows of 32 consecutive output columns: 16-byte stores
+          for (int i = 0; i < 16; ++i) {
+            const int j = c + i;
+            const float z = __uint_as_float(r[i]) * sh[h] + bh[h];
+            float o;
+            if (mode == EPI_GELU) o = gelu_erf(z);
+            else if (mode == EPI_SILU) o = silu_f(z);
+            else if (mode == EPI_SWIGLU) o = silu_f(z) * (__uint_as_float(ru[i]) * sh[1] + bh[1]);
+            else o = (j < v.n_valid ? wj[j] : 0.0f) * z;
+            tb[i * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+          }
+          __syncwarp();
+          // 16 token rows of 32 consecutive output columns: 16-byte stores
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          const int i = (lane >> 2) + 8 * h2, c8 = (lane & 3) * 8;
-          if (c + i < v.n_valid && col0 + c8 < v.n_out)
-            *reinterpret_cast<uint4*>(out + (int64_t)(v.row0 + c + i) * ld + col0 + c8) =
-                *reinterpret_cast<const uint4*>(tb + i * 32 + c8);
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int i = (lane >> 2) + 8 * h2, c8 = (lane & 3) * 8;
+            if (c + i < v.n_valid && colw + c8 < v.n_out)
+              *reinterpret_cast<uint4*>(out + (int64_t)(v.row0 + c + i) * ld + colw + c8) =
+                  *reinterpret_cast<const uint4*>(tb + i * 32 + c8);
+          }
+          __syncwarp();
         }
-        __syncwarp();
       }
       if (ph == 0) {
         // the last epilogue warp of the tile releases the chunk's counter
@@ -615,7 +626,7 @@ cudaError_t make_decode_plan(DecodePlan* plan, const DecodeArgs& args_in, const 
   const bool glu = a.mode0 == EPI_SWIGLU;
   a.nt = decode_token_tile(group_rows_max);
   const int NT = a.nt;
-  const int acc_cols = glu ? 2 * NT : NT;
+  const int acc_cols = 2 * NT;
   int cols = 32;
   while (cols < 2 * acc_cols) cols <<= 1;
   if (cols > 512) return cudaErrorInvalidValue;
@@ -625,23 +636,26 @@ cudaError_t make_decode_plan(DecodePlan* plan, const DecodeArgs& args_in, const 
   if (!has_routed && !has_shared) return cudaErrorInvalidValue;
   const int w1r = glu ? 2 * a.F : a.F, w1rs = glu ? 2 * a.Fs : a.Fs;
   DecodeMaps& m = plan->maps;
-  auto wmap = [&](CUtensorMap* mp, const void* base, int64_t rows, int64_t K) {
-    return fp8 ? encode_tensor_map_u8(mp, base, rows, K, 2 * DK, DM)
-               : encode_tensor_map_bf16(mp, base, rows, K, DK, DM);
+  // weight copies: 256 consecutive rows (both halves of a tile), or 128
+  // rows for SwiGLU's first Linear (gate and up rows are copied apart)
+  auto wmap = [&](CUtensorMap* mp, const void* base, int64_t rows, int64_t K, int box_rows) {
+    return fp8 ? encode_tensor_map_u8(mp, base, rows, K, 2 * DK, box_rows)
+               : encode_tensor_map_bf16(mp, base, rows, K, DK, box_rows);
   };
+  const int box0 = glu ? DM : 2 * DM;
   auto xmap = [&](CUtensorMap* mp, const void* base, int64_t rows, int64_t K) {
     return encode_tensor_map_bf16(mp, base, rows, K, DK, DBOX);
   };
   bool ok = true;
   if (has_routed) {
-    ok = ok && wmap(&m.wa0, t.W1, (int64_t)a.num_groups * w1r, a.H);
-    ok = ok && wmap(&m.wa1, t.W2, (int64_t)a.num_groups * a.H, a.F);
+    ok = ok && wmap(&m.wa0, t.W1, (int64_t)a.num_groups * w1r, a.H, box0);
+    ok = ok && wmap(&m.wa1, t.W2, (int64_t)a.num_groups * a.H, a.F, 2 * DM);
     ok = ok && xmap(&m.xa0, t.xp, t.R, a.H);
     ok = ok && xmap(&m.xa1, t.hid, t.R, a.F);
   }
   if (has_shared) {
-    ok = ok && wmap(&m.ws0, t.W1s, w1rs, a.H);
-    ok = ok && wmap(&m.ws1, t.W2s, a.H, a.Fs);
+    ok = ok && wmap(&m.ws0, t.W1s, w1rs, a.H, box0);
+    ok = ok && wmap(&m.ws1, t.W2s, a.H, a.Fs, 2 * DM);
     ok = ok && xmap(&m.xs0, t.x, a.shared_rows, a.H);
     ok = ok && xmap(&m.xs1, t.hid_s, a.shared_rows, a.Fs);
   }
@@ -652,18 +666,18 @@ cudaError_t make_decode_plan(DecodePlan* plan, const DecodeArgs& args_in, const 
   // E4M3: a short bf16 ring and as many code slots as fit, since those are
   // the bytes in flight from memory), the transpose buffers, gate weights,
   // barriers and group tables
-  const int a_stage = glu ? 2 * D_A_BYTES : D_A_BYTES;
+  const int a_stage = 2 * D_A_BYTES;
   const int x_stage = NT * DK * 2;
-  const int qslot = (glu ? 2 : 1) * D_Q_BYTES;
+  const int qslot = 2 * D_Q_BYTES;
   const int G = a.num_groups;
   const int n_bars = 2 * D_W_MAX + 2 * D_X_MAX + 2 * D_Q_MAX + 5;
   const int fixed = D_EPI_WARPS * 16 * 32 * 2 + D_EPI_WARPS * D_NT_MAX * 4 + n_bars * 8 + 16 +
                     5 * (G + 2) * 4;
   const int budget = 232448 - 1024 - fixed;
-  const int x_stages = D_X_MAX;
+  const int x_stages = fp8 ? D_X_MAX / 2 : D_X_MAX;   // E4M3: room for more code slots
   int w_stages, q_stages = 0;
   if (fp8) {
-    w_stages = glu ? 2 : 3;
+    w_stages = 2;
     q_stages = (budget - x_stages * x_stage - w_stages * a_stage) / qslot;
     if (q_stages > D_Q_MAX) q_stages = D_Q_MAX;
     if (q_stages < 2) return cudaErrorInvalidValue;

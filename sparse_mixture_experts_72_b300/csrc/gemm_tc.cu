@@ -623,6 +623,19 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
           if (P.bias) bz = __bfloat162float(P.bias[(size_t)cur.g * n_out + colw]);
           if (FP8 && P.b_scale) sz = P.b_scale[(size_t)cur.g * n_out + colw];
         }
+        // this warp's chunks: 8 tokens at c = cpart * 8 + i * CSTEP (at most
+        // NCH of them); their gate weights are fetched now, before the
+        // accumulator is ready: lane l holds the weight of token c_i + l % 8
+        constexpr int CSTEP = 8 * (EPI_WARPS / 4);
+        constexpr int NCH = 256 / CSTEP;
+        float wpre[NCH];
+#pragma unroll
+        for (int i = 0; i < NCH; ++i) {
+          const int tok = cpart * 8 + i * CSTEP + (lane & 7);
+          wpre[i] = (P.mode == EPI_SCALE && P.topk_w != nullptr && tok < rows_left)
+                        ? P.topk_w[P.perm[a_row + tok]]
+                        : 1.0f;
+        }
         int ok = 1;
         if (lane == 0) ok = mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, status) ? 1 : 0;
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -630,30 +643,37 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
         tc_fence_after();
         uint16_t* tb = trans_stage + (warp - 2) * 8 * 32;
         const uint32_t taddr = tmem_base + lane_addr + acc * BN;
-        for (int c = cpart * 8; c < n16; c += 8 * (EPI_WARPS / 4)) {
-          float wv = 1.0f;
-          if (P.mode == EPI_SCALE && P.topk_w != nullptr && lane < 8 && c + lane < rows_left)
-            wv = P.topk_w[P.perm[a_row + c + lane]];
-          uint32_t r[8];
-          tmem_ld_32x32b_x8(taddr + c, r);
+        // two chunks per TMEM round trip
+#pragma unroll
+        for (int i = 0; i < NCH; i += 2) {
+          const int c0 = cpart * 8 + i * CSTEP, c1 = c0 + CSTEP;
+          if (c0 >= n16) break;
+          uint32_t r0[8], r1[8];
+          tmem_ld_32x32b_x8(taddr + c0, r0);
+          if (c1 < n16) tmem_ld_32x32b_x8(taddr + c1, r1);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float z = __uint_as_float(r[i]) * sz + bz;
-            float o;
-            if (P.mode == EPI_GELU) o = gelu_erf(z);
-            else if (P.mode == EPI_SILU) o = silu_f(z);
-            else o = __shfl_sync(0xffffffffu, wv, i) * z;
-            tb[i * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+          for (int h = 0; h < 2; ++h) {
+            const int c = h ? c1 : c0;
+            if (c >= n16) break;
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+              const float z = __uint_as_float(h ? r1[t] : r0[t]) * sz + bz;
+              float o;
+              if (P.mode == EPI_GELU) o = gelu_erf(z);
+              else if (P.mode == EPI_SILU) o = silu_f(z);
+              else o = __shfl_sync(0xffffffffu, h ? wpre[i + 1] : wpre[i], t) * z;
+              tb[t * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+            }
+            __syncwarp();
+            {
+              const int t = lane >> 2, c8 = (lane & 3) * 8;
+              if (c + t < rows_left && colq + c8 < n_out)
+                *reinterpret_cast<uint4*>(P.out + (int64_t)(a_row + c + t) * P.ld_out + colq + c8) =
+                    *reinterpret_cast<const uint4*>(tb + t * 32 + c8);
+            }
+            __syncwarp();
           }
-          __syncwarp();
-          {
-            const int i = lane >> 2, c8 = (lane & 3) * 8;
-            if (c + i < rows_left && colq + c8 < n_out)
-              *reinterpret_cast<uint4*>(P.out + (int64_t)(a_row + c + i) * P.ld_out + colq + c8) =
-                  *reinterpret_cast<const uint4*>(tb + i * 32 + c8);
-          }
-          __syncwarp();
         }
       } else {
       const int r_in = warp_row0 + lane;

@@ -336,7 +336,7 @@ struct DecodePlan {
   int grid, smem;
   bool fp8;
 };
-// token rows per tile for groups of at most group_rows_max rows (16..64)
+// token rows per tile for groups of at most group_rows_max rows (16..32)
 int decode_token_tile(int64_t group_rows_max);
 // Upper bound of the token chunks (phase-1 counters) of a decode launch.
 inline int64_t decode_rows_done_len(int64_t R, int G, int64_t T) { return (R + 15) / 16 + G + (T + 15) / 16 + 1; }
