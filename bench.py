@@ -264,15 +264,17 @@ class ClockSampler:
 
 
 def algorithmic_work(w: wl.Workload, counts: np.ndarray, R: int):
-    """FLOPs and bytes each expert-FFN launch must do at minimum.
+    """FLOPs and bytes the expert-FFN launch must do at minimum (routed
+    experts and the shared expert, which is a group of the same launch).
 
     Per kept row: 2*H*F FLOPs in each Linear (two, or three for SwiGLU's
     gate, up and down).  Bytes: the weight
     matrices of every expert that received a row (F*H weights of 2 bytes
     (bf16) or 1 byte (E4M3) plus 4 bytes per row scale), the token rows
-    read (R*H bf16) and the weighted rows written (R*H bf16); the hidden
-    activations between the two Linears are the implementation's own round
-    trip and are not counted."""
+    read (R*H bf16) and the weighted rows written (R*H bf16); for the shared
+    expert its weights and T rows in and out; the hidden activations between
+    the two Linears are the implementation's own round trip and are not
+    counted."""
     hit = int((np.asarray(counts) > 0).sum())
     m = 3 if w.activation == "swiglu" else 2   # weight matrices per expert (gate, up, down)
     fp8 = w.weight_dtype == "e4m3"
@@ -281,17 +283,15 @@ def algorithmic_work(w: wl.Workload, counts: np.ndarray, R: int):
     def mats(F):                               # weight (+ scale) bytes of one expert
         scales = 4.0 * ((m - 1) * F + w.H) if fp8 else 0.0
         return wb * m * F * w.H + scales
-    out = {"expert_ffn": dict(flops=2.0 * m * R * w.H * w.F,
-                              bytes=hit * mats(w.F) + 2.0 * 2 * R * w.H)}
+    flops = 2.0 * m * R * w.H * w.F
+    nbytes = hit * mats(w.F) + 2.0 * 2 * R * w.H
     if w.F_shared:
-        Fs = w.F_shared
-        out["shared_ffn"] = dict(flops=2.0 * m * w.T * w.H * Fs,
-                                 bytes=mats(Fs) + 2.0 * 2 * w.T * w.H)
-    # the operand-swapped decode launch runs the routed and the shared experts
-    both = [out["expert_ffn"]] + ([out["shared_ffn"]] if w.F_shared else [])
-    out["expert_ffn_decode"] = dict(flops=sum(d["flops"] for d in both),
-                                    bytes=sum(d["bytes"] for d in both))
-    return out
+        # the shared expert is one more group of the same launch: all T rows
+        flops += 2.0 * m * w.T * w.H * w.F_shared
+        nbytes += mats(w.F_shared) + 2.0 * 2 * w.T * w.H
+    work = dict(flops=flops, bytes=nbytes)
+    # the token-row launch and the operand-swapped decode launch do the same work
+    return {"expert_ffn": work, "expert_ffn_decode": dict(work)}
 
 
 def forward_work(w: wl.Workload, counts: np.ndarray, R: int) -> dict:

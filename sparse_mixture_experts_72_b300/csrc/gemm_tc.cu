@@ -126,19 +126,33 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
 
 // Walks the tiles of a launch in increasing order: phase 0's tiles, then
 // phase 1's; inside a phase expert-major, then column block, then row block
-// (row block fastest, so the CTAs working at one time share a weight slab).
+// (row block fastest, so the CTAs working at one time share a weight slab),
+// and after the routed experts the shared expert (group G: rows_s rows in
+// mt_s row blocks of its own tensors).
 template <int TILE_M>
 struct TileCursor {
   int phase = 0, g = 0;
   __device__ __forceinline__ void locate(int tile, int tiles0, int nt0, int nt1,
-                                         const int32_t* mt_pre, const int32_t* seg, int& a_row,
-                                         int& rows_left, int& n, int& rb) {
+                                         const int32_t* mt_pre, const int32_t* seg, int G,
+                                         int mt_s, int rows_s, int& a_row, int& rows_left,
+                                         int& n, int& rb) {
     int local = tile;
     if (tile >= tiles0) {
       if (phase == 0) { phase = 1; g = 0; }
       local = tile - tiles0;
     }
     const int ntp = phase ? nt1 : nt0;
+    const int routed = mt_pre[G] * ntp;
+    if (local >= routed) {
+      g = G;
+      const int ls = local - routed;
+      n = ls / mt_s;
+      const int m = ls - n * mt_s;
+      rb = m;   // index into the shared expert's own counters
+      a_row = m * TILE_M;
+      rows_left = rows_s - m * TILE_M;
+      return;
+    }
     while (local >= mt_pre[g + 1] * ntp) ++g;   // groups without rows own no tiles
     const int mt = mt_pre[g + 1] - mt_pre[g];
     const int lg = local - mt_pre[g] * ntp;
@@ -159,7 +173,19 @@ struct PhaseView {
   const int32_t* perm;
   __nv_bfloat16* out;
   const float* b_scale;
-  __device__ __forceinline__ PhaseView(const GemmArgs& a, int p) {
+  __device__ __forceinline__ PhaseView(const GemmArgs& a, int p, bool sh) {
+    if (sh) {   // the shared expert: its own tensors, weight 1
+      n_out = p ? a.shp[1].n_out : a.shp[0].n_out;
+      K = p ? a.shp[1].K : a.shp[0].K;
+      mode = p ? a.shp[1].mode : a.shp[0].mode;
+      ld_out = p ? a.shp[1].ld_out : a.shp[0].ld_out;
+      bias = p ? a.shp[1].bias : a.shp[0].bias;
+      topk_w = nullptr;
+      perm = nullptr;
+      out = p ? a.shp[1].out : a.shp[0].out;
+      b_scale = p ? a.shp[1].b_scale : a.shp[0].b_scale;
+      return;
+    }
     n_out = p ? a.ph[1].n_out : a.ph[0].n_out;
     K = p ? a.ph[1].K : a.ph[0].K;
     mode = p ? a.ph[1].mode : a.ph[0].mode;
@@ -177,7 +203,11 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                         const __grid_constant__ CUtensorMap tmB0,
                         const __grid_constant__ CUtensorMap tmA1,
-                        const __grid_constant__ CUtensorMap tmB1, const GemmArgs args) {
+                        const __grid_constant__ CUtensorMap tmB1,
+                        const __grid_constant__ CUtensorMap tmSA0,
+                        const __grid_constant__ CUtensorMap tmSB0,
+                        const __grid_constant__ CUtensorMap tmSA1,
+                        const __grid_constant__ CUtensorMap tmSB1, const GemmArgs args) {
   using S = GemmShape<PAIR, FP8>;
   constexpr int STAGES = S::STAGES;
   constexpr int GEMM_THREADS = S::THREADS;
@@ -236,9 +266,22 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
   const int nt1 = two ? (args.ph[1].n_out + bno1 - 1) / bno1 : 0;
   const int nkb0 = (args.ph[0].K + BK - 1) / BK;
   const int nkb1 = two ? (args.ph[1].K + BK - 1) / BK : 0;
+  // the shared expert (group G): row blocks, and its phase-1 reduction length
+  const int rows_s = args.shared_rows;
+  const int mt_s = rows_s > 0 ? (rows_s + S::TILE_M - 1) / S::TILE_M : 0;
+  const int nt0s = mt_s > 0 ? (args.shp[0].n_out + bno0 - 1) / bno0 : 0;
+  const int nt1s = mt_s > 0 && two ? nt1 : 0;
+  const int nkb1s = mt_s > 0 && two ? (args.shp[1].K + BK - 1) / BK : 0;
   // releases that complete one row block: one per CTA of the tile for every
   // column block
-  const int rows_done_target = nt0 * PAIR;
+  const int rows_done_target = nt0 * PAIR, rows_done_target_s = nt0s * PAIR;
+  // per-tile choices between a routed expert and the shared one
+  auto map_a = [&](int ph, bool sh) { return sh ? (ph ? &tmSA1 : &tmSA0) : (ph ? &tmA1 : &tmA0); };
+  auto map_b = [&](int ph, bool sh) { return sh ? (ph ? &tmSB1 : &tmSB0) : (ph ? &tmB1 : &tmB0); };
+  auto nkb_of = [&](int ph, bool sh) { return ph ? (sh ? nkb1s : nkb1) : nkb0; };
+  auto n_out_of = [&](int ph, bool sh) {
+    return sh ? (ph ? args.shp[1].n_out : args.shp[0].n_out) : (ph ? args.ph[1].n_out : args.ph[0].n_out);
+  };
   // A copies: a_box rows each (the 128-row MMA also reads the rows after
   // them, which belong to no row of the tile and are never stored)
   constexpr bool SMALL_A = FP8 && PAIR == 1;
@@ -293,6 +336,14 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
       tma_prefetch_desc(&tmA1);
       tma_prefetch_desc(&tmB1);
     }
+    if (args.shared_rows > 0) {
+      tma_prefetch_desc(&tmSA0);
+      tma_prefetch_desc(&tmSB0);
+      if (two) {
+        tma_prefetch_desc(&tmSA1);
+        tma_prefetch_desc(&tmSB1);
+      }
+    }
 
   }
   if (warp == 1) {
@@ -336,8 +387,8 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
   }
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
-  const int tiles0 = mt_pre[G] * nt0;
-  const int total = tiles0 + (two ? mt_pre[G] * nt1 : 0);
+  const int tiles0 = mt_pre[G] * nt0 + mt_s * nt0s;
+  const int total = tiles0 + (two ? mt_pre[G] * nt1 + mt_s * nt1s : 0);
   long long tma_issued = 0;  // producer thread only
   long long q_issued = 0;    // FP8: the converters' issuing thread only
 
@@ -353,12 +404,14 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
       TileCursor<S::TILE_M> cur;
       for (int tile = unit; tile < total && ok; tile += units) {
         int a_row, rows_left, n, rb;
-        cur.locate(tile, tiles0, nt0, nt1, mt_pre, seg, a_row, rows_left, n, rb);
+        cur.locate(tile, tiles0, nt0, nt1, mt_pre, seg, G, mt_s, rows_s, a_row, rows_left, n, rb);
         const int ph = cur.phase;
-        const CUtensorMap* mA = ph ? &tmA1 : &tmA0;
-        const CUtensorMap* mB = ph ? &tmB1 : &tmB0;
-        const int nkb = ph ? nkb1 : nkb0;
-        const int n_out = ph ? args.ph[1].n_out : args.ph[0].n_out;
+        const bool sh = cur.g == G;
+        const int gi = sh ? 0 : cur.g;   // weight / bias block of the group
+        const CUtensorMap* mA = map_a(ph, sh);
+        const CUtensorMap* mB = map_b(ph, sh);
+        const int nkb = nkb_of(ph, sh);
+        const int n_out = n_out_of(ph, sh);
         if (SMALL_A && min(rows_left, S::TILE_M) > a_box) {
           // more rows in a group than the launch was planned for: the rows
           // past a_box are not loaded; report it (the tile is still run)
@@ -367,9 +420,10 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
         if (ph == 1) {
           // the A rows of this tile are phase 0's output: wait until every
           // phase-0 tile of the row block has been stored and released
-          const int* cnt = args.rows_done + rb;
+          const int* cnt = sh ? args.rows_done_s + rb : args.rows_done + rb;
+          const int target = sh ? rows_done_target_s : rows_done_target;
           const long long t0 = clock64();
-          while (ld_acquire_gpu(cnt) < rows_done_target) {
+          while (ld_acquire_gpu(cnt) < target) {
             if (*abort_flag) { ok = false; break; }
             if (clock64() - t0 > kWaitLimitCycles) {
               *abort_flag = 1;
@@ -385,8 +439,8 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
         // B rows of the tile: n_out-row blocks per group, or for SwiGLU 128
         // gate rows and the 128 matching up rows (the odd CTA of a pair, or
         // the second half of a single CTA's B tile, takes the up rows)
-        const int b_row = glu ? cur.g * 2 * n_out + (int)rank * n_out + n * (BN / 2)
-                              : cur.g * n_out + n * BN + (int)rank * S::B_ROWS;
+        const int b_row = glu ? gi * 2 * n_out + (int)rank * n_out + n * (BN / 2)
+                              : gi * n_out + n * BN + (int)rank * S::B_ROWS;
         const int a_row_cta = a_row + (int)rank * 128;
         // swapped tail tile: each CTA copies the usual 128-row token box,
         // starting at its half of the rows (the MMA's N reads only that half)
@@ -435,9 +489,9 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
       bool ok = true;
       TileCursor<S::TILE_M> cur;
       for (int tile = unit; tile < total && ok; tile += units) {
-        const int nkb = tile < tiles0 ? nkb0 : nkb1;
         int a_row, rows_left, n, rb;
-        cur.locate(tile, tiles0, nt0, nt1, mt_pre, seg, a_row, rows_left, n, rb);
+        cur.locate(tile, tiles0, nt0, nt1, mt_pre, seg, G, mt_s, rows_s, a_row, rows_left, n, rb);
+        const int nkb = nkb_of(cur.phase, cur.g == G);
         // swapped tail tile: M = the 256 weight rows, N = the token rows rounded to 16
         const bool sw = swapped_tail(cur.phase, rows_left);
         const uint32_t idesc =
@@ -511,15 +565,17 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
     const CUtensorMap* l_map = &tmB0;
     auto l_locate = [&]() {
       int a_row, rows_left, n, rb;
-      lcur.locate(l_tile, tiles0, nt0, nt1, mt_pre, seg, a_row, rows_left, n, rb);
+      lcur.locate(l_tile, tiles0, nt0, nt1, mt_pre, seg, G, mt_s, rows_s, a_row, rows_left, n, rb);
       const int ph = lcur.phase;
-      l_map = ph ? &tmB1 : &tmB0;
-      l_nkq = ((ph ? nkb1 : nkb0) + 1) / 2;  // Q slots of the tile
-      l_n_out = ph ? args.ph[1].n_out : args.ph[0].n_out;
+      const bool sh = lcur.g == G;
+      const int gi = sh ? 0 : lcur.g;
+      l_map = map_b(ph, sh);
+      l_nkq = (nkb_of(ph, sh) + 1) / 2;  // Q slots of the tile
+      l_n_out = n_out_of(ph, sh);
       l_glu = (ph ? args.ph[1].mode : args.ph[0].mode) == EPI_SWIGLU;
       // the B rows the producer of a bf16 tile would load (see above)
-      l_brow = l_glu ? lcur.g * 2 * l_n_out + (int)rank * l_n_out + n * (BN / 2)
-                     : lcur.g * l_n_out + n * BN + (int)rank * S::B_ROWS;
+      l_brow = l_glu ? gi * 2 * l_n_out + (int)rank * l_n_out + n * (BN / 2)
+                     : gi * l_n_out + n * BN + (int)rank * S::B_ROWS;
     };
     auto issue = [&](int slot) {
       const uint32_t dq = sBq + slot * S::BQ_BYTES;
@@ -544,8 +600,12 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
     }
     uint32_t qs = 0, qph = 0, cs = 0, cph = 0;
     bool ok = true;
+    TileCursor<S::TILE_M> ccur;
     for (int tile = unit; tile < total && ok; tile += units) {
-      const int nkb = tile < tiles0 ? nkb0 : nkb1;
+      int a_row_c, rows_left_c, n_c, rb_c;
+      ccur.locate(tile, tiles0, nt0, nt1, mt_pre, seg, G, mt_s, rows_s, a_row_c, rows_left_c, n_c,
+                  rb_c);
+      const int nkb = nkb_of(ccur.phase, ccur.g == G);
       for (int kb = 0; kb < nkb; ++kb) {
         // k-block kb is half kb % 2 of Q slot kb / 2 of the tile
         bool got = (kb & 1) ? true : mbar_wait_bounded(qfull_bar(qs), qph, abort_flag, status);
@@ -607,8 +667,10 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
     TileCursor<S::TILE_M> cur;
     for (int tile = unit; tile < total; tile += units) {
       int a_row, rows_left, n, rb;
-      cur.locate(tile, tiles0, nt0, nt1, mt_pre, seg, a_row, rows_left, n, rb);
-      const PhaseView P(args, cur.phase);
+      cur.locate(tile, tiles0, nt0, nt1, mt_pre, seg, G, mt_s, rows_s, a_row, rows_left, n, rb);
+      const bool sh = cur.g == G;
+      const int gi = sh ? 0 : cur.g;   // weight / bias block of the group
+      const PhaseView P(args, cur.phase, sh);
       const int n_out = P.n_out;
       if (swapped_tail(cur.phase, rows_left)) {
         // Swapped tail tile: output columns in TMEM lanes, token rows in
@@ -620,8 +682,8 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
         const int colw = colq + lane;
         float bz = 0.0f, sz = 1.0f;
         if (colw < n_out) {
-          if (P.bias) bz = __bfloat162float(P.bias[(size_t)cur.g * n_out + colw]);
-          if (FP8 && P.b_scale) sz = P.b_scale[(size_t)cur.g * n_out + colw];
+          if (P.bias) bz = __bfloat162float(P.bias[(size_t)gi * n_out + colw]);
+          if (FP8 && P.b_scale) sz = P.b_scale[(size_t)gi * n_out + colw];
         }
         // this warp's chunks: 8 tokens at c = cpart * 8 + i * CSTEP (at most
         // NCH of them); their gate weights are fetched now, before the
@@ -698,11 +760,11 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
 #pragma unroll
         for (int j2 = lane * 2; j2 < EPI_COLS; j2 += 64) {
           int c2 = col0 + j2;
-          size_t off = (size_t)cur.g * n_out + c2;
+          size_t off = (size_t)gi * n_out + c2;
           if (glu) {
             const bool up = j2 >= wcols;
             c2 = col0 + (up ? j2 - wcols : j2);
-            off = (size_t)cur.g * 2 * n_out + (up ? n_out : 0) + c2;
+            off = (size_t)gi * 2 * n_out + (up ? n_out : 0) + c2;
           }
           if (has_bias) {
             uint32_t b = 0u;
@@ -832,7 +894,7 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
         if (lane == 0 && atom_add_acqrel_cta(&stored_cnt[acc], 1u) == EPI_WARPS - 1) {
           stored_cnt[acc] = 0u;
           fence_proxy_async_global();
-          red_release_gpu_add(args.rows_done + rb, 1);
+          red_release_gpu_add((sh ? args.rows_done_s : args.rows_done) + rb, 1);
         }
       }
       tc_fence_before();
@@ -957,56 +1019,93 @@ bool encode_tensor_map_u8(CUtensorMap* map, const void* base, int64_t rows, int6
 
 cudaError_t make_gemm_plan(GemmPlan* plan, const GemmArgs& args_in, const __nv_bfloat16* A,
                            int64_t a_rows, const void* const B[2], const int64_t b_rows[2],
-                           bool fp8, int64_t group_rows_max, int num_sms) {
+                           bool fp8, int64_t group_rows_max, int num_sms,
+                           const __nv_bfloat16* A_s, const void* const* B_s,
+                           const int64_t* b_rows_s) {
   GemmArgs args = args_in;
   const int np = args.num_phases;
-  if (np < 1 || np > 2 || a_rows <= 0) return cudaErrorInvalidValue;
-  for (int p = 0; p < np; ++p)
-    if (b_rows[p] <= 0 || args.ph[p].K <= 0 || args.ph[p].n_out <= 0 ||
-        (fp8 && (args.ph[p].K % 16 != 0 || args.ph[p].b_scale == nullptr)))
+  const bool sh = args.shared_rows > 0;
+  if (np < 1 || np > 2 || a_rows < 0 || (a_rows == 0 && !sh)) return cudaErrorInvalidValue;
+  if (sh && (A_s == nullptr || B_s == nullptr || b_rows_s == nullptr || args.shp[0].out == nullptr))
+    return cudaErrorInvalidValue;
+  for (int p = 0; p < np; ++p) {
+    if ((a_rows > 0 && b_rows[p] <= 0) || args.ph[p].K <= 0 || args.ph[p].n_out <= 0 ||
+        (fp8 && (args.ph[p].K % 16 != 0 || (a_rows > 0 && args.ph[p].b_scale == nullptr))))
       return cudaErrorInvalidValue;
+    if (sh && (b_rows_s[p] <= 0 || args.shp[p].K <= 0 || args.shp[p].n_out <= 0 ||
+               (fp8 && (args.shp[p].K % 16 != 0 || args.shp[p].b_scale == nullptr))))
+      return cudaErrorInvalidValue;
+  }
   if (np == 2 && (args.rows_done == nullptr || args.ph[1].K != args.ph[0].n_out ||
                   args.ph[0].ld_out != args.ph[0].n_out))
     return cudaErrorInvalidValue;
+  if (np == 2 && sh && (args.rows_done_s == nullptr || args.shp[1].K != args.shp[0].n_out ||
+                        args.shp[0].ld_out != args.shp[0].n_out || args.shp[1].n_out != args.ph[1].n_out))
+    return cudaErrorInvalidValue;
   // CTA pairs (256-row tiles) once the average group holds enough rows to
   // fill them; single CTAs (128-row tiles) for decode-sized groups.
-  const int64_t avg_rows = a_rows / (args.num_groups > 0 ? args.num_groups : 1);
+  const int64_t avg_rows = a_rows > 0 ? a_rows / (args.num_groups > 0 ? args.num_groups : 1)
+                                      : (int64_t)args.shared_rows;
   const int pair = (avg_rows >= 192 && num_sms >= 2) ? 2 : 1;
   // FP8 single-CTA tiles copy the A rows a group can hold, in steps of 16
   int a_box = 128;
   if (fp8 && pair == 1 && group_rows_max > 0 && group_rows_max < 128)
     a_box = (int)((group_rows_max + 15) / 16 * 16);
   args.a_box = a_box;
-  for (int p = 0; p < np; ++p) {
-    // phase 1 reads phase 0's output [a_rows, n_out0] as its A operand
-    const __nv_bfloat16* a = p == 0 ? A : args.ph[0].out;
-    if (!encode_tensor_map_bf16(&plan->tmA[p], a, a_rows, args.ph[p].K, BK, a_box))
-      return cudaErrorInvalidValue;
-
+  auto encode_b = [&](CUtensorMap* m, const void* b, int64_t rows, int p, int K) {
     // SwiGLU tiles load 128 gate and 128 up rows: two 128-row boxes
     const int box_b = args.ph[p].mode == EPI_SWIGLU ? BN / 2 : BN / pair;
-    const bool ok = fp8 ? encode_tensor_map_u8(&plan->tmB[p], B[p], b_rows[p], args.ph[p].K,
-                                                 2 * BK, box_b)
-                        : encode_tensor_map_bf16(&plan->tmB[p], B[p], b_rows[p], args.ph[p].K,
-                                                 BK, box_b);
-    if (!ok) return cudaErrorInvalidValue;
+    return fp8 ? encode_tensor_map_u8(m, b, rows, K, 2 * BK, box_b)
+               : encode_tensor_map_bf16(m, b, rows, K, BK, box_b);
+  };
+  for (int p = 0; p < np; ++p) {
+    if (a_rows > 0) {
+      // phase 1 reads phase 0's output [a_rows, n_out0] as its A operand
+      const __nv_bfloat16* a = p == 0 ? A : args.ph[0].out;
+      if (!encode_tensor_map_bf16(&plan->tmA[p], a, a_rows, args.ph[p].K, BK, a_box))
+        return cudaErrorInvalidValue;
+      if (!encode_b(&plan->tmB[p], B[p], b_rows[p], p, args.ph[p].K)) return cudaErrorInvalidValue;
+    }
+    if (sh) {
+      const __nv_bfloat16* a = p == 0 ? A_s : args.shp[0].out;
+      if (!encode_tensor_map_bf16(&plan->tmS[2 * p], a, args.shared_rows, args.shp[p].K, BK, a_box))
+        return cudaErrorInvalidValue;
+      if (!encode_b(&plan->tmS[2 * p + 1], B_s[p], b_rows_s[p], p, args.shp[p].K))
+        return cudaErrorInvalidValue;
+    }
   }
   if (np == 1) {
     plan->tmA[1] = plan->tmA[0];
     plan->tmB[1] = plan->tmB[0];
-
+    plan->tmS[2] = plan->tmS[0];
+    plan->tmS[3] = plan->tmS[1];
+  }
+  // maps a launch never reads still have to be valid descriptors
+  if (a_rows == 0) {
+    plan->tmA[0] = plan->tmS[0];
+    plan->tmB[0] = plan->tmS[1];
+    plan->tmA[1] = plan->tmS[2];
+    plan->tmB[1] = plan->tmS[3];
+  }
+  if (!sh) {
+    plan->tmS[0] = plan->tmA[0];
+    plan->tmS[1] = plan->tmB[0];
+    plan->tmS[2] = plan->tmA[1];
+    plan->tmS[3] = plan->tmB[1];
   }
   args.swap_tail = pair == 2 ? 1 : 0;
   plan->args = args;
   plan->pair = pair;
   plan->fp8 = fp8;
   const int64_t tile_m = 128 * pair;
-  int64_t n_tiles = 0;
+  int64_t n_tiles = 0, n_tiles_s = 0;
   for (int p = 0; p < np; ++p) {
     const int bno = args.ph[p].mode == EPI_SWIGLU ? BN / 2 : BN;
     n_tiles += (args.ph[p].n_out + bno - 1) / bno;
+    if (sh) n_tiles_s += (args.shp[p].n_out + bno - 1) / bno;
   }
-  const int64_t max_tiles = ((a_rows + tile_m - 1) / tile_m + args.num_groups) * n_tiles;
+  const int64_t max_tiles = ((a_rows + tile_m - 1) / tile_m + args.num_groups) * n_tiles +
+                            (sh ? (args.shared_rows + tile_m - 1) / tile_m * n_tiles_s : 0);
   const int64_t max_units = num_sms / pair;
   const int64_t units = max_tiles < max_units ? max_tiles : max_units;
   plan->grid = (int)(units * pair);
@@ -1059,7 +1158,8 @@ static cudaError_t launch_gemm_t(const GemmPlan& plan, cudaStream_t st) {
   }
   if ((int)cfg.gridDim.x > PAIR * max_units) cfg.gridDim.x = PAIR * max_units;
   return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<PAIR, FP8>, plan.tmA[0], plan.tmB[0],
-                            plan.tmA[1], plan.tmB[1], plan.args);
+                            plan.tmA[1], plan.tmB[1], plan.tmS[0], plan.tmS[1], plan.tmS[2],
+                            plan.tmS[3], plan.args);
 }
 
 cudaError_t launch_gemm(const GemmPlan& plan, cudaStream_t st, LaunchTrace* tr) {

@@ -263,9 +263,16 @@ struct GemmArgs {
                                  // FP8 single-CTA tiles the bound on a group's rows
   int32_t swap_tail;             // CTA pairs: a group's last row block of fewer than 256
                                  // rows runs operand-swapped (set by make_gemm_plan)
+  // the always-on shared expert as group G of the same launch: shared_rows
+  // rows (T; 0 = none) of its own A tensors (x, then its Hid), its own
+  // weights, outputs (shp[p].out) and row-block counters; weight 1
+  int32_t shared_rows;
+  GemmPhase shp[2];
+  int32_t* rows_done_s;
 };
 
 struct GemmPlan {
+  CUtensorMap tmS[4];  // shared expert: A phase 0 (x), B phase 0 (W1s), A phase 1 (its Hid), B phase 1
   CUtensorMap tmA[2];  // per phase: A [rows, K] bf16, box 64 x 128, 128B swizzle
   CUtensorMap tmB[2];  // per phase: B [G * n_out, K] bf16, box 64 x (256 / pair), 128B
                        // swizzle; FP8 B: E4M3 bytes, the same box unswizzled
@@ -286,9 +293,13 @@ inline int64_t gemm_rows_done_len(int64_t a_rows, int G) { return (a_rows + 127)
 // group_rows_max bounds the rows of any one group (tokens per expert); FP8
 // launches of small groups copy only that many A rows per k-block (a group
 // that exceeds it records MOE_ERR_INVALID_ARG in the status word).
+// With args.shared_rows > 0, A_s is its phase-0 A tensor (x) and
+// B_s / b_rows_s its weights (W1s, W2s); a_rows may then be 0.
 cudaError_t make_gemm_plan(GemmPlan* plan, const GemmArgs& args, const __nv_bfloat16* A,
                            int64_t a_rows, const void* const B[2], const int64_t b_rows[2],
-                           bool fp8, int64_t group_rows_max, int num_sms);
+                           bool fp8, int64_t group_rows_max, int num_sms,
+                           const __nv_bfloat16* A_s = nullptr, const void* const* B_s = nullptr,
+                           const int64_t* b_rows_s = nullptr);
 cudaError_t launch_gemm(const GemmPlan& plan, cudaStream_t st, LaunchTrace* tr);
 bool tensor_map_encoder_available();
 // TMA map of a row-major byte matrix [rows, K] (E4M3 codes), 128B swizzle

@@ -443,14 +443,16 @@ moe_status_t do_ffn(const moe_config_t& c, const uint16_t* x, const int32_t* per
     MOE_CUDA(launch_decode(p, st, tr));
     return MOE_OK;
   }
-  if (R > 0) {
+  const bool sh = c.F_shared > 0 && c.T > 0;
+  if (R > 0 || sh) {
     bf* xp = at<bf>(ws, L.xp);
     bf* hid = at<bf>(ws, L.hid);
-    if (!gathered)
+    if (!gathered && R > 0)
       MOE_CUDA(launch_gather(reinterpret_cast<const bf*>(x), perm, offsets, c.N, slots_of(c), R,
                              c.H, xp, st, tr));
     // one persistent launch: Hid = act(X_perm W1_e^T + b1_e), then
-    // y = w * (Hid W2_e^T + b2_e), row block by row block
+    // y = w * (Hid W2_e^T + b2_e), row block by row block; the shared expert
+    // is group N of the same launch (all T rows, weight 1)
     GemmArgs g{};
     g.offsets = offsets;
     g.num_groups = c.N;
@@ -476,54 +478,47 @@ moe_status_t do_ffn(const moe_config_t& c, const uint16_t* x, const int32_t* per
     g.rows_done = at<int32_t>(ws, L.rows_done);
     g.status = status;
     g.skip_producer = take_suppress_producer();
+    const void* Bs[2] = {W.W1s, W.W2s};
+    int64_t b_rows_s[2] = {0, 0};
+    if (sh) {
+      g.shared_rows = c.T;
+      g.shp[0].n_out = c.F_shared;
+      g.shp[0].K = c.H;
+      g.shp[0].mode = act_mode;
+      g.shp[0].bias = reinterpret_cast<const bf*>(W.b1s);
+      g.shp[0].out = at<bf>(ws, L.hid_s);
+      g.shp[0].ld_out = c.F_shared;
+      g.shp[1].n_out = c.H;
+      g.shp[1].K = c.F_shared;
+      g.shp[1].mode = EPI_SCALE;
+      g.shp[1].bias = reinterpret_cast<const bf*>(W.b2s);
+      g.shp[1].out = reinterpret_cast<bf*>(y_shared);
+      g.shp[1].ld_out = c.H;
+      if (fp8) {
+        g.shp[0].b_scale = W.s1s;
+        g.shp[1].b_scale = W.s2s;
+      }
+      g.rows_done_s = at<int32_t>(ws, L.rows_done_s);
+      b_rows_s[0] = w1_rows(c, c.F_shared);
+      b_rows_s[1] = c.H;
+    }
     const void* B[2] = {W.W1, W.W2};
     const int64_t b_rows[2] = {(int64_t)c.N * w1_rows(c, c.F), (int64_t)c.N * c.H};
     GemmPlan p;
-    MOE_CUDA(make_gemm_plan(&p, g, xp, R, B, b_rows, fp8, group_rows_max(c), sms));
-    MOE_CUDA(launch_gemm(p, st, tr));
-  }
-  if (c.F_shared > 0 && c.T > 0) {
-    GemmArgs g{};
-    g.offsets = nullptr;
-    g.num_groups = 1;
-    g.rows_single = c.T;
-    g.num_phases = 2;
-    g.ph[0].n_out = c.F_shared;
-    g.ph[0].K = c.H;
-    g.ph[0].mode = act_mode;
-    g.ph[0].bias = reinterpret_cast<const bf*>(W.b1s);
-    g.ph[0].out = at<bf>(ws, L.hid_s);
-    g.ph[0].ld_out = c.F_shared;
-    g.ph[1].n_out = c.H;
-    g.ph[1].K = c.F_shared;
-    g.ph[1].mode = EPI_SCALE;
-    g.ph[1].bias = reinterpret_cast<const bf*>(W.b2s);
-    g.ph[1].out = reinterpret_cast<bf*>(y_shared);
-    g.ph[1].ld_out = c.H;
-    if (fp8) {
-      g.ph[0].b_scale = W.s1s;
-      g.ph[1].b_scale = W.s2s;
-    }
-    g.rows_done = at<int32_t>(ws, L.rows_done_s);
-    g.status = status;
-    g.skip_producer = take_suppress_producer();
-    const void* B[2] = {W.W1s, W.W2s};
-    const int64_t b_rows[2] = {w1_rows(c, c.F_shared), (int64_t)c.H};
-    GemmPlan p;
-    MOE_CUDA(make_gemm_plan(&p, g, reinterpret_cast<const bf*>(x), c.T, B, b_rows, fp8, c.T,
-                            sms));
+    // the rows one group can hold: an expert's (capacity, at most one per
+    // token) or the shared expert's T
+    const int64_t gmax = sh ? (int64_t)c.T : group_rows_max(c);
+    MOE_CUDA(make_gemm_plan(&p, g, xp, R, B, b_rows, fp8, gmax, sms,
+                            reinterpret_cast<const bf*>(x), Bs, b_rows_s));
     MOE_CUDA(launch_gemm(p, st, tr));
   }
   return MOE_OK;
 }
 
 int ffn_num_launches(const moe_config_t& c, bool gathered) {
+  // [gather] + one launch for the routed and the shared experts
   const bool rows = max_rows_of(c) > 0, sh = c.F_shared > 0 && c.T > 0;
-  if (decode_ffn(c)) return (rows && !gathered ? 1 : 0) + (rows || sh ? 1 : 0);
-  int n = 0;
-  if (rows) n += gathered ? 1 : 2;
-  if (sh) n += 1;
-  return n;
+  return (rows && !gathered ? 1 : 0) + (rows || sh ? 1 : 0);
 }
 
 // Names of the launches moe_forward makes, in order (moe_forward_launch_name).
@@ -554,14 +549,8 @@ int forward_launch_names(const moe_config_t& c, const char** names, int cap) {
   } else {
     add("permute_scan");
   }
-  if (decode_ffn(c)) {
-    if (rows && !gathered) add("gather_rows");
-    if (rows || sh) add("expert_ffn_decode");
-  } else {
-    if (rows && !gathered) add("gather_rows");
-    if (rows) add("expert_ffn");
-    if (sh) add("shared_ffn");
-  }
+  if (rows && !gathered) add("gather_rows");
+  if (rows || sh) add(decode_ffn(c) ? "expert_ffn_decode" : "expert_ffn");
   if (c.T > 0) add("combine");
   return n;
 }

@@ -95,9 +95,10 @@ def _wcfg(w):
 
 
 def test_launch_names_cover_every_launch(lib):
-    """One name per launch moe_forward enqueues; the expert FFN runs as the
-    operand-swapped decode launch (shared expert included) exactly when the
-    experts hold at most 64 rows on average."""
+    """One name per launch moe_forward enqueues; the expert FFN (shared
+    expert included) runs as the operand-swapped decode launch exactly when
+    the experts hold at most 64 rows on average, else as the token-row
+    launch."""
     import moe_workloads as wl
     for w in list(wl.WORKLOADS.values()) + list(wl.TEST_WORKLOADS.values()):
         c = _wcfg(w)
@@ -108,7 +109,9 @@ def test_launch_names_cover_every_launch(lib):
         R = lib.moe_max_rows(C.byref(c))
         decode = R <= 64 * w.N
         assert ("expert_ffn_decode" in names) == (decode and (R > 0 or w.F_shared > 0)), w.name
-        assert ("shared_ffn" in names) == (w.F_shared > 0 and not decode), w.name
+        # the shared expert is a group of the expert-FFN launch on both paths
+        assert "shared_ffn" not in names, w.name
+        assert ("expert_ffn" in names) == (not decode and (R > 0 or w.F_shared > 0)), w.name
         assert names[-1] == "combine", w.name
     for name in ("mixtral_decode", "deepseek_decode", "mixtral_decode_fp8", "tiny"):
         c = _wcfg(wl.get_workload(name))

@@ -62,7 +62,11 @@ def test_algorithmic_work_counts():
     assert work["expert_ffn"]["bytes"] == 2 * (2 * 8 * 4096 * 1024 + 2 * 8192 * 1024)
     d = wl.WORKLOADS["deepseek_prefill"]
     wk = bench.algorithmic_work(d, np.ones(d.N), d.T * d.k)
-    assert "shared_ffn" in wk and wk["shared_ffn"]["flops"] == 4 * d.T * d.F_shared * d.H
+    # the shared expert is part of the expert-FFN launch
+    assert wk["expert_ffn"]["flops"] == 4 * d.T * d.k * d.F * d.H + 4 * d.T * d.F_shared * d.H
+    assert wk["expert_ffn"]["bytes"] == (d.N * 2 * 2 * d.F * d.H + 2 * 2 * d.T * d.k * d.H +
+                                         2 * 2 * d.F_shared * d.H + 2 * 2 * d.T * d.H)
+    assert wk["expert_ffn_decode"] == wk["expert_ffn"]
     # SwiGLU: gate, up and down matrices
     s = wl.WORKLOADS["mixtral_swiglu_decode"]
     ws = bench.algorithmic_work(s, np.full(s.N, 16), 128)
