@@ -56,10 +56,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits for the phase with the given parity to complete.  Returns false if
-// another role of the CTA has already given up (abort flag set) or if the
-// wait itself runs past kWaitLimitCycles; in the latter case it sets the
-// abort flag and records MOE_ERR_TIMEOUT in the status word.
 // Parity wait with cluster-scope acquire: for phases completed by arrivals
 // (release.cluster) from the peer CTA of a pair.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
@@ -74,6 +70,7 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
   return ok != 0;
 }
 
+// mbar_wait_bounded (below) with a cluster-scope acquire.
 __device__ __forceinline__ bool mbar_wait_bounded_cluster(uint32_t bar, uint32_t parity,
                                                           volatile int* abort_flag, int* status) {
   const long long t0 = clock64();
@@ -88,6 +85,10 @@ __device__ __forceinline__ bool mbar_wait_bounded_cluster(uint32_t bar, uint32_t
   return true;
 }
 
+// Waits for the phase with the given parity to complete.  Returns false if
+// another role of the CTA has already given up (abort flag set) or if the
+// wait itself runs past kWaitLimitCycles; in the latter case it sets the
+// abort flag and records MOE_ERR_TIMEOUT in the status word.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   volatile int* abort_flag, int* status) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -335,6 +336,11 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
+}
+
+// 32-bit store into another CTA of the cluster (shared::cluster address).
+__device__ __forceinline__ void st_shared_cluster_s32(uint32_t cluster_addr, int v) {
+  asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ void cluster_sync_all() {

@@ -269,6 +269,11 @@ struct GemmArgs {
   int32_t shared_rows;
   GemmPhase shp[2];
   int32_t* rows_done_s;
+  // bf16 weights: a launch-wide tile counter (zeroed before the launch) from
+  // which the CTAs (pairs) take their next tile as they finish the last one;
+  // nullptr: tile t runs on CTA (pair) t % grid.  make_gemm_plan keeps it
+  // only for bf16 launches of many tiles per CTA (pair).
+  int32_t* tile_counter;
 };
 
 struct GemmPlan {

@@ -92,8 +92,9 @@ WsLayout layout_of(const moe_config_t& c) {
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o += align_up(bytes > 0 ? bytes : 1); return at; };
   // The header every call zeroes first: [0] status word, [1] router ticket,
-  // [2] permute ticket, then the row-block counters of the routed and the shared expert FFN
-  // launches (phase 0 -> phase 1 hand-over).
+  // [2] permute ticket (or the fused dispatch's flag), [3] the expert FFN
+  // launch's tile counter, then the row-block counters of the routed and the
+  // shared expert FFN (phase 0 -> phase 1 hand-over).
   int64_t nrd = R > 0 ? gemm_rows_done_len(R, (int)N) : 0;
   const int64_t nrd_s = (c.F_shared > 0 && T > 0) ? gemm_rows_done_len(T, 1) : 0;
   if (T > 0 && decode_ffn(c)) {
@@ -477,6 +478,7 @@ moe_status_t do_ffn(const moe_config_t& c, const uint16_t* x, const int32_t* per
     }
     g.rows_done = at<int32_t>(ws, L.rows_done);
     g.status = status;
+    g.tile_counter = fp8 ? nullptr : status + 3;   // zeroed with the header
     g.skip_producer = take_suppress_producer();
     const void* Bs[2] = {W.W1s, W.W2s};
     int64_t b_rows_s[2] = {0, 0};
