@@ -313,7 +313,7 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
   // in columns.  Not for SwiGLU first Linears (gate and up rows would land in
   // different CTAs).
   auto swapped_tail = [&](int ph, int rows_left) {
-    return PAIR == 2 && args.swap_tail != 0 && rows_left < S::TILE_M &&
+    return PAIR == 2 && rows_left <= args.swap_tail && rows_left < S::TILE_M &&
            (ph ? args.ph[1].mode : args.ph[0].mode) != EPI_SWIGLU;
   };
 
@@ -783,19 +783,19 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
           if (P.bias) bz = __bfloat162float(P.bias[(size_t)gi * n_out + colw]);
           if (FP8 && P.b_scale) sz = P.b_scale[(size_t)gi * n_out + colw];
         }
-        // this warp's chunks: 8 tokens at c = cpart * 8 + i * CSTEP (at most
-        // NCH of them); their gate weights are fetched now, before the
-        // accumulator is ready: lane l holds the weight of token c_i + l % 8
+        // this warp's chunks: 8 tokens at c = cpart * 8 + i * CSTEP, two per
+        // TMEM round trip; lane l holds the gate weight of token c + l % 8.
+        // The loop stays rolled (an unrolled one, with every activation
+        // inlined, made the whole launch slower through its code size); the
+        // weights of the next two chunks are fetched one pass ahead, those
+        // of the first two before the accumulator is ready.
         constexpr int CSTEP = 8 * (EPI_WARPS / 4);
-        constexpr int NCH = 256 / CSTEP;
-        float wpre[NCH];
-#pragma unroll
-        for (int i = 0; i < NCH; ++i) {
-          const int tok = cpart * 8 + i * CSTEP + (lane & 7);
-          wpre[i] = (P.mode == EPI_SCALE && P.topk_w != nullptr && tok < rows_left)
-                        ? P.topk_w[P.perm[a_row + tok]]
-                        : 1.0f;
-        }
+        const bool gate_w = P.mode == EPI_SCALE && P.topk_w != nullptr;
+        auto gate_of = [&](int c) {
+          const int tok = c + (lane & 7);
+          return gate_w && tok < rows_left ? P.topk_w[P.perm[a_row + tok]] : 1.0f;
+        };
+        float wn0 = gate_of(cpart * 8), wn1 = gate_of(cpart * 8 + CSTEP);
         int ok = 1;
         if (lane == 0) ok = mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, status) ? 1 : 0;
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -803,37 +803,44 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
         tc_fence_after();
         uint16_t* tb = trans_stage + (warp - 2) * 8 * 32;
         const uint32_t taddr = tmem_base + lane_addr + acc * BN;
-        // two chunks per TMEM round trip
+        // one 8-token chunk: activation (or gate weight), then the transpose
+        // into 16-byte stores along the output rows
+        auto chunk = [&](const uint32_t* r, int c, float wv) {
+          float o[8];
+          if (P.mode == EPI_GELU) {
 #pragma unroll
-        for (int i = 0; i < NCH; i += 2) {
-          const int c0 = cpart * 8 + i * CSTEP, c1 = c0 + CSTEP;
-          if (c0 >= n16) break;
+            for (int t = 0; t < 8; ++t) o[t] = gelu_erf(__uint_as_float(r[t]) * sz + bz);
+          } else if (P.mode == EPI_SILU) {
+#pragma unroll
+            for (int t = 0; t < 8; ++t) o[t] = silu_f(__uint_as_float(r[t]) * sz + bz);
+          } else {
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+              o[t] = __shfl_sync(0xffffffffu, wv, t) * (__uint_as_float(r[t]) * sz + bz);
+          }
+#pragma unroll
+          for (int t = 0; t < 8; ++t) tb[t * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(o[t]));
+          __syncwarp();
+          const int t = lane >> 2, c8 = (lane & 3) * 8;
+          if (c + t < rows_left && colq + c8 < n_out)
+            *reinterpret_cast<uint4*>(P.out + (int64_t)(a_row + c + t) * P.ld_out + colq + c8) =
+                *reinterpret_cast<const uint4*>(tb + t * 32 + c8);
+          __syncwarp();
+        };
+#pragma unroll 1
+        for (int c0 = cpart * 8; c0 < n16; c0 += 2 * CSTEP) {
+          const int c1 = c0 + CSTEP;
+          const float w0 = wn0, w1 = wn1;
+          if (c0 + 2 * CSTEP < n16) {
+            wn0 = gate_of(c0 + 2 * CSTEP);
+            wn1 = gate_of(c1 + 2 * CSTEP);
+          }
           uint32_t r0[8], r1[8];
           tmem_ld_32x32b_x8(taddr + c0, r0);
           if (c1 < n16) tmem_ld_32x32b_x8(taddr + c1, r1);
           tmem_ld_wait();
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int c = h ? c1 : c0;
-            if (c >= n16) break;
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-              const float z = __uint_as_float(h ? r1[t] : r0[t]) * sz + bz;
-              float o;
-              if (P.mode == EPI_GELU) o = gelu_erf(z);
-              else if (P.mode == EPI_SILU) o = silu_f(z);
-              else o = __shfl_sync(0xffffffffu, h ? wpre[i + 1] : wpre[i], t) * z;
-              tb[t * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
-            }
-            __syncwarp();
-            {
-              const int t = lane >> 2, c8 = (lane & 3) * 8;
-              if (c + t < rows_left && colq + c8 < n_out)
-                *reinterpret_cast<uint4*>(P.out + (int64_t)(a_row + c + t) * P.ld_out + colq + c8) =
-                    *reinterpret_cast<const uint4*>(tb + t * 32 + c8);
-            }
-            __syncwarp();
-          }
+          chunk(r0, c0, w0);
+          if (c1 < n16) chunk(r1, c1, w1);
         }
       } else {
       const int r_in = warp_row0 + lane;
@@ -927,22 +934,25 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
         }
       } else if (warp_has_rows && col0 < n_out) {
         const uint32_t taddr = tmem_base + lane_addr + acc * BN + cpart * EPI_COLS;
+        // CW = 16 columns per TMEM load: half the inlined activation code of
+        // 32-wide passes, which matters for the instruction cache
+        constexpr int CW = 16;
 #pragma unroll 1
-        for (int c = 0; c < EPI_COLS / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(taddr + c * 32, r);
+        for (int c = 0; c < EPI_COLS / CW; ++c) {
+          uint32_t r[CW];
+          tmem_ld_32x32b_x16(taddr + c * CW, r);
           tmem_ld_wait();
-          float v[32];
+          float v[CW];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+          for (int i = 0; i < CW; ++i) v[i] = __uint_as_float(r[i]);
           if (has_scale) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] *= my_scale[c * 32 + i];
+            for (int i = 0; i < CW; ++i) v[i] *= my_scale[c * CW + i];
           }
           if (has_bias) {
 #pragma unroll
-            for (int j8 = 0; j8 < 4; ++j8) {
-              const uint4 u = *reinterpret_cast<const uint4*>(my_bias + c * 32 + 8 * j8);
+            for (int j8 = 0; j8 < CW / 8; ++j8) {
+              const uint4 u = *reinterpret_cast<const uint4*>(my_bias + c * CW + 8 * j8);
               v[8 * j8 + 0] += bf16lo(u.x); v[8 * j8 + 1] += bf16hi(u.x);
               v[8 * j8 + 2] += bf16lo(u.y); v[8 * j8 + 3] += bf16hi(u.y);
               v[8 * j8 + 4] += bf16lo(u.z); v[8 * j8 + 5] += bf16hi(u.z);
@@ -951,31 +961,31 @@ __global__ void __launch_bounds__(GemmShape<PAIR, FP8>::THREADS, 1)
           }
           if (P.mode == EPI_GELU) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
+            for (int i = 0; i < CW; ++i) v[i] = gelu_erf(v[i]);
           } else if (P.mode == EPI_SILU) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = silu_f(v[i]);
+            for (int i = 0; i < CW; ++i) v[i] = silu_f(v[i]);
           } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] *= wscale;
+            for (int i = 0; i < CW; ++i) v[i] *= wscale;
           }
-          uint4 o[4];
+          uint4 o[CW / 8];
 #pragma unroll
-          for (int j8 = 0; j8 < 4; ++j8) {
+          for (int j8 = 0; j8 < CW / 8; ++j8) {
             o[j8].x = pack_bf16x2(v[8 * j8 + 0], v[8 * j8 + 1]);
             o[j8].y = pack_bf16x2(v[8 * j8 + 2], v[8 * j8 + 3]);
             o[j8].z = pack_bf16x2(v[8 * j8 + 4], v[8 * j8 + 5]);
             o[j8].w = pack_bf16x2(v[8 * j8 + 6], v[8 * j8 + 7]);
           }
-          const int col = col0 + c * 32;
+          const int col = col0 + c * CW;
           uint4* dst = reinterpret_cast<uint4*>(orow + col);
           if (row_ok) {
             if (full_cols) {
 #pragma unroll
-              for (int j8 = 0; j8 < 4; ++j8) dst[j8] = o[j8];
+              for (int j8 = 0; j8 < CW / 8; ++j8) dst[j8] = o[j8];
             } else {
 #pragma unroll
-              for (int j8 = 0; j8 < 4; ++j8)
+              for (int j8 = 0; j8 < CW / 8; ++j8)
                 if (col + 8 * j8 < n_out) dst[j8] = o[j8];
             }
           }
@@ -1115,6 +1125,10 @@ bool encode_tensor_map_u8(CUtensorMap* map, const void* base, int64_t rows, int6
   return r == CUDA_SUCCESS;
 }
 
+// CTA pairs: a group's last row block runs operand-swapped when it holds at
+// most this many rows.
+constexpr int kSwapTailRows = 255;
+
 // Launches with at least this many tiles (row blocks without tails x column
 // blocks) per CTA pair (or CTA) take their tiles in dynamic order.
 constexpr int64_t kDynamicTilesPerUnit = 100;
@@ -1195,7 +1209,7 @@ cudaError_t make_gemm_plan(GemmPlan* plan, const GemmArgs& args_in, const __nv_b
     plan->tmS[2] = plan->tmA[1];
     plan->tmS[3] = plan->tmB[1];
   }
-  args.swap_tail = pair == 2 ? 1 : 0;
+  args.swap_tail = pair == 2 ? kSwapTailRows : 0;
   plan->args = args;
   plan->pair = pair;
   plan->fp8 = fp8;

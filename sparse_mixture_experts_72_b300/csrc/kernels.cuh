@@ -261,8 +261,9 @@ struct GemmArgs {
   int32_t skip_producer;         // failure injection: the TMA producer issues nothing
   int32_t a_box;                 // rows per A copy (set by make_gemm_plan): 128, or for
                                  // FP8 single-CTA tiles the bound on a group's rows
-  int32_t swap_tail;             // CTA pairs: a group's last row block of fewer than 256
-                                 // rows runs operand-swapped (set by make_gemm_plan)
+  int32_t swap_tail;             // CTA pairs: a group's last row block of at most this
+                                 // many rows (and fewer than 256) runs operand-swapped;
+                                 // 0: none (set by make_gemm_plan)
   // the always-on shared expert as group G of the same launch: shared_rows
   // rows (T; 0 = none) of its own A tensors (x, then its Hid), its own
   // weights, outputs (shp[p].out) and row-block counters; weight 1
