@@ -87,7 +87,7 @@ def load_peaks():
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for f in ("gemm_tc.cu", "common.cuh", "kernels.cuh"):
+    for f in ("gemm_tc.cu", "decode_tc.cu", "common.cuh", "kernels.cuh"):
         with open(os.path.join(ROOT, "sparse_mixture_experts_72_b300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -643,7 +643,8 @@ def config_entry(w, res, ms, peaks, peak_src):
             "steps": res["K"], "step_ms_min": res["step_ms_min"], "step_ms_max": res["step_ms_max"],
             "kept_rows": res["R"], "experts_hit": int((res["counts"] > 0).sum()),
             "ffn": None if roof is None else {k: roof[k] for k in
-                                              ("bound", "achieved", "unit", "frac", "launch_ms")},
+                                              ("bound", "achieved", "unit", "frac", "launch_ms",
+                                               "traffic")},
             "forward": forward_roofline(res, ms, peaks, peak_src),
             "launch_ms": res["per_ms"], "clocks": res["clocks"]}
 
