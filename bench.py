@@ -21,6 +21,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -85,11 +86,21 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def code_without_comments(src: str) -> str:
+    """C++ source without its comments and blank lines (the kernels' code)."""
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return "\n".join(l.rstrip() for l in src.splitlines() if l.strip())
+
+
 def kernel_source_hash() -> str:
+    """Hash of the FFN kernels' code (comments excluded): DRAM traffic taken
+    on other code is not reported."""
     h = hashlib.sha256()
     for f in ("gemm_tc.cu", "decode_tc.cu", "common.cuh", "kernels.cuh"):
-        with open(os.path.join(ROOT, "sparse_mixture_experts_72_b300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "sparse_mixture_experts_72_b300", "csrc", f),
+                  encoding="utf-8") as fh:
+            h.update(code_without_comments(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

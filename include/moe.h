@@ -263,11 +263,11 @@ moe_status_t moe_permute(const moe_config_t* cfg, const int32_t* topk_idx, const
  * Two kernels serve it.  When the experts hold at most 64 rows on average
  * (moe_max_rows(cfg) <= 64 N: decode-sized batches) the operands are
  * swapped: each expert's weights are the 128-row operand of the tensor-core
- * MMA and its token rows the narrow one, and the shared expert is one more
- * group of the same launch; any row count per expert is computed.
- * Otherwise token rows are the 128- or 256-row operand (CTA pairs for groups
- * of 192 rows or more on average) and the shared expert has a launch of its
- * own.  There, offsets must give no expert more rows than the config allows
+ * MMA and its token rows the narrow one; any row count per expert is
+ * computed.  Otherwise token rows are the 128- or 256-row operand (CTA pairs
+ * for groups of 192 rows or more on average).  In both kernels the shared
+ * expert is one more group of the same launch (T rows, weight 1).  In the
+ * token-row kernel, offsets must give no expert more rows than the config allows
  * (at most T for token choice, since a token picks distinct experts, and at
  * most the capacity when one applies), as moe_permute and moe_expert_choice
  * produce: FP8 launches with groups below 128 rows copy only that many rows

@@ -15,8 +15,11 @@
 //
 // One launch runs the whole expert FFN as two phases over one persistent
 // grid: phase 0 (Hid = GELU(X W1^T + b1)) and phase 1 (y = w (Hid W2^T +
-// b2)).  The tile list is phase 0's tiles followed by phase 1's; CTAs take
-// tiles round-robin.  When the last of a CTA's epilogue warps has stored a
+// b2)), for the routed experts and, as group G with its own tensors and
+// weight 1, the always-on shared expert ("混合专家模型 MoE 架构深度解析" §3).
+// The tile list is phase 0's tiles followed by phase 1's; CTAs (pairs) take
+// them round-robin or, in long bf16 launches, from a launch-wide counter
+// (dynamic order).  When the last of a CTA's epilogue warps has stored a
 // phase-0 tile (a CTA-scope acquire-release count in shared memory), it
 // releases a per-row-block counter in global memory (red.release.gpu), and
 // the TMA producer acquires the counter of a phase-1 tile's row block

@@ -152,3 +152,13 @@ def test_bench_defaults_to_the_largest_prefill_config():
     assert set(bench.PER_CONFIG) == {"moelayer", "mixtral_prefill", "mixtral_decode",
                                      "deepseek_prefill", "deepseek_decode", "switch_capacity",
                                      "mixtral_decode_fp8"}
+
+
+def test_traffic_hash_ignores_comments_only():
+    src = "// a\nint f(int x) {  // b\n  /* c\n d */ return x + 1;\n}\n"
+    same = "int f(int x) {\n   return x + 1;\n}\n// other words\n"
+    other = "int f(int x) {\n  return x + 2;\n}\n"
+    c = bench.code_without_comments
+    assert c(src) == c(same)
+    assert c(src) != c(other)
+    assert "a" not in c(src).split() and "return x + 1;" in c(src)
